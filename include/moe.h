@@ -1,0 +1,173 @@
+/*
+ * moe.h -- C ABI of a single-GPU Mixture-of-Experts expert layer for GB300 (sm_103a).
+ *
+ * One GPU holds all E experts.  A training step of the layer is three calls on
+ * one CUDA stream:
+ *
+ *   moe_plan      router logits -> top-k experts and gate weights, per-expert
+ *                 counts, exclusive offsets and the stable token -> row table;
+ *   moe_forward   dispatch (row gather), GroupGEMM -> SwiGLU -> GroupGEMM, gated combine;
+ *   moe_backward  combine backward, dgrad GroupGEMMs, weight-gradient Transposed
+ *                 GroupGEMM, dispatch backward.
+ *
+ * Sources (by page title and section):
+ *   [UniEP]  "UniEP: Unified Expert-Parallel MoE MegaKernel for LLM Training"
+ *   [MoonEP] "MoonEP: Balanced Expert Parallelism for MoE Training via Dynamic Redundant Experts"
+ *
+ * Conventions for every entry point
+ *   - Dimensions: T tokens, H hidden, F per-expert FFN width, E experts, k
+ *     experts per token, R = T*k grouped rows.
+ *   - Every pointer argument is a DEVICE pointer owned by the caller, except
+ *     the structs passed by address (host memory) and the host outputs of
+ *     moe_get_status.  The library never allocates or frees memory and never
+ *     synchronises, except moe_get_status, which synchronises the stream.
+ *   - Tensors are dense row-major.  bf16 tensors are passed as void* (IEEE
+ *     bfloat16 bit patterns).  Every device pointer must be 16-byte aligned.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy stream).
+ *   - Return value: 0 on success, a negative MOE_ERR_* code when the host
+ *     rejected the call (nothing was launched), or MOE_ERR_LAUNCH.  Errors the
+ *     GPU detects are recorded in the workspace status word and read back with
+ *     moe_get_status.
+ *   - Results are bitwise reproducible: the same inputs give the same bits on
+ *     every call and for every grid size.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+/* ---- error codes ---------------------------------------------------------- */
+#define MOE_OK 0
+#define MOE_ERR_ARG (-1)     /* null pointer, non-positive dimension, k > E, k > 32, R >= 2^31 */
+#define MOE_ERR_ALIGN (-2)   /* a pointer is not 16-byte aligned */
+#define MOE_ERR_WS (-3)      /* workspace smaller than moe_workspace_bytes() */
+#define MOE_ERR_LAUNCH (-4)  /* a CUDA launch or API call failed */
+#define MOE_ERR_SHAPE (-5)   /* H or F not a multiple of 128, or E > 1024 */
+#define MOE_ERR_DEVICE (-6)  /* current device is not compute capability 10.3 */
+/* recorded by the GPU in the workspace status word */
+#define MOE_ERR_TIMEOUT 1    /* a bounded wait inside a kernel expired; the kernel returned */
+#define MOE_ERR_NONFINITE 2  /* a router logit was NaN or infinite */
+#define MOE_ERR_BOUNDS 3     /* an index computed on the GPU fell outside its buffer; the access was skipped */
+
+/* ---- shapes and tables ------------------------------------------------------ */
+typedef struct {
+  int32_t T, H, F, E, k;
+} moe_dims;
+
+/* Routing state of one step.  Filled by moe_plan, read unchanged by
+ * moe_forward and moe_backward of the same step (the plan object of the
+ * MoonEP Buffer API: "The Buffer API: Dispatch, Combine, Prefetch, and Reduce").
+ * All device buffers, caller-allocated. */
+typedef struct {
+  int32_t *topk_ids; /* [T,k]  expert of slot j of token t; descending logit, ties to the lower id */
+  float *topk_w;     /* [T,k]  renormalised gate weight of that slot (fp32) */
+  int32_t *counts;   /* [E]    rows per expert n_e */
+  int32_t *offsets;  /* [E+1]  exclusive prefix of counts; offsets[E] = R */
+  int32_t *dest;     /* [T,k]  grouped row of slot (t,j): offsets[e] + #{t' < t routed to e} */
+  int32_t *row_src;  /* [R]    token of each grouped row (inverse of dest) */
+  uint8_t *row_slot; /* [R]    slot j of each grouped row */
+  int32_t *tiles;    /* [moe_plan_tiles_elems(d)]  128-row GEMM tiles of the grouped buffer (internal) */
+} moe_plan_t;
+
+/* Tensors the forward stores for the backward (caller-allocated, bf16). */
+typedef struct {
+  void *Xp; /* [R,H]   dispatched rows, grouped by expert */
+  void *GU; /* [R,2F]  G = Xp W1 in columns [0,F), U = Xp W3 in columns [F,2F) (bf16 of fp32 accumulators) */
+  void *h;  /* [R,F]   silu(G) * U */
+  void *Y;  /* [R,H]   expert outputs h W2, one row per (token, slot) */
+} moe_saved_t;
+
+/* Row gradients the backward produces on its way (caller-allocated, bf16). */
+typedef struct {
+  void *dY;  /* [R,H]   w[t,j] * dout[t] on the grouped row of (t,j) */
+  void *dGU; /* [R,2F]  dG in columns [0,F), dU in columns [F,2F) */
+  void *dXp; /* [R,H]   gradient of the dispatched rows */
+} moe_grads_t;
+
+/* Options (may be NULL for defaults). */
+typedef struct {
+  int32_t grid;     /* CTAs of the persistent kernels; 0 = one per SM.  Results do not depend on it. */
+  int32_t reserved; /* must be 0 */
+  void **events;    /* optional: 2*n_events cudaEvent_t recorded around each kernel of the call */
+  int32_t n_events; /* capacity of events/2; kernels beyond it are not timed */
+  int32_t reserved2;
+} moe_opts;
+
+/* ---- sizes ------------------------------------------------------------------ */
+
+/* Bytes of the scratch workspace every call of one step needs (status word,
+ * per-chunk counts and bitmaps of the routing, task cursors).  Caller-allocated;
+ * pass the same workspace to moe_plan, moe_forward and moe_backward of a step.
+ * Returns 0 for invalid dims. */
+MOE_API size_t moe_workspace_bytes(moe_dims d);
+
+/* int32 elements of moe_plan_t.tiles.  Returns 0 for invalid dims. */
+MOE_API size_t moe_plan_tiles_elems(moe_dims d);
+
+/* ---- the layer -------------------------------------------------------------- */
+
+/* Gating and the deterministic token -> row table.
+ * [UniEP] background, Forward Propagation (top-k routing; stable sort keeping
+ * the original token order) and section 3.1 Deterministic Token Mapping,
+ * Algorithm 1 (counts per source, exclusive prefix over sources, base + local
+ * stable index).  Here the sources are 256-token chunks of one GPU.
+ *   logits  [T,E] fp32, device.  plan: every field allocated by the caller.
+ *   T = 0 is a no-op.  NaN/inf logits set MOE_ERR_NONFINITE in the status word. */
+MOE_API int moe_plan(moe_dims d, const float *logits, const moe_plan_t *plan, void *ws, size_t ws_bytes, void *stream);
+
+/* Forward pass: Xp = x[row_src]; per expert e on rows [offsets[e], offsets[e+1]):
+ * G = Xp W1[e], U = Xp W3[e], h = silu(G) * U, Y = h W2[e]; then
+ * out[t] = sum_j w[t,j] * Y[dest[t,j]] (fp32, slots in order, rounded to bf16).
+ * [UniEP] Forward Propagation (Figure 1) and section 3, Top-k accumulation
+ * constraint; [MoonEP] zero-copy dispatch.
+ *   x [T,H], W1 [E,H,F], W3 [E,H,F], W2 [E,F,H], out [T,H]: bf16, device.
+ *   saved: filled with Xp, GU, h, Y for the backward. */
+MOE_API int moe_forward(moe_dims d, const void *x, const void *W1, const void *W3, const void *W2, const moe_plan_t *plan,
+                const moe_saved_t *saved, void *out, void *ws, size_t ws_bytes, const moe_opts *opts, void *stream);
+
+/* Backward pass given dout = dL/dout [T,H] (bf16):
+ *   dY[dest[t,j]] = w[t,j] dout[t];  dgate[t,j] = <dout[t], Y[dest[t,j]]>  (fp32)
+ *   dH = dY W2[e]^T;  dG = dH U s (1 + G (1 - s)), dU = dH G s with s = sigmoid(G)
+ *   dXp = dG W1[e]^T + dU W3[e]^T;  dx[t] = sum_j dXp[dest[t,j]]
+ *   dW1[e] = Xp_e^T dG_e, dW3[e] = Xp_e^T dU_e, dW2[e] = h_e^T dY_e  (fp32; n_e = 0 gives zeros)
+ * The weight gradients reduce over each expert's rows in ascending row order
+ * with one owner per output tile, so they are bitwise reproducible.
+ * [UniEP] Backward Propagation and Numerical Stability (Transposed GroupGEMM
+ * along the accumulation dimension); [MoonEP] the dispatch gradient is a combine.
+ *   dx [T,H] bf16; dW1, dW3 [E,H,F], dW2 [E,F,H], dgate [T,k]: fp32, device. */
+MOE_API int moe_backward(moe_dims d, const void *dout, const void *W1, const void *W3, const void *W2, const moe_plan_t *plan,
+                 const moe_saved_t *saved, const moe_grads_t *grads, void *dx, float *dW1, float *dW3, float *dW2,
+                 float *dgate, void *ws, size_t ws_bytes, const moe_opts *opts, void *stream);
+
+/* Synchronises `stream`, copies the status word out of the workspace and clears it.
+ * device_status: 0 or a positive MOE_ERR_* code; where/detail: which kernel/task
+ * and index reported it (may be NULL).  Returns 0 or MOE_ERR_LAUNCH. */
+MOE_API int moe_get_status(void *ws, void *stream, int32_t *device_status, int32_t *where, int32_t *detail);
+
+/* Clears the status word (asynchronous on stream). */
+MOE_API int moe_clear_status(void *ws, void *stream);
+
+/* ---- introspection ---------------------------------------------------------- */
+MOE_API const char *moe_strerror(int code);
+MOE_API int32_t moe_version(void);
+/* Number of kernels this library has launched in this process. */
+MOE_API uint64_t moe_launch_count(void);
+/* Name of the i-th kernel a call launches (call: 0 plan, 1 forward, 2 backward); NULL past the end. */
+MOE_API const char *moe_kernel_name(int32_t call, int32_t i);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

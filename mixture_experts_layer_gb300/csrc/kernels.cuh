@@ -1,0 +1,115 @@
+// Declarations shared between the kernel files and the C ABI (host side).
+#pragma once
+
+#include <atomic>
+
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kChunk = 256;               // tokens per routing chunk (one "source" of the mapping)
+constexpr int kChunkWords = kChunk / 32;  // bitmap words per expert and chunk
+constexpr int kTileRows = 128;            // rows of a GEMM tile (the tcgen05 M)
+
+// Layout of moe_plan_t.tiles (int32): [0] number of 128-row tiles; [1 + e]
+// first tile of expert e (E + 1 entries); then, from tiles_entry_base(E),
+// one int4 {expert, first row, rows, 0} per tile in expert order.
+__host__ __device__ inline int tiles_entry_base(int E) { return ((E + 2) + 3) & ~3; }
+
+__host__ __device__ inline long long tiles_capacity(long long R, int E) { return R / kTileRows + E + 1; }
+
+extern std::atomic<unsigned long long> g_launches;
+
+// Records the caller's timing events around each kernel and counts launches.
+struct LaunchHook {
+  void** events = nullptr;
+  int n_events = 0;
+  int idx = 0;
+  void before(cudaStream_t s) {
+    if (events && idx < n_events) cudaEventRecord(static_cast<cudaEvent_t>(events[2 * idx]), s);
+  }
+  void after(cudaStream_t s) {
+    if (events && idx < n_events) cudaEventRecord(static_cast<cudaEvent_t>(events[2 * idx + 1]), s);
+    ++idx;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+  }
+};
+
+struct PlanLaunch {
+  const float* logits;
+  int T, E, k;
+  int32_t* ids;
+  float* w;
+  uint32_t* gbm;
+  int32_t* ccount;
+  int32_t* cbase;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* tiles;
+  int32_t* dest;
+  int32_t* row_src;
+  uint8_t* row_slot;
+  WsHeader* ws;
+};
+cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t s, LaunchHook& hook);
+
+struct RowsLaunch {
+  int T, H, k, R;
+  int grid;  // CTAs (256 threads each)
+  const int32_t* dest;
+  const int32_t* row_src;
+  const float* w;
+  WsHeader* ws;
+};
+// Xp[r] = x[row_src[r]]
+cudaError_t launch_gather(const RowsLaunch& p, const void* x, void* Xp, cudaStream_t s, LaunchHook& hook);
+// out[t] = bf16(sum_j w[t,j] Y[dest[t,j]])
+cudaError_t launch_combine(const RowsLaunch& p, const void* Y, void* out, cudaStream_t s, LaunchHook& hook);
+// dY[dest[t,j]] = bf16(w[t,j] dout[t]); dgate[t,j] = <dout[t], Y[dest[t,j]]>
+cudaError_t launch_combine_bwd(const RowsLaunch& p, const void* dout, const void* Y, void* dY, float* dgate,
+                               cudaStream_t s, LaunchHook& hook);
+// dx[t] = bf16(sum_j dXp[dest[t,j]])
+cudaError_t launch_unpermute(const RowsLaunch& p, const void* dXp, void* dx, cudaStream_t s, LaunchHook& hook);
+
+enum GemmMode : int {
+  kFwd1 = 0,    // [G|U] = Xp [W1|W3], h = silu(G) U           (A K-major, B MN-major)
+  kFwd2 = 1,    // Y = h W2                                    (A K-major, B MN-major)
+  kDgrad2 = 2,  // dH = dY W2^T, SwiGLU backward -> dG, dU      (A K-major, B K-major)
+  kDgrad1 = 3,  // dXp = [dG dU] [W1 W3]^T                      (A K-major, B K-major)
+  kWgrad13 = 4, // dW1 = Xp^T dG, dW3 = Xp^T dU per expert      (A MN-major, B MN-major)
+  kWgrad2 = 5,  // dW2 = h^T dY per expert                      (A MN-major, B MN-major)
+};
+
+struct GemmLaunch {
+  int T, H, F, E, k, R;
+  int grid;
+  int bn;  // N of one tile: 256, or 128 when the N extent is not a multiple of 256
+  const int32_t* tiles;
+  const int32_t* offsets;
+  const int32_t* counts;
+  // operands (bf16)
+  const void* Xp;
+  const void* W1;
+  const void* W3;
+  const void* W2;
+  const void* h;
+  const void* GU;
+  const void* dY;
+  const void* dGU;
+  // outputs
+  void* out_h;    // kFwd1
+  void* out_GU;   // kFwd1
+  void* out_Y;    // kFwd2
+  void* out_dGU;  // kDgrad2
+  void* out_dXp;  // kDgrad1
+  float* dW1;     // kWgrad13
+  float* dW3;     // kWgrad13
+  float* dW2;     // kWgrad2
+  WsHeader* ws;
+};
+cudaError_t launch_gemm(GemmMode mode, const GemmLaunch& p, cudaStream_t s, LaunchHook& hook);
+
+// Driver entry point for tensor-map encoding (resolved once through the runtime).
+bool tensor_map_encoder_ready();
+
+}  // namespace moe

@@ -1,0 +1,338 @@
+// Host side of the C ABI declared in include/moe.h: argument checks, workspace
+// layout, and the launch sequence of each call.  No memory is allocated here.
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+
+std::atomic<unsigned long long> g_launches{0};
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  int sms = 0;
+  int ok = -1;  // -1 unknown, 0 not sm_103, 1 ok
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+int device_info(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_LAUNCH;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (d.ok < 0) {
+    int major = 0, minor = 0, n = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MOE_ERR_LAUNCH;
+    d.sms = n;
+    d.ok = (major == 10 && minor == 3) ? 1 : 0;
+  }
+  if (!d.ok) return MOE_ERR_DEVICE;
+  *sms = d.sms;
+  return MOE_OK;
+}
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+int check_dims(const moe_dims& d) {
+  if (d.T < 0 || d.H <= 0 || d.F <= 0 || d.E <= 0 || d.k <= 0) return MOE_ERR_ARG;
+  if (d.k > d.E || d.k > 32) return MOE_ERR_ARG;
+  if (static_cast<long long>(d.T) * d.k >= (1ll << 31)) return MOE_ERR_ARG;
+  if (d.H % 128 != 0 || d.F % 128 != 0 || d.E > 1024) return MOE_ERR_SHAPE;
+  if (static_cast<long long>(d.E) * d.H >= (1ll << 31) || static_cast<long long>(d.E) * d.F >= (1ll << 31))
+    return MOE_ERR_SHAPE;
+  return MOE_OK;
+}
+
+struct WsLayout {
+  size_t ccount, cbase, gbm, total;
+};
+
+WsLayout ws_layout(const moe_dims& d) {
+  const size_t nchunks = (static_cast<size_t>(d.T) + kChunk - 1) / kChunk;
+  WsLayout L;
+  size_t off = align256(sizeof(WsHeader));
+  L.ccount = off;
+  off = align256(off + nchunks * d.E * 4);
+  L.cbase = off;
+  off = align256(off + nchunks * d.E * 4);
+  L.gbm = off;
+  off = align256(off + nchunks * d.E * kChunkWords * 4);
+  L.total = off;
+  return L;
+}
+
+bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_ws(const moe_dims& d, void* ws, size_t ws_bytes) {
+  if (!aligned16(ws)) return ws == nullptr ? MOE_ERR_ARG : MOE_ERR_ALIGN;
+  if (ws_bytes < ws_layout(d).total) return MOE_ERR_WS;
+  return MOE_OK;
+}
+
+int check_ptrs(std::initializer_list<const void*> ps) {
+  for (const void* p : ps) {
+    if (p == nullptr) return MOE_ERR_ARG;
+    if (!aligned16(p)) return MOE_ERR_ALIGN;
+  }
+  return MOE_OK;
+}
+
+int check_plan(const moe_plan_t* plan) {
+  if (plan == nullptr) return MOE_ERR_ARG;
+  int rc = check_ptrs({plan->topk_ids, plan->topk_w, plan->counts, plan->offsets, plan->dest, plan->row_src,
+                       plan->tiles});
+  if (rc) return rc;
+  return plan->row_slot == nullptr ? MOE_ERR_ARG : MOE_OK;
+}
+
+LaunchHook make_hook(const moe_opts* o) {
+  LaunchHook h;
+  if (o != nullptr && o->events != nullptr && o->n_events > 0) {
+    h.events = o->events;
+    h.n_events = o->n_events;
+  }
+  return h;
+}
+
+int grid_for(const moe_opts* o, int sms) {
+  if (o != nullptr && o->grid > 0) return o->grid < sms ? o->grid : sms;
+  return sms;
+}
+
+int finish(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH; }
+
+const char* const kPlanKernels[] = {"route_topk", "route_scan", "route_rank", nullptr};
+const char* const kFwdKernels[] = {"gather_rows", "gemm_fwd1_swiglu", "gemm_fwd2", "combine", nullptr};
+const char* const kBwdKernels[] = {"combine_bwd", "gemm_dgrad2_swiglu_bwd", "gemm_dgrad1", "gemm_wgrad13",
+                                   "gemm_wgrad2", "unpermute", nullptr};
+
+GemmLaunch gemm_common(const moe_dims& d, const moe_plan_t* plan, WsHeader* ws, int grid) {
+  GemmLaunch g{};
+  g.T = d.T;
+  g.H = d.H;
+  g.F = d.F;
+  g.E = d.E;
+  g.k = d.k;
+  g.R = d.T * d.k;
+  g.grid = grid;
+  g.tiles = plan->tiles;
+  g.offsets = plan->offsets;
+  g.counts = plan->counts;
+  g.ws = ws;
+  return g;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_workspace_bytes(moe_dims d) {
+  if (check_dims(d) != MOE_OK) return 0;
+  return ws_layout(d).total;
+}
+
+size_t moe_plan_tiles_elems(moe_dims d) {
+  if (check_dims(d) != MOE_OK) return 0;
+  return static_cast<size_t>(tiles_entry_base(d.E)) +
+         4 * static_cast<size_t>(tiles_capacity(static_cast<long long>(d.T) * d.k, d.E));
+}
+
+int moe_plan(moe_dims d, const float* logits, const moe_plan_t* plan, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if ((rc = check_ws(d, ws, ws_bytes))) return rc;
+  if (d.T == 0) return MOE_OK;
+  if ((rc = check_plan(plan))) return rc;
+  if ((rc = check_ptrs({logits}))) return rc;
+  int sms = 0;
+  if ((rc = device_info(&sms))) return rc;
+  const WsLayout L = ws_layout(d);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  PlanLaunch p;
+  p.logits = logits;
+  p.T = d.T;
+  p.E = d.E;
+  p.k = d.k;
+  p.ids = plan->topk_ids;
+  p.w = plan->topk_w;
+  p.gbm = reinterpret_cast<uint32_t*>(w + L.gbm);
+  p.ccount = reinterpret_cast<int32_t*>(w + L.ccount);
+  p.cbase = reinterpret_cast<int32_t*>(w + L.cbase);
+  p.counts = plan->counts;
+  p.offsets = plan->offsets;
+  p.tiles = plan->tiles;
+  p.dest = plan->dest;
+  p.row_src = plan->row_src;
+  p.row_slot = plan->row_slot;
+  p.ws = reinterpret_cast<WsHeader*>(w);
+  LaunchHook hook;
+  return finish(launch_plan(p, static_cast<cudaStream_t>(stream), hook));
+}
+
+int moe_forward(moe_dims d, const void* x, const void* W1, const void* W3, const void* W2, const moe_plan_t* plan,
+                const moe_saved_t* saved, void* out, void* ws, size_t ws_bytes, const moe_opts* opts,
+                void* stream) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if ((rc = check_ws(d, ws, ws_bytes))) return rc;
+  if (opts != nullptr && (opts->reserved != 0 || opts->grid < 0)) return MOE_ERR_ARG;
+  if (d.T == 0) return MOE_OK;
+  if ((rc = check_plan(plan))) return rc;
+  if (saved == nullptr) return MOE_ERR_ARG;
+  if ((rc = check_ptrs({x, W1, W3, W2, out, saved->Xp, saved->GU, saved->h, saved->Y}))) return rc;
+  int sms = 0;
+  if ((rc = device_info(&sms))) return rc;
+  if (!tensor_map_encoder_ready()) return MOE_ERR_LAUNCH;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  WsHeader* wsh = static_cast<WsHeader*>(ws);
+  const int grid = grid_for(opts, sms);
+  LaunchHook hook = make_hook(opts);
+
+  RowsLaunch r{d.T, d.H, d.k, d.T * d.k, grid * 8, plan->dest, plan->row_src, plan->topk_w, wsh};
+  cudaError_t e = launch_gather(r, x, saved->Xp, s, hook);
+  if (e != cudaSuccess) return MOE_ERR_LAUNCH;
+
+  GemmLaunch g = gemm_common(d, plan, wsh, grid);
+  g.Xp = saved->Xp;
+  g.W1 = W1;
+  g.W3 = W3;
+  g.W2 = W2;
+  g.out_h = saved->h;
+  g.out_GU = saved->GU;
+  g.bn = 256;
+  if ((e = launch_gemm(kFwd1, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
+  g.h = saved->h;
+  g.out_Y = saved->Y;
+  g.bn = (d.H % 256 == 0) ? 256 : 128;
+  if ((e = launch_gemm(kFwd2, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
+  return finish(launch_combine(r, saved->Y, out, s, hook));
+}
+
+int moe_backward(moe_dims d, const void* dout, const void* W1, const void* W3, const void* W2,
+                 const moe_plan_t* plan, const moe_saved_t* saved, const moe_grads_t* grads, void* dx, float* dW1,
+                 float* dW3, float* dW2, float* dgate, void* ws, size_t ws_bytes, const moe_opts* opts,
+                 void* stream) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if ((rc = check_ws(d, ws, ws_bytes))) return rc;
+  if (opts != nullptr && (opts->reserved != 0 || opts->grid < 0)) return MOE_ERR_ARG;
+  if ((rc = check_ptrs({dW1, dW3, dW2}))) return rc;
+  if (d.T > 0) {
+    if ((rc = check_plan(plan))) return rc;
+    if (saved == nullptr || grads == nullptr) return MOE_ERR_ARG;
+    if ((rc = check_ptrs({dout, W1, W3, W2, dx, dgate, saved->Xp, saved->GU, saved->h, saved->Y, grads->dY,
+                          grads->dGU, grads->dXp})))
+      return rc;
+  }
+  int sms = 0;
+  if ((rc = device_info(&sms))) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (d.T == 0) {
+    // No rows: every weight gradient is zero.
+    const size_t n = static_cast<size_t>(d.E) * d.H * d.F * sizeof(float);
+    if (cudaMemsetAsync(dW1, 0, n, s) != cudaSuccess || cudaMemsetAsync(dW3, 0, n, s) != cudaSuccess ||
+        cudaMemsetAsync(dW2, 0, n, s) != cudaSuccess)
+      return MOE_ERR_LAUNCH;
+    return MOE_OK;
+  }
+  if (!tensor_map_encoder_ready()) return MOE_ERR_LAUNCH;
+  WsHeader* wsh = static_cast<WsHeader*>(ws);
+  const int grid = grid_for(opts, sms);
+  LaunchHook hook = make_hook(opts);
+
+  RowsLaunch r{d.T, d.H, d.k, d.T * d.k, grid * 8, plan->dest, plan->row_src, plan->topk_w, wsh};
+  cudaError_t e = launch_combine_bwd(r, dout, saved->Y, grads->dY, dgate, s, hook);
+  if (e != cudaSuccess) return MOE_ERR_LAUNCH;
+
+  GemmLaunch g = gemm_common(d, plan, wsh, grid);
+  g.W1 = W1;
+  g.W3 = W3;
+  g.W2 = W2;
+  g.Xp = saved->Xp;
+  g.h = saved->h;
+  g.GU = saved->GU;
+  g.dY = grads->dY;
+  g.dGU = grads->dGU;
+  g.out_dGU = grads->dGU;
+  g.out_dXp = grads->dXp;
+  g.dW1 = dW1;
+  g.dW3 = dW3;
+  g.dW2 = dW2;
+  g.bn = (d.F % 256 == 0) ? 256 : 128;
+  if ((e = launch_gemm(kDgrad2, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
+  g.bn = (d.H % 256 == 0) ? 256 : 128;
+  if ((e = launch_gemm(kDgrad1, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
+  g.bn = 256;
+  if ((e = launch_gemm(kWgrad13, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
+  g.bn = (d.H % 256 == 0) ? 256 : 128;
+  if ((e = launch_gemm(kWgrad2, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
+  return finish(launch_unpermute(r, grads->dXp, dx, s, hook));
+}
+
+int moe_get_status(void* ws, void* stream, int32_t* device_status, int32_t* where, int32_t* detail) {
+  if (ws == nullptr || device_status == nullptr) return MOE_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_LAUNCH;
+  int32_t h[3] = {0, 0, 0};
+  if (cudaMemcpy(h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_LAUNCH;
+  *device_status = h[0];
+  if (where) *where = h[1];
+  if (detail) *detail = h[2];
+  if (h[0] != 0) {
+    const int32_t z[3] = {0, 0, 0};
+    if (cudaMemcpy(ws, z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return MOE_ERR_LAUNCH;
+  }
+  return MOE_OK;
+}
+
+int moe_clear_status(void* ws, void* stream) {
+  if (ws == nullptr) return MOE_ERR_ARG;
+  return cudaMemsetAsync(ws, 0, sizeof(WsHeader), static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_LAUNCH;
+}
+
+const char* moe_strerror(int code) {
+  switch (code) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_ARG: return "invalid argument (null pointer, dimension, k > E or k > 32, R too large)";
+    case MOE_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case MOE_ERR_WS: return "workspace smaller than moe_workspace_bytes()";
+    case MOE_ERR_LAUNCH: return "CUDA launch or API call failed";
+    case MOE_ERR_SHAPE: return "unsupported shape (H, F must be multiples of 128; E <= 1024)";
+    case MOE_ERR_DEVICE: return "current device is not compute capability 10.3 (GB300)";
+    case MOE_ERR_TIMEOUT: return "a bounded wait in a kernel expired";
+    case MOE_ERR_NONFINITE: return "non-finite router logit";
+    case MOE_ERR_BOUNDS: return "index out of bounds detected on the GPU";
+    default: return "unknown error";
+  }
+}
+
+int32_t moe_version(void) { return 1; }
+
+uint64_t moe_launch_count(void) { return g_launches.load(); }
+
+const char* moe_kernel_name(int32_t call, int32_t i) {
+  const char* const* t = call == 0 ? kPlanKernels : call == 1 ? kFwdKernels : call == 2 ? kBwdKernels : nullptr;
+  if (t == nullptr || i < 0) return nullptr;
+  for (int j = 0; j <= i; ++j)
+    if (t[j] == nullptr) return nullptr;
+  return t[i];
+}
+
+}  // extern "C"

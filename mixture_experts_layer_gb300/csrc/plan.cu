@@ -1,0 +1,267 @@
+// Routing: router logits -> top-k experts and gate weights -> the stable
+// token -> grouped-row table.
+//
+// The table follows section 3.1 (Deterministic Token Mapping, Algorithm 1) of
+// "UniEP: Unified Expert-Parallel MoE MegaKernel for LLM Training": every
+// source counts its tokens per expert, an exclusive prefix over the sources
+// gives each source its base inside an expert's segment, and a source places
+// its tokens at base + their stable index among its own tokens.  The sources
+// here are 256-token chunks of one GPU instead of ranks, so no atomics decide
+// any position and the order inside each expert is the original token order.
+//
+//   route_topk  one CTA per chunk: warp-wide top-k per token, renormalised
+//               weights, and a per-chunk bitmap bm[e][w] whose bit b says
+//               "token 32w+b of the chunk chose expert e" (a warp ballot in
+//               shared memory); writes the bitmap and per-chunk counts.
+//   route_scan  one CTA: exclusive prefix of the counts over chunks (per
+//               expert) and over experts, and the 128-row GEMM tile table.
+//   route_rank  one CTA per chunk: stable index = popcount of the bitmap below
+//               the token; dest, row_src, row_slot.
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+
+template <int NV>
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                         int32_t* __restrict__ ids, float* __restrict__ wts,
+                                                         uint32_t* __restrict__ gbm, int32_t* __restrict__ ccount,
+                                                         WsHeader* ws) {
+  extern __shared__ uint32_t bm[];  // [E][kChunkWords]
+  const int chunk = blockIdx.x;
+  for (int i = threadIdx.x; i < E * kChunkWords; i += blockDim.x) bm[i] = 0;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int tl = warp; tl < kChunk; tl += 8) {
+    const int t = chunk * kChunk + tl;
+    if (t >= T) break;
+    float v[NV];
+    uint32_t taken = 0;
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int e = lane + 32 * i;
+      float a = -INFINITY;
+      if (e < E) {
+        a = logits[static_cast<size_t>(t) * E + e];
+        if (!isfinite(a)) {
+          bad = true;
+          a = -INFINITY;
+        }
+      } else {
+        taken |= 1u << i;  // padding lanes are never chosen
+      }
+      v[i] = a;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) report(ws, MOE_ERR_NONFINITE, 0, t);
+    int my_id = 0;
+    float my_v = 0.f;
+    for (int j = 0; j < k; ++j) {
+      // Largest untaken logit, ties to the lower expert id: a total order, so
+      // every lane ends the butterfly with the same winner.
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const int e = lane + 32 * i;
+        if (!((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
+          bv = v[i];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (ov > bv || (ov == bv && oi < bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (lane == j) {
+        my_id = bi;
+        my_v = bv;
+      }
+    }
+    // w_j = exp(l_j - l_max) / sum_{i<k} exp(l_i - l_max); the sum runs in slot order.
+    const float m = __shfl_sync(0xffffffffu, my_v, 0);
+    const float ex = (lane < k) ? expf(my_v - m) : 0.f;
+    float s = 0.f;
+    for (int j = 0; j < k; ++j) s += __shfl_sync(0xffffffffu, ex, j);
+    if (lane < k) {
+      ids[static_cast<size_t>(t) * k + lane] = my_id;
+      wts[static_cast<size_t>(t) * k + lane] = ex / s;
+      atomicOr(&bm[my_id * kChunkWords + (tl >> 5)], 1u << (tl & 31));
+    }
+  }
+  __syncthreads();
+  uint32_t* out = gbm + static_cast<size_t>(chunk) * E * kChunkWords;
+  for (int i = threadIdx.x; i < E * kChunkWords; i += blockDim.x) out[i] = bm[i];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int c = 0;
+#pragma unroll
+    for (int w = 0; w < kChunkWords; ++w) c += __popc(bm[e * kChunkWords + w]);
+    ccount[static_cast<size_t>(chunk) * E + e] = c;
+  }
+}
+
+__global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* __restrict__ ccount, int nchunks, int E,
+                                                          int32_t* __restrict__ cbase, int32_t* __restrict__ counts,
+                                                          int32_t* __restrict__ offsets, int32_t* __restrict__ tiles) {
+  __shared__ int32_t ne[1024];
+  __shared__ int32_t wsum_n[32], wsum_m[32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Per expert: exclusive prefix of the chunk counts (the O_all of Algorithm 1).
+  for (int e = warp; e < E; e += 32) {
+    int run = 0;
+    for (int c0 = 0; c0 < nchunks; c0 += 32) {
+      const int c = c0 + lane;
+      const int v = (c < nchunks) ? ccount[static_cast<size_t>(c) * E + e] : 0;
+      int incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      if (c < nchunks) cbase[static_cast<size_t>(c) * E + e] = run + incl - v;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) ne[e] = run;
+  }
+  __syncthreads();
+  // Exclusive prefix over experts of the row counts and of the 128-row tile counts.
+  const int e = threadIdx.x;
+  const int n = (e < E) ? ne[e] : 0;
+  const int mt = (n + kTileRows - 1) / kTileRows;
+  int in_n = n, in_m = mt;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int yn = __shfl_up_sync(0xffffffffu, in_n, off);
+    const int ym = __shfl_up_sync(0xffffffffu, in_m, off);
+    if (lane >= off) {
+      in_n += yn;
+      in_m += ym;
+    }
+  }
+  if (lane == 31) {
+    wsum_n[warp] = in_n;
+    wsum_m[warp] = in_m;
+  }
+  __syncthreads();
+  int base_n = 0, base_m = 0;
+  for (int w = 0; w < warp; ++w) {
+    base_n += wsum_n[w];
+    base_m += wsum_m[w];
+  }
+  const int ex_n = base_n + in_n - n, ex_m = base_m + in_m - mt;
+  const int entries = tiles_entry_base(E);
+  if (e < E) {
+    counts[e] = n;
+    offsets[e] = ex_n;
+    tiles[1 + e] = ex_m;
+    for (int i = 0; i < mt; ++i) {
+      int4 ent;
+      ent.x = e;
+      ent.y = ex_n + kTileRows * i;
+      ent.z = min(kTileRows, n - kTileRows * i);
+      ent.w = 0;
+      reinterpret_cast<int4*>(tiles + entries)[ex_m + i] = ent;
+    }
+  }
+  if (e == E - 1) {
+    offsets[E] = ex_n + n;
+    tiles[1 + E] = ex_m + mt;
+    tiles[0] = ex_m + mt;
+  }
+}
+
+__global__ void __launch_bounds__(256) route_rank_kernel(const int32_t* __restrict__ ids,
+                                                         const uint32_t* __restrict__ gbm,
+                                                         const int32_t* __restrict__ cbase,
+                                                         const int32_t* __restrict__ offsets, int T, int E, int k,
+                                                         int R, int32_t* __restrict__ dest,
+                                                         int32_t* __restrict__ row_src,
+                                                         uint8_t* __restrict__ row_slot, WsHeader* ws) {
+  extern __shared__ uint32_t sm[];
+  uint32_t* words = sm;                    // [E][kChunkWords]
+  uint32_t* pre = sm + E * kChunkWords;    // exclusive popcount prefix per expert
+  const int chunk = blockIdx.x;
+  const uint32_t* src = gbm + static_cast<size_t>(chunk) * E * kChunkWords;
+  for (int i = threadIdx.x; i < E * kChunkWords; i += blockDim.x) words[i] = src[i];
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    uint32_t run = 0;
+#pragma unroll
+    for (int w = 0; w < kChunkWords; ++w) {
+      pre[e * kChunkWords + w] = run;
+      run += __popc(words[e * kChunkWords + w]);
+    }
+  }
+  __syncthreads();
+  const int t0 = chunk * kChunk;
+  const int n_items = min(kChunk, T - t0) * k;
+  for (int i = threadIdx.x; i < n_items; i += blockDim.x) {
+    const int tl = i / k, j = i - tl * k;
+    const int t = t0 + tl;
+    const size_t tk = static_cast<size_t>(t) * k + j;
+    const int e = ids[tk];
+    if (e < 0 || e >= E) {
+      report(ws, MOE_ERR_BOUNDS, 2, t);
+      continue;
+    }
+    const int w = tl >> 5, b = tl & 31;
+    const int rank = pre[e * kChunkWords + w] + __popc(words[e * kChunkWords + w] & ((1u << b) - 1u));
+    const int r = offsets[e] + cbase[static_cast<size_t>(chunk) * E + e] + rank;
+    if (r < 0 || r >= R) {
+      report(ws, MOE_ERR_BOUNDS, 2, t);
+      continue;
+    }
+    dest[tk] = r;
+    row_src[r] = t;
+    row_slot[r] = static_cast<uint8_t>(j);
+  }
+}
+
+cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t s, LaunchHook& hook) {
+  const int nchunks = (p.T + kChunk - 1) / kChunk;
+  const size_t bm_bytes = static_cast<size_t>(p.E) * kChunkWords * 4;
+  const int nv = (p.E + 31) / 32;
+  hook.before(s);
+  switch (nv <= 1 ? 1 : nv <= 2 ? 2 : nv <= 4 ? 4 : nv <= 8 ? 8 : nv <= 16 ? 16 : 32) {
+#define MOE_TOPK_CASE(NV)                                                                                  \
+  case NV:                                                                                                 \
+    route_topk_kernel<NV><<<nchunks, 256, bm_bytes, s>>>(p.logits, p.T, p.E, p.k, p.ids, p.w, p.gbm,      \
+                                                         p.ccount, p.ws);                                  \
+    break;
+    MOE_TOPK_CASE(1)
+    MOE_TOPK_CASE(2)
+    MOE_TOPK_CASE(4)
+    MOE_TOPK_CASE(8)
+    MOE_TOPK_CASE(16)
+    MOE_TOPK_CASE(32)
+#undef MOE_TOPK_CASE
+  }
+  hook.after(s);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  hook.before(s);
+  route_scan_kernel<<<1, 1024, 0, s>>>(p.ccount, nchunks, p.E, p.cbase, p.counts, p.offsets, p.tiles);
+  hook.after(s);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  if (2 * bm_bytes > 48 * 1024) {
+    err = cudaFuncSetAttribute(route_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(2 * bm_bytes));
+    if (err != cudaSuccess) return err;
+  }
+  hook.before(s);
+  route_rank_kernel<<<nchunks, 256, 2 * bm_bytes, s>>>(p.ids, p.gbm, p.cbase, p.offsets, p.T, p.E, p.k,
+                                                       p.T * p.k, p.dest, p.row_src, p.row_slot, p.ws);
+  hook.after(s);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

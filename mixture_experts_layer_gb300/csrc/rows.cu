@@ -1,0 +1,214 @@
+// Row-wise, HBM-bound steps of the layer: dispatch (row gather), gated
+// combine, combine backward, dispatch backward.  One warp per row or token,
+// 16-byte vector loads and stores, grid-stride over the rows.
+//
+// Sources: "UniEP: Unified Expert-Parallel MoE MegaKernel for LLM Training",
+// section 3.1 (Comm-Worker: one warp per token, 128-bit vector loads) and
+// section 5 (Relay & Reduce Workers: one warp aggregates one token's top-k
+// replicas with vector loads and stores, no shared memory); the reduction
+// waits for all k contributions and sums them in a fixed order (section 3,
+// Top-k accumulation constraint).  "MoonEP: Balanced Expert Parallelism for
+// MoE Training via Dynamic Redundant Experts": zero-copy dispatch, and the
+// gradient of dispatch is a combine of each token's k row gradients.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kMaxK = 32;
+
+__device__ __forceinline__ uint4 ldg_nc(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+  f[0] = bf16lo(v.x); f[1] = bf16hi(v.x);
+  f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
+  f[4] = bf16lo(v.z); f[5] = bf16hi(v.z);
+  f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  uint4 v;
+  v.x = pack_bf16x2(f[0], f[1]);
+  v.y = pack_bf16x2(f[2], f[3]);
+  v.z = pack_bf16x2(f[4], f[5]);
+  v.w = pack_bf16x2(f[6], f[7]);
+  return v;
+}
+
+__global__ void __launch_bounds__(kThreads) gather_rows_kernel(const uint4* __restrict__ x,
+                                                                 const int32_t* __restrict__ row_src,
+                                                                 uint4* __restrict__ Xp, int R, int T, int hv,
+                                                                 WsHeader* ws) {
+  const int lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * (kThreads / 32);
+  for (int r = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); r < R; r += nwarps) {
+    const int t = row_src[r];
+    if (t < 0 || t >= T) {
+      if (lane == 0) report(ws, MOE_ERR_BOUNDS, 10, r);
+      continue;
+    }
+    const uint4* src = x + static_cast<size_t>(t) * hv;
+    uint4* dst = Xp + static_cast<size_t>(r) * hv;
+    int v = lane;
+    for (; v + 96 < hv; v += 128) {
+      const uint4 a = ldg_nc(src + v), b = ldg_nc(src + v + 32), c = ldg_nc(src + v + 64),
+                  d = ldg_nc(src + v + 96);
+      dst[v] = a;
+      dst[v + 32] = b;
+      dst[v + 64] = c;
+      dst[v + 96] = d;
+    }
+    for (; v < hv; v += 32) dst[v] = ldg_nc(src + v);
+  }
+}
+
+// Loads the k (row, weight) pairs of token t into lanes 0..k-1; returns false
+// (and reports) if a row index is out of range.
+__device__ __forceinline__ bool token_rows(const int32_t* dest, const float* w, int t, int k, int R, int lane,
+                                           int& my_r, float& my_w, WsHeader* ws, int where) {
+  my_r = 0;
+  my_w = 0.f;
+  if (lane < k) {
+    my_r = dest[static_cast<size_t>(t) * k + lane];
+    if (w != nullptr) my_w = w[static_cast<size_t>(t) * k + lane];
+  }
+  const bool bad = lane < k && (my_r < 0 || my_r >= R);
+  if (__any_sync(0xffffffffu, bad)) {
+    if (lane == 0) report(ws, MOE_ERR_BOUNDS, where, t);
+    return false;
+  }
+  return true;
+}
+
+__global__ void __launch_bounds__(kThreads) combine_kernel(const uint4* __restrict__ Y,
+                                                             const int32_t* __restrict__ dest,
+                                                             const float* __restrict__ w, uint4* __restrict__ out,
+                                                             int T, int k, int R, int hv, WsHeader* ws) {
+  const int lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * (kThreads / 32);
+  for (int t = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); t < T; t += nwarps) {
+    int my_r;
+    float my_w;
+    if (!token_rows(dest, w, t, k, R, lane, my_r, my_w, ws, 11)) continue;
+    for (int v = lane; v < hv; v += 32) {
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int j = 0; j < k; ++j) {
+        const int r = __shfl_sync(0xffffffffu, my_r, j);
+        const float wj = __shfl_sync(0xffffffffu, my_w, j);
+        float y[8];
+        unpack8(ldg_nc(Y + static_cast<size_t>(r) * hv + v), y);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, y[i], acc[i]);
+      }
+      out[static_cast<size_t>(t) * hv + v] = pack8(acc);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) combine_bwd_kernel(const uint4* __restrict__ dout,
+                                                                 const uint4* __restrict__ Y,
+                                                                 const int32_t* __restrict__ dest,
+                                                                 const float* __restrict__ w,
+                                                                 uint4* __restrict__ dY, float* __restrict__ dgate,
+                                                                 int T, int k, int R, int hv, WsHeader* ws) {
+  const int lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * (kThreads / 32);
+  for (int t = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); t < T; t += nwarps) {
+    int my_r;
+    float my_w;
+    if (!token_rows(dest, w, t, k, R, lane, my_r, my_w, ws, 12)) continue;
+    // Lane-partial dot products, one per slot; the dot of slot j is
+    // accumulated by lane j's register after the loop.
+    float my_dot = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int r = __shfl_sync(0xffffffffu, my_r, j);
+      const float wj = __shfl_sync(0xffffffffu, my_w, j);
+      float part = 0.f;
+      for (int v = lane; v < hv; v += 32) {
+        float d[8], y[8], g[8];
+        unpack8(ldg_nc(dout + static_cast<size_t>(t) * hv + v), d);
+        unpack8(ldg_nc(Y + static_cast<size_t>(r) * hv + v), y);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          part = fmaf(d[i], y[i], part);
+          g[i] = wj * d[i];
+        }
+        dY[static_cast<size_t>(r) * hv + v] = pack8(g);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+      if (lane == j) my_dot = part;
+    }
+    if (lane < k) dgate[static_cast<size_t>(t) * k + lane] = my_dot;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) unpermute_kernel(const uint4* __restrict__ dXp,
+                                                               const int32_t* __restrict__ dest,
+                                                               uint4* __restrict__ dx, int T, int k, int R, int hv,
+                                                               WsHeader* ws) {
+  const int lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * (kThreads / 32);
+  for (int t = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); t < T; t += nwarps) {
+    int my_r;
+    float my_w;
+    if (!token_rows(dest, nullptr, t, k, R, lane, my_r, my_w, ws, 13)) continue;
+    for (int v = lane; v < hv; v += 32) {
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int j = 0; j < k; ++j) {
+        const int r = __shfl_sync(0xffffffffu, my_r, j);
+        float y[8];
+        unpack8(ldg_nc(dXp + static_cast<size_t>(r) * hv + v), y);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] += y[i];
+      }
+      dx[static_cast<size_t>(t) * hv + v] = pack8(acc);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gather(const RowsLaunch& p, const void* x, void* Xp, cudaStream_t s, LaunchHook& hook) {
+  hook.before(s);
+  gather_rows_kernel<<<p.grid, kThreads, 0, s>>>(static_cast<const uint4*>(x), p.row_src, static_cast<uint4*>(Xp),
+                                                  p.R, p.T, p.H / 8, p.ws);
+  hook.after(s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const RowsLaunch& p, const void* Y, void* out, cudaStream_t s, LaunchHook& hook) {
+  hook.before(s);
+  combine_kernel<<<p.grid, kThreads, 0, s>>>(static_cast<const uint4*>(Y), p.dest, p.w, static_cast<uint4*>(out),
+                                              p.T, p.k, p.R, p.H / 8, p.ws);
+  hook.after(s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_bwd(const RowsLaunch& p, const void* dout, const void* Y, void* dY, float* dgate,
+                               cudaStream_t s, LaunchHook& hook) {
+  hook.before(s);
+  combine_bwd_kernel<<<p.grid, kThreads, 0, s>>>(static_cast<const uint4*>(dout), static_cast<const uint4*>(Y),
+                                                  p.dest, p.w, static_cast<uint4*>(dY), dgate, p.T, p.k, p.R,
+                                                  p.H / 8, p.ws);
+  hook.after(s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unpermute(const RowsLaunch& p, const void* dXp, void* dx, cudaStream_t s, LaunchHook& hook) {
+  hook.before(s);
+  unpermute_kernel<<<p.grid, kThreads, 0, s>>>(static_cast<const uint4*>(dXp), p.dest, static_cast<uint4*>(dx),
+                                                p.T, p.k, p.R, p.H / 8, p.ws);
+  hook.after(s);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

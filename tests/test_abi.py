@@ -1,0 +1,56 @@
+"""The C ABI library builds, loads without a GPU, exports every entry point
+include/moe.h declares, and rejects bad arguments on the host (no GPU call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mixture_experts_layer_gb300 as M
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "moe.h")
+
+
+def declared():
+    src = open(HEADER).read()
+    return re.findall(r"^MOE_API\s+[\w\s\*]+?\**\s*(moe_\w+)\s*\(", src, flags=re.M)
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared()
+    assert len(names) >= 11
+    L = M.lib()
+    for n in names:
+        assert hasattr(L, n), n
+        assert hasattr(M, n), f"binding lacks {n}"
+    assert M.moe_version() >= 1
+    assert M.moe_kernel_name(1, 1) == "gemm_fwd1_swiglu"
+    assert M.moe_kernel_name(2, 6) is None
+
+
+def test_workspace_sizes():
+    for T, H, F, E, k in [(256, 128, 256, 8, 2), (4096, 2048, 1408, 64, 6), (131072, 4096, 1536, 128, 8)]:
+        d = M.moe_dims(T, H, F, E, k)
+        assert M.moe_workspace_bytes(d) > 0
+        assert M.moe_plan_tiles_elems(d) >= (T * k) // 128 * 4
+    assert M.moe_workspace_bytes(M.moe_dims(16, 128, 128, 4, 5)) == 0   # k > E
+    assert M.moe_workspace_bytes(M.moe_dims(16, 100, 128, 4, 2)) == 0   # H % 128
+    assert M.moe_workspace_bytes(M.moe_dims(16, 128, 128, 2048, 2)) == 0  # E too large
+    assert M.moe_workspace_bytes(M.moe_dims(16, 128, 128, 64, 33)) == 0   # k > 32
+
+
+def test_host_side_rejections():
+    d = M.moe_dims(16, 128, 128, 4, 2)
+    plan = M.moe_plan_t()
+    ws = ctypes.create_string_buffer(M.moe_workspace_bytes(d) + 64)
+    base = ctypes.addressof(ws)
+    aligned = (base + 15) & ~15
+    n = M.moe_workspace_bytes(d)
+    assert M.moe_plan(d, aligned, plan, 0, n) == M.MOE_ERR_ARG            # no workspace
+    assert M.moe_plan(d, aligned, plan, aligned + 4, n) == M.MOE_ERR_ALIGN  # misaligned workspace
+    assert M.moe_plan(d, aligned, plan, aligned, n - 1) == M.MOE_ERR_WS     # too small
+    assert M.moe_plan(d, aligned, plan, aligned, n) == M.MOE_ERR_ARG        # plan fields are null
+    bad = M.moe_dims(16, 128, 128, 4, 0)
+    assert M.moe_plan(bad, aligned, plan, aligned, n) == M.MOE_ERR_ARG
+    assert M.moe_plan(M.moe_dims(16, 96, 128, 4, 2), aligned, plan, aligned, n) == M.MOE_ERR_SHAPE
+    assert "aligned" in M.moe_strerror(M.MOE_ERR_ALIGN)
