@@ -1,0 +1,457 @@
+#!/usr/bin/env python
+"""Throughput of one forward+backward step of the MoE expert layer on GB300.
+
+A step is the whole hot path over one batch of synthetic tokens: routing
+(top-k, counts, offsets, stable row table), dispatch, GroupGEMM -> SwiGLU ->
+GroupGEMM, gated combine, combine backward, both dgrad GroupGEMMs, the
+weight-gradient Transposed GroupGEMMs and the dispatch backward.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  `value` is tokens/s over all ranks with the
+inputs resident in HBM; `e2e` is the same metric through the C ABI with the
+step's inputs copied from pinned host memory and its outputs copied back inside
+the timed region.  Under torchrun every rank runs an independent replica of the
+layer on its own tokens (weak scaling, no collective on the data path).
+
+`--impl reference` times the CPU oracle instead (rank 0 only), on a bounded
+sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s fwd+bwd; GEMM % BF16 peak; permute GB/s % HBM"
+UNIT = "tokens/s"
+
+FWD_KERNELS = ["gather_rows", "gemm_fwd1_swiglu", "gemm_fwd2", "combine"]
+BWD_KERNELS = ["combine_bwd", "gemm_dgrad2_swiglu_bwd", "gemm_dgrad1", "gemm_wgrad13", "gemm_wgrad2", "unpermute"]
+N_PLAN_KERNELS = 3
+
+
+def work_per_kernel(T, H, F, E, k):
+    """Algorithmic FLOPs and HBM bytes of one launch of each kernel (padding and re-reads not counted)."""
+    R = T * k
+    b = {
+        "plan": 4 * T * E + 12 * T * k + 4 * R,
+        "gather_rows": 2 * T * H + 2 * R * H + 4 * R,
+        "gemm_fwd1_swiglu": 2 * R * H + 4 * E * H * F + 6 * R * F,
+        "gemm_fwd2": 2 * R * F + 2 * E * F * H + 2 * R * H,
+        "combine": 2 * R * H + 2 * T * H + 8 * R,
+        "combine_bwd": 2 * T * H + 4 * R * H + 12 * R,
+        "gemm_dgrad2_swiglu_bwd": 2 * R * H + 2 * E * F * H + 8 * R * F,
+        "gemm_dgrad1": 4 * R * F + 4 * E * H * F + 2 * R * H,
+        "gemm_wgrad13": 2 * R * H + 4 * R * F + 8 * E * H * F,
+        "gemm_wgrad2": 2 * R * F + 2 * R * H + 4 * E * H * F,
+        "unpermute": 2 * R * H + 2 * T * H + 4 * R,
+    }
+    f = {
+        "gemm_fwd1_swiglu": 4 * R * H * F,
+        "gemm_fwd2": 2 * R * H * F,
+        "gemm_dgrad2_swiglu_bwd": 2 * R * H * F,
+        "gemm_dgrad1": 4 * R * H * F,
+        "gemm_wgrad13": 4 * R * H * F,
+        "gemm_wgrad2": 2 * R * H * F,
+    }
+    return f, b
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def profiled_traffic(kernel: str):
+    """DRAM bytes per launch of a kernel from the committed ncu summary, or None.
+
+    profiles/traffic.txt holds lines `kernel source_sha dram_bytes_per_launch workload`;
+    a line counts only while the kernel's source file is unchanged.
+    """
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = os.path.join(ROOT, "mixture_experts_layer_gb300", "csrc",
+                       "gemm.cu" if kernel.startswith("gemm") else "rows.cu" if kernel != "plan" else "plan.cu")
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel and parts[1] == sha:
+            return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle leg
+# ---------------------------------------------------------------------------
+def oracle_sample_inputs(shape, seed, T_s):
+    """First T_s tokens of the workload (same bits as the GPU's), weights as float64 arrays."""
+    import numpy as np
+    import torch
+
+    import moe_synth as S
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    full = S.layer_inputs(shape, seed, device=dev)
+    f64 = lambda t: t.detach().to("cpu", torch.float64).numpy()
+    d = {"x": f64(full["x"][:T_s]), "dout": f64(full["dout"][:T_s]),
+         "logits": full["logits"][:T_s].cpu().numpy(),
+         "W": (f64(full["W1"]), f64(full["W3"]), f64(full["W2"]))}
+    del full
+    if dev == "cuda":
+        torch.cuda.empty_cache()
+    return d
+
+
+def time_oracle_step(inp, shape):
+    import oracle.moe_oracle as O
+    t0 = time.perf_counter()
+    O.layer_step(inp["x"], inp["logits"], inp["dout"], inp["W"], shape.k, shape.E, mirror=True)
+    return time.perf_counter() - t0
+
+
+def oracle_threads():
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(v):
+            try:
+                return int(os.environ[v])
+            except ValueError:
+                pass
+    return os.cpu_count() or 1
+
+
+def run_reference(args):
+    import moe_synth as S
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    shape = S.CONFIGS[args.config]
+    seed = S.config_seed(args.config)
+    steps, warm = args.steps, args.warmup
+    # Size the sample so the whole run stays within a few minutes.
+    budget = min(8.0, 150.0 / max(1, steps + warm))
+    probe_T = 64
+    inp = oracle_sample_inputs(shape, seed, shape.T)
+    sub = lambda n: dict(inp, x=inp["x"][:n], dout=inp["dout"][:n], logits=inp["logits"][:n])
+    t_probe = time_oracle_step(sub(probe_T), shape)
+    T_s = int(max(16, min(shape.T, probe_T * budget / max(t_probe, 1e-6))))
+    sample = sub(T_s)
+    for _ in range(warm):
+        time_oracle_step(sample, shape)
+    t = 0.0
+    for _ in range(steps):
+        t += time_oracle_step(sample, shape)
+    value = T_s * steps / t
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": warm, "ms_per_step": 1000.0 * t / steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(shape, args.config),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
+                         "sample": f"first {T_s} of {shape.T} tokens per step (plan + forward + backward incl. "
+                                   f"weight gradients over those tokens' rows), numpy float64 oracle"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(shape, idx):
+    return {"workload": f"{shape.name} MoE expert layer fwd+bwd, T={shape.T} H={shape.H} F={shape.F} "
+                        f"E={shape.E} k={shape.k}, bf16 in / fp32 accumulate, all experts on one GPU",
+            "config_index": idx, "T": shape.T, "H": shape.H, "F": shape.F, "E": shape.E, "k": shape.k,
+            "l2": "inputs larger than L2 (expert weights alone exceed the 129 MB L2)"}
+
+
+# ---------------------------------------------------------------------------
+# GPU leg
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+
+    import moe_synth as S
+    import mixture_experts_layer_gb300 as M
+    from mixture_experts_layer_gb300.layer import MoELayer
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    shape = S.CONFIGS[args.config]
+    T, H, F, E, k = shape.T, shape.H, shape.F, shape.E, shape.k
+    seed = S.config_seed(args.config) + 1000 * rank  # each replica its own tokens
+    M.lib()
+    inp = S.layer_inputs(shape, seed, device=dev)
+    layer = MoELayer(T, H, F, E, k, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    nf, nb = len(FWD_KERNELS), len(BWD_KERNELS)
+
+    def step(opts_f=None, opts_b=None):
+        layer.plan(inp["logits"])
+        layer.forward(inp["x"], inp["W1"], inp["W3"], inp["W2"], opts=opts_f)
+        layer.backward(inp["dout"], inp["W1"], inp["W3"], inp["W2"], opts=opts_b)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = layer.status()
+    if st[0] != 0:
+        raise RuntimeError(f"device status {st}")
+
+    # Per-kernel events of every timed step (recorded on the launching stream).
+    evs_f = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nf)] for _ in range(args.steps)]
+    evs_b = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nb)] for _ in range(args.steps)]
+    opts_f = []
+    keep = []
+    for e in evs_f:
+        o = layer.opts(events=e)
+        keep.append(layer._ev_keep)
+        opts_f.append(o)
+    opts_b = []
+    for e in evs_b:
+        o = layer.opts(events=e)
+        keep.append(layer._ev_keep)
+        opts_b.append(o)
+
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    l0 = M.moe_launch_count()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(opts_f[i], opts_b[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    launches = M.moe_launch_count() - l0
+    barrier(world)
+    clk = clocks.stop()
+    ms_local = t_start.elapsed_time(t_end)
+    ms_total = max_over_ranks(ms_local, world)
+    st = layer.status()
+    if st[0] != 0:
+        raise RuntimeError(f"device status {st}")
+
+    # Per-kernel average durations.
+    names = FWD_KERNELS + BWD_KERNELS
+    per = {n: 0.0 for n in names}
+    for i in range(args.steps):
+        for j, n in enumerate(FWD_KERNELS):
+            per[n] += evs_f[i][2 * j].elapsed_time(evs_f[i][2 * j + 1])
+        for j, n in enumerate(BWD_KERNELS):
+            per[n] += evs_b[i][2 * j].elapsed_time(evs_b[i][2 * j + 1])
+    per = {n: v / args.steps for n, v in per.items()}
+    flops, bytes_ = work_per_kernel(T, H, F, E, k)
+    peaks = load_peaks()
+    long_region = ms_total > 1000.0
+    tc_peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
+    kern = {}
+    for n, ms in per.items():
+        ent = {"ms": round(ms, 4), "gbs": round(bytes_[n] / (ms * 1e-3) / 1e9, 1),
+               "hbm_frac": round(bytes_[n] / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)}
+        if n in flops:
+            tf = flops[n] / (ms * 1e-3) / 1e12
+            ent["tflops"] = round(tf, 1)
+            ent["tensor_frac"] = round(tf / tc_peak, 3)
+        kern[n] = ent
+    dom = max(per, key=per.get)
+    if dom in flops:
+        ach = flops[dom] / (per[dom] * 1e-3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 1), "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": round(ach / tc_peak, 4), "traffic": profiled_traffic(dom),
+                "peak_kind": ("sustained" if long_region else "burst") + f" bf16, {peaks['source']}"}
+    else:
+        ach = bytes_[dom] / (per[dom] * 1e-3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": profiled_traffic(dom),
+                "peak_kind": f"copy bandwidth, {peaks['source']}"}
+
+    # End-to-end through the C ABI: inputs from pinned host memory, outputs back to it.
+    h_x = inp["x"].cpu().pin_memory()
+    h_lg = inp["logits"].cpu().pin_memory()
+    h_do = inp["dout"].cpu().pin_memory()
+    h_out = torch.empty_like(h_x).pin_memory()
+    h_dx = torch.empty_like(h_x).pin_memory()
+    d_x, d_lg, d_do = torch.empty_like(inp["x"]), torch.empty_like(inp["logits"]), torch.empty_like(inp["dout"])
+
+    def e2e_step():
+        d_x.copy_(h_x, non_blocking=True)
+        d_lg.copy_(h_lg, non_blocking=True)
+        d_do.copy_(h_do, non_blocking=True)
+        layer.plan(d_lg)
+        layer.forward(d_x, inp["W1"], inp["W3"], inp["W2"])
+        layer.backward(d_do, inp["W1"], inp["W3"], inp["W2"])
+        h_out.copy_(layer.out, non_blocking=True)
+        h_dx.copy_(layer.dx, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    h2d = h_x.numel() * 2 + h_lg.numel() * 4 + h_do.numel() * 2
+    d2h = h_out.numel() * 2 + h_dx.numel() * 2
+
+    ms_step = ms_total / args.steps
+    value = world * T * args.steps / (ms_total * 1e-3)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(workload_config(shape, args.config), parallelism=f"replicas x{world}" if world > 1 else "1 GPU"),
+        "roofline": roof,
+        "e2e": {"value": round(world * T * args.steps / (e2e_ms * 1e-3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "kernels": kern,
+        "step_gemm_tflops": round(sum(flops.values()) / (ms_step * 1e-3) / 1e12, 1),
+    }
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(shape, args.config)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(shape, idx):
+    """The oracle, as it stands, on a bounded sample of the same workload (~10-30 s)."""
+    import moe_synth as S
+    inp = oracle_sample_inputs(shape, S.config_seed(idx), shape.T)
+    sub = lambda n: dict(inp, x=inp["x"][:n], dout=inp["dout"][:n], logits=inp["logits"][:n])
+    t64 = time_oracle_step(sub(64), shape)
+    T_s = int(max(64, min(shape.T, 64 * 12.0 / max(t64, 1e-6))))
+    t = time_oracle_step(sub(T_s), shape)
+    return {"value": round(T_s / t, 2), "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
+            "sample": f"first {T_s} of {shape.T} tokens (plan + forward + backward incl. weight gradients over "
+                      f"those tokens' rows), numpy float64 oracle, {t:.1f} s"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
