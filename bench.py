@@ -297,6 +297,9 @@ def run_ours(args):
     # Per-kernel events of every timed step (recorded on the launching stream).
     evs_f = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nf)] for _ in range(args.steps)]
     evs_b = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nb)] for _ in range(args.steps)]
+    for e in [e for row in evs_f + evs_b for e in row]:
+        e.record(stream)  # torch creates the CUDA event on first record
+    torch.cuda.synchronize()
     opts_f = []
     keep = []
     for e in evs_f:

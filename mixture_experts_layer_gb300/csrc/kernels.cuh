@@ -25,11 +25,16 @@ struct LaunchHook {
   void** events = nullptr;
   int n_events = 0;
   int idx = 0;
+  // Timing is optional: a null or unusable event is skipped, and a failed
+  // record is cleared so it cannot be mistaken for a failed kernel launch.
+  static void record(void* ev, cudaStream_t s) {
+    if (ev != nullptr && cudaEventRecord(static_cast<cudaEvent_t>(ev), s) != cudaSuccess) (void)cudaGetLastError();
+  }
   void before(cudaStream_t s) {
-    if (events && idx < n_events) cudaEventRecord(static_cast<cudaEvent_t>(events[2 * idx]), s);
+    if (events && idx < n_events) record(events[2 * idx], s);
   }
   void after(cudaStream_t s) {
-    if (events && idx < n_events) cudaEventRecord(static_cast<cudaEvent_t>(events[2 * idx + 1]), s);
+    if (events && idx < n_events) record(events[2 * idx + 1], s);
     ++idx;
     g_launches.fetch_add(1, std::memory_order_relaxed);
   }
