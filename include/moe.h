@@ -158,6 +158,39 @@ MOE_API int moe_get_status(void *ws, void *stream, int32_t *device_status, int32
 /* Clears the status word (asynchronous on stream). */
 MOE_API int moe_clear_status(void *ws, void *stream);
 
+/* ---- routing without a workspace ------------------------------------------------ */
+
+/* Size of the fixed device buffer moe_plan_noalloc uses instead of a workspace. */
+#define MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
+#define MOE_ERR_TOO_LARGE (-7) /* moe_plan_noalloc: the dims need more scratch than MOE_NOALLOC_SCRATCH_BYTES */
+
+/* Same routing as moe_plan (same kernels, same results), for callers that
+ * cannot allocate device memory while they run: code that must not call
+ * cudaMalloc because it runs inside an engine or plugin whose memory plan is
+ * fixed before execution, on a real-time path where an allocation could block,
+ * or in a process without a device allocator of its own.  There is no
+ * counterpart on the pages; it is an interface convenience.
+ *
+ * Its scratch (per-chunk counts, bases and bitmaps) lives in one file-scope
+ * device array of MOE_NOALLOC_SCRATCH_BYTES inside the library, which every GPU
+ * that loads the library holds until the process exits.  The call allocates
+ * and frees nothing.
+ *   - Limit: dims whose scratch exceeds the buffer (roughly
+ *     ceil(T/256) * E * 40 bytes plus alignment) return MOE_ERR_TOO_LARGE
+ *     before anything is launched; e.g. T = 131072 with E = 128 fits.
+ *   - status: device pointer to 4 int32 (caller-owned, zero before first use);
+ *     the first device-detected error is recorded there as in a workspace and
+ *     is read and cleared by moe_get_status(status, ...).
+ *   - Set-up: the first call on each device looks up the array's device
+ *     address (with that device current) and caches it; make that first call
+ *     before any stream capture.
+ *   - Every call uses the same array and leaves its contents behind; the
+ *     kernels overwrite every scratch word before reading it, so nothing has to
+ *     start at zero.  Calls that overlap on the GPU (on different streams, or
+ *     from different threads) race on the array: serialise them.
+ * Other arguments and errors as moe_plan. */
+MOE_API int moe_plan_noalloc(moe_dims d, const float *logits, const moe_plan_t *plan, int32_t *status, void *stream);
+
 /* ---- introspection ---------------------------------------------------------- */
 MOE_API const char *moe_strerror(int code);
 MOE_API int32_t moe_version(void);

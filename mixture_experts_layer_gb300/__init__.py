@@ -17,7 +17,7 @@ __all__ = [
     "moe_dims", "moe_plan_t", "moe_saved_t", "moe_grads_t", "moe_opts", "MoeError",
     "moe_workspace_bytes", "moe_plan_tiles_elems", "moe_plan", "moe_forward", "moe_backward",
     "moe_get_status", "moe_clear_status", "moe_strerror", "moe_version", "moe_launch_count",
-    "moe_kernel_name", "check", "lib", "lib_path",
+    "moe_kernel_name", "moe_plan_noalloc", "check", "lib", "lib_path",
 ]
 
 MOE_OK = 0
@@ -27,6 +27,8 @@ MOE_ERR_WS = -3
 MOE_ERR_LAUNCH = -4
 MOE_ERR_SHAPE = -5
 MOE_ERR_DEVICE = -6
+MOE_ERR_TOO_LARGE = -7
+MOE_NOALLOC_SCRATCH_BYTES = 4 << 20
 MOE_ERR_TIMEOUT = 1
 MOE_ERR_NONFINITE = 2
 MOE_ERR_BOUNDS = 3
@@ -95,6 +97,7 @@ def lib() -> ctypes.CDLL:
                 "moe_version": (c_int32, []),
                 "moe_launch_count": (c_uint64, []),
                 "moe_kernel_name": (c_char_p, [c_int32, c_int32]),
+                "moe_plan_noalloc": (c_int, [moe_dims, vp, POINTER(moe_plan_t), vp, vp]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -163,3 +166,7 @@ def moe_launch_count() -> int:
 def moe_kernel_name(call: int, i: int):
     v = lib().moe_kernel_name(call, i)
     return None if v is None else v.decode()
+
+
+def moe_plan_noalloc(d, logits, plan, status, stream=0) -> int:
+    return lib().moe_plan_noalloc(d, _p(logits), byref(plan), _p(status), _p(stream))

@@ -319,6 +319,7 @@ const char* moe_strerror(int code) {
     case MOE_ERR_TIMEOUT: return "a bounded wait in a kernel expired";
     case MOE_ERR_NONFINITE: return "non-finite router logit";
     case MOE_ERR_BOUNDS: return "index out of bounds detected on the GPU";
+    case MOE_ERR_TOO_LARGE: return "dims need more scratch than moe_plan_noalloc's fixed buffer (MOE_NOALLOC_SCRATCH_BYTES)";
     default: return "unknown error";
   }
 }

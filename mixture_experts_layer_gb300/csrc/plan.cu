@@ -265,3 +265,98 @@ cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t s, LaunchHook& hook) {
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// Routing without a caller-provided workspace (moe_plan_noalloc).
+//
+// For callers that may not allocate device memory while they run, the scratch
+// of the three routing kernels (per-chunk counts, bases and bitmaps) lives in
+// the file-scope array below.  Host code must not use the array's name as a
+// device address: it only names a host-side stand-in.  The device address is
+// looked up once per device with cudaGetSymbolAddress (with that device
+// current) and passed to the kernels like any workspace pointer.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace moe {
+namespace {
+
+constexpr size_t kNoAllocBytes = MOE_NOALLOC_SCRATCH_BYTES;
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+size_t na_align(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Device address of g_noalloc_scratch on the current device (looked up once).
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return MOE_ERR_LAUNCH;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return MOE_ERR_LAUNCH;
+    if (major != 10 || minor != 3) return MOE_ERR_DEVICE;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_LAUNCH;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return MOE_OK;
+}
+
+bool na_ok_ptr(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace moe
+
+extern "C" int moe_plan_noalloc(moe_dims d, const float* logits, const moe_plan_t* plan, int32_t* status,
+                                void* stream) {
+  using namespace moe;
+  if (d.T < 0 || d.H <= 0 || d.F <= 0 || d.E <= 0 || d.k <= 0 || d.k > d.E || d.k > 32 ||
+      static_cast<long long>(d.T) * d.k >= (1ll << 31))
+    return MOE_ERR_ARG;
+  if (d.H % 128 != 0 || d.F % 128 != 0 || d.E > 1024) return MOE_ERR_SHAPE;
+  const size_t nchunks = (static_cast<size_t>(d.T) + kChunk - 1) / kChunk;
+  const size_t ccount = 0;
+  const size_t cbase = na_align(ccount + nchunks * d.E * 4);
+  const size_t gbm = na_align(cbase + nchunks * d.E * 4);
+  const size_t total = na_align(gbm + nchunks * d.E * kChunkWords * 4);
+  if (total > kNoAllocBytes) return MOE_ERR_TOO_LARGE;
+  if (d.T == 0) return MOE_OK;
+  if (plan == nullptr || plan->row_slot == nullptr) return MOE_ERR_ARG;
+  const void* ptrs[] = {logits, status, plan->topk_ids, plan->topk_w, plan->counts, plan->offsets, plan->dest,
+                        plan->row_src, plan->tiles};
+  for (const void* q : ptrs) {
+    if (q == nullptr) return MOE_ERR_ARG;
+    if (!na_ok_ptr(q)) return MOE_ERR_ALIGN;
+  }
+  void* scratch = nullptr;
+  const int rc = noalloc_scratch(&scratch);
+  if (rc != MOE_OK) return rc;
+  uint8_t* w = static_cast<uint8_t*>(scratch);
+  PlanLaunch p;
+  p.logits = logits;
+  p.T = d.T;
+  p.E = d.E;
+  p.k = d.k;
+  p.ids = plan->topk_ids;
+  p.w = plan->topk_w;
+  p.ccount = reinterpret_cast<int32_t*>(w + ccount);
+  p.cbase = reinterpret_cast<int32_t*>(w + cbase);
+  p.gbm = reinterpret_cast<uint32_t*>(w + gbm);
+  p.counts = plan->counts;
+  p.offsets = plan->offsets;
+  p.tiles = plan->tiles;
+  p.dest = plan->dest;
+  p.row_src = plan->row_src;
+  p.row_slot = plan->row_slot;
+  p.ws = reinterpret_cast<WsHeader*>(status);  // only status/where/detail are written
+  LaunchHook hook;
+  return launch_plan(p, static_cast<cudaStream_t>(stream), hook) == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
+}
