@@ -17,16 +17,22 @@
 //   warp 0     TMA producer: fills a ring of shared-memory stages
 //   warp 1     allocates tensor memory, issues tcgen05.mma (one elected lane)
 //   warps 2-5  epilogue: tcgen05.ld of the fp32 accumulator, fused
-//              elementwise work (SwiGLU forward or backward), global stores.
+//              elementwise work (SwiGLU forward or backward), stores.  The fp32
+//              weight gradients go out through swizzled shared-memory staging
+//              and TMA bulk stores, one 32x32 box per warp, double-buffered.
 // The accumulator is double-buffered in tensor memory (2 x 256 columns), so the
 // epilogue of one tile overlaps the main loop of the next.
 //
-// Operand layouts in shared memory are the 128-byte-swizzled canonical forms:
+// Tiles are 128 rows x 256 columns (the last tile of an N extent that is an odd
+// multiple of 128 is 128 wide).  Operand layouts in shared memory are the
+// 128-byte-swizzled canonical forms:
 //   K-major  (rows of 64 K-elements, 128 B each, 8-row atoms of 1 KB):
 //            SBO = 1024 B between 8-row groups; +32 B per K step of 16.
 //   MN-major (panels of 64 MN-elements x 64 K-rows, 8 KB each):
 //            LBO = 8192 B between panels, SBO = 1024 B between 8-row K groups;
 //            +2048 B per K step of 16.
+#include <string.h>
+
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -35,51 +41,40 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
+constexpr int BN = 256;
 constexpr int kThreads = 192;
-constexpr int kEpiWarp0 = 2;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccStride = 256;  // TMEM columns per accumulator buffer
+constexpr uint32_t kAccStride = 256;   // TMEM columns per accumulator buffer
 constexpr int kPanelBytes = 64 * 128;  // one MN-major panel: 64 K-rows x 128 B
+constexpr int kABytes = BM * BK * 2;
+constexpr int kBBytesMax = BN * BK * 2;
+constexpr int kStageBytes = kABytes + kBBytesMax;
+constexpr int kStageOutBytes = 32 * 128;  // one warp's 32x32 fp32 staging box
 
 template <int MODE>
-struct ModeTraits;
-template <>
-struct ModeTraits<kFwd1> {
-  static constexpr bool a_mn = false, b_mn = true, wgrad = false;
-};
-template <>
-struct ModeTraits<kFwd2> {
-  static constexpr bool a_mn = false, b_mn = true, wgrad = false;
-};
-template <>
-struct ModeTraits<kDgrad2> {
-  static constexpr bool a_mn = false, b_mn = false, wgrad = false;
-};
-template <>
-struct ModeTraits<kDgrad1> {
-  static constexpr bool a_mn = false, b_mn = false, wgrad = false;
-};
-template <>
-struct ModeTraits<kWgrad13> {
-  static constexpr bool a_mn = true, b_mn = true, wgrad = true;
-};
-template <>
-struct ModeTraits<kWgrad2> {
-  static constexpr bool a_mn = true, b_mn = true, wgrad = true;
+struct ModeTraits {
+  static constexpr bool wgrad = (MODE == kWgrad13 || MODE == kWgrad2);
+  static constexpr bool a_mn = wgrad;
+  static constexpr bool b_mn = (MODE == kFwd1 || MODE == kFwd2 || wgrad);
+  // Output columns per tile are 2 x 128 (two weights side by side) or up to 256.
+  static constexpr bool paired = (MODE == kFwd1 || MODE == kWgrad13);
+  static constexpr int kStages = wgrad ? 3 : 4;
+  static constexpr int kStagingBytes = wgrad ? 4 * 2 * kStageOutBytes : 0;
+  static constexpr int kSmemBytes = kStages * kStageBytes + kStagingBytes + 1024 /*align*/ + 256 /*barriers*/;
 };
 
-template <int BN>
-struct Cfg {
-  static constexpr int kABytes = BM * BK * 2;
-  static constexpr int kBBytes = BN * BK * 2;
-  static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = (BN == 256) ? 4 : 6;
-  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+struct Maps {
+  CUtensorMap a;   // A operand
+  CUtensorMap b0;  // B operand (full-width box)
+  CUtensorMap b1;  // second B tensor (W3), full-width box
+  CUtensorMap b2;  // B, 128-row box for a 128-wide tail tile (K-major B only)
+  CUtensorMap b3;  // W3, 128-row box
+  CUtensorMap o0;  // fp32 output (weight gradients), 32x32 box
+  CUtensorMap o1;
 };
 
 struct GemmParams {
   int H, F, E, R;
-  int bn;
   const int32_t* tiles;
   const int32_t* offsets;
   const int32_t* counts;
@@ -97,97 +92,112 @@ struct Tile {
   int nrows;  // valid rows of the tile (forward/dgrad) or rows of the expert (wgrad)
   int m0;     // wgrad: first output row inside the expert's weight
   int n0;     // first output column
+  int nw;     // MMA N of the tile: 256, or 128 for a tail tile
   int kblocks;
 };
 
-template <int MODE, int BN>
+template <int MODE>
+__device__ __forceinline__ int n_extent(const GemmParams& p) {
+  return (MODE == kFwd2 || MODE == kDgrad1 || MODE == kWgrad2) ? p.H : p.F;
+}
+
+template <int MODE>
+__device__ __forceinline__ int n_ntiles(const GemmParams& p) {
+  if (ModeTraits<MODE>::paired) return p.F / 128;
+  return (n_extent<MODE>(p) + BN - 1) / BN;
+}
+
+template <int MODE>
 __device__ __forceinline__ int n_tiles(const GemmParams& p) {
-  if (MODE == kWgrad13) return p.E * (p.H / BM) * (p.F / 128);
-  if (MODE == kWgrad2) return p.E * (p.F / BM) * (p.H / BN);
-  const int nn = (MODE == kFwd1) ? p.F / 128 : (MODE == kFwd2 || MODE == kDgrad1) ? p.H / BN : p.F / BN;
+  const int nn = n_ntiles<MODE>(p);
+  if (MODE == kWgrad13) return p.E * (p.H / BM) * nn;
+  if (MODE == kWgrad2) return p.E * (p.F / BM) * nn;
   return __ldg(p.tiles) * nn;
 }
 
-template <int MODE, int BN>
+template <int MODE>
 __device__ __forceinline__ Tile decode(const GemmParams& p, int tile) {
   Tile t;
-  if (MODE == kWgrad13 || MODE == kWgrad2) {
+  const int nn = n_ntiles<MODE>(p);
+  int nt;
+  if (ModeTraits<MODE>::wgrad) {
     const int MT = (MODE == kWgrad13) ? p.H / BM : p.F / BM;
-    const int NT = (MODE == kWgrad13) ? p.F / 128 : p.H / BN;
-    t.e = tile / (MT * NT);
-    const int rem = tile - t.e * MT * NT;
-    const int nt = rem / MT;
+    t.e = tile / (MT * nn);
+    const int rem = tile - t.e * MT * nn;
+    nt = rem / MT;
     t.m0 = (rem - nt * MT) * BM;
-    t.n0 = nt * ((MODE == kWgrad13) ? 128 : BN);
     t.row0 = __ldg(p.offsets + t.e);
     t.nrows = __ldg(p.counts + t.e);
     t.kblocks = (t.nrows + BK - 1) / BK;
-    return t;
+  } else {
+    const int entries = tiles_entry_base(p.E);
+    const int4* ent = reinterpret_cast<const int4*>(p.tiles + entries);
+    // Tiles of one expert are ordered (n tile, m tile) with m fastest, so the CTAs
+    // working side by side share the same weight columns (L2 reuse).
+    const int q = tile / nn;
+    const int e = __ldg(&ent[q].x);
+    const int first = __ldg(p.tiles + 1 + e);
+    const int cnt = __ldg(p.tiles + 2 + e) - first;
+    const int local = tile - nn * first;
+    nt = local / cnt;
+    const int mt = first + (local - nt * cnt);
+    const int4 en = ent[mt];
+    t.e = e;
+    t.row0 = en.y;
+    t.nrows = en.z;
+    t.m0 = 0;
+    const int K = (MODE == kFwd1 || MODE == kDgrad2) ? p.H : (MODE == kFwd2) ? p.F : 2 * p.F;
+    t.kblocks = K / BK;
   }
-  const int nn = (MODE == kFwd1) ? p.F / 128 : (MODE == kFwd2 || MODE == kDgrad1) ? p.H / BN : p.F / BN;
-  const int entries = tiles_entry_base(p.E);
-  const int4* ent = reinterpret_cast<const int4*>(p.tiles + entries);
-  // Tiles of one expert are ordered (n tile, m tile) with m fastest, so the CTAs
-  // working side by side share the same weight columns (L2 reuse).
-  const int q = tile / nn;
-  const int e = __ldg(&ent[q].x);
-  const int first = __ldg(p.tiles + 1 + e);
-  const int cnt = __ldg(p.tiles + 2 + e) - first;
-  const int local = tile - nn * first;
-  const int nt = local / cnt;
-  const int mt = first + (local - nt * cnt);
-  const int4 en = ent[mt];
-  t.e = e;
-  t.row0 = en.y;
-  t.nrows = en.z;
-  t.m0 = 0;
-  t.n0 = nt * ((MODE == kFwd1) ? 128 : BN);
-  const int K = (MODE == kFwd1 || MODE == kDgrad2) ? p.H : (MODE == kFwd2) ? p.F : 2 * p.F;
-  t.kblocks = K / BK;
+  if (ModeTraits<MODE>::paired) {
+    t.n0 = nt * 128;
+    t.nw = 256;
+  } else {
+    t.n0 = nt * BN;
+    t.nw = min(BN, n_extent<MODE>(p) - t.n0);
+  }
   return t;
 }
 
 // Issues the TMA loads of one k-block into stage buffers sA / sB.
-template <int MODE, int BN>
-__device__ __forceinline__ void load_kblock(const GemmParams& p, const Tile& t, int kb, uint8_t* sA, uint8_t* sB,
-                                            uint64_t* bar, const CUtensorMap* mA, const CUtensorMap* mB0,
-                                            const CUtensorMap* mB1) {
+template <int MODE>
+__device__ __forceinline__ void load_kblock(const GemmParams& p, const Maps& m, const Tile& t, int kb, uint8_t* sA,
+                                            uint8_t* sB, uint64_t* bar) {
   const int k0 = kb * BK;
+  const bool tail = t.nw < BN;
   if (MODE == kFwd1) {
-    tma_load_2d(sA, mA, bar, k0, t.row0);
+    tma_load_2d(sA, &m.a, bar, k0, t.row0);
     const int y = t.e * p.H + k0;
-    tma_load_2d(sB + 0 * kPanelBytes, mB0, bar, t.n0, y);
-    tma_load_2d(sB + 1 * kPanelBytes, mB0, bar, t.n0 + 64, y);
-    tma_load_2d(sB + 2 * kPanelBytes, mB1, bar, t.n0, y);
-    tma_load_2d(sB + 3 * kPanelBytes, mB1, bar, t.n0 + 64, y);
+    tma_load_2d(sB + 0 * kPanelBytes, &m.b0, bar, t.n0, y);
+    tma_load_2d(sB + 1 * kPanelBytes, &m.b0, bar, t.n0 + 64, y);
+    tma_load_2d(sB + 2 * kPanelBytes, &m.b1, bar, t.n0, y);
+    tma_load_2d(sB + 3 * kPanelBytes, &m.b1, bar, t.n0 + 64, y);
   } else if (MODE == kFwd2) {
-    tma_load_2d(sA, mA, bar, k0, t.row0);
+    tma_load_2d(sA, &m.a, bar, k0, t.row0);
     const int y = t.e * p.F + k0;
-#pragma unroll
-    for (int q = 0; q < BN / 64; ++q) tma_load_2d(sB + q * kPanelBytes, mB0, bar, t.n0 + 64 * q, y);
+    for (int q = 0; q < t.nw / 64; ++q) tma_load_2d(sB + q * kPanelBytes, &m.b0, bar, t.n0 + 64 * q, y);
   } else if (MODE == kDgrad2) {
-    tma_load_2d(sA, mA, bar, k0, t.row0);
-    tma_load_2d(sB, mB0, bar, k0, t.e * p.F + t.n0);
+    tma_load_2d(sA, &m.a, bar, k0, t.row0);
+    tma_load_2d(sB, tail ? &m.b2 : &m.b0, bar, k0, t.e * p.F + t.n0);
   } else if (MODE == kDgrad1) {
-    tma_load_2d(sA, mA, bar, k0, t.row0);
+    tma_load_2d(sA, &m.a, bar, k0, t.row0);
     if (k0 < p.F)
-      tma_load_2d(sB, mB0, bar, k0, t.e * p.H + t.n0);
+      tma_load_2d(sB, tail ? &m.b2 : &m.b0, bar, k0, t.e * p.H + t.n0);
     else
-      tma_load_2d(sB, mB1, bar, k0 - p.F, t.e * p.H + t.n0);
+      tma_load_2d(sB, tail ? &m.b3 : &m.b1, bar, k0 - p.F, t.e * p.H + t.n0);
   } else if (MODE == kWgrad13) {
     const int y = t.row0 + k0;
-    tma_load_2d(sA, mA, bar, t.m0, y);
-    tma_load_2d(sA + kPanelBytes, mA, bar, t.m0 + 64, y);
-    tma_load_2d(sB + 0 * kPanelBytes, mB0, bar, t.n0, y);
-    tma_load_2d(sB + 1 * kPanelBytes, mB0, bar, t.n0 + 64, y);
-    tma_load_2d(sB + 2 * kPanelBytes, mB0, bar, p.F + t.n0, y);
-    tma_load_2d(sB + 3 * kPanelBytes, mB0, bar, p.F + t.n0 + 64, y);
+    tma_load_2d(sA, &m.a, bar, t.m0, y);
+    tma_load_2d(sA + kPanelBytes, &m.a, bar, t.m0 + 64, y);
+    tma_load_2d(sB + 0 * kPanelBytes, &m.b0, bar, t.n0, y);
+    tma_load_2d(sB + 1 * kPanelBytes, &m.b0, bar, t.n0 + 64, y);
+    tma_load_2d(sB + 2 * kPanelBytes, &m.b0, bar, p.F + t.n0, y);
+    tma_load_2d(sB + 3 * kPanelBytes, &m.b0, bar, p.F + t.n0 + 64, y);
   } else {  // kWgrad2
     const int y = t.row0 + k0;
-    tma_load_2d(sA, mA, bar, t.m0, y);
-    tma_load_2d(sA + kPanelBytes, mA, bar, t.m0 + 64, y);
-#pragma unroll
-    for (int q = 0; q < BN / 64; ++q) tma_load_2d(sB + q * kPanelBytes, mB0, bar, t.n0 + 64 * q, y);
+    tma_load_2d(sA, &m.a, bar, t.m0, y);
+    tma_load_2d(sA + kPanelBytes, &m.a, bar, t.m0 + 64, y);
+    for (int q = 0; q < t.nw / 64; ++q) tma_load_2d(sB + q * kPanelBytes, &m.b0, bar, t.n0 + 64 * q, y);
   }
 }
 
@@ -211,41 +221,62 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* 
           pack_bf16x2(v[i + 6], v[i + 7]));
 }
 
-__device__ __forceinline__ void store_row_f32(float* dst, const uint32_t* r) {
-#pragma unroll
-  for (int i = 0; i < 32; i += 4) st_v4(dst + i, r[i], r[i + 1], r[i + 2], r[i + 3]);
-}
-
 __device__ __forceinline__ void store_zero_f32(float* dst) {
 #pragma unroll
   for (int i = 0; i < 32; i += 4) st_v4(dst + i, 0u, 0u, 0u, 0u);
 }
 
-template <int MODE, int BN>
-__device__ __forceinline__ void epilogue(const GemmParams& p, const Tile& t, uint32_t tacc, int row) {
-  constexpr int NCOLS = (MODE == kFwd1 || MODE == kWgrad13) ? 128 : BN;
-  if (MODE == kWgrad13 || MODE == kWgrad2) {
-    float* d0 = (MODE == kWgrad13) ? p.f0 + (static_cast<size_t>(t.e) * p.H + t.m0 + row) * p.F + t.n0
-                                   : p.f0 + (static_cast<size_t>(t.e) * p.F + t.m0 + row) * p.H + t.n0;
-    float* d1 = (MODE == kWgrad13) ? p.f1 + (static_cast<size_t>(t.e) * p.H + t.m0 + row) * p.F + t.n0 : nullptr;
+// One warp's fp32 output path: its 32 rows x 32 columns go to a 128B-swizzled
+// staging box in shared memory, then one lane issues a TMA bulk store.  Two
+// boxes per warp alternate; a box is reused only after its previous store has
+// finished reading shared memory.
+struct OutStager {
+  uint8_t* buf;  // 2 boxes of 4 KB, 1024-byte aligned
+  int next = 0;
+  __device__ __forceinline__ void put(const CUtensorMap* map, const uint32_t (&r)[32], int x, int y, int lane) {
+    uint8_t* box = buf + next * kStageOutBytes;
+    if (lane == 0) bulk_wait_read<1>();
+    __syncwarp();
+    const uint32_t row = smem_u32(box) + lane * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      st_shared_v4(row + ((j ^ (lane & 7)) << 4), r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(map, box, x, y);
+      bulk_commit();
+    }
+    next ^= 1;
+  }
+};
+
+template <int MODE>
+__device__ __forceinline__ void epilogue(const GemmParams& p, const Maps& m, const Tile& t, uint32_t tacc, int q,
+                                         int lane, OutStager& st) {
+  const int row = q * 32 + lane;
+  if (ModeTraits<MODE>::wgrad) {
+    const int NC = (MODE == kWgrad13) ? 128 : t.nw;
+    const int y = (MODE == kWgrad13) ? t.e * p.H + t.m0 + q * 32 : t.e * p.F + t.m0 + q * 32;
 #pragma unroll 1
-    for (int c = 0; c < NCOLS; c += 32) {
+    for (int c = 0; c < NC; c += 32) {
       uint32_t r[32];
       tc_ld_32x32b_x32(tacc + c, r);
       tc_wait_ld();
-      store_row_f32(d0 + c, r);
+      st.put(&m.o0, r, t.n0 + c, y, lane);
       if (MODE == kWgrad13) {
         tc_ld_32x32b_x32(tacc + 128 + c, r);
         tc_wait_ld();
-        store_row_f32(d1 + c, r);
+        st.put(&m.o1, r, t.n0 + c, y, lane);
       }
     }
     return;
   }
+  const int NC = ModeTraits<MODE>::paired ? 128 : t.nw;
   const bool valid = row < t.nrows;
   const size_t grow = static_cast<size_t>(t.row0) + row;
 #pragma unroll 1
-  for (int c = 0; c < NCOLS; c += 32) {
+  for (int c = 0; c < NC; c += 32) {
     if (MODE == kFwd1) {
       uint32_t g[32], u[32];
       tc_ld_32x32b_x32(tacc + c, g);
@@ -278,12 +309,12 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, const Tile& t, uin
           const uint4 gq = ld_v4(gsrc + i), uq = ld_v4(usrc + i);
           const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w}, uw[4] = {uq.x, uq.y, uq.z, uq.w};
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
+          for (int qq = 0; qq < 4; ++qq) {
 #pragma unroll
             for (int hbit = 0; hbit < 2; ++hbit) {
-              const int ii = i + 2 * q + hbit;
-              const float G = hbit ? bf16hi(gw[q]) : bf16lo(gw[q]);
-              const float U = hbit ? bf16hi(uw[q]) : bf16lo(uw[q]);
+              const int ii = i + 2 * qq + hbit;
+              const float G = hbit ? bf16hi(gw[qq]) : bf16lo(gw[qq]);
+              const float U = hbit ? bf16hi(uw[qq]) : bf16lo(uw[qq]);
               const float dh = __uint_as_float(d[ii]);
               const float s = 1.0f / (1.0f + expf(-G));
               dg[ii] = dh * U * s * (1.0f + G * (1.0f - s));
@@ -308,21 +339,20 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, const Tile& t, uin
   }
 }
 
-template <int MODE, int BN>
-__global__ void __launch_bounds__(kThreads, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB0,
-                        const __grid_constant__ CUtensorMap mB1, const GemmParams p) {
-  using C = Cfg<BN>;
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ Maps maps,
+                                                                   const GemmParams p) {
   using TR = ModeTraits<MODE>;
-  constexpr int S = C::kStages;
-  constexpr int NMMA = (MODE == kFwd1 || MODE == kWgrad13) ? 256 : BN;
-  constexpr uint32_t kIdesc = idesc_bf16_f32(BM, NMMA, TR::a_mn, TR::b_mn);
+  constexpr int S = TR::kStages;
   constexpr uint32_t kAStep = TR::a_mn ? 2048u : 32u;
   constexpr uint32_t kBStep = TR::b_mn ? 2048u : 32u;
+  constexpr uint32_t kIdesc256 = idesc_bf16_f32(BM, 256, TR::a_mn, TR::b_mn);
+  constexpr uint32_t kIdesc128 = idesc_bf16_f32(BM, 128, TR::a_mn, TR::b_mn);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * C::kStageBytes);
+  uint8_t* staging = smem + S * kStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + TR::kStagingBytes);
   uint64_t* empty = full + S;
   uint64_t* tfull = empty + S;
   uint64_t* tempty = tfull + 2;
@@ -345,9 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_fence_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&mA);
-    tma_prefetch_desc(&mB0);
-    tma_prefetch_desc(&mB1);
+    tma_prefetch_desc(&maps.a);
+    tma_prefetch_desc(&maps.b0);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -357,26 +386,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int ntiles = n_tiles<MODE, BN>(p);
+  const int ntiles = n_tiles<MODE>(p);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     int s = 0;
     uint32_t ph = 0;
-    uint32_t issued = 0;        // bit i: stage i was ever filled
-    uint32_t last_parity = 0;   // bit i: parity of stage i's last fill
+    uint32_t issued = 0;       // bit i: stage i was ever filled
+    uint32_t last_parity = 0;  // bit i: parity of stage i's last fill
     bool ok = true;
     for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-      const Tile t = decode<MODE, BN>(p, tile);
+      const Tile t = decode<MODE>(p, tile);
       for (int kb = 0; kb < t.kblocks; ++kb) {
         if (!mbar_wait(&empty[s], ph ^ 1u, p.ws, 100 + MODE, abort_flag)) {
           ok = false;
           break;
         }
         if (elect_one()) {
-          mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-          uint8_t* sA = smem + s * C::kStageBytes;
-          load_kblock<MODE, BN>(p, t, kb, sA, sA + C::kABytes, &full[s], &mA, &mB0, &mB1);
+          mbar_arrive_expect_tx(&full[s], kABytes + t.nw * 128);
+          uint8_t* sA = smem + s * kStageBytes;
+          load_kblock<MODE>(p, maps, t, kb, sA, sA + kABytes, &full[s]);
         }
         __syncwarp();
         issued |= 1u << s;
@@ -398,29 +427,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_ph = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-      const Tile t = decode<MODE, BN>(p, tile);
+      const Tile t = decode<MODE>(p, tile);
       if (t.kblocks == 0) continue;  // empty expert (wgrad): the epilogue writes zeros
       if (!mbar_wait(&tempty[acc], acc_ph ^ 1u, p.ws, 120 + MODE, abort_flag)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * kAccStride;
+      const uint32_t idesc = (t.nw == 256) ? kIdesc256 : kIdesc128;
       for (int kb = 0; kb < t.kblocks; ++kb) {
         if (!mbar_wait(&full[s], ph, p.ws, 130 + MODE, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        uint8_t* sA = smem + s * C::kStageBytes;
-        uint8_t* sB = sA + C::kABytes;
+        uint8_t* sA = smem + s * kStageBytes;
+        uint8_t* sB = sA + kABytes;
         if (TR::wgrad) {
           // The expert's last k-block may run past its rows: zero those K rows
           // of both operands so rows of the next expert add nothing.
           const int valid = t.nrows - kb * BK;
           if (valid < BK) {
-            constexpr int kPanels = 2 + NMMA / 64;
-            const int nchunks = (BK - valid) * 8 * kPanels;
-            for (int i = lane; i < nchunks; i += 32) {
-              const int panel = i / ((BK - valid) * 8);
-              const int rem = i - panel * (BK - valid) * 8;
+            const int panels = 2 + t.nw / 64;
+            const int per_panel = (BK - valid) * 8;
+            for (int i = lane; i < per_panel * panels; i += 32) {
+              const int panel = i / per_panel;
+              const int rem = i - panel * per_panel;
               const int rr = valid + (rem >> 3);
               uint8_t* base = (panel < 2) ? sA + panel * kPanelBytes : sB + (panel - 2) * kPanelBytes;
               *reinterpret_cast<uint4*>(base + rr * 128 + (rem & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
@@ -435,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t ad = smem_desc_sw128(a0 + kk * kAStep, TR::a_mn ? kPanelBytes : 16, 1024);
             const uint64_t bd = smem_desc_sw128(b0 + kk * kBStep, TR::b_mn ? kPanelBytes : 16, 1024);
-            tc_mma_bf16(d_tmem, ad, bd, kIdesc, (kb | kk) != 0);
+            tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0);
           }
           tc_commit(&empty[s]);
         }
@@ -455,13 +485,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
+    OutStager st;
+    st.buf = staging + q * 2 * kStageOutBytes;
     int acc = 0;
     uint32_t acc_ph = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-      const Tile t = decode<MODE, BN>(p, tile);
+      const Tile t = decode<MODE>(p, tile);
       if (t.kblocks == 0) {
         if (TR::wgrad) {
-          constexpr int NC = (MODE == kWgrad13) ? 128 : BN;
+          const int NC = (MODE == kWgrad13) ? 128 : t.nw;
           float* d0 = (MODE == kWgrad13) ? p.f0 + (static_cast<size_t>(t.e) * p.H + t.m0 + row) * p.F + t.n0
                                          : p.f0 + (static_cast<size_t>(t.e) * p.F + t.m0 + row) * p.H + t.n0;
           for (int c = 0; c < NC; c += 32) store_zero_f32(d0 + c);
@@ -475,13 +507,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&tfull[acc], acc_ph, p.ws, 140 + MODE, abort_flag)) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccStride;
-      epilogue<MODE, BN>(p, t, tacc, row);
+      epilogue<MODE>(p, maps, t, tacc, q, lane, st);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
       acc ^= 1;
       if (acc == 0) acc_ph ^= 1u;
     }
+    // Bulk stores must finish reading shared memory (and land) before the CTA exits.
+    if (TR::wgrad && lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -509,33 +544,30 @@ EncodeFn encoder() {
   return fn;
 }
 
-// 2-D bf16 tensor [outer, inner] (inner contiguous), box {box_inner, box_outer}, 128-byte swizzle.
+// 2-D tensor [outer, inner] (inner contiguous), box {box_inner, box_outer}, 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
-              uint32_t box_outer) {
+              uint32_t box_outer, bool f32 = false) {
   EncodeFn enc = encoder();
   if (!enc) return false;
+  const uint64_t esz = f32 ? 4 : 2;
   const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint64_t strides[1] = {inner * esz};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE, int BN>
-cudaError_t launch_mode(const GemmLaunch& L, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                        const GemmParams& p, cudaStream_t s, LaunchHook& hook) {
-  using C = Cfg<BN>;
-  auto kern = grouped_gemm_kernel<MODE, BN>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+template <int MODE>
+cudaError_t launch_mode(const GemmLaunch& L, const Maps& maps, const GemmParams& p, cudaStream_t s,
+                        LaunchHook& hook) {
+  constexpr int kSmem = ModeTraits<MODE>::kSmemBytes;
+  auto kern = grouped_gemm_kernel<MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
   hook.before(s);
-  kern<<<L.grid, kThreads, C::kSmemBytes, s>>>(a, b0, b1, p);
+  kern<<<L.grid, kThreads, kSmem, s>>>(maps, p);
   hook.after(s);
   return cudaGetLastError();
 }
@@ -546,14 +578,13 @@ bool tensor_map_encoder_ready() { return encoder() != nullptr; }
 
 cudaError_t launch_gemm(GemmMode mode, const GemmLaunch& L, cudaStream_t s, LaunchHook& hook) {
   const uint64_t R = L.R, H = L.H, F = L.F, E = L.E;
-  const uint32_t bn = L.bn;
-  CUtensorMap a, b0, b1;
+  Maps m;
+  memset(&m, 0, sizeof(m));
   GemmParams p{};
   p.H = L.H;
   p.F = L.F;
   p.E = L.E;
   p.R = L.R;
-  p.bn = L.bn;
   p.tiles = L.tiles;
   p.offsets = L.offsets;
   p.counts = L.counts;
@@ -561,57 +592,47 @@ cudaError_t launch_gemm(GemmMode mode, const GemmLaunch& L, cudaStream_t s, Laun
   bool ok = true;
   switch (mode) {
     case kFwd1:
-      ok = make_map(&a, L.Xp, H, R, 64, BM) && make_map(&b0, L.W1, F, E * H, 64, 64) &&
-           make_map(&b1, L.W3, F, E * H, 64, 64);
+      ok = make_map(&m.a, L.Xp, H, R, 64, BM) && make_map(&m.b0, L.W1, F, E * H, 64, 64) &&
+           make_map(&m.b1, L.W3, F, E * H, 64, 64);
       p.out0 = static_cast<__nv_bfloat16*>(L.out_h);
       p.out1 = static_cast<__nv_bfloat16*>(L.out_GU);
       break;
     case kFwd2:
-      ok = make_map(&a, L.h, F, R, 64, BM) && make_map(&b0, L.W2, H, E * F, 64, 64);
-      b1 = b0;
+      ok = make_map(&m.a, L.h, F, R, 64, BM) && make_map(&m.b0, L.W2, H, E * F, 64, 64);
       p.out0 = static_cast<__nv_bfloat16*>(L.out_Y);
       break;
     case kDgrad2:
-      ok = make_map(&a, L.dY, H, R, 64, BM) && make_map(&b0, L.W2, H, E * F, 64, bn);
-      b1 = b0;
+      ok = make_map(&m.a, L.dY, H, R, 64, BM) && make_map(&m.b0, L.W2, H, E * F, 64, BN) &&
+           make_map(&m.b2, L.W2, H, E * F, 64, 128);
       p.out0 = static_cast<__nv_bfloat16*>(L.out_dGU);
       p.aux = static_cast<const __nv_bfloat16*>(L.GU);
       break;
     case kDgrad1:
-      ok = make_map(&a, L.dGU, 2 * F, R, 64, BM) && make_map(&b0, L.W1, F, E * H, 64, bn) &&
-           make_map(&b1, L.W3, F, E * H, 64, bn);
+      ok = make_map(&m.a, L.dGU, 2 * F, R, 64, BM) && make_map(&m.b0, L.W1, F, E * H, 64, BN) &&
+           make_map(&m.b1, L.W3, F, E * H, 64, BN) && make_map(&m.b2, L.W1, F, E * H, 64, 128) &&
+           make_map(&m.b3, L.W3, F, E * H, 64, 128);
       p.out0 = static_cast<__nv_bfloat16*>(L.out_dXp);
       break;
     case kWgrad13:
-      ok = make_map(&a, L.Xp, H, R, 64, 64) && make_map(&b0, L.dGU, 2 * F, R, 64, 64);
-      b1 = b0;
+      ok = make_map(&m.a, L.Xp, H, R, 64, 64) && make_map(&m.b0, L.dGU, 2 * F, R, 64, 64) &&
+           make_map(&m.o0, L.dW1, F, E * H, 32, 32, true) && make_map(&m.o1, L.dW3, F, E * H, 32, 32, true);
       p.f0 = L.dW1;
       p.f1 = L.dW3;
       break;
     case kWgrad2:
-      ok = make_map(&a, L.h, F, R, 64, 64) && make_map(&b0, L.dY, H, R, 64, 64);
-      b1 = b0;
+      ok = make_map(&m.a, L.h, F, R, 64, 64) && make_map(&m.b0, L.dY, H, R, 64, 64) &&
+           make_map(&m.o0, L.dW2, H, E * F, 32, 32, true);
       p.f0 = L.dW2;
       break;
   }
   if (!ok) return cudaErrorInvalidValue;
   switch (mode) {
-    case kFwd1:
-      return launch_mode<kFwd1, 256>(L, a, b0, b1, p, s, hook);
-    case kFwd2:
-      return bn == 256 ? launch_mode<kFwd2, 256>(L, a, b0, b1, p, s, hook)
-                       : launch_mode<kFwd2, 128>(L, a, b0, b1, p, s, hook);
-    case kDgrad2:
-      return bn == 256 ? launch_mode<kDgrad2, 256>(L, a, b0, b1, p, s, hook)
-                       : launch_mode<kDgrad2, 128>(L, a, b0, b1, p, s, hook);
-    case kDgrad1:
-      return bn == 256 ? launch_mode<kDgrad1, 256>(L, a, b0, b1, p, s, hook)
-                       : launch_mode<kDgrad1, 128>(L, a, b0, b1, p, s, hook);
-    case kWgrad13:
-      return launch_mode<kWgrad13, 256>(L, a, b0, b1, p, s, hook);
-    case kWgrad2:
-      return bn == 256 ? launch_mode<kWgrad2, 256>(L, a, b0, b1, p, s, hook)
-                       : launch_mode<kWgrad2, 128>(L, a, b0, b1, p, s, hook);
+    case kFwd1: return launch_mode<kFwd1>(L, m, p, s, hook);
+    case kFwd2: return launch_mode<kFwd2>(L, m, p, s, hook);
+    case kDgrad2: return launch_mode<kDgrad2>(L, m, p, s, hook);
+    case kDgrad1: return launch_mode<kDgrad1>(L, m, p, s, hook);
+    case kWgrad13: return launch_mode<kWgrad13>(L, m, p, s, hook);
+    case kWgrad2: return launch_mode<kWgrad2>(L, m, p, s, hook);
   }
   return cudaErrorInvalidValue;
 }
