@@ -293,6 +293,17 @@ def run_ours(args):
     st = layer.status()
     if st[0] != 0:
         raise RuntimeError(f"device status {st}")
+    if args.profile:
+        # One more step and nothing else: the launch sequence a profiler captures.
+        step()
+        torch.cuda.synchronize()
+        st = layer.status()
+        if st[0] != 0:
+            raise RuntimeError(f"device status {st}")
+        if rank == 0:
+            print(json.dumps({"profile_step": "done", "config": workload_config(shape, args.config),
+                              "kernels_per_step": N_PLAN_KERNELS + nf + nb}), flush=True)
+        return
 
     # Per-kernel events of every timed step (recorded on the launching stream).
     evs_f = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nf)] for _ in range(args.steps)]
@@ -447,6 +458,8 @@ def main():
     ap.add_argument("--config", type=int, default=1)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="run the warm-up steps and one more step only (for ncu captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
