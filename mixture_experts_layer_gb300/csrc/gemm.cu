@@ -13,13 +13,15 @@
 //   - section 3 (Persistent Worker Architecture): one resident CTA per SM
 //     loops over the tile list.
 //
-// Kernel structure (one CTA per SM, 192 threads):
+// Kernel structure (one CTA per SM, 320 threads):
 //   warp 0     TMA producer: fills a ring of shared-memory stages
 //   warp 1     allocates tensor memory, issues tcgen05.mma (one elected lane)
-//   warps 2-5  epilogue: tcgen05.ld of the fp32 accumulator, fused
-//              elementwise work (SwiGLU forward or backward), stores.  The fp32
-//              weight gradients go out through swizzled shared-memory staging
-//              and TMA bulk stores, one 32x32 box per warp, double-buffered.
+//   warps 2-9  epilogue, two warps per TMEM lane quarter (32 rows), each taking
+//              half of the tile's columns: tcgen05.ld of the fp32 accumulator
+//              (the next chunk's load in flight while this one is stored),
+//              fused elementwise work (SwiGLU forward or backward), stores.  The
+//              fp32 weight gradients go out through swizzled shared-memory
+//              staging and TMA bulk stores, one 32x32 box per warp at a time.
 // The accumulator is double-buffered in tensor memory (2 x 256 columns), so the
 // epilogue of one tile overlaps the main loop of the next.
 //
@@ -42,7 +44,8 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int BN = 256;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each taking half of the columns
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccStride = 256;   // TMEM columns per accumulator buffer
 constexpr int kPanelBytes = 64 * 128;  // one MN-major panel: 64 K-rows x 128 B
@@ -50,6 +53,7 @@ constexpr int kABytes = BM * BK * 2;
 constexpr int kBBytesMax = BN * BK * 2;
 constexpr int kStageBytes = kABytes + kBBytesMax;
 constexpr int kStageOutBytes = 32 * 128;  // one warp's 32x32 fp32 staging box
+constexpr int kOutBoxes = 2;              // staging boxes per epilogue warp (stores in flight)
 
 template <int MODE>
 struct ModeTraits {
@@ -59,7 +63,7 @@ struct ModeTraits {
   // Output columns per tile are 2 x 128 (two weights side by side) or up to 256.
   static constexpr bool paired = (MODE == kFwd1 || MODE == kWgrad13);
   static constexpr int kStages = wgrad ? 3 : 4;
-  static constexpr int kStagingBytes = wgrad ? 4 * 2 * kStageOutBytes : 0;
+  static constexpr int kStagingBytes = wgrad ? kEpiWarps * kOutBoxes * kStageOutBytes : 0;
   static constexpr int kSmemBytes = kStages * kStageBytes + kStagingBytes + 1024 /*align*/ + 256 /*barriers*/;
 };
 
@@ -227,15 +231,15 @@ __device__ __forceinline__ void store_zero_f32(float* dst) {
 }
 
 // One warp's fp32 output path: its 32 rows x 32 columns go to a 128B-swizzled
-// staging box in shared memory, then one lane issues a TMA bulk store.  Two
-// boxes per warp alternate; a box is reused only after its previous store has
-// finished reading shared memory.
+// staging box in shared memory, then one lane issues a TMA bulk store.  The
+// warp cycles through kOutBoxes boxes, so that many stores are in flight; a box
+// is reused only after its previous store has finished reading shared memory.
 struct OutStager {
-  uint8_t* buf;  // 2 boxes of 4 KB, 1024-byte aligned
+  uint8_t* buf;  // kOutBoxes boxes of 4 KB, 1024-byte aligned
   int next = 0;
   __device__ __forceinline__ void put(const CUtensorMap* map, const uint32_t (&r)[32], int x, int y, int lane) {
     uint8_t* box = buf + next * kStageOutBytes;
-    if (lane == 0) bulk_wait_read<1>();
+    if (lane == 0) bulk_wait_read<kOutBoxes - 1>();
     __syncwarp();
     const uint32_t row = smem_u32(box) + lane * 128;
 #pragma unroll
@@ -247,36 +251,58 @@ struct OutStager {
       tma_store_2d(map, box, x, y);
       bulk_commit();
     }
-    next ^= 1;
+    next = (next + 1 == kOutBoxes) ? 0 : next + 1;
   }
 };
 
 template <int MODE>
 __device__ __forceinline__ void epilogue(const GemmParams& p, const Maps& m, const Tile& t, uint32_t tacc, int q,
-                                         int lane, OutStager& st) {
+                                         int half, int lane, OutStager& st) {
   const int row = q * 32 + lane;
+  // This warp's columns: [c_lo, c_hi) of each output (NC / 2 is a multiple of 32).
+  const int NCall = ModeTraits<MODE>::paired ? 128 : t.nw;
+  const int c_lo = half * (NCall / 2), c_hi = c_lo + NCall / 2;
   if (ModeTraits<MODE>::wgrad) {
-    const int NC = (MODE == kWgrad13) ? 128 : t.nw;
     const int y = (MODE == kWgrad13) ? t.e * p.H + t.m0 + q * 32 : t.e * p.F + t.m0 + q * 32;
+    uint32_t a0[32], a1[32];
+    tc_ld_32x32b_x32(tacc + c_lo, a0);
+    if (MODE == kWgrad13) tc_ld_32x32b_x32(tacc + 128 + c_lo, a1);
+    tc_wait_ld();
 #pragma unroll 1
-    for (int c = 0; c < NC; c += 32) {
-      uint32_t r[32];
-      tc_ld_32x32b_x32(tacc + c, r);
-      tc_wait_ld();
-      st.put(&m.o0, r, t.n0 + c, y, lane);
-      if (MODE == kWgrad13) {
-        tc_ld_32x32b_x32(tacc + 128 + c, r);
+    for (int c = c_lo; c < c_hi; c += 32) {
+      const bool more = c + 32 < c_hi;
+      uint32_t b0[32], b1[32];
+      if (more) {  // next chunk's accumulator load overlaps this chunk's stores
+        tc_ld_32x32b_x32(tacc + c + 32, b0);
+        if (MODE == kWgrad13) tc_ld_32x32b_x32(tacc + 128 + c + 32, b1);
+      }
+      st.put(&m.o0, a0, t.n0 + c, y, lane);
+      if (MODE == kWgrad13) st.put(&m.o1, a1, t.n0 + c, y, lane);
+      if (more) {
         tc_wait_ld();
-        st.put(&m.o1, r, t.n0 + c, y, lane);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          a0[i] = b0[i];
+          if (MODE == kWgrad13) a1[i] = b1[i];
+        }
       }
     }
     return;
   }
-  const int NC = ModeTraits<MODE>::paired ? 128 : t.nw;
+  const int NC = c_hi;
   const bool valid = row < t.nrows;
   const size_t grow = static_cast<size_t>(t.row0) + row;
+  uint4 gcur[4], ucur[4];
+  if (MODE == kDgrad2 && valid) {
+    const __nv_bfloat16* gsrc = p.aux + grow * (2 * p.F) + t.n0 + c_lo;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      gcur[i] = ld_v4(gsrc + 8 * i);
+      ucur[i] = ld_v4(gsrc + p.F + 8 * i);
+    }
+  }
 #pragma unroll 1
-  for (int c = 0; c < NC; c += 32) {
+  for (int c = c_lo; c < NC; c += 32) {
     if (MODE == kFwd1) {
       uint32_t g[32], u[32];
       tc_ld_32x32b_x32(tacc + c, g);
@@ -288,7 +314,7 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, const Maps& m, con
         for (int i = 0; i < 32; ++i) {
           const float a = __uint_as_float(g[i]);
           const float b = __uint_as_float(u[i]);
-          hv[i] = a / (1.0f + expf(-a)) * b;
+          hv[i] = a * __frcp_rn(1.0f + expf(-a)) * b;
           gv[i] = a;
           uv[i] = b;
         }
@@ -297,33 +323,47 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, const Maps& m, con
         store_row_bf16(p.out1 + grow * (2 * p.F) + p.F + t.n0 + c, uv);
       }
     } else if (MODE == kDgrad2) {
+      // G and U of this row are read from global memory; the loads of the
+      // next 32 columns are issued before this chunk's arithmetic.
       uint32_t d[32];
       tc_ld_32x32b_x32(tacc + c, d);
+      uint4 gn[4], un[4];
+      if (valid && c + 32 < NC) {
+        const __nv_bfloat16* gsrc = p.aux + grow * (2 * p.F) + t.n0 + c + 32;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          gn[i] = ld_v4(gsrc + 8 * i);
+          un[i] = ld_v4(gsrc + p.F + 8 * i);
+        }
+      }
       tc_wait_ld();
       if (valid) {
-        const __nv_bfloat16* gsrc = p.aux + grow * (2 * p.F) + t.n0 + c;
-        const __nv_bfloat16* usrc = gsrc + p.F;
         float dg[32], du[32];
 #pragma unroll
-        for (int i = 0; i < 32; i += 8) {
-          const uint4 gq = ld_v4(gsrc + i), uq = ld_v4(usrc + i);
-          const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w}, uw[4] = {uq.x, uq.y, uq.z, uq.w};
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t gw[4] = {gcur[i].x, gcur[i].y, gcur[i].z, gcur[i].w};
+          const uint32_t uw[4] = {ucur[i].x, ucur[i].y, ucur[i].z, ucur[i].w};
 #pragma unroll
           for (int qq = 0; qq < 4; ++qq) {
 #pragma unroll
             for (int hbit = 0; hbit < 2; ++hbit) {
-              const int ii = i + 2 * qq + hbit;
+              const int ii = 8 * i + 2 * qq + hbit;
               const float G = hbit ? bf16hi(gw[qq]) : bf16lo(gw[qq]);
               const float U = hbit ? bf16hi(uw[qq]) : bf16lo(uw[qq]);
               const float dh = __uint_as_float(d[ii]);
-              const float s = 1.0f / (1.0f + expf(-G));
-              dg[ii] = dh * U * s * (1.0f + G * (1.0f - s));
-              du[ii] = dh * G * s;
+              const float sg = __frcp_rn(1.0f + expf(-G));
+              dg[ii] = dh * U * sg * (1.0f + G * (1.0f - sg));
+              du[ii] = dh * G * sg;
             }
           }
         }
         store_row_bf16(p.out0 + grow * (2 * p.F) + t.n0 + c, dg);
         store_row_bf16(p.out0 + grow * (2 * p.F) + p.F + t.n0 + c, du);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          gcur[i] = gn[i];
+          ucur[i] = un[i];
+        }
       }
     } else {  // kFwd2 (Y) or kDgrad1 (dXp): plain bf16 store, row stride H
       uint32_t d[32];
@@ -369,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 4);
+      mbar_init(&tempty[i], kEpiWarps);
     }
     *abort_flag = 0;
     mbar_fence_init();
@@ -441,19 +481,19 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         tc_fence_after();
         uint8_t* sA = smem + s * kStageBytes;
         uint8_t* sB = sA + kABytes;
+        // The expert's last k-block (weight gradients) may run past its rows:
+        // only the K steps of 16 that hold valid rows are issued, and inside
+        // the last of them the rows past the expert are zeroed in operand A, so
+        // rows of the next expert (finite values in B) add nothing.
+        int nkk = BK / 16;
         if (TR::wgrad) {
-          // The expert's last k-block may run past its rows: zero those K rows
-          // of both operands so rows of the next expert add nothing.
           const int valid = t.nrows - kb * BK;
           if (valid < BK) {
-            const int panels = 2 + t.nw / 64;
-            const int per_panel = (BK - valid) * 8;
-            for (int i = lane; i < per_panel * panels; i += 32) {
-              const int panel = i / per_panel;
-              const int rem = i - panel * per_panel;
-              const int rr = valid + (rem >> 3);
-              uint8_t* base = (panel < 2) ? sA + panel * kPanelBytes : sB + (panel - 2) * kPanelBytes;
-              *reinterpret_cast<uint4*>(base + rr * 128 + (rem & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+            nkk = (valid + 15) >> 4;
+            const int z0 = valid, nz = nkk * 16 - valid;  // < 16 rows to clear
+            for (int i = lane; i < nz * 16; i += 32) {
+              const int r = z0 + (i >> 4), panel = (i >> 3) & 1, chunk = i & 7;
+              *reinterpret_cast<uint4*>(sA + panel * kPanelBytes + r * 128 + chunk * 16) = make_uint4(0u, 0u, 0u, 0u);
             }
             fence_proxy_async_smem();
           }
@@ -463,9 +503,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
           const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = smem_desc_sw128(a0 + kk * kAStep, TR::a_mn ? kPanelBytes : 16, 1024);
-            const uint64_t bd = smem_desc_sw128(b0 + kk * kBStep, TR::b_mn ? kPanelBytes : 16, 1024);
-            tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+            if (kk < nkk) {
+              const uint64_t ad = smem_desc_sw128(a0 + kk * kAStep, TR::a_mn ? kPanelBytes : 16, 1024);
+              const uint64_t bd = smem_desc_sw128(b0 + kk * kBStep, TR::b_mn ? kPanelBytes : 16, 1024);
+              tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+            }
           }
           tc_commit(&empty[s]);
         }
@@ -483,23 +525,25 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int q = warp & 3;              // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;    // which half of the columns
     const int row = q * 32 + lane;
     OutStager st;
-    st.buf = staging + q * 2 * kStageOutBytes;
+    st.buf = staging + (warp - 2) * kOutBoxes * kStageOutBytes;
     int acc = 0;
     uint32_t acc_ph = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
       const Tile t = decode<MODE>(p, tile);
       if (t.kblocks == 0) {
         if (TR::wgrad) {
-          const int NC = (MODE == kWgrad13) ? 128 : t.nw;
+          const int NCall = (MODE == kWgrad13) ? 128 : t.nw;
+          const int c_lo = half * (NCall / 2), c_hi = c_lo + NCall / 2;
           float* d0 = (MODE == kWgrad13) ? p.f0 + (static_cast<size_t>(t.e) * p.H + t.m0 + row) * p.F + t.n0
                                          : p.f0 + (static_cast<size_t>(t.e) * p.F + t.m0 + row) * p.H + t.n0;
-          for (int c = 0; c < NC; c += 32) store_zero_f32(d0 + c);
+          for (int c = c_lo; c < c_hi; c += 32) store_zero_f32(d0 + c);
           if (MODE == kWgrad13) {
             float* d1 = p.f1 + (static_cast<size_t>(t.e) * p.H + t.m0 + row) * p.F + t.n0;
-            for (int c = 0; c < NC; c += 32) store_zero_f32(d1 + c);
+            for (int c = c_lo; c < c_hi; c += 32) store_zero_f32(d1 + c);
           }
         }
         continue;
@@ -507,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       if (!mbar_wait(&tfull[acc], acc_ph, p.ws, 140 + MODE, abort_flag)) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccStride;
-      epilogue<MODE>(p, maps, t, tacc, q, lane, st);
+      epilogue<MODE>(p, maps, t, tacc, q, half, lane, st);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);

@@ -24,77 +24,90 @@
 
 namespace moe {
 
-template <int NV>
-__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
-                                                         int32_t* __restrict__ ids, float* __restrict__ wts,
-                                                         uint32_t* __restrict__ gbm, int32_t* __restrict__ ccount,
-                                                         WsHeader* ws) {
+constexpr int kTopkThreads = 512;
+
+// NV = logits per lane (E <= 32 * NV); TPW = tokens whose logits a warp loads
+// at once, so several rows' loads are in flight before the selection starts.
+template <int NV, int TPW>
+__global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float* __restrict__ logits, int T, int E,
+                                                                  int k, int32_t* __restrict__ ids,
+                                                                  float* __restrict__ wts, uint32_t* __restrict__ gbm,
+                                                                  int32_t* __restrict__ ccount, WsHeader* ws) {
   extern __shared__ uint32_t bm[];  // [E][kChunkWords]
+  constexpr int kWarps = kTopkThreads / 32;
   const int chunk = blockIdx.x;
   for (int i = threadIdx.x; i < E * kChunkWords; i += blockDim.x) bm[i] = 0;
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int tl = warp; tl < kChunk; tl += 8) {
-    const int t = chunk * kChunk + tl;
-    if (t >= T) break;
-    float v[NV];
-    uint32_t taken = 0;
-    bool bad = false;
+  for (int tb = warp * TPW; tb < kChunk; tb += kWarps * TPW) {
+    float v[TPW][NV];
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int e = lane + 32 * i;
-      float a = -INFINITY;
-      if (e < E) {
-        a = logits[static_cast<size_t>(t) * E + e];
-        if (!isfinite(a)) {
-          bad = true;
-          a = -INFINITY;
-        }
-      } else {
-        taken |= 1u << i;  // padding lanes are never chosen
-      }
-      v[i] = a;
-    }
-    if (__any_sync(0xffffffffu, bad) && lane == 0) report(ws, MOE_ERR_NONFINITE, 0, t);
-    int my_id = 0;
-    float my_v = 0.f;
-    for (int j = 0; j < k; ++j) {
-      // Largest untaken logit, ties to the lower expert id: a total order, so
-      // every lane ends the butterfly with the same winner.
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
+    for (int u = 0; u < TPW; ++u) {
+      const int t = chunk * kChunk + tb + u;
 #pragma unroll
       for (int i = 0; i < NV; ++i) {
         const int e = lane + 32 * i;
-        if (!((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
-          bv = v[i];
-          bi = e;
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (ov > bv || (ov == bv && oi < bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (lane == j) {
-        my_id = bi;
-        my_v = bv;
+        v[u][i] = (t < T && e < E) ? logits[static_cast<size_t>(t) * E + e] : -INFINITY;
       }
     }
-    // w_j = exp(l_j - l_max) / sum_{i<k} exp(l_i - l_max); the sum runs in slot order.
-    const float m = __shfl_sync(0xffffffffu, my_v, 0);
-    const float ex = (lane < k) ? expf(my_v - m) : 0.f;
-    float s = 0.f;
-    for (int j = 0; j < k; ++j) s += __shfl_sync(0xffffffffu, ex, j);
-    if (lane < k) {
-      ids[static_cast<size_t>(t) * k + lane] = my_id;
-      wts[static_cast<size_t>(t) * k + lane] = ex / s;
-      atomicOr(&bm[my_id * kChunkWords + (tl >> 5)], 1u << (tl & 31));
+#pragma unroll
+    for (int u = 0; u < TPW; ++u) {
+      const int tl = tb + u;
+      const int t = chunk * kChunk + tl;
+      if (t >= T) break;
+      uint32_t taken = 0;
+      bool bad = false;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const int e = lane + 32 * i;
+        if (e >= E) {
+          taken |= 1u << i;  // padding lanes are never chosen
+        } else if (!isfinite(v[u][i])) {
+          bad = true;
+          v[u][i] = -INFINITY;
+        }
+      }
+      if (__any_sync(0xffffffffu, bad) && lane == 0) report(ws, MOE_ERR_NONFINITE, 0, t);
+      int my_id = 0;
+      float my_v = 0.f;
+      for (int j = 0; j < k; ++j) {
+        // Largest untaken logit, ties to the lower expert id: a total order, so
+        // every lane ends the butterfly with the same winner.
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+          const int e = lane + 32 * i;
+          if (!((taken >> i) & 1u) && (v[u][i] > bv || (v[u][i] == bv && e < bi))) {
+            bv = v[u][i];
+            bi = e;
+          }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+          const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+          if (ov > bv || (ov == bv && oi < bi)) {
+            bv = ov;
+            bi = oi;
+          }
+        }
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        if (lane == j) {
+          my_id = bi;
+          my_v = bv;
+        }
+      }
+      // w_j = exp(l_j - l_max) / sum_{i<k} exp(l_i - l_max); the sum runs in slot order.
+      const float m = __shfl_sync(0xffffffffu, my_v, 0);
+      const float ex = (lane < k) ? expf(my_v - m) : 0.f;
+      float sum = 0.f;
+      for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, ex, j);
+      if (lane < k) {
+        ids[static_cast<size_t>(t) * k + lane] = my_id;
+        wts[static_cast<size_t>(t) * k + lane] = ex / sum;
+        atomicOr(&bm[my_id * kChunkWords + (tl >> 5)], 1u << (tl & 31));
+      }
     }
   }
   __syncthreads();
@@ -231,17 +244,17 @@ cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t s, LaunchHook& hook) {
   const int nv = (p.E + 31) / 32;
   hook.before(s);
   switch (nv <= 1 ? 1 : nv <= 2 ? 2 : nv <= 4 ? 4 : nv <= 8 ? 8 : nv <= 16 ? 16 : 32) {
-#define MOE_TOPK_CASE(NV)                                                                                  \
-  case NV:                                                                                                 \
-    route_topk_kernel<NV><<<nchunks, 256, bm_bytes, s>>>(p.logits, p.T, p.E, p.k, p.ids, p.w, p.gbm,      \
-                                                         p.ccount, p.ws);                                  \
+#define MOE_TOPK_CASE(NV, TPW)                                                                               \
+  case NV:                                                                                                   \
+    route_topk_kernel<NV, TPW><<<nchunks, kTopkThreads, bm_bytes, s>>>(p.logits, p.T, p.E, p.k, p.ids, p.w, \
+                                                                       p.gbm, p.ccount, p.ws);              \
     break;
-    MOE_TOPK_CASE(1)
-    MOE_TOPK_CASE(2)
-    MOE_TOPK_CASE(4)
-    MOE_TOPK_CASE(8)
-    MOE_TOPK_CASE(16)
-    MOE_TOPK_CASE(32)
+    MOE_TOPK_CASE(1, 8)
+    MOE_TOPK_CASE(2, 8)
+    MOE_TOPK_CASE(4, 4)
+    MOE_TOPK_CASE(8, 2)
+    MOE_TOPK_CASE(16, 1)
+    MOE_TOPK_CASE(32, 1)
 #undef MOE_TOPK_CASE
   }
   hook.after(s);

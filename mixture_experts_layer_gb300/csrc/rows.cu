@@ -70,12 +70,14 @@ __global__ void __launch_bounds__(kThreads) gather_rows_kernel(const uint4* __re
   }
 }
 
-// Loads the k (row, weight) pairs of token t into lanes 0..k-1; returns false
-// (and reports) if a row index is out of range.
+// The k (row, weight) pairs of token t, held in registers by every lane
+// (K = compile-time bound on k).  Returns false (and reports) if a row index is
+// out of range.
+template <int K>
 __device__ __forceinline__ bool token_rows(const int32_t* dest, const float* w, int t, int k, int R, int lane,
-                                           int& my_r, float& my_w, WsHeader* ws, int where) {
-  my_r = 0;
-  my_w = 0.f;
+                                           int (&rows)[K], float (&ws_)[K], WsHeader* ws, int where) {
+  int my_r = 0;
+  float my_w = 0.f;
   if (lane < k) {
     my_r = dest[static_cast<size_t>(t) * k + lane];
     if (w != nullptr) my_w = w[static_cast<size_t>(t) * k + lane];
@@ -85,9 +87,16 @@ __device__ __forceinline__ bool token_rows(const int32_t* dest, const float* w, 
     if (lane == 0) report(ws, MOE_ERR_BOUNDS, where, t);
     return false;
   }
+#pragma unroll
+  for (int j = 0; j < K; ++j) {
+    rows[j] = __shfl_sync(0xffffffffu, my_r, j);
+    ws_[j] = __shfl_sync(0xffffffffu, my_w, j);
+  }
   return true;
 }
 
+// out[t] = bf16(sum_j w[t,j] Y[dest[t,j]]), slots in ascending order.
+template <int K>
 __global__ void __launch_bounds__(kThreads) combine_kernel(const uint4* __restrict__ Y,
                                                              const int32_t* __restrict__ dest,
                                                              const float* __restrict__ w, uint4* __restrict__ out,
@@ -95,24 +104,33 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const uint4* __restri
   const int lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * (kThreads / 32);
   for (int t = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); t < T; t += nwarps) {
-    int my_r;
-    float my_w;
-    if (!token_rows(dest, w, t, k, R, lane, my_r, my_w, ws, 11)) continue;
+    int rows[K];
+    float wj[K];
+    if (!token_rows<K>(dest, w, t, k, R, lane, rows, wj, ws, 11)) continue;
     for (int v = lane; v < hv; v += 32) {
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int j = 0; j < k; ++j) {
-        const int r = __shfl_sync(0xffffffffu, my_r, j);
-        const float wj = __shfl_sync(0xffffffffu, my_w, j);
-        float y[8];
-        unpack8(ldg_nc(Y + static_cast<size_t>(r) * hv + v), y);
+      uint4 y[K];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, y[i], acc[i]);
+      for (int j = 0; j < K; ++j)
+        if (j < k) y[j] = ldg_nc(Y + static_cast<size_t>(rows[j]) * hv + v);
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < K; ++j) {
+        if (j < k) {
+          float f[8];
+          unpack8(y[j], f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[j], f[i], acc[i]);
+        }
       }
       out[static_cast<size_t>(t) * hv + v] = pack8(acc);
     }
   }
 }
 
+// dY[dest[t,j]] = bf16(w[t,j] dout[t]); dgate[t,j] = <dout[t], Y[dest[t,j]]>.
+// Each lane accumulates its columns in order; the lanes' partial sums are then
+// combined by a fixed butterfly, so the result does not depend on the grid.
+template <int K>
 __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(const uint4* __restrict__ dout,
                                                                  const uint4* __restrict__ Y,
                                                                  const int32_t* __restrict__ dest,
@@ -122,35 +140,45 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(const uint4* __re
   const int lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * (kThreads / 32);
   for (int t = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); t < T; t += nwarps) {
-    int my_r;
-    float my_w;
-    if (!token_rows(dest, w, t, k, R, lane, my_r, my_w, ws, 12)) continue;
-    // Lane-partial dot products, one per slot; the dot of slot j is
-    // accumulated by lane j's register after the loop.
-    float my_dot = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const int r = __shfl_sync(0xffffffffu, my_r, j);
-      const float wj = __shfl_sync(0xffffffffu, my_w, j);
-      float part = 0.f;
-      for (int v = lane; v < hv; v += 32) {
-        float d[8], y[8], g[8];
-        unpack8(ldg_nc(dout + static_cast<size_t>(t) * hv + v), d);
-        unpack8(ldg_nc(Y + static_cast<size_t>(r) * hv + v), y);
+    int rows[K];
+    float wj[K];
+    if (!token_rows<K>(dest, w, t, k, R, lane, rows, wj, ws, 12)) continue;
+    float part[K];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          part = fmaf(d[i], y[i], part);
-          g[i] = wj * d[i];
+    for (int j = 0; j < K; ++j) part[j] = 0.f;
+    for (int v = lane; v < hv; v += 32) {
+      float d[8];
+      unpack8(ldg_nc(dout + static_cast<size_t>(t) * hv + v), d);
+      uint4 y[K];
+#pragma unroll
+      for (int j = 0; j < K; ++j)
+        if (j < k) y[j] = ldg_nc(Y + static_cast<size_t>(rows[j]) * hv + v);
+#pragma unroll
+      for (int j = 0; j < K; ++j) {
+        if (j < k) {
+          float f[8], g[8];
+          unpack8(y[j], f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            part[j] = fmaf(d[i], f[i], part[j]);
+            g[i] = wj[j] * d[i];
+          }
+          dY[static_cast<size_t>(rows[j]) * hv + v] = pack8(g);
         }
-        dY[static_cast<size_t>(r) * hv + v] = pack8(g);
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-      if (lane == j) my_dot = part;
     }
-    if (lane < k) dgate[static_cast<size_t>(t) * k + lane] = my_dot;
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+      float s = part[j];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      if (j < k && lane == 0) dgate[static_cast<size_t>(t) * k + j] = s;
+    }
   }
 }
 
+// dx[t] = bf16(sum_j dXp[dest[t,j]]), slots in ascending order.
+template <int K>
 __global__ void __launch_bounds__(kThreads) unpermute_kernel(const uint4* __restrict__ dXp,
                                                                const int32_t* __restrict__ dest,
                                                                uint4* __restrict__ dx, int T, int k, int R, int hv,
@@ -158,17 +186,23 @@ __global__ void __launch_bounds__(kThreads) unpermute_kernel(const uint4* __rest
   const int lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * (kThreads / 32);
   for (int t = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); t < T; t += nwarps) {
-    int my_r;
-    float my_w;
-    if (!token_rows(dest, nullptr, t, k, R, lane, my_r, my_w, ws, 13)) continue;
+    int rows[K];
+    float wj[K];
+    if (!token_rows<K>(dest, nullptr, t, k, R, lane, rows, wj, ws, 13)) continue;
     for (int v = lane; v < hv; v += 32) {
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int j = 0; j < k; ++j) {
-        const int r = __shfl_sync(0xffffffffu, my_r, j);
-        float y[8];
-        unpack8(ldg_nc(dXp + static_cast<size_t>(r) * hv + v), y);
+      uint4 y[K];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] += y[i];
+      for (int j = 0; j < K; ++j)
+        if (j < k) y[j] = ldg_nc(dXp + static_cast<size_t>(rows[j]) * hv + v);
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < K; ++j) {
+        if (j < k) {
+          float f[8];
+          unpack8(y[j], f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] += f[i];
+        }
       }
       dx[static_cast<size_t>(t) * hv + v] = pack8(acc);
     }
@@ -187,8 +221,12 @@ cudaError_t launch_gather(const RowsLaunch& p, const void* x, void* Xp, cudaStre
 
 cudaError_t launch_combine(const RowsLaunch& p, const void* Y, void* out, cudaStream_t s, LaunchHook& hook) {
   hook.before(s);
-  combine_kernel<<<p.grid, kThreads, 0, s>>>(static_cast<const uint4*>(Y), p.dest, p.w, static_cast<uint4*>(out),
-                                              p.T, p.k, p.R, p.H / 8, p.ws);
+  if (p.k <= 8)
+    combine_kernel<8><<<p.grid, kThreads, 0, s>>>(static_cast<const uint4*>(Y), p.dest, p.w,
+                                                   static_cast<uint4*>(out), p.T, p.k, p.R, p.H / 8, p.ws);
+  else
+    combine_kernel<kMaxK><<<p.grid, kThreads, 0, s>>>(static_cast<const uint4*>(Y), p.dest, p.w,
+                                                       static_cast<uint4*>(out), p.T, p.k, p.R, p.H / 8, p.ws);
   hook.after(s);
   return cudaGetLastError();
 }
@@ -196,17 +234,27 @@ cudaError_t launch_combine(const RowsLaunch& p, const void* Y, void* out, cudaSt
 cudaError_t launch_combine_bwd(const RowsLaunch& p, const void* dout, const void* Y, void* dY, float* dgate,
                                cudaStream_t s, LaunchHook& hook) {
   hook.before(s);
-  combine_bwd_kernel<<<p.grid, kThreads, 0, s>>>(static_cast<const uint4*>(dout), static_cast<const uint4*>(Y),
-                                                  p.dest, p.w, static_cast<uint4*>(dY), dgate, p.T, p.k, p.R,
-                                                  p.H / 8, p.ws);
+  if (p.k <= 8)
+    combine_bwd_kernel<8><<<p.grid, kThreads, 0, s>>>(static_cast<const uint4*>(dout), static_cast<const uint4*>(Y),
+                                                       p.dest, p.w, static_cast<uint4*>(dY), dgate, p.T, p.k, p.R,
+                                                       p.H / 8, p.ws);
+  else
+    combine_bwd_kernel<kMaxK><<<p.grid, kThreads, 0, s>>>(static_cast<const uint4*>(dout),
+                                                           static_cast<const uint4*>(Y), p.dest, p.w,
+                                                           static_cast<uint4*>(dY), dgate, p.T, p.k, p.R, p.H / 8,
+                                                           p.ws);
   hook.after(s);
   return cudaGetLastError();
 }
 
 cudaError_t launch_unpermute(const RowsLaunch& p, const void* dXp, void* dx, cudaStream_t s, LaunchHook& hook) {
   hook.before(s);
-  unpermute_kernel<<<p.grid, kThreads, 0, s>>>(static_cast<const uint4*>(dXp), p.dest, static_cast<uint4*>(dx),
-                                                p.T, p.k, p.R, p.H / 8, p.ws);
+  if (p.k <= 8)
+    unpermute_kernel<8><<<p.grid, kThreads, 0, s>>>(static_cast<const uint4*>(dXp), p.dest,
+                                                     static_cast<uint4*>(dx), p.T, p.k, p.R, p.H / 8, p.ws);
+  else
+    unpermute_kernel<kMaxK><<<p.grid, kThreads, 0, s>>>(static_cast<const uint4*>(dXp), p.dest,
+                                                         static_cast<uint4*>(dx), p.T, p.k, p.R, p.H / 8, p.ws);
   hook.after(s);
   return cudaGetLastError();
 }
