@@ -36,8 +36,10 @@ if ROOT not in sys.path:
 METRIC = "MoE-layer tokens/s fwd+bwd; GEMM % BF16 peak; permute GB/s % HBM"
 UNIT = "tokens/s"
 
-FWD_KERNELS = ["gather_rows", "gemm_fwd1_swiglu", "gemm_fwd2", "combine"]
+FWD_KERNELS = ["fused_forward", "combine"]
+FWD_KERNELS_PHASED = ["gather_rows", "gemm_fwd1_swiglu", "gemm_fwd2", "combine"]
 BWD_KERNELS = ["combine_bwd", "gemm_dgrad2_swiglu_bwd", "gemm_dgrad1", "gemm_wgrad13", "gemm_wgrad2", "unpermute"]
+BWD_KERNELS_FUSED = ["combine_bwd", "fused_backward", "unpermute"]
 N_PLAN_KERNELS = 3
 
 
@@ -57,7 +59,14 @@ def work_per_kernel(T, H, F, E, k):
         "gemm_wgrad2": 2 * R * F + 2 * R * H + 4 * E * H * F,
         "unpermute": 2 * R * H + 2 * T * H + 4 * R,
     }
+    # Fused forward: reads x, row_src and every weight once; writes Xp, GU, h and Y.
+    b["fused_forward"] = 2 * T * H + 4 * R + 6 * E * H * F + 2 * R * H + 6 * R * F + 2 * R * H
+    # Fused backward: reads dY, GU, Xp, h and every weight once; writes dGU, dXp and dW1, dW3, dW2 (fp32).
+    b["fused_backward"] = (2 * R * H + 4 * R * F + 2 * R * H + 2 * R * F + 6 * E * H * F
+                           + 4 * R * F + 2 * R * H + 12 * E * H * F)
     f = {
+        "fused_forward": 6 * R * H * F,
+        "fused_backward": 12 * R * H * F,
         "gemm_fwd1_swiglu": 4 * R * H * F,
         "gemm_fwd2": 2 * R * H * F,
         "gemm_dgrad2_swiglu_bwd": 2 * R * H * F,
@@ -280,9 +289,14 @@ def run_ours(args):
     inp = S.layer_inputs(shape, seed, device=dev)
     layer = MoELayer(T, H, F, E, k, device=dev)
     stream = torch.cuda.current_stream(dev)
-    nf, nb = len(FWD_KERNELS), len(BWD_KERNELS)
+    fwd_names = FWD_KERNELS_PHASED if args.schedule == 1 else FWD_KERNELS
+    bwd_names = BWD_KERNELS_FUSED if args.schedule == 2 else BWD_KERNELS
+    nf, nb = len(fwd_names), len(bwd_names)
+    base_opts = layer.opts(schedule=args.schedule)
 
     def step(opts_f=None, opts_b=None, ev_plan=None):
+        opts_f = opts_f if opts_f is not None else base_opts
+        opts_b = opts_b if opts_b is not None else base_opts
         if ev_plan is not None:
             ev_plan[0].record(stream)
         layer.plan(inp["logits"])
@@ -319,12 +333,12 @@ def run_ours(args):
     opts_f = []
     keep = []
     for e in evs_f:
-        o = layer.opts(events=e)
+        o = layer.opts(events=e, schedule=args.schedule)
         keep.append(layer._ev_keep)
         opts_f.append(o)
     opts_b = []
     for e in evs_b:
-        o = layer.opts(events=e)
+        o = layer.opts(events=e, schedule=args.schedule)
         keep.append(layer._ev_keep)
         opts_b.append(o)
 
@@ -351,13 +365,13 @@ def run_ours(args):
         raise RuntimeError(f"device status {st}")
 
     # Per-kernel average durations.
-    names = ["plan"] + FWD_KERNELS + BWD_KERNELS
+    names = ["plan"] + fwd_names + bwd_names
     per = {n: 0.0 for n in names}
     for i in range(args.steps):
         per["plan"] += evs_p[i][0].elapsed_time(evs_p[i][1])
-        for j, n in enumerate(FWD_KERNELS):
+        for j, n in enumerate(fwd_names):
             per[n] += evs_f[i][2 * j].elapsed_time(evs_f[i][2 * j + 1])
-        for j, n in enumerate(BWD_KERNELS):
+        for j, n in enumerate(bwd_names):
             per[n] += evs_b[i][2 * j].elapsed_time(evs_b[i][2 * j + 1])
     per = {n: v / args.steps for n, v in per.items()}
     flops, bytes_ = work_per_kernel(T, H, F, E, k)
@@ -409,8 +423,8 @@ def run_ours(args):
         d_lg.copy_(h_lg, non_blocking=True)
         d_do.copy_(h_do, non_blocking=True)
         layer.plan(d_lg)
-        layer.forward(d_x, inp["W1"], inp["W3"], inp["W2"])
-        layer.backward(d_do, inp["W1"], inp["W3"], inp["W2"])
+        layer.forward(d_x, inp["W1"], inp["W3"], inp["W2"], opts=base_opts)
+        layer.backward(d_do, inp["W1"], inp["W3"], inp["W2"], opts=base_opts)
         h_out.copy_(layer.out, non_blocking=True)
         h_dx.copy_(layer.dx, non_blocking=True)
 
@@ -435,7 +449,9 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(workload_config(shape, args.config), parallelism=f"replicas x{world}" if world > 1 else "1 GPU"),
+        "config": dict(workload_config(shape, args.config), parallelism=f"replicas x{world}" if world > 1 else "1 GPU",
+                       schedule={0: "fused forward, per-GEMM backward", 1: "one launch per phase",
+                                 2: "fused forward, fused backward"}[args.schedule]),
         "roofline": roof,
         "e2e": {"value": round(world * T * args.steps / (e2e_ms * 1e-3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -475,6 +491,9 @@ def main():
     ap.add_argument("--config", type=int, default=1)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--schedule", type=int, default=0, choices=[0, 1, 2],
+                    help="0: fused persistent forward, one persistent kernel per backward GEMM; "
+                         "1: one launch per phase; 2: fused forward and fused backward")
     ap.add_argument("--profile", action="store_true",
                     help="run the warm-up steps and one more step only (for ncu captures)")
     args = ap.parse_args()

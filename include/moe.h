@@ -98,7 +98,12 @@ typedef struct {
 /* Options (may be NULL for defaults). */
 typedef struct {
   int32_t grid;     /* CTAs of the persistent kernels; 0 = one per SM.  Results do not depend on it. */
-  int32_t reserved; /* must be 0 */
+  int32_t schedule; /* 0 (default): the forward's gather, GEMM1 and GEMM2 run as one persistent
+                       kernel with a task cursor and per-tile readiness counters; the backward's
+                       four GEMMs run as four persistent kernels.
+                       1: one launch per phase in both passes.
+                       2: as 0, and the backward's four GEMMs also run as one persistent kernel.
+                       All three give the same bits. */
   void **events;    /* optional: 2*n_events cudaEvent_t recorded around each kernel of the call */
   int32_t n_events; /* capacity of events/2; kernels beyond it are not timed */
   int32_t reserved2;
@@ -107,7 +112,8 @@ typedef struct {
 /* ---- sizes ------------------------------------------------------------------ */
 
 /* Bytes of the scratch workspace every call of one step needs (status word,
- * per-chunk counts and bitmaps of the routing, task cursors).  Caller-allocated;
+ * per-chunk counts and bitmaps of the routing, task cursor and per-tile
+ * readiness counters of the persistent kernels).  Caller-allocated;
  * pass the same workspace to moe_plan, moe_forward and moe_backward of a step.
  * Returns 0 for invalid dims. */
 MOE_API size_t moe_workspace_bytes(moe_dims d);
@@ -184,10 +190,11 @@ MOE_API int moe_clear_status(void *ws, void *stream);
  *   - Set-up: the first call on each device looks up the array's device
  *     address (with that device current) and caches it; make that first call
  *     before any stream capture.
- *   - Every call uses the same array and leaves its contents behind; the
- *     kernels overwrite every scratch word before reading it, so nothing has to
- *     start at zero.  Calls that overlap on the GPU (on different streams, or
- *     from different threads) race on the array: serialise them.
+ *   - Every call uses the same array and leaves its contents behind; each
+ *     call clears the words that must start at zero (the per-chunk counts)
+ *     with an asynchronous memset on `stream` before its kernels run.  Calls
+ *     that overlap on the GPU (on different streams, or from different
+ *     threads) race on the array: serialise them.
  * Other arguments and errors as moe_plan. */
 MOE_API int moe_plan_noalloc(moe_dims d, const float *logits, const moe_plan_t *plan, int32_t *status, void *stream);
 
@@ -196,7 +203,8 @@ MOE_API const char *moe_strerror(int code);
 MOE_API int32_t moe_version(void);
 /* Number of kernels this library has launched in this process. */
 MOE_API uint64_t moe_launch_count(void);
-/* Name of the i-th kernel a call launches (call: 0 plan, 1 forward, 2 backward); NULL past the end. */
+/* Name of the i-th kernel a call launches (call: 0 plan, 1 forward, 2 backward, 3 forward with
+ * schedule = 1, 4 backward with schedule = 2); NULL past the end. */
 MOE_API const char *moe_kernel_name(int32_t call, int32_t i);
 
 #ifdef __cplusplus

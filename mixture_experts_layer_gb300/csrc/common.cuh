@@ -149,6 +149,56 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Generic-proxy data made visible GPU-wide by other threads, ordered before
+// this thread's later async-proxy (TMA) reads of global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ int ld_relaxed_gpu(const int32_t* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Scoreboard wait: spins until *c >= target.  The common case -- the
+// dependency finished long ago -- costs one relaxed load and an acquire fence.
+// Bounded like mbar_wait.
+__device__ __forceinline__ bool wait_counter(const int32_t* c, int target, WsHeader* ws, int where,
+                                             volatile int* abort_flag) {
+  if (ld_relaxed_gpu(c) >= target) {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    return true;
+  }
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    for (int i = 0; i < 8; ++i) {
+      __nanosleep(64);
+      if (ld_acquire_gpu(c) >= target) return true;
+    }
+    if (abort_flag != nullptr && *abort_flag) return false;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      report(ws, MOE_ERR_TIMEOUT, where, target);
+      if (abort_flag != nullptr) *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+// Scoreboard signal from one warp: every lane's earlier global stores become
+// visible GPU-wide before lane 0 bumps the counter.
+__device__ __forceinline__ void signal_counter(int32_t* c, int lane) {
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) atomicAdd(c, 1);
+}
+
 // ---------------------------------------------------------------------------
 // tcgen05: tensor memory, MMA, commit, load.
 // ---------------------------------------------------------------------------

@@ -98,6 +98,7 @@ struct Tile {
   int n0;     // first output column
   int nw;     // MMA N of the tile: 256, or 128 for a tail tile
   int kblocks;
+  int mt;     // forward/dgrad: index of the 128-row tile in the plan's tile table
 };
 
 template <int MODE>
@@ -133,6 +134,7 @@ __device__ __forceinline__ Tile decode(const GemmParams& p, int tile) {
     t.row0 = __ldg(p.offsets + t.e);
     t.nrows = __ldg(p.counts + t.e);
     t.kblocks = (t.nrows + BK - 1) / BK;
+    t.mt = -1;
   } else {
     const int entries = tiles_entry_base(p.E);
     const int4* ent = reinterpret_cast<const int4*>(p.tiles + entries);
@@ -150,6 +152,7 @@ __device__ __forceinline__ Tile decode(const GemmParams& p, int tile) {
     t.row0 = en.y;
     t.nrows = en.z;
     t.m0 = 0;
+    t.mt = mt;
     const int K = (MODE == kFwd1 || MODE == kDgrad2) ? p.H : (MODE == kFwd2) ? p.F : 2 * p.F;
     t.kblocks = K / BK;
   }
@@ -217,14 +220,6 @@ __device__ __forceinline__ uint4 ld_v4(const void* p) {
   return v;
 }
 
-// Stores 32 fp32 accumulator values of one row as bf16 (64 bytes).
-__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* v) {
-#pragma unroll
-  for (int i = 0; i < 32; i += 8)
-    st_v4(dst + i, pack_bf16x2(v[i], v[i + 1]), pack_bf16x2(v[i + 2], v[i + 3]), pack_bf16x2(v[i + 4], v[i + 5]),
-          pack_bf16x2(v[i + 6], v[i + 7]));
-}
-
 __device__ __forceinline__ void store_zero_f32(float* dst) {
 #pragma unroll
   for (int i = 0; i < 32; i += 4) st_v4(dst + i, 0u, 0u, 0u, 0u);
@@ -255,6 +250,26 @@ struct OutStager {
   }
 };
 
+// Weight-gradient K tail: the last k-block of an expert holds `valid` < 64 of
+// its rows.  The MMAs cover ceil(valid/16)*16 rows; the rows in between that
+// belong to the next expert are cleared in both operands (A: 2 panels, B: nw/64
+// panels), so neither stale values nor the next expert's rows contribute.
+__device__ __forceinline__ int clear_k_tail(uint8_t* sA, uint8_t* sB, int valid, int nw, int lane) {
+  const int nkk = (valid + 15) >> 4;
+  const int nz = nkk * 16 - valid;  // < 16 rows
+  const int panels = 2 + nw / 64;
+  // Lane -> (row offset lane / 8, 16-byte chunk lane % 8); 4 rows per pass.
+  for (int r = valid + (lane >> 3); r < valid + nz; r += 4) {
+    const int off = r * 128 + (lane & 7) * 16;
+    for (int pnl = 0; pnl < panels; ++pnl) {
+      uint8_t* base = pnl < 2 ? sA + pnl * kPanelBytes : sB + (pnl - 2) * kPanelBytes;
+      *reinterpret_cast<uint4*>(base + off) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  fence_proxy_async_smem();
+  return nkk;
+}
+
 template <int MODE>
 __device__ __forceinline__ void epilogue(const GemmParams& p, const Maps& m, const Tile& t, uint32_t tacc, int q,
                                          int half, int lane, OutStager& st) {
@@ -264,32 +279,28 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, const Maps& m, con
   const int c_lo = half * (NCall / 2), c_hi = c_lo + NCall / 2;
   if (ModeTraits<MODE>::wgrad) {
     const int y = (MODE == kWgrad13) ? t.e * p.H + t.m0 + q * 32 : t.e * p.F + t.m0 + q * 32;
-    uint32_t a0[32], a1[32];
-    tc_ld_32x32b_x32(tacc + c_lo, a0);
-    if (MODE == kWgrad13) tc_ld_32x32b_x32(tacc + 128 + c_lo, a1);
-    tc_wait_ld();
 #pragma unroll 1
-    for (int c = c_lo; c < c_hi; c += 32) {
-      const bool more = c + 32 < c_hi;
-      uint32_t b0[32], b1[32];
-      if (more) {  // next chunk's accumulator load overlaps this chunk's stores
-        tc_ld_32x32b_x32(tacc + c + 32, b0);
-        if (MODE == kWgrad13) tc_ld_32x32b_x32(tacc + 128 + c + 32, b1);
-      }
-      st.put(&m.o0, a0, t.n0 + c, y, lane);
-      if (MODE == kWgrad13) st.put(&m.o1, a1, t.n0 + c, y, lane);
-      if (more) {
-        tc_wait_ld();
+    for (int out = 0; out < ((MODE == kWgrad13) ? 2 : 1); ++out) {
+      const CUtensorMap* map = out ? &m.o1 : &m.o0;
+      const uint32_t tbase = tacc + (out ? 128 : 0);
+      uint32_t a[32];
+      tc_ld_32x32b_x32(tbase + c_lo, a);
+      tc_wait_ld();
+#pragma unroll 1
+      for (int c = c_lo; c < c_hi; c += 32) {
+        const bool more = c + 32 < c_hi;
+        uint32_t b[32];
+        if (more) tc_ld_32x32b_x32(tbase + c + 32, b);  // next chunk in flight during this chunk's stores
+        st.put(map, a, t.n0 + c, y, lane);
+        if (more) {
+          tc_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          a0[i] = b0[i];
-          if (MODE == kWgrad13) a1[i] = b1[i];
+          for (int i = 0; i < 32; ++i) a[i] = b[i];
         }
       }
     }
     return;
   }
-  const int NC = c_hi;
   const bool valid = row < t.nrows;
   const size_t grow = static_cast<size_t>(t.row0) + row;
   uint4 gcur[4], ucur[4];
@@ -302,25 +313,30 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, const Maps& m, con
     }
   }
 #pragma unroll 1
-  for (int c = c_lo; c < NC; c += 32) {
+  for (int c = c_lo; c < c_hi; c += 32) {
     if (MODE == kFwd1) {
       uint32_t g[32], u[32];
       tc_ld_32x32b_x32(tacc + c, g);
       tc_ld_32x32b_x32(tacc + 128 + c, u);
       tc_wait_ld();
       if (valid) {
-        float hv[32], gv[32], uv[32];
+        uint32_t hw[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float a = __uint_as_float(g[i]);
-          const float b = __uint_as_float(u[i]);
-          hv[i] = a * __frcp_rn(1.0f + expf(-a)) * b;
-          gv[i] = a;
-          uv[i] = b;
+        for (int i = 0; i < 16; ++i) {
+          const float a0 = __uint_as_float(g[2 * i]), a1 = __uint_as_float(g[2 * i + 1]);
+          const float b0 = __uint_as_float(u[2 * i]), b1 = __uint_as_float(u[2 * i + 1]);
+          hw[i] = pack_bf16x2(a0 * __frcp_rn(1.0f + expf(-a0)) * b0, a1 * __frcp_rn(1.0f + expf(-a1)) * b1);
+          g[i] = pack_bf16x2(a0, a1);  // G, U packed in place (entries i < 16 are no longer needed)
+          u[i] = pack_bf16x2(b0, b1);
         }
-        store_row_bf16(p.out0 + grow * p.F + t.n0 + c, hv);
-        store_row_bf16(p.out1 + grow * (2 * p.F) + t.n0 + c, gv);
-        store_row_bf16(p.out1 + grow * (2 * p.F) + p.F + t.n0 + c, uv);
+        __nv_bfloat16* hdst = p.out0 + grow * p.F + t.n0 + c;
+        __nv_bfloat16* gdst = p.out1 + grow * (2 * p.F) + t.n0 + c;
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) st_v4(hdst + 2 * i, hw[i], hw[i + 1], hw[i + 2], hw[i + 3]);
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) st_v4(gdst + 2 * i, g[i], g[i + 1], g[i + 2], g[i + 3]);
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) st_v4(gdst + p.F + 2 * i, u[i], u[i + 1], u[i + 2], u[i + 3]);
       }
     } else if (MODE == kDgrad2) {
       // G and U of this row are read from global memory; the loads of the
@@ -328,7 +344,7 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, const Maps& m, con
       uint32_t d[32];
       tc_ld_32x32b_x32(tacc + c, d);
       uint4 gn[4], un[4];
-      if (valid && c + 32 < NC) {
+      if (valid && c + 32 < c_hi) {
         const __nv_bfloat16* gsrc = p.aux + grow * (2 * p.F) + t.n0 + c + 32;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -338,27 +354,30 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, const Maps& m, con
       }
       tc_wait_ld();
       if (valid) {
-        float dg[32], du[32];
+        __nv_bfloat16* ddst = p.out0 + grow * (2 * p.F) + t.n0 + c;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const uint32_t gw[4] = {gcur[i].x, gcur[i].y, gcur[i].z, gcur[i].w};
           const uint32_t uw[4] = {ucur[i].x, ucur[i].y, ucur[i].z, ucur[i].w};
+          uint32_t dgw[4], duw[4];
 #pragma unroll
           for (int qq = 0; qq < 4; ++qq) {
+            float dg2[2], du2[2];
 #pragma unroll
             for (int hbit = 0; hbit < 2; ++hbit) {
-              const int ii = 8 * i + 2 * qq + hbit;
               const float G = hbit ? bf16hi(gw[qq]) : bf16lo(gw[qq]);
               const float U = hbit ? bf16hi(uw[qq]) : bf16lo(uw[qq]);
-              const float dh = __uint_as_float(d[ii]);
+              const float dh = __uint_as_float(d[8 * i + 2 * qq + hbit]);
               const float sg = __frcp_rn(1.0f + expf(-G));
-              dg[ii] = dh * U * sg * (1.0f + G * (1.0f - sg));
-              du[ii] = dh * G * sg;
+              dg2[hbit] = dh * U * sg * (1.0f + G * (1.0f - sg));
+              du2[hbit] = dh * G * sg;
             }
+            dgw[qq] = pack_bf16x2(dg2[0], dg2[1]);
+            duw[qq] = pack_bf16x2(du2[0], du2[1]);
           }
+          st_v4(ddst + 8 * i, dgw[0], dgw[1], dgw[2], dgw[3]);
+          st_v4(ddst + p.F + 8 * i, duw[0], duw[1], duw[2], duw[3]);
         }
-        store_row_bf16(p.out0 + grow * (2 * p.F) + t.n0 + c, dg);
-        store_row_bf16(p.out0 + grow * (2 * p.F) + p.F + t.n0 + c, du);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           gcur[i] = gn[i];
@@ -370,10 +389,13 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, const Maps& m, con
       tc_ld_32x32b_x32(tacc + c, d);
       tc_wait_ld();
       if (valid) {
-        float v[32];
+        __nv_bfloat16* dst = p.out0 + grow * p.H + t.n0 + c;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(d[i]);
-        store_row_bf16(p.out0 + grow * p.H + t.n0 + c, v);
+        for (int i = 0; i < 32; i += 8)
+          st_v4(dst + i, pack_bf16x2(__uint_as_float(d[i]), __uint_as_float(d[i + 1])),
+                pack_bf16x2(__uint_as_float(d[i + 2]), __uint_as_float(d[i + 3])),
+                pack_bf16x2(__uint_as_float(d[i + 4]), __uint_as_float(d[i + 5])),
+                pack_bf16x2(__uint_as_float(d[i + 6]), __uint_as_float(d[i + 7])));
       }
     }
   }
@@ -482,21 +504,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         uint8_t* sA = smem + s * kStageBytes;
         uint8_t* sB = sA + kABytes;
         // The expert's last k-block (weight gradients) may run past its rows:
-        // only the K steps of 16 that hold valid rows are issued, and inside
-        // the last of them the rows past the expert are zeroed in operand A, so
-        // rows of the next expert (finite values in B) add nothing.
+        // only the K steps of 16 that hold valid rows are issued (clear_k_tail).
         int nkk = BK / 16;
         if (TR::wgrad) {
           const int valid = t.nrows - kb * BK;
-          if (valid < BK) {
-            nkk = (valid + 15) >> 4;
-            const int z0 = valid, nz = nkk * 16 - valid;  // < 16 rows to clear
-            for (int i = lane; i < nz * 16; i += 32) {
-              const int r = z0 + (i >> 4), panel = (i >> 3) & 1, chunk = i & 7;
-              *reinterpret_cast<uint4*>(sA + panel * kPanelBytes + r * 128 + chunk * 16) = make_uint4(0u, 0u, 0u, 0u);
-            }
-            fence_proxy_async_smem();
-          }
+          if (valid < BK) nkk = clear_k_tail(sA, sB, valid, t.nw, lane);
           __syncwarp();
         }
         if (elect_one()) {
@@ -570,6 +582,639 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 }
 
 // ---------------------------------------------------------------------------
+// Fused persistent forward: dispatch row gathers, GEMM1 (+SwiGLU) tiles and
+// GEMM2 tiles in one launch.
+//
+// "UniEP: Unified Expert-Parallel MoE MegaKernel for LLM Training", section 3:
+// persistent workers (one CTA per SM) take tasks from a global atomic cursor
+// over a linearised task space -- dispatch tasks first, then computation tasks
+// (here: row gathers, then GEMM1 tiles, then GEMM2 tiles, each in ascending
+// expert order, the priority order of section 4) -- and a scoreboard in global
+// memory says when a computation may start: a GEMM1 tile once its 128 rows are
+// gathered, a GEMM2 tile once every GEMM1 tile of its rows has stored h.  A task
+// waits only on tasks with smaller indices, which running CTAs have already
+// taken, so progress never needs every CTA to be resident.
+//
+// Inside a CTA the producer warp takes the tasks and hands them to the MMA warp
+// and the epilogue warps through a small ring in shared memory.  The epilogue
+// warps also execute the gather tasks (one warp per row, 16-byte vectors).
+// ---------------------------------------------------------------------------
+constexpr int kTaskRing = 4;
+constexpr int kTaskEnd = -1;
+constexpr int kTaskGather = -2;
+
+struct FusedFwdParams {
+  GemmParams p1;  // GEMM1: out0 = h, out1 = GU
+  GemmParams p2;  // GEMM2: out0 = Y
+  const uint4* x;
+  uint4* Xp;
+  const int32_t* row_src;
+  int T;
+  int32_t* cursor;
+  int32_t* cnt_gather;  // per 128-row tile: epilogue warps done gathering its rows
+  int32_t* cnt_g1;      // per 128-row tile: GEMM1 epilogue warps done storing h
+};
+
+struct FusedFwdMaps {
+  Maps g1;
+  Maps g2;
+};
+
+struct FwdTask {
+  int kind;  // kTaskGather, kFwd1 or kFwd2
+  Tile t;
+};
+
+__device__ __forceinline__ FwdTask fwd_decode(const FusedFwdParams& f, int task) {
+  const int nmt = __ldg(f.p1.tiles);
+  const int nn1 = f.p1.F / 128;
+  FwdTask k;
+  if (task < nmt) {
+    const int4 en = __ldg(reinterpret_cast<const int4*>(f.p1.tiles + tiles_entry_base(f.p1.E)) + task);
+    k.kind = kTaskGather;
+    k.t.e = en.x;
+    k.t.row0 = en.y;
+    k.t.nrows = en.z;
+    k.t.mt = task;
+    k.t.m0 = k.t.n0 = k.t.nw = k.t.kblocks = 0;
+  } else if (task < nmt * (1 + nn1)) {
+    k.kind = kFwd1;
+    k.t = decode<kFwd1>(f.p1, task - nmt);
+  } else {
+    k.kind = kFwd2;
+    k.t = decode<kFwd2>(f.p2, task - nmt * (1 + nn1));
+  }
+  return k;
+}
+
+__device__ __forceinline__ uint4 ld_nc_v4(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Dispatch of one 128-row tile by one epilogue warp (rows ew, ew+8, ...):
+// Xp[r] = x[row_src[r]] ("MoonEP": zero-copy dispatch into the expert-grouped layout).
+__device__ __forceinline__ void gather_rows_task(const FusedFwdParams& f, const Tile& t, int ew, int lane) {
+  const int hv = f.p1.H / 8;
+  for (int i = ew; i < t.nrows; i += kEpiWarps) {
+    const int r = t.row0 + i;
+    const int tok = __ldg(f.row_src + r);
+    if (tok < 0 || tok >= f.T) {
+      if (lane == 0) report(f.p1.ws, MOE_ERR_BOUNDS, 20, r);
+      continue;
+    }
+    const uint4* src = f.x + static_cast<size_t>(tok) * hv;
+    uint4* dst = f.Xp + static_cast<size_t>(r) * hv;
+    int v = lane;
+    for (; v + 96 < hv; v += 128) {
+      const uint4 a = ld_nc_v4(src + v), b = ld_nc_v4(src + v + 32), c = ld_nc_v4(src + v + 64),
+                  d = ld_nc_v4(src + v + 96);
+      dst[v] = a;
+      dst[v + 32] = b;
+      dst[v + 64] = c;
+      dst[v + 96] = d;
+    }
+    for (; v < hv; v += 32) dst[v] = ld_nc_v4(src + v);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) fused_forward_kernel(const __grid_constant__ FusedFwdMaps maps,
+                                                                    const FusedFwdParams f) {
+  constexpr int S = 4;
+  constexpr uint32_t kIdesc256 = idesc_bf16_f32(BM, 256, false, true);
+  constexpr uint32_t kIdesc128 = idesc_bf16_f32(BM, 128, false, true);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * kStageBytes);
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* rfull = tempty + 2;
+  uint64_t* rempty = rfull + kTaskRing;
+  volatile int* ring = reinterpret_cast<volatile int*>(rempty + kTaskRing);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(ring) + kTaskRing);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  WsHeader* ws = f.p1.ws;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], kEpiWarps);
+    }
+    for (int i = 0; i < kTaskRing; ++i) {
+      mbar_init(&rfull[i], 1);
+      mbar_init(&rempty[i], 1 + kEpiWarps);
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int nmt = __ldg(f.p1.tiles);
+  const int nn1 = f.p1.F / 128;
+  const int nn2 = (f.p1.H + BN - 1) / BN;
+  const int total = nmt * (1 + nn1 + nn2);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer + task fetch
+    int s = 0, slot = 0;
+    uint32_t ph = 0, rph = 0;
+    uint32_t issued = 0, last_parity = 0;
+    // The next task id is fetched one task ahead, so the atomic's round trip
+    // overlaps the current task's work.
+    int next = (lane == 0) ? atomicAdd(f.cursor, 1) : 0;
+    while (true) {
+      if (!mbar_wait(&rempty[slot], rph ^ 1u, ws, 150, abort_flag)) break;
+      int task = 0;
+      if (lane == 0) {
+        task = next;
+        if (task >= total || *abort_flag) task = kTaskEnd;
+        if (task != kTaskEnd) next = atomicAdd(f.cursor, 1);
+        ring[slot] = task;
+      }
+      task = __shfl_sync(0xffffffffu, task, 0);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rfull[slot]);
+      if (++slot == kTaskRing) {
+        slot = 0;
+        rph ^= 1u;
+      }
+      if (task == kTaskEnd) break;
+      const FwdTask k = fwd_decode(f, task);
+      if (k.kind == kTaskGather) continue;
+      // Scoreboard: the tile's input rows must be complete.
+      const bool g1 = (k.kind == kFwd1);
+      if (!wait_counter(g1 ? f.cnt_gather + k.t.mt : f.cnt_g1 + k.t.mt, g1 ? kEpiWarps : nn1 * kEpiWarps, ws,
+                        g1 ? 151 : 152, abort_flag))
+        continue;  // abort: the consumers see the flag and stop
+      fence_proxy_async_global();
+      for (int kb = 0; kb < k.t.kblocks; ++kb) {
+        if (!mbar_wait(&empty[s], ph ^ 1u, ws, 153, abort_flag)) break;
+        if (elect_one()) {
+          mbar_arrive_expect_tx(&full[s], kABytes + k.t.nw * 128);
+          uint8_t* sA = smem + s * kStageBytes;
+          if (g1)
+            load_kblock<kFwd1>(f.p1, maps.g1, k.t, kb, sA, sA + kABytes, &full[s]);
+          else
+            load_kblock<kFwd2>(f.p2, maps.g2, k.t, kb, sA, sA + kABytes, &full[s]);
+        }
+        __syncwarp();
+        issued |= 1u << s;
+        last_parity = (last_parity & ~(1u << s)) | (ph << s);
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+    for (int i = 0; i < S; ++i)
+      if ((issued >> i) & 1u) mbar_wait(&full[i], (last_parity >> i) & 1u, ws, 154, nullptr);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    int s = 0, slot = 0, acc = 0;
+    uint32_t ph = 0, rph = 0, acc_ph = 0;
+    bool ok = true;
+    while (ok) {
+      if (!mbar_wait(&rfull[slot], rph, ws, 155, abort_flag)) break;
+      const int task = ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rempty[slot]);
+      if (++slot == kTaskRing) {
+        slot = 0;
+        rph ^= 1u;
+      }
+      if (task == kTaskEnd) break;
+      const FwdTask k = fwd_decode(f, task);
+      if (k.kind == kTaskGather) continue;
+      if (!mbar_wait(&tempty[acc], acc_ph ^ 1u, ws, 156, abort_flag)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * kAccStride;
+      const uint32_t idesc = (k.t.nw == 256) ? kIdesc256 : kIdesc128;
+      for (int kb = 0; kb < k.t.kblocks; ++kb) {
+        if (!mbar_wait(&full[s], ph, ws, 157, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (elect_one()) {
+          const uint32_t a0 = smem_u32(smem + s * kStageBytes), b0 = a0 + kABytes;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = smem_desc_sw128(a0 + kk * 32u, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(b0 + kk * 2048u, kPanelBytes, 1024);
+            tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+          }
+          tc_commit(&empty[s]);
+        }
+        __syncwarp();
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (elect_one()) tc_commit(&tfull[acc]);
+      __syncwarp();
+      acc ^= 1;
+      if (acc == 0) acc_ph ^= 1u;
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue + gathers
+    const int ew = warp - 2;
+    const int q = warp & 3;
+    const int half = ew >> 2;
+    OutStager st;  // unused by the forward modes
+    st.buf = nullptr;
+    int slot = 0, acc = 0;
+    uint32_t rph = 0, acc_ph = 0;
+    while (true) {
+      if (!mbar_wait(&rfull[slot], rph, ws, 158, abort_flag)) break;
+      const int task = ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rempty[slot]);
+      if (++slot == kTaskRing) {
+        slot = 0;
+        rph ^= 1u;
+      }
+      if (task == kTaskEnd) break;
+      const FwdTask k = fwd_decode(f, task);
+      if (k.kind == kTaskGather) {
+        gather_rows_task(f, k.t, ew, lane);
+        signal_counter(f.cnt_gather + k.t.mt, lane);
+        continue;
+      }
+      if (!mbar_wait(&tfull[acc], acc_ph, ws, 159, abort_flag)) break;
+      tc_fence_after();
+      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccStride;
+      if (k.kind == kFwd1)
+        epilogue<kFwd1>(f.p1, maps.g1, k.t, tacc, q, half, lane, st);
+      else
+        epilogue<kFwd2>(f.p2, maps.g2, k.t, tacc, q, half, lane, st);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_ph ^= 1u;
+      if (k.kind == kFwd1) signal_counter(f.cnt_g1 + k.t.mt, lane);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// ---------------------------------------------------------------------------
+// Fused persistent backward: dgrad GEMM2 (+SwiGLU backward), dgrad GEMM1 and
+// both weight-gradient Transposed GroupGEMMs in one launch.
+//
+// The weight-gradient tiles are bound by their fp32 stores to HBM, the dgrad
+// tiles by the tensor cores and the operand feed, so the task list interleaves
+// them, expert by expert, with a skew of kBwdSkew experts: stage s holds the
+// dgrad2 tiles of expert s and then the dgrad1, wgrad13 and wgrad2 tiles of
+// expert s - kBwdSkew.  Scoreboard ("UniEP: Unified Expert-Parallel MoE
+// MegaKernel for LLM Training", section 3): a dgrad1 tile needs every dgrad2
+// tile of its 128 rows, a wgrad13 tile needs every dgrad2 tile of its expert;
+// the dgrad2 epilogue warps count themselves done per 128-row tile and per
+// expert.  As in the forward, a task waits only on smaller task indices, and a
+// producer fetches its next task id one task ahead (still in increasing order).
+// ---------------------------------------------------------------------------
+constexpr int kBwdSkew = 2;
+constexpr int kBwdStages = 3;
+
+struct FusedBwdParams {
+  GemmParams d2;   // out0 = dGU, aux = GU
+  GemmParams d1;   // out0 = dXp
+  GemmParams w13;  // f0 = dW1, f1 = dW3
+  GemmParams w2;   // f0 = dW2
+  int32_t* cursor;
+  int32_t* cnt_d2;  // per 128-row tile: dgrad2 epilogue warps done storing dG, dU
+  int32_t* cnt_e;   // per expert: the same count over all of the expert's tiles
+};
+
+struct FusedBwdMaps {
+  Maps d2, d1, w13, w2;
+};
+
+struct BwdTask {
+  int kind;  // kDgrad2, kDgrad1, kWgrad13, kWgrad2
+  Tile t;
+};
+
+__device__ __forceinline__ int bwd_stage_start(const int32_t* tiles, int E, int s, int nnF2, int nnH2, int per_w) {
+  const int a = min(s, E);
+  const int b = max(0, min(s - kBwdSkew, E));
+  return nnF2 * __ldg(tiles + 1 + a) + nnH2 * __ldg(tiles + 1 + b) + per_w * b;
+}
+
+__device__ __forceinline__ BwdTask bwd_decode(const FusedBwdParams& f, int task) {
+  const GemmParams& p = f.d2;
+  const int E = p.E;
+  const int nnF2 = (p.F + BN - 1) / BN;   // dgrad2 N tiles
+  const int nnH2 = (p.H + BN - 1) / BN;   // dgrad1 / wgrad2 N tiles
+  const int n_w13 = (p.H / BM) * (p.F / 128);
+  const int n_w2 = (p.F / BM) * nnH2;
+  const int per_w = n_w13 + n_w2;
+  // Binary search of the stage s with start(s) <= task < start(s + 1).
+  int lo = 0, hi = E + kBwdSkew;  // stages 0 .. E + kBwdSkew - 1
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (bwd_stage_start(p.tiles, E, mid, nnF2, nnH2, per_w) <= task)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  const int s = lo;
+  int o = task - bwd_stage_start(p.tiles, E, s, nnF2, nnH2, per_w);
+  BwdTask k;
+  if (s < E) {
+    const int first = __ldg(p.tiles + 1 + s);
+    const int n_d2 = nnF2 * (__ldg(p.tiles + 2 + s) - first);
+    if (o < n_d2) {
+      k.kind = kDgrad2;
+      k.t = decode<kDgrad2>(f.d2, nnF2 * first + o);
+      return k;
+    }
+    o -= n_d2;
+  }
+  const int e = s - kBwdSkew;  // 0 <= e < E here
+  const int first = __ldg(p.tiles + 1 + e);
+  const int n_d1 = nnH2 * (__ldg(p.tiles + 2 + e) - first);
+  if (o < n_d1) {
+    k.kind = kDgrad1;
+    k.t = decode<kDgrad1>(f.d1, nnH2 * first + o);
+  } else if (o < n_d1 + n_w13) {
+    k.kind = kWgrad13;
+    k.t = decode<kWgrad13>(f.w13, e * n_w13 + (o - n_d1));
+  } else {
+    k.kind = kWgrad2;
+    k.t = decode<kWgrad2>(f.w2, e * n_w2 + (o - n_d1 - n_w13));
+  }
+  return k;
+}
+
+__device__ __forceinline__ uint32_t bwd_idesc(int kind, int nw) {
+  const bool mn = (kind == kWgrad13 || kind == kWgrad2);
+  return nw == 256 ? (mn ? idesc_bf16_f32(BM, 256, true, true) : idesc_bf16_f32(BM, 256, false, false))
+                   : (mn ? idesc_bf16_f32(BM, 128, true, true) : idesc_bf16_f32(BM, 128, false, false));
+}
+
+__global__ void __launch_bounds__(kThreads, 1) fused_backward_kernel(const __grid_constant__ FusedBwdMaps maps,
+                                                                     const FusedBwdParams f) {
+  constexpr int S = kBwdStages;
+  constexpr int kStaging = kEpiWarps * kOutBoxes * kStageOutBytes;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* staging = smem + S * kStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + kStaging);
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* rfull = tempty + 2;
+  uint64_t* rempty = rfull + kTaskRing;
+  volatile int* ring = reinterpret_cast<volatile int*>(rempty + kTaskRing);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(ring) + kTaskRing);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  WsHeader* ws = f.d2.ws;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], kEpiWarps);
+    }
+    for (int i = 0; i < kTaskRing; ++i) {
+      mbar_init(&rfull[i], 1);
+      mbar_init(&rempty[i], 1 + kEpiWarps);
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const GemmParams& P = f.d2;
+  const int nnF2 = (P.F + BN - 1) / BN;
+  const int nnH2 = (P.H + BN - 1) / BN;
+  const int total = bwd_stage_start(P.tiles, P.E, P.E + kBwdSkew, nnF2, nnH2,
+                                    (P.H / BM) * (P.F / 128) + (P.F / BM) * nnH2);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer + task fetch
+    int s = 0, slot = 0;
+    uint32_t ph = 0, rph = 0;
+    uint32_t issued = 0, last_parity = 0;
+    int next = (lane == 0) ? atomicAdd(f.cursor, 1) : 0;  // one task ahead
+    while (true) {
+      if (!mbar_wait(&rempty[slot], rph ^ 1u, ws, 160, abort_flag)) break;
+      int task = 0;
+      if (lane == 0) {
+        task = next;
+        if (task >= total || *abort_flag) task = kTaskEnd;
+        if (task != kTaskEnd) next = atomicAdd(f.cursor, 1);
+        ring[slot] = task;
+      }
+      task = __shfl_sync(0xffffffffu, task, 0);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rfull[slot]);
+      if (++slot == kTaskRing) {
+        slot = 0;
+        rph ^= 1u;
+      }
+      if (task == kTaskEnd) break;
+      const BwdTask k = bwd_decode(f, task);
+      // Scoreboard: dG, dU of the rows this tile reads must be complete.
+      bool ready = true;
+      if (k.kind == kDgrad1) {
+        ready = wait_counter(f.cnt_d2 + k.t.mt, nnF2 * kEpiWarps, ws, 161, abort_flag);
+      } else if (k.kind == kWgrad13) {
+        const int n_mt = __ldg(P.tiles + 2 + k.t.e) - __ldg(P.tiles + 1 + k.t.e);
+        ready = wait_counter(f.cnt_e + k.t.e, n_mt * nnF2 * kEpiWarps, ws, 162, abort_flag);
+      }
+      if (!ready) continue;  // abort: the consumers see the flag and stop
+      if (k.kind == kDgrad1 || k.kind == kWgrad13) fence_proxy_async_global();
+      for (int kb = 0; kb < k.t.kblocks; ++kb) {
+        if (!mbar_wait(&empty[s], ph ^ 1u, ws, 163, abort_flag)) break;
+        if (elect_one()) {
+          mbar_arrive_expect_tx(&full[s], kABytes + k.t.nw * 128);
+          uint8_t* sA = smem + s * kStageBytes;
+          switch (k.kind) {
+            case kDgrad2: load_kblock<kDgrad2>(f.d2, maps.d2, k.t, kb, sA, sA + kABytes, &full[s]); break;
+            case kDgrad1: load_kblock<kDgrad1>(f.d1, maps.d1, k.t, kb, sA, sA + kABytes, &full[s]); break;
+            case kWgrad13: load_kblock<kWgrad13>(f.w13, maps.w13, k.t, kb, sA, sA + kABytes, &full[s]); break;
+            default: load_kblock<kWgrad2>(f.w2, maps.w2, k.t, kb, sA, sA + kABytes, &full[s]); break;
+          }
+        }
+        __syncwarp();
+        issued |= 1u << s;
+        last_parity = (last_parity & ~(1u << s)) | (ph << s);
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+    for (int i = 0; i < S; ++i)
+      if ((issued >> i) & 1u) mbar_wait(&full[i], (last_parity >> i) & 1u, ws, 164, nullptr);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    int s = 0, slot = 0, acc = 0;
+    uint32_t ph = 0, rph = 0, acc_ph = 0;
+    bool ok = true;
+    while (ok) {
+      if (!mbar_wait(&rfull[slot], rph, ws, 165, abort_flag)) break;
+      const int task = ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rempty[slot]);
+      if (++slot == kTaskRing) {
+        slot = 0;
+        rph ^= 1u;
+      }
+      if (task == kTaskEnd) break;
+      const BwdTask k = bwd_decode(f, task);
+      if (k.t.kblocks == 0) continue;  // empty expert (wgrad): the epilogue writes zeros
+      const bool mn = (k.kind == kWgrad13 || k.kind == kWgrad2);
+      if (!mbar_wait(&tempty[acc], acc_ph ^ 1u, ws, 166, abort_flag)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * kAccStride;
+      const uint32_t idesc = bwd_idesc(k.kind, k.t.nw);
+      const uint32_t a_step = mn ? 2048u : 32u;
+      const uint32_t a_lbo = mn ? kPanelBytes : 16u;
+      const uint32_t b_step = mn ? 2048u : 32u;
+      const uint32_t b_lbo = mn ? kPanelBytes : 16u;
+      for (int kb = 0; kb < k.t.kblocks; ++kb) {
+        if (!mbar_wait(&full[s], ph, ws, 167, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint8_t* sA = smem + s * kStageBytes;
+        int nkk = BK / 16;
+        if (mn) {
+          // Last k-block of the expert: only the K steps holding valid rows.
+          const int valid = k.t.nrows - kb * BK;
+          if (valid < BK) nkk = clear_k_tail(sA, sA + kABytes, valid, k.t.nw, lane);
+          __syncwarp();
+        }
+        if (elect_one()) {
+          const uint32_t a0 = smem_u32(sA), b0 = a0 + kABytes;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            if (kk < nkk) {
+              const uint64_t ad = smem_desc_sw128(a0 + kk * a_step, a_lbo, 1024);
+              const uint64_t bd = smem_desc_sw128(b0 + kk * b_step, b_lbo, 1024);
+              tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+            }
+          }
+          tc_commit(&empty[s]);
+        }
+        __syncwarp();
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (elect_one()) tc_commit(&tfull[acc]);
+      __syncwarp();
+      acc ^= 1;
+      if (acc == 0) acc_ph ^= 1u;
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2;
+    const int q = warp & 3;
+    const int half = ew >> 2;
+    const int row = q * 32 + lane;
+    OutStager st;
+    st.buf = staging + ew * kOutBoxes * kStageOutBytes;
+    int slot = 0, acc = 0;
+    uint32_t rph = 0, acc_ph = 0;
+    while (true) {
+      if (!mbar_wait(&rfull[slot], rph, ws, 168, abort_flag)) break;
+      const int task = ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rempty[slot]);
+      if (++slot == kTaskRing) {
+        slot = 0;
+        rph ^= 1u;
+      }
+      if (task == kTaskEnd) break;
+      const BwdTask k = bwd_decode(f, task);
+      if (k.t.kblocks == 0) {  // empty expert: zero weight gradients
+        const bool w13 = (k.kind == kWgrad13);
+        const GemmParams& gp = w13 ? f.w13 : f.w2;
+        const int NCall = w13 ? 128 : k.t.nw;
+        const int c_lo = half * (NCall / 2), c_hi = c_lo + NCall / 2;
+        float* d0 = w13 ? gp.f0 + (static_cast<size_t>(k.t.e) * gp.H + k.t.m0 + row) * gp.F + k.t.n0
+                        : gp.f0 + (static_cast<size_t>(k.t.e) * gp.F + k.t.m0 + row) * gp.H + k.t.n0;
+        for (int c = c_lo; c < c_hi; c += 32) store_zero_f32(d0 + c);
+        if (w13) {
+          float* d1 = gp.f1 + (static_cast<size_t>(k.t.e) * gp.H + k.t.m0 + row) * gp.F + k.t.n0;
+          for (int c = c_lo; c < c_hi; c += 32) store_zero_f32(d1 + c);
+        }
+        continue;
+      }
+      if (!mbar_wait(&tfull[acc], acc_ph, ws, 169, abort_flag)) break;
+      tc_fence_after();
+      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccStride;
+      switch (k.kind) {
+        case kDgrad2: epilogue<kDgrad2>(f.d2, maps.d2, k.t, tacc, q, half, lane, st); break;
+        case kDgrad1: epilogue<kDgrad1>(f.d1, maps.d1, k.t, tacc, q, half, lane, st); break;
+        case kWgrad13: epilogue<kWgrad13>(f.w13, maps.w13, k.t, tacc, q, half, lane, st); break;
+        default: epilogue<kWgrad2>(f.w2, maps.w2, k.t, tacc, q, half, lane, st); break;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_ph ^= 1u;
+      if (k.kind == kDgrad2) {
+        signal_counter(f.cnt_d2 + k.t.mt, lane);
+        if (lane == 0) atomicAdd(f.cnt_e + k.t.e, 1);  // ordered by the fence in signal_counter
+      }
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -619,6 +1264,93 @@ cudaError_t launch_mode(const GemmLaunch& L, const Maps& maps, const GemmParams&
 }  // namespace
 
 bool tensor_map_encoder_ready() { return encoder() != nullptr; }
+
+cudaError_t launch_fused_backward(const GemmLaunch& L, int32_t* cursor, int32_t* cnt_d2, int32_t* cnt_e,
+                                  cudaStream_t s, LaunchHook& hook) {
+  const uint64_t R = L.R, H = L.H, F = L.F, E = L.E;
+  FusedBwdMaps m;
+  memset(&m, 0, sizeof(m));
+  bool ok = make_map(&m.d2.a, L.dY, H, R, 64, BM) && make_map(&m.d2.b0, L.W2, H, E * F, 64, BN) &&
+            make_map(&m.d2.b2, L.W2, H, E * F, 64, 128);
+  ok = ok && make_map(&m.d1.a, L.dGU, 2 * F, R, 64, BM) && make_map(&m.d1.b0, L.W1, F, E * H, 64, BN) &&
+       make_map(&m.d1.b1, L.W3, F, E * H, 64, BN) && make_map(&m.d1.b2, L.W1, F, E * H, 64, 128) &&
+       make_map(&m.d1.b3, L.W3, F, E * H, 64, 128);
+  ok = ok && make_map(&m.w13.a, L.Xp, H, R, 64, 64) && make_map(&m.w13.b0, L.dGU, 2 * F, R, 64, 64) &&
+       make_map(&m.w13.o0, L.dW1, F, E * H, 32, 32, true) && make_map(&m.w13.o1, L.dW3, F, E * H, 32, 32, true);
+  ok = ok && make_map(&m.w2.a, L.h, F, R, 64, 64) && make_map(&m.w2.b0, L.dY, H, R, 64, 64) &&
+       make_map(&m.w2.o0, L.dW2, H, E * F, 32, 32, true);
+  if (!ok) return cudaErrorInvalidValue;
+  GemmParams p{};
+  p.H = L.H;
+  p.F = L.F;
+  p.E = L.E;
+  p.R = L.R;
+  p.tiles = L.tiles;
+  p.offsets = L.offsets;
+  p.counts = L.counts;
+  p.ws = L.ws;
+  FusedBwdParams f{};
+  f.d2 = p;
+  f.d2.out0 = static_cast<__nv_bfloat16*>(L.out_dGU);
+  f.d2.aux = static_cast<const __nv_bfloat16*>(L.GU);
+  f.d1 = p;
+  f.d1.out0 = static_cast<__nv_bfloat16*>(L.out_dXp);
+  f.w13 = p;
+  f.w13.f0 = L.dW1;
+  f.w13.f1 = L.dW3;
+  f.w2 = p;
+  f.w2.f0 = L.dW2;
+  f.cursor = cursor;
+  f.cnt_d2 = cnt_d2;
+  f.cnt_e = cnt_e;
+  constexpr int kSmem = kBwdStages * kStageBytes + kEpiWarps * kOutBoxes * kStageOutBytes + 1024 + 512;
+  cudaError_t e = cudaFuncSetAttribute(fused_backward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  hook.before(s);
+  fused_backward_kernel<<<L.grid, kThreads, kSmem, s>>>(m, f);
+  hook.after(s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fused_forward(const GemmLaunch& L, const void* x, const int32_t* row_src, int32_t* cursor,
+                                 int32_t* cnt_gather, int32_t* cnt_g1, cudaStream_t s, LaunchHook& hook) {
+  const uint64_t R = L.R, H = L.H, F = L.F, E = L.E;
+  FusedFwdMaps m;
+  memset(&m, 0, sizeof(m));
+  if (!(make_map(&m.g1.a, L.Xp, H, R, 64, BM) && make_map(&m.g1.b0, L.W1, F, E * H, 64, 64) &&
+        make_map(&m.g1.b1, L.W3, F, E * H, 64, 64) && make_map(&m.g2.a, L.out_h, F, R, 64, BM) &&
+        make_map(&m.g2.b0, L.W2, H, E * F, 64, 64)))
+    return cudaErrorInvalidValue;
+  FusedFwdParams f{};
+  GemmParams p{};
+  p.H = L.H;
+  p.F = L.F;
+  p.E = L.E;
+  p.R = L.R;
+  p.tiles = L.tiles;
+  p.offsets = L.offsets;
+  p.counts = L.counts;
+  p.ws = L.ws;
+  f.p1 = p;
+  f.p1.out0 = static_cast<__nv_bfloat16*>(L.out_h);
+  f.p1.out1 = static_cast<__nv_bfloat16*>(L.out_GU);
+  f.p2 = p;
+  f.p2.out0 = static_cast<__nv_bfloat16*>(L.out_Y);
+  f.x = static_cast<const uint4*>(x);
+  f.Xp = static_cast<uint4*>(const_cast<void*>(L.Xp));
+  f.row_src = row_src;
+  f.T = L.T;
+  f.cursor = cursor;
+  f.cnt_gather = cnt_gather;
+  f.cnt_g1 = cnt_g1;
+  constexpr int kSmem = 4 * kStageBytes + 1024 + 512;
+  cudaError_t e = cudaFuncSetAttribute(fused_forward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  hook.before(s);
+  fused_forward_kernel<<<L.grid, kThreads, kSmem, s>>>(m, f);
+  hook.after(s);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gemm(GemmMode mode, const GemmLaunch& L, cudaStream_t s, LaunchHook& hook) {
   const uint64_t R = L.R, H = L.H, F = L.F, E = L.E;

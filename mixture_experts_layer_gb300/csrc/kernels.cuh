@@ -46,7 +46,8 @@ struct PlanLaunch {
   int32_t* ids;
   float* w;
   uint32_t* gbm;
-  int32_t* ccount;
+  int32_t* ticket;  // 16 words, then ccount; both cleared by launch_plan
+  int32_t* ccount;  // [nchunks][E] = ticket + 16
   int32_t* cbase;
   int32_t* counts;
   int32_t* offsets;
@@ -113,6 +114,16 @@ struct GemmLaunch {
   WsHeader* ws;
 };
 cudaError_t launch_gemm(GemmMode mode, const GemmLaunch& p, cudaStream_t s, LaunchHook& hook);
+
+// The forward's gather, GEMM1 and GEMM2 as one persistent kernel (task cursor
+// and per-tile counters must be zero at launch).
+cudaError_t launch_fused_forward(const GemmLaunch& L, const void* x, const int32_t* row_src, int32_t* cursor,
+                                 int32_t* cnt_gather, int32_t* cnt_g1, cudaStream_t s, LaunchHook& hook);
+
+// dgrad2, dgrad1 and both weight-gradient GEMMs as one persistent kernel
+// (task cursor and per-tile counters must be zero at launch).
+cudaError_t launch_fused_backward(const GemmLaunch& L, int32_t* cursor, int32_t* cnt_d2, int32_t* cnt_e,
+                                  cudaStream_t s, LaunchHook& hook);
 
 // Driver entry point for tensor-map encoding (resolved once through the runtime).
 bool tensor_map_encoder_ready();

@@ -56,19 +56,26 @@ int check_dims(const moe_dims& d) {
 }
 
 struct WsLayout {
-  size_t ccount, cbase, gbm, total;
+  size_t ccount, cbase, gbm, sched, sched_bytes, total;
+  size_t cap;  // capacity of the 128-row tile table
 };
 
 WsLayout ws_layout(const moe_dims& d) {
   const size_t nchunks = (static_cast<size_t>(d.T) + kChunk - 1) / kChunk;
   WsLayout L;
   size_t off = align256(sizeof(WsHeader));
-  L.ccount = off;
-  off = align256(off + nchunks * d.E * 4);
+  L.ccount = off;  // 16-word ticket, then the per-chunk counts
+  off = align256(off + (16 + nchunks * d.E) * 4);
   L.cbase = off;
   off = align256(off + nchunks * d.E * 4);
   L.gbm = off;
   off = align256(off + nchunks * d.E * kChunkWords * 4);
+  // Scheduling words of the persistent kernels: a task cursor (padded to 64 B)
+  // and two counters per 128-row tile.
+  L.cap = static_cast<size_t>(tiles_capacity(static_cast<long long>(d.T) * d.k, d.E));
+  L.sched = off;
+  L.sched_bytes = 64 + 2 * L.cap * 4;
+  off = align256(off + L.sched_bytes);
   L.total = off;
   return L;
 }
@@ -114,9 +121,11 @@ int grid_for(const moe_opts* o, int sms) {
 int finish(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH; }
 
 const char* const kPlanKernels[] = {"route_topk", "route_scan", "route_rank", nullptr};
-const char* const kFwdKernels[] = {"gather_rows", "gemm_fwd1_swiglu", "gemm_fwd2", "combine", nullptr};
+const char* const kFwdKernels[] = {"fused_forward", "combine", nullptr};
+const char* const kFwdKernelsPhased[] = {"gather_rows", "gemm_fwd1_swiglu", "gemm_fwd2", "combine", nullptr};
 const char* const kBwdKernels[] = {"combine_bwd", "gemm_dgrad2_swiglu_bwd", "gemm_dgrad1", "gemm_wgrad13",
                                    "gemm_wgrad2", "unpermute", nullptr};
+const char* const kBwdKernelsFused[] = {"combine_bwd", "fused_backward", "unpermute", nullptr};
 
 GemmLaunch gemm_common(const moe_dims& d, const moe_plan_t* plan, WsHeader* ws, int grid) {
   GemmLaunch g{};
@@ -171,7 +180,8 @@ int moe_plan(moe_dims d, const float* logits, const moe_plan_t* plan, void* ws, 
   p.ids = plan->topk_ids;
   p.w = plan->topk_w;
   p.gbm = reinterpret_cast<uint32_t*>(w + L.gbm);
-  p.ccount = reinterpret_cast<int32_t*>(w + L.ccount);
+  p.ticket = reinterpret_cast<int32_t*>(w + L.ccount);
+  p.ccount = p.ticket + 16;
   p.cbase = reinterpret_cast<int32_t*>(w + L.cbase);
   p.counts = plan->counts;
   p.offsets = plan->offsets;
@@ -190,7 +200,7 @@ int moe_forward(moe_dims d, const void* x, const void* W1, const void* W3, const
   int rc = check_dims(d);
   if (rc) return rc;
   if ((rc = check_ws(d, ws, ws_bytes))) return rc;
-  if (opts != nullptr && (opts->reserved != 0 || opts->grid < 0)) return MOE_ERR_ARG;
+  if (opts != nullptr && (opts->schedule < 0 || opts->schedule > 2 || opts->grid < 0)) return MOE_ERR_ARG;
   if (d.T == 0) return MOE_OK;
   if ((rc = check_plan(plan))) return rc;
   if (saved == nullptr) return MOE_ERR_ARG;
@@ -204,9 +214,6 @@ int moe_forward(moe_dims d, const void* x, const void* W1, const void* W3, const
   LaunchHook hook = make_hook(opts);
 
   RowsLaunch r{d.T, d.H, d.k, d.T * d.k, grid * 8, plan->dest, plan->row_src, plan->topk_w, wsh};
-  cudaError_t e = launch_gather(r, x, saved->Xp, s, hook);
-  if (e != cudaSuccess) return MOE_ERR_LAUNCH;
-
   GemmLaunch g = gemm_common(d, plan, wsh, grid);
   g.Xp = saved->Xp;
   g.W1 = W1;
@@ -214,12 +221,26 @@ int moe_forward(moe_dims d, const void* x, const void* W1, const void* W3, const
   g.W2 = W2;
   g.out_h = saved->h;
   g.out_GU = saved->GU;
-  g.bn = 256;
-  if ((e = launch_gemm(kFwd1, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
   g.h = saved->h;
   g.out_Y = saved->Y;
-  g.bn = (d.H % 256 == 0) ? 256 : 128;
-  if ((e = launch_gemm(kFwd2, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
+  cudaError_t e;
+  if (opts == nullptr || opts->schedule != 1) {
+    const WsLayout L = ws_layout(d);
+    uint8_t* sched = static_cast<uint8_t*>(ws) + L.sched;
+    if (cudaMemsetAsync(sched, 0, L.sched_bytes, s) != cudaSuccess) return MOE_ERR_LAUNCH;
+    int32_t* cursor = reinterpret_cast<int32_t*>(sched);
+    int32_t* cnt_gather = reinterpret_cast<int32_t*>(sched + 64);
+    int32_t* cnt_g1 = cnt_gather + L.cap;
+    e = launch_fused_forward(g, x, plan->row_src, cursor, cnt_gather, cnt_g1, s, hook);
+    if (e != cudaSuccess) return MOE_ERR_LAUNCH;
+  } else {
+    e = launch_gather(r, x, saved->Xp, s, hook);
+    if (e != cudaSuccess) return MOE_ERR_LAUNCH;
+    g.bn = 256;
+    if ((e = launch_gemm(kFwd1, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
+    g.bn = (d.H % 256 == 0) ? 256 : 128;
+    if ((e = launch_gemm(kFwd2, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
+  }
   return finish(launch_combine(r, saved->Y, out, s, hook));
 }
 
@@ -230,7 +251,7 @@ int moe_backward(moe_dims d, const void* dout, const void* W1, const void* W3, c
   int rc = check_dims(d);
   if (rc) return rc;
   if ((rc = check_ws(d, ws, ws_bytes))) return rc;
-  if (opts != nullptr && (opts->reserved != 0 || opts->grid < 0)) return MOE_ERR_ARG;
+  if (opts != nullptr && (opts->schedule < 0 || opts->schedule > 2 || opts->grid < 0)) return MOE_ERR_ARG;
   if ((rc = check_ptrs({dW1, dW3, dW2}))) return rc;
   if (d.T > 0) {
     if ((rc = check_plan(plan))) return rc;
@@ -273,14 +294,24 @@ int moe_backward(moe_dims d, const void* dout, const void* W1, const void* W3, c
   g.dW1 = dW1;
   g.dW3 = dW3;
   g.dW2 = dW2;
-  g.bn = (d.F % 256 == 0) ? 256 : 128;
-  if ((e = launch_gemm(kDgrad2, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
-  g.bn = (d.H % 256 == 0) ? 256 : 128;
-  if ((e = launch_gemm(kDgrad1, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
-  g.bn = 256;
-  if ((e = launch_gemm(kWgrad13, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
-  g.bn = (d.H % 256 == 0) ? 256 : 128;
-  if ((e = launch_gemm(kWgrad2, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
+  if (opts != nullptr && opts->schedule == 2) {
+    const WsLayout L = ws_layout(d);
+    uint8_t* sched = static_cast<uint8_t*>(ws) + L.sched;
+    if (cudaMemsetAsync(sched, 0, L.sched_bytes, s) != cudaSuccess) return MOE_ERR_LAUNCH;
+    int32_t* cursor = reinterpret_cast<int32_t*>(sched);
+    int32_t* cnt_d2 = reinterpret_cast<int32_t*>(sched + 64);
+    int32_t* cnt_e = cnt_d2 + L.cap;
+    if ((e = launch_fused_backward(g, cursor, cnt_d2, cnt_e, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
+  } else {
+    g.bn = (d.F % 256 == 0) ? 256 : 128;
+    if ((e = launch_gemm(kDgrad2, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
+    g.bn = (d.H % 256 == 0) ? 256 : 128;
+    if ((e = launch_gemm(kDgrad1, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
+    g.bn = 256;
+    if ((e = launch_gemm(kWgrad13, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
+    g.bn = (d.H % 256 == 0) ? 256 : 128;
+    if ((e = launch_gemm(kWgrad2, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
+  }
   return finish(launch_unpermute(r, grads->dXp, dx, s, hook));
 }
 
@@ -329,7 +360,12 @@ int32_t moe_version(void) { return 1; }
 uint64_t moe_launch_count(void) { return g_launches.load(); }
 
 const char* moe_kernel_name(int32_t call, int32_t i) {
-  const char* const* t = call == 0 ? kPlanKernels : call == 1 ? kFwdKernels : call == 2 ? kBwdKernels : nullptr;
+  const char* const* t = call == 0   ? kPlanKernels
+                         : call == 1 ? kFwdKernels
+                         : call == 2 ? kBwdKernels
+                         : call == 3 ? kFwdKernelsPhased
+                         : call == 4 ? kBwdKernelsFused
+                                     : nullptr;
   if (t == nullptr || i < 0) return nullptr;
   for (int j = 0; j <= i; ++j)
     if (t[j] == nullptr) return nullptr;

@@ -9,14 +9,15 @@
 // here are 256-token chunks of one GPU instead of ranks, so no atomics decide
 // any position and the order inside each expert is the original token order.
 //
-//   route_topk  one CTA per chunk: warp-wide top-k per token, renormalised
-//               weights, and a per-chunk bitmap bm[e][w] whose bit b says
-//               "token 32w+b of the chunk chose expert e" (a warp ballot in
-//               shared memory); writes the bitmap and per-chunk counts.
-//   route_scan  one CTA: exclusive prefix of the counts over chunks (per
-//               expert) and over experts, and the 128-row GEMM tile table.
-//   route_rank  one CTA per chunk: stable index = popcount of the bitmap below
-//               the token; dest, row_src, row_slot.
+//   route_topk  one CTA per 64 tokens: warp-wide top-k per token, renormalised
+//               weights, and its part of the chunk bitmap bm[e][w] whose bit b
+//               says "token 32w+b of the chunk chose expert e" (a warp ballot in
+//               shared memory); per-chunk counts by integer atomics.
+//   route_scan  one warp per expert: exclusive prefix of the counts over
+//               chunks; the last CTA takes the prefix over experts and writes
+//               the 128-row GEMM tile table.
+//   route_rank  one CTA per 64 tokens: stable index = popcount of the chunk's
+//               bitmap below the token; dest, row_src, row_slot.
 #include <math.h>
 
 #include "common.cuh"
@@ -24,26 +25,32 @@
 
 namespace moe {
 
-constexpr int kTopkThreads = 512;
+constexpr int kTopkTokens = 64;    // tokens per top-k / rank CTA: two bitmap words per expert
+constexpr int kTopkThreads = 256;  // 8 warps x 8 tokens
+constexpr int kScanWarps = 8;      // experts per scan CTA
 
 // NV = logits per lane (E <= 32 * NV); TPW = tokens whose logits a warp loads
 // at once, so several rows' loads are in flight before the selection starts.
+// One CTA covers 64 consecutive tokens: it owns two words of its chunk's bitmap
+// per expert (written plainly) and adds its per-expert counts to the chunk's
+// counts with integer atomics (the sum does not depend on their order).
 template <int NV, int TPW>
 __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float* __restrict__ logits, int T, int E,
                                                                   int k, int32_t* __restrict__ ids,
                                                                   float* __restrict__ wts, uint32_t* __restrict__ gbm,
                                                                   int32_t* __restrict__ ccount, WsHeader* ws) {
-  extern __shared__ uint32_t bm[];  // [E][kChunkWords]
-  constexpr int kWarps = kTopkThreads / 32;
-  const int chunk = blockIdx.x;
-  for (int i = threadIdx.x; i < E * kChunkWords; i += blockDim.x) bm[i] = 0;
+  extern __shared__ uint32_t sm[];
+  uint32_t* bm = sm;            // [E][2] bitmap words of this CTA's 64 tokens
+  int* cnt = reinterpret_cast<int*>(sm + 2 * E);  // [E]
+  for (int i = threadIdx.x; i < 3 * E; i += blockDim.x) sm[i] = 0;
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int tb = warp * TPW; tb < kChunk; tb += kWarps * TPW) {
+  const int t0 = blockIdx.x * kTopkTokens;
+  for (int tb = warp * (kTopkTokens / 8); tb < (warp + 1) * (kTopkTokens / 8); tb += TPW) {
     float v[TPW][NV];
 #pragma unroll
     for (int u = 0; u < TPW; ++u) {
-      const int t = chunk * kChunk + tb + u;
+      const int t = t0 + tb + u;
 #pragma unroll
       for (int i = 0; i < NV; ++i) {
         const int e = lane + 32 * i;
@@ -53,7 +60,7 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float* _
 #pragma unroll
     for (int u = 0; u < TPW; ++u) {
       const int tl = tb + u;
-      const int t = chunk * kChunk + tl;
+      const int t = t0 + tl;
       if (t >= T) break;
       uint32_t taken = 0;
       bool bad = false;
@@ -106,29 +113,34 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float* _
       if (lane < k) {
         ids[static_cast<size_t>(t) * k + lane] = my_id;
         wts[static_cast<size_t>(t) * k + lane] = ex / sum;
-        atomicOr(&bm[my_id * kChunkWords + (tl >> 5)], 1u << (tl & 31));
+        atomicOr(&bm[my_id * 2 + (tl >> 5)], 1u << (tl & 31));
+        atomicAdd(&cnt[my_id], 1);
       }
     }
   }
   __syncthreads();
+  const int chunk = t0 / kChunk;
+  const int w0 = (t0 % kChunk) / 32;
   uint32_t* out = gbm + static_cast<size_t>(chunk) * E * kChunkWords;
-  for (int i = threadIdx.x; i < E * kChunkWords; i += blockDim.x) out[i] = bm[i];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int c = 0;
-#pragma unroll
-    for (int w = 0; w < kChunkWords; ++w) c += __popc(bm[e * kChunkWords + w]);
-    ccount[static_cast<size_t>(chunk) * E + e] = c;
-  }
+  for (int i = threadIdx.x; i < 2 * E; i += blockDim.x) out[(i >> 1) * kChunkWords + w0 + (i & 1)] = bm[i];
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    if (cnt[e] != 0) atomicAdd(&ccount[static_cast<size_t>(chunk) * E + e], cnt[e]);
 }
 
-__global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* __restrict__ ccount, int nchunks, int E,
-                                                          int32_t* __restrict__ cbase, int32_t* __restrict__ counts,
-                                                          int32_t* __restrict__ offsets, int32_t* __restrict__ tiles) {
-  __shared__ int32_t ne[1024];
-  __shared__ int32_t wsum_n[32], wsum_m[32];
+// Per expert (one warp each): exclusive prefix of the chunk counts over the
+// chunks -- the O_all of Algorithm 1 -- and the expert's row count.  The last
+// CTA to finish (ticket) then takes the prefix over experts and writes the
+// 128-row tile table.
+__global__ void __launch_bounds__(32 * kScanWarps) route_scan_kernel(const int32_t* __restrict__ ccount,
+                                                                     int nchunks, int E, int32_t* __restrict__ cbase,
+                                                                     int32_t* __restrict__ counts,
+                                                                     int32_t* __restrict__ offsets,
+                                                                     int32_t* __restrict__ tiles, int32_t* ticket) {
+  __shared__ int s_last;
+  __shared__ int s_wsum_n[32], s_wsum_m[32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Per expert: exclusive prefix of the chunk counts (the O_all of Algorithm 1).
-  for (int e = warp; e < E; e += 32) {
+  const int e = blockIdx.x * kScanWarps + warp;
+  if (e < E) {
     int run = 0;
     for (int c0 = 0; c0 < nchunks; c0 += 32) {
       const int c = c0 + lane;
@@ -142,14 +154,28 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* __restr
       if (c < nchunks) cbase[static_cast<size_t>(c) * E + e] = run + incl - v;
       run += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane == 0) ne[e] = run;
+    if (lane == 0) counts[e] = run;
   }
+  __threadfence();
   __syncthreads();
-  // Exclusive prefix over experts of the row counts and of the 128-row tile counts.
-  const int e = threadIdx.x;
-  const int n = (e < E) ? ne[e] : 0;
-  const int mt = (n + kTileRows - 1) / kTileRows;
-  int in_n = n, in_m = mt;
+  if (threadIdx.x == 0) s_last = (atomicAdd(ticket, 1) == static_cast<int>(gridDim.x) - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // Last CTA: exclusive prefix over experts of the row counts and of the
+  // 128-row tile counts.  Thread i takes experts [i * per, (i + 1) * per).
+  const int per = (E + blockDim.x - 1) / blockDim.x;
+  const int e0 = threadIdx.x * per;
+  int my_n = 0, my_m = 0;
+  for (int i = 0; i < per; ++i) {
+    const int ee = e0 + i;
+    if (ee < E) {
+      const int n = __ldcg(counts + ee);
+      my_n += n;
+      my_m += (n + kTileRows - 1) / kTileRows;
+    }
+  }
+  int in_n = my_n, in_m = my_m;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
     const int yn = __shfl_up_sync(0xffffffffu, in_n, off);
@@ -160,37 +186,43 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* __restr
     }
   }
   if (lane == 31) {
-    wsum_n[warp] = in_n;
-    wsum_m[warp] = in_m;
+    s_wsum_n[warp] = in_n;
+    s_wsum_m[warp] = in_m;
   }
   __syncthreads();
-  int base_n = 0, base_m = 0;
+  int run_n = in_n - my_n, run_m = in_m - my_m;
   for (int w = 0; w < warp; ++w) {
-    base_n += wsum_n[w];
-    base_m += wsum_m[w];
+    run_n += s_wsum_n[w];
+    run_m += s_wsum_m[w];
   }
-  const int ex_n = base_n + in_n - n, ex_m = base_m + in_m - mt;
   const int entries = tiles_entry_base(E);
-  if (e < E) {
-    counts[e] = n;
-    offsets[e] = ex_n;
-    tiles[1 + e] = ex_m;
-    for (int i = 0; i < mt; ++i) {
+  for (int i = 0; i < per; ++i) {
+    const int ee = e0 + i;
+    if (ee >= E) break;
+    const int n = __ldcg(counts + ee);
+    const int mt = (n + kTileRows - 1) / kTileRows;
+    offsets[ee] = run_n;
+    tiles[1 + ee] = run_m;
+    for (int j = 0; j < mt; ++j) {
       int4 ent;
-      ent.x = e;
-      ent.y = ex_n + kTileRows * i;
-      ent.z = min(kTileRows, n - kTileRows * i);
+      ent.x = ee;
+      ent.y = run_n + kTileRows * j;
+      ent.z = min(kTileRows, n - kTileRows * j);
       ent.w = 0;
-      reinterpret_cast<int4*>(tiles + entries)[ex_m + i] = ent;
+      reinterpret_cast<int4*>(tiles + entries)[run_m + j] = ent;
     }
-  }
-  if (e == E - 1) {
-    offsets[E] = ex_n + n;
-    tiles[1 + E] = ex_m + mt;
-    tiles[0] = ex_m + mt;
+    run_n += n;
+    run_m += mt;
+    if (ee == E - 1) {
+      offsets[E] = run_n;
+      tiles[1 + E] = run_m;
+      tiles[0] = run_m;
+    }
   }
 }
 
+// One CTA per 64 tokens: stable index = popcount of the chunk's bitmap below
+// the token; dest, row_src, row_slot.
 __global__ void __launch_bounds__(256) route_rank_kernel(const int32_t* __restrict__ ids,
                                                          const uint32_t* __restrict__ gbm,
                                                          const int32_t* __restrict__ cbase,
@@ -199,23 +231,23 @@ __global__ void __launch_bounds__(256) route_rank_kernel(const int32_t* __restri
                                                          int32_t* __restrict__ row_src,
                                                          uint8_t* __restrict__ row_slot, WsHeader* ws) {
   extern __shared__ uint32_t sm[];
-  uint32_t* words = sm;                    // [E][kChunkWords]
-  uint32_t* pre = sm + E * kChunkWords;    // exclusive popcount prefix per expert
-  const int chunk = blockIdx.x;
+  uint32_t* words = sm;     // [E][2]: this CTA's two words
+  uint32_t* pre = sm + 2 * E;  // [E][2]: popcount of the chunk's words before each
+  const int t0 = blockIdx.x * kTopkTokens;
+  const int chunk = t0 / kChunk;
+  const int w0 = (t0 % kChunk) / 32;
   const uint32_t* src = gbm + static_cast<size_t>(chunk) * E * kChunkWords;
-  for (int i = threadIdx.x; i < E * kChunkWords; i += blockDim.x) words[i] = src[i];
-  __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     uint32_t run = 0;
-#pragma unroll
-    for (int w = 0; w < kChunkWords; ++w) {
-      pre[e * kChunkWords + w] = run;
-      run += __popc(words[e * kChunkWords + w]);
-    }
+    for (int w = 0; w < w0; ++w) run += __popc(src[e * kChunkWords + w]);
+    const uint32_t a = src[e * kChunkWords + w0], b = src[e * kChunkWords + w0 + 1];
+    words[2 * e] = a;
+    words[2 * e + 1] = b;
+    pre[2 * e] = run;
+    pre[2 * e + 1] = run + __popc(a);
   }
   __syncthreads();
-  const int t0 = chunk * kChunk;
-  const int n_items = min(kChunk, T - t0) * k;
+  const int n_items = min(kTopkTokens, T - t0) * k;
   for (int i = threadIdx.x; i < n_items; i += blockDim.x) {
     const int tl = i / k, j = i - tl * k;
     const int t = t0 + tl;
@@ -226,7 +258,7 @@ __global__ void __launch_bounds__(256) route_rank_kernel(const int32_t* __restri
       continue;
     }
     const int w = tl >> 5, b = tl & 31;
-    const int rank = pre[e * kChunkWords + w] + __popc(words[e * kChunkWords + w] & ((1u << b) - 1u));
+    const int rank = pre[2 * e + w] + __popc(words[2 * e + w] & ((1u << b) - 1u));
     const int r = offsets[e] + cbase[static_cast<size_t>(chunk) * E + e] + rank;
     if (r < 0 || r >= R) {
       report(ws, MOE_ERR_BOUNDS, 2, t);
@@ -240,14 +272,19 @@ __global__ void __launch_bounds__(256) route_rank_kernel(const int32_t* __restri
 
 cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t s, LaunchHook& hook) {
   const int nchunks = (p.T + kChunk - 1) / kChunk;
-  const size_t bm_bytes = static_cast<size_t>(p.E) * kChunkWords * 4;
+  const int nblocks = (p.T + kTopkTokens - 1) / kTopkTokens;
   const int nv = (p.E + 31) / 32;
+  // The chunk counts and the scan's ticket start at zero (the bitmap words are
+  // all written by the top-k CTAs).
+  cudaError_t err = cudaMemsetAsync(p.ticket, 0, (16 + static_cast<size_t>(nchunks) * p.E) * 4, s);
+  if (err != cudaSuccess) return err;
+  const size_t topk_smem = static_cast<size_t>(p.E) * 3 * 4;
   hook.before(s);
   switch (nv <= 1 ? 1 : nv <= 2 ? 2 : nv <= 4 ? 4 : nv <= 8 ? 8 : nv <= 16 ? 16 : 32) {
-#define MOE_TOPK_CASE(NV, TPW)                                                                               \
-  case NV:                                                                                                   \
-    route_topk_kernel<NV, TPW><<<nchunks, kTopkThreads, bm_bytes, s>>>(p.logits, p.T, p.E, p.k, p.ids, p.w, \
-                                                                       p.gbm, p.ccount, p.ws);              \
+#define MOE_TOPK_CASE(NV, TPW)                                                                                 \
+  case NV:                                                                                                     \
+    route_topk_kernel<NV, TPW><<<nblocks, kTopkThreads, topk_smem, s>>>(p.logits, p.T, p.E, p.k, p.ids, p.w, \
+                                                                        p.gbm, p.ccount, p.ws);              \
     break;
     MOE_TOPK_CASE(1, 8)
     MOE_TOPK_CASE(2, 8)
@@ -258,21 +295,17 @@ cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t s, LaunchHook& hook) {
 #undef MOE_TOPK_CASE
   }
   hook.after(s);
-  cudaError_t err = cudaGetLastError();
+  err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   hook.before(s);
-  route_scan_kernel<<<1, 1024, 0, s>>>(p.ccount, nchunks, p.E, p.cbase, p.counts, p.offsets, p.tiles);
+  route_scan_kernel<<<(p.E + kScanWarps - 1) / kScanWarps, 32 * kScanWarps, 0, s>>>(
+      p.ccount, nchunks, p.E, p.cbase, p.counts, p.offsets, p.tiles, p.ticket);
   hook.after(s);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  if (2 * bm_bytes > 48 * 1024) {
-    err = cudaFuncSetAttribute(route_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(2 * bm_bytes));
-    if (err != cudaSuccess) return err;
-  }
   hook.before(s);
-  route_rank_kernel<<<nchunks, 256, 2 * bm_bytes, s>>>(p.ids, p.gbm, p.cbase, p.offsets, p.T, p.E, p.k,
-                                                       p.T * p.k, p.dest, p.row_src, p.row_slot, p.ws);
+  route_rank_kernel<<<nblocks, 256, static_cast<size_t>(p.E) * 4 * 4, s>>>(
+      p.ids, p.gbm, p.cbase, p.offsets, p.T, p.E, p.k, p.T * p.k, p.dest, p.row_src, p.row_slot, p.ws);
   hook.after(s);
   return cudaGetLastError();
 }
@@ -336,8 +369,8 @@ extern "C" int moe_plan_noalloc(moe_dims d, const float* logits, const moe_plan_
     return MOE_ERR_ARG;
   if (d.H % 128 != 0 || d.F % 128 != 0 || d.E > 1024) return MOE_ERR_SHAPE;
   const size_t nchunks = (static_cast<size_t>(d.T) + kChunk - 1) / kChunk;
-  const size_t ccount = 0;
-  const size_t cbase = na_align(ccount + nchunks * d.E * 4);
+  const size_t ccount = 0;  // 16-word ticket, then the per-chunk counts
+  const size_t cbase = na_align(ccount + (16 + nchunks * d.E) * 4);
   const size_t gbm = na_align(cbase + nchunks * d.E * 4);
   const size_t total = na_align(gbm + nchunks * d.E * kChunkWords * 4);
   if (total > kNoAllocBytes) return MOE_ERR_TOO_LARGE;
@@ -360,7 +393,8 @@ extern "C" int moe_plan_noalloc(moe_dims d, const float* logits, const moe_plan_
   p.k = d.k;
   p.ids = plan->topk_ids;
   p.w = plan->topk_w;
-  p.ccount = reinterpret_cast<int32_t*>(w + ccount);
+  p.ticket = reinterpret_cast<int32_t*>(w + ccount);
+  p.ccount = p.ticket + 16;
   p.cbase = reinterpret_cast<int32_t*>(w + cbase);
   p.gbm = reinterpret_cast<uint32_t*>(w + gbm);
   p.counts = plan->counts;

@@ -70,9 +70,10 @@ class MoELayer:
             stream = torch.cuda.current_stream()
         return stream.cuda_stream
 
-    def opts(self, grid=0, events=None):
+    def opts(self, grid=0, events=None, schedule=0):
         o = moe_opts()
         o.grid = grid
+        o.schedule = schedule
         if events:
             arr = (ctypes_void_p_array(len(events)))(*[e.cuda_event for e in events])
             self._ev_keep = arr

@@ -39,6 +39,14 @@ def shape_inputs(shape: S.LayerShape, seed: int, bias=None, device="cuda"):
     return d
 
 
+def poison(layer):
+    """Fill every intermediate and output buffer with NaN, so a kernel that reads
+    a value before it is written, or skips a write, cannot go unnoticed."""
+    for n in ("Xp", "GU", "h", "Y", "out", "dY", "dGU", "dXp", "dx", "dW1", "dW3", "dW2", "dgate", "w"):
+        if hasattr(layer, n):
+            getattr(layer, n).fill_(float("nan"))
+
+
 def run_gpu(layer, inp, opts=None):
     layer.plan(inp["logits"])
     layer.forward(inp["x"], inp["W1"], inp["W3"], inp["W2"], opts=opts)

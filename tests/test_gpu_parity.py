@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import moe_synth as S
-from helpers import check_backward, check_forward, check_tables, run_gpu, run_oracle, shape_inputs
+from helpers import check_backward, check_forward, check_tables, poison, run_gpu, run_oracle, shape_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -47,6 +47,7 @@ def test_layer_matches_oracle(lib_loaded, name):
     shape, seed, _ = CASES[name]
     inp = shape_inputs(shape, seed, _bias(name, shape))
     layer = MoELayer(shape.T, shape.H, shape.F, shape.E, shape.k)
+    poison(layer)
     run_gpu(layer, inp)
     ref = run_oracle(inp, shape.k, shape.E)
     check_tables(layer, ref)
