@@ -87,22 +87,29 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
-def profiled_traffic(kernel: str):
+def profiled_traffic(kernel: str, workload: str):
     """DRAM bytes per launch of a kernel from the committed ncu summary, or None.
 
     profiles/traffic.txt holds lines `kernel source_sha dram_bytes_per_launch workload`;
-    a line counts only while the kernel's source file is unchanged.
+    a line counts only for its own workload and while the kernel's source file
+    is unchanged.
     """
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    src = os.path.join(ROOT, "mixture_experts_layer_gb300", "csrc",
-                       "gemm.cu" if kernel.startswith("gemm") else "rows.cu" if kernel != "plan" else "plan.cu")
+    if kernel.startswith(("gemm", "fused")):
+        name = "gemm.cu"
+    elif kernel.startswith("route") or kernel == "plan":
+        name = "plan.cu"
+    else:
+        name = "rows.cu"
+    src = os.path.join(ROOT, "mixture_experts_layer_gb300", "csrc", name)
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     for line in open(path):
         parts = line.split()
-        if len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel and parts[1] == sha:
+        if (len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == sha
+                and parts[3] == workload):
             return float(parts[2])
     return None
 
@@ -237,11 +244,13 @@ def run_reference(args):
     steps, warm = args.steps, args.warmup
     # Size the sample so the whole run stays within a few minutes.
     budget = min(8.0, 150.0 / max(1, steps + warm))
-    probe_T = 64
     inp = oracle_sample_inputs(shape, seed, shape.T)
     sub = lambda n: dict(inp, x=inp["x"][:n], dout=inp["dout"][:n], logits=inp["logits"][:n])
-    t_probe = time_oracle_step(sub(probe_T), shape)
-    T_s = int(max(16, min(shape.T, probe_T * budget / max(t_probe, 1e-6))))
+    # Fixed cost plus a part linear in the tokens, fitted from two probes.
+    t_a = time_oracle_step(sub(16), shape)
+    t_b = time_oracle_step(sub(64), shape)
+    slope = max((t_b - t_a) / 48.0, 1e-9)
+    T_s = int(max(16, min(shape.T, 64 + (budget - t_b) / slope)))
     sample = sub(T_s)
     for _ in range(warm):
         time_oracle_step(sample, shape)
@@ -286,6 +295,20 @@ def run_ours(args):
     T, H, F, E, k = shape.T, shape.H, shape.F, shape.E, shape.k
     seed = S.config_seed(args.config) + 1000 * rank  # each replica its own tokens
     M.lib()
+    if args.profile and args.part == "plan":
+        # Routing only: the logits and the plan's tables are all that is allocated.
+        lg = S.layer_inputs(shape, seed, device=dev, with_weights=False)["logits"]
+        layer = MoELayer(T, H, F, E, k, device=dev, plan_only=True)
+        for _ in range(args.warmup + 1):
+            layer.plan(lg)
+        torch.cuda.synchronize()
+        st = layer.status()
+        if st[0] != 0:
+            raise RuntimeError(f"device status {st}")
+        if rank == 0:
+            print(json.dumps({"profile_step": "done", "part": "plan", "config": workload_config(shape, args.config),
+                              "kernels_per_step": N_PLAN_KERNELS}), flush=True)
+        return
     inp = S.layer_inputs(shape, seed, device=dev)
     layer = MoELayer(T, H, F, E, k, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -396,12 +419,12 @@ def run_ours(args):
     if dom in flops and t_tc >= t_hbm:
         ach = flops[dom] / (per[dom] * 1e-3) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 1), "peak": tc_peak, "unit": "TFLOP/s",
-                "frac": round(ach / tc_peak, 4), "traffic": profiled_traffic(dom),
+                "frac": round(ach / tc_peak, 4), "traffic": profiled_traffic(dom, shape.name),
                 "peak_kind": ("sustained" if long_region else "burst") + f" bf16 of {peaks['source']}"}
     else:
         ach = bytes_[dom] / (per[dom] * 1e-3) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": profiled_traffic(dom),
+                "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": profiled_traffic(dom, shape.name),
                 "peak_kind": f"copy bandwidth of {peaks['source']}"}
     roof["algorithmic_per_launch"] = flops[dom] if roof["bound"] == "tensor" else bytes_[dom]
     for n, ent in kern.items():
@@ -458,7 +481,7 @@ def run_ours(args):
         "gpu_launches": int(launches),
         "clocks": clk,
         "kernels": kern,
-        "step_gemm_tflops": round(sum(flops.values()) / (ms_step * 1e-3) / 1e12, 1),
+        "step_gemm_tflops": round(18 * T * k * H * F / (ms_step * 1e-3) / 1e12, 1),
     }
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -475,8 +498,12 @@ def cpu_baseline(shape, idx):
     import moe_synth as S
     inp = oracle_sample_inputs(shape, S.config_seed(idx), shape.T)
     sub = lambda n: dict(inp, x=inp["x"][:n], dout=inp["dout"][:n], logits=inp["logits"][:n])
-    t64 = time_oracle_step(sub(64), shape)
-    T_s = int(max(64, min(shape.T, 64 * 12.0 / max(t64, 1e-6))))
+    # The oracle's cost is a fixed part (per-expert weight arrays) plus a part
+    # linear in the tokens: fit both from two probes and size the sample for ~12 s.
+    t_a = time_oracle_step(sub(64), shape)
+    t_b = time_oracle_step(sub(256), shape)
+    slope = max((t_b - t_a) / 192.0, 1e-9)
+    T_s = int(max(256, min(shape.T, 256 + (12.0 - t_b) / slope)))
     t = time_oracle_step(sub(T_s), shape)
     return {"value": round(T_s / t, 2), "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
             "sample": f"first {T_s} of {shape.T} tokens (plan + forward + backward incl. weight gradients over "
@@ -496,6 +523,8 @@ def main():
                          "1: one launch per phase; 2: fused forward and fused backward")
     ap.add_argument("--profile", action="store_true",
                     help="run the warm-up steps and one more step only (for ncu captures)")
+    ap.add_argument("--part", default="step", choices=["step", "plan"],
+                    help="with --profile: the whole step, or the routing kernels alone (plan buffers only)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

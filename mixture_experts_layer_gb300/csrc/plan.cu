@@ -9,16 +9,21 @@
 // here are 256-token chunks of one GPU instead of ranks, so no atomics decide
 // any position and the order inside each expert is the original token order.
 //
-//   route_topk  one CTA per 64 tokens: warp-wide top-k per token, renormalised
-//               weights, and its part of the chunk bitmap bm[e][w] whose bit b
-//               says "token 32w+b of the chunk chose expert e" (a warp ballot in
-//               shared memory); per-chunk counts by integer atomics.
+//   route_topk  one CTA per 64 tokens: top-k per token (four threads per
+//               token with a min/max selection network where E % 4 == 0,
+//               E <= 256 and k <= 8; a warp-wide argmax per pick otherwise),
+//               renormalised weights, and its part of the chunk bitmap bm[e][w]
+//               whose bit b says "token 32w+b of the chunk chose expert e";
+//               per-chunk counts by integer atomics.
 //   route_scan  one warp per expert: exclusive prefix of the counts over
-//               chunks; the last CTA takes the prefix over experts and writes
-//               the 128-row GEMM tile table.
-//   route_rank  one CTA per 64 tokens: stable index = popcount of the chunk's
-//               bitmap below the token; dest, row_src, row_slot.
+//               chunks; the last CTA takes the prefix over experts (offsets,
+//               first 128-row GEMM tile of each expert).
+//   route_rank  one CTA per chunk: stable index = popcount of the chunk's
+//               bitmap below the token; dest, row_src, row_slot; a share of
+//               the GEMM tile entries.
 #include <math.h>
+
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.cuh"
@@ -127,10 +132,272 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float* _
     if (cnt[e] != 0) atomicAdd(&ccount[static_cast<size_t>(chunk) * E + e], cnt[e]);
 }
 
+// Fast path of the same selection for E % 4 == 0, E <= 256 and k <= 8: four
+// threads per token, each holding a quarter of its logits (16-byte vectors
+// 4i + q of the row, so a warp's loads are whole sectors).
+//   1. Each thread sorts its values in blocks of 8 (Batcher's 19-comparator
+//      network) and merges the blocks keeping the 8 largest (bitonic split +
+//      3-stage sort); two shuffle rounds merge the four threads' lists the same
+//      way.  Only values move, so no id comparisons are needed: the four
+//      threads end with the token's 8 largest values, sorted, s[0] >= ... >= s[7].
+//   2. th = s[k-1]; `need` of the top k equal th.  Each thread lists its values
+//      >= th (with their ids) in shared memory.  When the token has exactly k
+//      such values -- no extra ties at the threshold, the usual case -- all of
+//      them are chosen; otherwise one thread rescans the row in ascending id
+//      order, taking every value > th and the first `need` equal to th.
+//   3. Slot of a chosen (x, e): #{m < k : s[m] > x}, plus, when x occurs more
+//      than once in the top k, the number of chosen equal values with a lower
+//      id -- the total order (value desc, id asc) of the warp-per-token path.
+// Weights: exp(s[m] - s[0]) summed over m < k in slot order, then
+// exp(x - s[0]) / sum: the same arithmetic as the warp-per-token path.
+// Non-finite logits are detected with one fused multiply-add per value
+// (x * 0 is NaN exactly for NaN and +-inf); a warp that holds one maps them to
+// -inf and reports MOE_ERR_NONFINITE, as the warp-per-token path does.
+constexpr int kTopkFastK = 8;
+
+// Compare-exchange, descending.
+__device__ __forceinline__ void cx_desc(float& a, float& b) {
+  const float hi = fmaxf(a, b), lo = fminf(a, b);
+  a = hi;
+  b = lo;
+}
+
+// Sorts 8 values descending (Batcher's odd-even merge sort, 19 comparators).
+__device__ __forceinline__ void sort8_desc(float* a) {
+  cx_desc(a[0], a[1]); cx_desc(a[2], a[3]); cx_desc(a[4], a[5]); cx_desc(a[6], a[7]);
+  cx_desc(a[0], a[2]); cx_desc(a[1], a[3]); cx_desc(a[4], a[6]); cx_desc(a[5], a[7]);
+  cx_desc(a[1], a[2]); cx_desc(a[5], a[6]);
+  cx_desc(a[0], a[4]); cx_desc(a[1], a[5]); cx_desc(a[2], a[6]); cx_desc(a[3], a[7]);
+  cx_desc(a[2], a[4]); cx_desc(a[3], a[5]);
+  cx_desc(a[1], a[2]); cx_desc(a[3], a[4]); cx_desc(a[5], a[6]);
+}
+
+// a := the 8 largest of a and b (both sorted descending), sorted descending.
+__device__ __forceinline__ void merge8_top(float* a, const float* b) {
+#pragma unroll
+  for (int m = 0; m < 8; ++m) a[m] = fmaxf(a[m], b[7 - m]);
+#pragma unroll
+  for (int d = 4; d > 0; d >>= 1)
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+      if ((m & d) == 0) cx_desc(a[m], a[m + d]);
+}
+
+template <int NV4, bool FULL>
+__global__ void __launch_bounds__(kTopkThreads) route_topk4_kernel(const float* __restrict__ logits, int T, int E,
+                                                                   int k, int32_t* __restrict__ ids,
+                                                                   float* __restrict__ wts,
+                                                                   uint32_t* __restrict__ gbm,
+                                                                   int32_t* __restrict__ ccount, WsHeader* ws) {
+  constexpr int NV = 4 * NV4;                    // values per thread
+  constexpr int NB = (NV + 7) / 8;               // blocks of 8
+  extern __shared__ uint32_t sm[];
+  uint32_t* bm = sm;                             // [E][2]
+  int* cnt = reinterpret_cast<int*>(sm + 2 * E); // [E]
+  float* cand_x = reinterpret_cast<float*>(cnt + E);  // [64 tokens][8] chosen values (tie path)
+  for (int i = threadIdx.x; i < 3 * E; i += blockDim.x) sm[i] = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int tl = threadIdx.x >> 2, q = threadIdx.x & 3;
+  const int t = blockIdx.x * kTopkTokens + tl;
+  const bool live = t < T;
+  const float* row = logits + static_cast<size_t>(live ? t : 0) * E;
+
+  float v[NB * 8];
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV4; ++i) {
+    const int e0 = 16 * i + 4 * q;
+    float4 f = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    if (live && (FULL || e0 < E)) {
+      f = __ldg(reinterpret_cast<const float4*>(row + e0));
+      acc = fmaf(f.x, 0.f, acc);
+      acc = fmaf(f.y, 0.f, acc);
+      acc = fmaf(f.z, 0.f, acc);
+      acc = fmaf(f.w, 0.f, acc);
+    }
+    v[4 * i] = f.x;
+    v[4 * i + 1] = f.y;
+    v[4 * i + 2] = f.z;
+    v[4 * i + 3] = f.w;
+  }
+#pragma unroll
+  for (int j = NV; j < NB * 8; ++j) v[j] = -INFINITY;
+  const bool bad = acc != acc;
+  if (__any_sync(0xffffffffu, bad)) {
+#pragma unroll
+    for (int j = 0; j < NV; ++j)
+      if (!isfinite(v[j])) v[j] = -INFINITY;
+    if (bad) report(ws, MOE_ERR_NONFINITE, 0, t);
+  }
+
+  // 1. the token's 8 largest values, sorted
+  float s[8];
+  {
+    float b[NB][8];
+#pragma unroll
+    for (int blk = 0; blk < NB; ++blk) {
+#pragma unroll
+      for (int m = 0; m < 8; ++m) b[blk][m] = v[8 * blk + m];
+      sort8_desc(b[blk]);
+    }
+#pragma unroll
+    for (int m = 0; m < 8; ++m) s[m] = b[0][m];
+#pragma unroll
+    for (int blk = 1; blk < NB; ++blk) merge8_top(s, b[blk]);
+  }
+#pragma unroll
+  for (int mask = 1; mask <= 2; mask <<= 1) {
+    float o[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) o[m] = __shfl_xor_sync(0xffffffffu, s[m], mask);
+    merge8_top(s, o);
+  }
+  float th = s[0];
+#pragma unroll
+  for (int m = 1; m < 8; ++m)
+    if (m < k) th = s[m];
+  int need = 0;
+#pragma unroll
+  for (int m = 0; m < 8; ++m) need += (m < k && s[m] == th) ? 1 : 0;
+
+  // 2. this thread's values >= th, as a bit mask over its value index j
+  //    (value j of thread q is expert 16 (j / 4) + 4 q + j % 4)
+  using Mask = typename std::conditional<(NV > 32), unsigned long long, uint32_t>::type;
+  Mask msk = 0;
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    const int e = 16 * (j >> 2) + 4 * q + (j & 3);
+    if ((FULL || e < E) && v[j] >= th) msk |= Mask(1) << j;
+  }
+  const int n = (NV > 32) ? __popcll(static_cast<unsigned long long>(msk)) : __popc(static_cast<uint32_t>(msk));
+  int ntot = n;
+  ntot += __shfl_xor_sync(0xffffffffu, ntot, 1);
+  ntot += __shfl_xor_sync(0xffffffffu, ntot, 2);
+  int nq[4];
+  Mask mq[4];
+#pragma unroll
+  for (int qq = 0; qq < 4; ++qq) {
+    nq[qq] = __shfl_sync(0xffffffffu, n, (lane & ~3) + qq);
+    if (NV > 32) {
+      const uint32_t lo = __shfl_sync(0xffffffffu, static_cast<uint32_t>(msk), (lane & ~3) + qq);
+      const uint32_t hi = __shfl_sync(0xffffffffu, static_cast<uint32_t>(static_cast<unsigned long long>(msk) >> 32),
+                                      (lane & ~3) + qq);
+      mq[qq] = static_cast<Mask>((static_cast<unsigned long long>(hi) << 32) | lo);
+    } else {
+      mq[qq] = static_cast<Mask>(__shfl_sync(0xffffffffu, static_cast<uint32_t>(msk), (lane & ~3) + qq));
+    }
+  }
+  // Expert of the li-th set bit of thread qq's mask.
+  auto expert_of = [&](int qq, int li) {
+    const Mask m = qq == 0 ? mq[0] : qq == 1 ? mq[1] : qq == 2 ? mq[2] : mq[3];
+    int j;
+    if (NV > 32) {
+      const uint32_t lo = static_cast<uint32_t>(static_cast<unsigned long long>(m));
+      const int nlo = __popc(lo);
+      j = li < nlo ? static_cast<int>(__fns(lo, 0, li + 1))
+                   : 32 + static_cast<int>(__fns(static_cast<uint32_t>(static_cast<unsigned long long>(m) >> 32),
+                                                 0, li - nlo + 1));
+    } else {
+      j = static_cast<int>(__fns(static_cast<uint32_t>(m), 0, li + 1));
+    }
+    return 16 * (j >> 2) + 4 * qq + (j & 3);
+  };
+
+  // Weights: exp(s[m] - s[0]) for m = q and q + 4 here, gathered over the
+  // token's four threads and summed in slot order.
+  const float m0 = s[0];
+  const float sq = q == 0 ? s[0] : q == 1 ? s[1] : q == 2 ? s[2] : s[3];
+  const float sq4 = q == 0 ? s[4] : q == 1 ? s[5] : q == 2 ? s[6] : s[7];
+  const float exa = (live && q < k) ? expf(sq - m0) : 0.f;
+  const float exb = (live && q + 4 < k) ? expf(sq4 - m0) : 0.f;
+  float ex[8];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    ex[m] = __shfl_sync(0xffffffffu, exa, (lane & ~3) + m);
+    ex[m + 4] = __shfl_sync(0xffffffffu, exb, (lane & ~3) + m);
+  }
+  float sum = 0.f;
+#pragma unroll
+  for (int m = 0; m < 8; ++m)
+    if (m < k) sum += ex[m];
+  if (live) {
+    // 3. slots of the chosen values; writes
+    auto emit = [&](float x, int e, int ties_below) {
+      int slot = ties_below;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) slot += (m < k && s[m] > x) ? 1 : 0;
+      if (e < 0 || e >= E || slot >= k) {
+        report(ws, MOE_ERR_BOUNDS, 1, t);
+        return;
+      }
+      float exs = ex[0];
+#pragma unroll
+      for (int m = 1; m < 8; ++m)
+        if (slot == m) exs = ex[m];
+      ids[static_cast<size_t>(t) * k + slot] = e;
+      wts[static_cast<size_t>(t) * k + slot] = exs / sum;
+      atomicOr(&bm[e * 2 + (tl >> 5)], 1u << (tl & 31));
+      atomicAdd(&cnt[e], 1);
+    };
+    if (ntot == k) {
+      // The token's k chosen values, spread evenly: this thread takes entries
+      // q and q + 4 of the concatenation of the four threads' lists; the
+      // values are read back from the row (an L1 hit).
+      for (int c = q; c < k; c += 4) {
+        const int qq = c < nq[0] ? 0 : c < nq[0] + nq[1] ? 1 : c < nq[0] + nq[1] + nq[2] ? 2 : 3;
+        const int li = c - (qq > 0 ? nq[0] : 0) - (qq > 1 ? nq[1] : 0) - (qq > 2 ? nq[2] : 0);
+        const int e = expert_of(qq, li);
+        float x = __ldg(row + e);
+        if (!isfinite(x)) x = -INFINITY;
+        int dup = 0;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) dup += (m < k && s[m] == x) ? 1 : 0;
+        int ties_below = 0;
+        if (dup > 1) {  // equal chosen values: the lower ids take the earlier slots
+          for (int q2 = 0; q2 < 4; ++q2)
+            for (int l2 = 0; l2 < nq[q2]; ++l2) {
+              const int e2 = expert_of(q2, l2);
+              float x2 = __ldg(row + e2);
+              if (!isfinite(x2)) x2 = -INFINITY;
+              ties_below += (x2 == x && e2 < e) ? 1 : 0;
+            }
+        }
+        emit(x, e, ties_below);
+      }
+    } else if (q == 0) {
+      // More values equal th than slots left: ascending id order, every value
+      // > th and the first `need` equal to th; equal chosen values take slots
+      // in id order.
+      float* chosen = cand_x + tl * kTopkFastK;
+      int left = need, nch = 0;
+      for (int e = 0; e < E && nch < k; ++e) {
+        float x = row[e];
+        if (!isfinite(x)) x = -INFINITY;
+        if (!(x > th || (x == th && left > 0))) continue;
+        if (!(x > th)) --left;
+        int below = 0;
+        for (int c = 0; c < nch; ++c) below += (chosen[c] == x) ? 1 : 0;
+        chosen[nch++] = x;
+        emit(x, e, below);
+      }
+    }
+  }
+  __syncthreads();
+  const int t0 = blockIdx.x * kTopkTokens;
+  const int chunk = t0 / kChunk;
+  const int w0 = (t0 % kChunk) / 32;
+  uint32_t* out = gbm + static_cast<size_t>(chunk) * E * kChunkWords;
+  for (int i = threadIdx.x; i < 2 * E; i += blockDim.x) out[(i >> 1) * kChunkWords + w0 + (i & 1)] = bm[i];
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    if (cnt[e] != 0) atomicAdd(&ccount[static_cast<size_t>(chunk) * E + e], cnt[e]);
+}
+
 // Per expert (one warp each): exclusive prefix of the chunk counts over the
 // chunks -- the O_all of Algorithm 1 -- and the expert's row count.  The last
-// CTA to finish (ticket) then takes the prefix over experts and writes the
-// 128-row tile table.
+// CTA to finish (ticket) then takes the prefix over experts of the row counts
+// (offsets) and of the 128-row tile counts (first tile of each expert); the
+// tile entries themselves are written by route_rank.
 __global__ void __launch_bounds__(32 * kScanWarps) route_scan_kernel(const int32_t* __restrict__ ccount,
                                                                      int nchunks, int E, int32_t* __restrict__ cbase,
                                                                      int32_t* __restrict__ counts,
@@ -142,17 +409,26 @@ __global__ void __launch_bounds__(32 * kScanWarps) route_scan_kernel(const int32
   const int e = blockIdx.x * kScanWarps + warp;
   if (e < E) {
     int run = 0;
-    for (int c0 = 0; c0 < nchunks; c0 += 32) {
-      const int c = c0 + lane;
-      const int v = (c < nchunks) ? ccount[static_cast<size_t>(c) * E + e] : 0;
-      int incl = v;
+    // 8 x 32 chunks per pass: all of a pass's loads are in flight before its scans.
+    for (int c0 = 0; c0 < nchunks; c0 += 256) {
+      int v[8];
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += y;
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + 32 * u + lane;
+        v[u] = (c < nchunks) ? ccount[static_cast<size_t>(c) * E + e] : 0;
       }
-      if (c < nchunks) cbase[static_cast<size_t>(c) * E + e] = run + incl - v;
-      run += __shfl_sync(0xffffffffu, incl, 31);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + 32 * u + lane;
+        int incl = v[u];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += y;
+        }
+        if (c < nchunks) cbase[static_cast<size_t>(c) * E + e] = run + incl - v[u];
+        run += __shfl_sync(0xffffffffu, incl, 31);
+      }
     }
     if (lane == 0) counts[e] = run;
   }
@@ -195,24 +471,14 @@ __global__ void __launch_bounds__(32 * kScanWarps) route_scan_kernel(const int32
     run_n += s_wsum_n[w];
     run_m += s_wsum_m[w];
   }
-  const int entries = tiles_entry_base(E);
   for (int i = 0; i < per; ++i) {
     const int ee = e0 + i;
     if (ee >= E) break;
     const int n = __ldcg(counts + ee);
-    const int mt = (n + kTileRows - 1) / kTileRows;
     offsets[ee] = run_n;
     tiles[1 + ee] = run_m;
-    for (int j = 0; j < mt; ++j) {
-      int4 ent;
-      ent.x = ee;
-      ent.y = run_n + kTileRows * j;
-      ent.z = min(kTileRows, n - kTileRows * j);
-      ent.w = 0;
-      reinterpret_cast<int4*>(tiles + entries)[run_m + j] = ent;
-    }
     run_n += n;
-    run_m += mt;
+    run_m += (n + kTileRows - 1) / kTileRows;
     if (ee == E - 1) {
       offsets[E] = run_n;
       tiles[1 + E] = run_m;
@@ -221,52 +487,147 @@ __global__ void __launch_bounds__(32 * kScanWarps) route_scan_kernel(const int32
   }
 }
 
-// One CTA per 64 tokens: stable index = popcount of the chunk's bitmap below
-// the token; dest, row_src, row_slot.
+// One CTA per 256-token chunk: stable index = popcount of the chunk's bitmap
+// below the token; dest, row_src, row_slot.  The chunk's rows of expert e form
+// one run [base_e, base_e + c_e) of the grouped buffer, so the inverse table is
+// first assembled in shared memory in expert order and then written run by
+// run (contiguous stores instead of one scattered store per row).  Each CTA
+// also writes its share of the 128-row tile entries {expert, first row, rows}.
+constexpr int kRankItems = 8;  // items per thread whose ids are loaded before the prologue
+
 __global__ void __launch_bounds__(256) route_rank_kernel(const int32_t* __restrict__ ids,
                                                          const uint32_t* __restrict__ gbm,
                                                          const int32_t* __restrict__ cbase,
-                                                         const int32_t* __restrict__ offsets, int T, int E, int k,
-                                                         int R, int32_t* __restrict__ dest,
-                                                         int32_t* __restrict__ row_src,
+                                                         const int32_t* __restrict__ offsets,
+                                                         const int32_t* __restrict__ counts,
+                                                         int32_t* __restrict__ tiles, int T, int E, int k, int R,
+                                                         int32_t* __restrict__ dest, int32_t* __restrict__ row_src,
                                                          uint8_t* __restrict__ row_slot, WsHeader* ws) {
   extern __shared__ uint32_t sm[];
-  uint32_t* words = sm;     // [E][2]: this CTA's two words
-  uint32_t* pre = sm + 2 * E;  // [E][2]: popcount of the chunk's words before each
-  const int t0 = blockIdx.x * kTopkTokens;
-  const int chunk = t0 / kChunk;
-  const int w0 = (t0 % kChunk) / 32;
-  const uint32_t* src = gbm + static_cast<size_t>(chunk) * E * kChunkWords;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    uint32_t run = 0;
-    for (int w = 0; w < w0; ++w) run += __popc(src[e * kChunkWords + w]);
-    const uint32_t a = src[e * kChunkWords + w0], b = src[e * kChunkWords + w0 + 1];
-    words[2 * e] = a;
-    words[2 * e + 1] = b;
-    pre[2 * e] = run;
-    pre[2 * e + 1] = run + __popc(a);
+  __shared__ int s_wsum[8];
+  uint32_t* words = sm;                                      // [E][8] the chunk's bitmap words
+  uint32_t* lpre = words + kChunkWords * E;                  // [E][8] rank within the chunk of each word's first token
+  int* base = reinterpret_cast<int*>(lpre + kChunkWords * E);  // [E] first grouped row of the chunk's run of e
+  int* loff = base + E;                                      // [E + 1] start of e's run in the staging arrays
+  int* tstart = loff + E + 1;                                // [E + 1] first tile of each expert
+  int* st_src = tstart + E + 1;                              // [256 k] staging: token of each run position
+  uint16_t* st_e = reinterpret_cast<uint16_t*>(st_src + kChunk * k);  // expert of each run position
+  uint8_t* st_slot = reinterpret_cast<uint8_t*>(st_e + kChunk * k);   // slot of each run position
+  const int chunk = blockIdx.x;
+  const int t0 = chunk * kChunk;
+  const int n_items = min(kChunk, T - t0) * k;
+  const int32_t* my_ids = ids + static_cast<size_t>(t0) * k;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // Item i is slot i % k of token t0 + i / k.  The first kRankItems ids of
+  // this thread are loaded before the prologue so their latency overlaps it.
+  int ev[kRankItems];
+#pragma unroll
+  for (int u = 0; u < kRankItems; ++u) {
+    const int i = threadIdx.x + 256 * u;
+    ev[u] = (i < n_items) ? __ldg(my_ids + i) : 0;
   }
+  const uint4* src = reinterpret_cast<const uint4*>(gbm + static_cast<size_t>(chunk) * E * kChunkWords);
+  // Thread tid owns experts [tid * per, tid * per + per): their words, local
+  // prefixes and chunk counts; a block-wide scan of the counts gives loff.
+  const int per = (E + 255) / 256;
+  int my_cnt = 0;
+  for (int u = 0; u < per; ++u) {
+    const int e = threadIdx.x * per + u;
+    if (e >= E) break;
+    const uint4 a = __ldg(src + 2 * e), b = __ldg(src + 2 * e + 1);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    base[e] = __ldg(offsets + e) + __ldg(cbase + static_cast<size_t>(chunk) * E + e);
+    uint32_t run = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      words[e * 8 + j] = w[j];
+      lpre[e * 8 + j] = run;
+      run += __popc(w[j]);
+    }
+    loff[e] = my_cnt;  // thread-local prefix, completed below
+    my_cnt += static_cast<int>(run);
+  }
+  int incl = my_cnt;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) s_wsum[warp] = incl;
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) tstart[e] = __ldg(tiles + 1 + e);
   __syncthreads();
-  const int n_items = min(kTopkTokens, T - t0) * k;
-  for (int i = threadIdx.x; i < n_items; i += blockDim.x) {
+  int excl = incl - my_cnt;
+  for (int w = 0; w < warp; ++w) excl += s_wsum[w];
+  for (int u = 0; u < per; ++u) {
+    const int e = threadIdx.x * per + u;
+    if (e >= E) break;
+    loff[e] += excl;
+  }
+  if (threadIdx.x == 255) loff[E] = excl + my_cnt;
+  __syncthreads();
+
+  auto place = [&](int i, int e) {
     const int tl = i / k, j = i - tl * k;
     const int t = t0 + tl;
-    const size_t tk = static_cast<size_t>(t) * k + j;
-    const int e = ids[tk];
     if (e < 0 || e >= E) {
       report(ws, MOE_ERR_BOUNDS, 2, t);
-      continue;
+      return;
     }
     const int w = tl >> 5, b = tl & 31;
-    const int rank = pre[2 * e + w] + __popc(words[2 * e + w] & ((1u << b) - 1u));
-    const int r = offsets[e] + cbase[static_cast<size_t>(chunk) * E + e] + rank;
+    const int rho = static_cast<int>(lpre[e * 8 + w] + __popc(words[e * 8 + w] & ((1u << b) - 1u)));
+    const int r = base[e] + rho;
     if (r < 0 || r >= R) {
       report(ws, MOE_ERR_BOUNDS, 2, t);
+      return;
+    }
+    dest[static_cast<size_t>(t0) * k + i] = r;
+    const int pos = loff[e] + rho;
+    if (pos < 0 || pos >= kChunk * k) {
+      report(ws, MOE_ERR_BOUNDS, 2, t);
+      return;
+    }
+    st_src[pos] = t;
+    st_e[pos] = static_cast<uint16_t>(e);
+    st_slot[pos] = static_cast<uint8_t>(j);
+  };
+#pragma unroll
+  for (int u = 0; u < kRankItems; ++u) {
+    const int i = threadIdx.x + 256 * u;
+    if (i < n_items) place(i, ev[u]);
+  }
+  for (int i = threadIdx.x + 256 * kRankItems; i < n_items; i += 256) place(i, __ldg(my_ids + i));
+  __syncthreads();
+  // Run positions in expert order -> consecutive grouped rows.
+  const int n_pos = min(loff[E], kChunk * k);
+  for (int pos = threadIdx.x; pos < n_pos; pos += 256) {
+    const int e = st_e[pos];
+    const int r = e < E ? base[e] + (pos - loff[e]) : -1;
+    if (r < 0 || r >= R) {
+      report(ws, MOE_ERR_BOUNDS, 2, t0);
       continue;
     }
-    dest[tk] = r;
-    row_src[r] = t;
-    row_slot[r] = static_cast<uint8_t>(j);
+    row_src[r] = st_src[pos];
+    row_slot[r] = st_slot[pos];
+  }
+
+  // Tile entries [m0, m1) of this CTA: the expert of tile m is the last e
+  // with tstart[e] <= m.
+  const int ntiles = tstart[E];
+  const int tper = (ntiles + gridDim.x - 1) / gridDim.x;
+  const int m0 = blockIdx.x * tper, m1 = min(ntiles, m0 + tper);
+  int4* ent = reinterpret_cast<int4*>(tiles + tiles_entry_base(E));
+  for (int m = m0 + threadIdx.x; m < m1; m += blockDim.x) {
+    int lo = 0, hi = E;  // tstart[lo] <= m < tstart[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (tstart[mid] <= m)
+        lo = mid;
+      else
+        hi = mid;
+    }
+    const int j = m - tstart[lo];
+    const int n = __ldg(counts + lo);
+    ent[m] = make_int4(lo, __ldg(offsets + lo) + kTileRows * j, min(kTileRows, n - kTileRows * j), 0);
   }
 }
 
@@ -280,6 +641,29 @@ cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t s, LaunchHook& hook) {
   if (err != cudaSuccess) return err;
   const size_t topk_smem = static_cast<size_t>(p.E) * 3 * 4;
   hook.before(s);
+  const int nv4 = (p.E + 15) / 16;
+  if (p.E % 4 == 0 && p.E <= 256 && p.k <= kTopkFastK) {
+    const size_t smem4 = (static_cast<size_t>(p.E) * 3 + static_cast<size_t>(kTopkTokens) * kTopkFastK) * 4;
+    const bool full = (p.E % 16) == 0;
+    switch ((nv4 <= 1 ? 1 : nv4 <= 2 ? 2 : nv4 <= 4 ? 4 : nv4 <= 8 ? 8 : 16) * (full ? 1 : -1)) {
+#define MOE_TOPK4_CASE(NV4, FULL)                                                                              \
+  case (FULL ? NV4 : -NV4):                                                                                    \
+    route_topk4_kernel<NV4, FULL><<<nblocks, kTopkThreads, smem4, s>>>(p.logits, p.T, p.E, p.k, p.ids, p.w,    \
+                                                                       p.gbm, p.ccount, p.ws);                 \
+    break;
+      MOE_TOPK4_CASE(1, true)
+      MOE_TOPK4_CASE(2, true)
+      MOE_TOPK4_CASE(4, true)
+      MOE_TOPK4_CASE(8, true)
+      MOE_TOPK4_CASE(16, true)
+      MOE_TOPK4_CASE(1, false)
+      MOE_TOPK4_CASE(2, false)
+      MOE_TOPK4_CASE(4, false)
+      MOE_TOPK4_CASE(8, false)
+      MOE_TOPK4_CASE(16, false)
+#undef MOE_TOPK4_CASE
+    }
+  } else {
   switch (nv <= 1 ? 1 : nv <= 2 ? 2 : nv <= 4 ? 4 : nv <= 8 ? 8 : nv <= 16 ? 16 : 32) {
 #define MOE_TOPK_CASE(NV, TPW)                                                                                 \
   case NV:                                                                                                     \
@@ -294,6 +678,7 @@ cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t s, LaunchHook& hook) {
     MOE_TOPK_CASE(32, 1)
 #undef MOE_TOPK_CASE
   }
+  }
   hook.after(s);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
@@ -304,8 +689,15 @@ cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t s, LaunchHook& hook) {
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   hook.before(s);
-  route_rank_kernel<<<nblocks, 256, static_cast<size_t>(p.E) * 4 * 4, s>>>(
-      p.ids, p.gbm, p.cbase, p.offsets, p.T, p.E, p.k, p.T * p.k, p.dest, p.row_src, p.row_slot, p.ws);
+  const size_t rank_smem = (static_cast<size_t>(2 * kChunkWords) * p.E + 3 * static_cast<size_t>(p.E) + 2) * 4 +
+                           static_cast<size_t>(kChunk) * p.k * 7;
+  if (rank_smem > 48 * 1024) {
+    err = cudaFuncSetAttribute(route_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(rank_smem));
+    if (err != cudaSuccess) return err;
+  }
+  route_rank_kernel<<<nchunks, 256, rank_smem, s>>>(p.ids, p.gbm, p.cbase, p.offsets, p.counts, p.tiles, p.T, p.E,
+                                                    p.k, p.T * p.k, p.dest, p.row_src, p.row_slot, p.ws);
   hook.after(s);
   return cudaGetLastError();
 }

@@ -22,7 +22,7 @@ def _empty(shape, dtype, device):
 class MoELayer:
     """Buffers of plan, forward and backward for fixed (T, H, F, E, k)."""
 
-    def __init__(self, T, H, F, E, k, device="cuda", with_backward=True):
+    def __init__(self, T, H, F, E, k, device="cuda", with_backward=True, plan_only=False):
         self.dims = moe_dims(T, H, F, E, k)
         self.T, self.H, self.F, self.E, self.k = T, H, F, E, k
         R = T * k
@@ -47,6 +47,8 @@ class MoELayer:
         self.plan_s = moe_plan_t(self.ids.data_ptr(), self.w.data_ptr(), self.counts.data_ptr(),
                                  self.offsets.data_ptr(), self.dest.data_ptr(), self.row_src.data_ptr(),
                                  self.row_slot.data_ptr(), self.tiles.data_ptr())
+        if plan_only:  # routing tables only (profiling the routing kernels)
+            return
         self.Xp = _empty((R, H), bf, dev)
         self.GU = _empty((R, 2 * F), bf, dev)
         self.h = _empty((R, F), bf, dev)
