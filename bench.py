@@ -36,8 +36,8 @@ if ROOT not in sys.path:
 METRIC = "MoE-layer tokens/s fwd+bwd; GEMM % BF16 peak; permute GB/s % HBM"
 UNIT = "tokens/s"
 
-FWD_KERNELS = ["fused_forward", "combine"]
-FWD_KERNELS_PHASED = ["gather_rows", "gemm_fwd1_swiglu", "gemm_fwd2", "combine"]
+FWD_KERNELS = ["gather_rows", "gemm_fwd1_swiglu", "gemm_fwd2", "combine"]
+FWD_KERNELS_FUSED = ["fused_forward", "combine"]
 BWD_KERNELS = ["combine_bwd", "gemm_dgrad2_swiglu_bwd", "gemm_dgrad1", "gemm_wgrad13", "gemm_wgrad2", "unpermute"]
 BWD_KERNELS_FUSED = ["combine_bwd", "fused_backward", "unpermute"]
 N_PLAN_KERNELS = 3
@@ -312,10 +312,10 @@ def run_ours(args):
     inp = S.layer_inputs(shape, seed, device=dev)
     layer = MoELayer(T, H, F, E, k, device=dev)
     stream = torch.cuda.current_stream(dev)
-    fwd_names = FWD_KERNELS_PHASED if args.schedule == 1 else FWD_KERNELS
+    fwd_names = FWD_KERNELS_FUSED if args.schedule in (1, 2) else FWD_KERNELS
     bwd_names = BWD_KERNELS_FUSED if args.schedule == 2 else BWD_KERNELS
     nf, nb = len(fwd_names), len(bwd_names)
-    base_opts = layer.opts(schedule=args.schedule)
+    base_opts = layer.opts(schedule=args.schedule, cta_pair=args.cta_pair)
 
     def step(opts_f=None, opts_b=None, ev_plan=None):
         opts_f = opts_f if opts_f is not None else base_opts
@@ -356,12 +356,12 @@ def run_ours(args):
     opts_f = []
     keep = []
     for e in evs_f:
-        o = layer.opts(events=e, schedule=args.schedule)
+        o = layer.opts(events=e, schedule=args.schedule, cta_pair=args.cta_pair)
         keep.append(layer._ev_keep)
         opts_f.append(o)
     opts_b = []
     for e in evs_b:
-        o = layer.opts(events=e, schedule=args.schedule)
+        o = layer.opts(events=e, schedule=args.schedule, cta_pair=args.cta_pair)
         keep.append(layer._ev_keep)
         opts_b.append(o)
 
@@ -473,8 +473,11 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": dict(workload_config(shape, args.config), parallelism=f"replicas x{world}" if world > 1 else "1 GPU",
-                       schedule={0: "fused forward, per-GEMM backward", 1: "one launch per phase",
-                                 2: "fused forward, fused backward"}[args.schedule]),
+                       schedule={0: "one persistent launch per phase", 1: "fused persistent forward, per-GEMM backward",
+                                 2: "fused forward, fused backward"}[args.schedule],
+                       gemm_tiles={0: "two-CTA 256x256 pair tiles (cta_group::2) except dgrad2: 128x256 single-CTA",
+                                   1: "single-CTA 128x256 tiles (cta_group::1)",
+                                   2: "two-CTA 256x256 pair tiles (cta_group::2)"}[args.cta_pair]),
         "roofline": roof,
         "e2e": {"value": round(world * T * args.steps / (e2e_ms * 1e-3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -519,8 +522,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--schedule", type=int, default=0, choices=[0, 1, 2],
-                    help="0: fused persistent forward, one persistent kernel per backward GEMM; "
-                         "1: one launch per phase; 2: fused forward and fused backward")
+                    help="0: one persistent launch per phase; 1: fused persistent forward, one persistent "
+                         "kernel per backward GEMM; 2: fused forward and fused backward")
+    ap.add_argument("--cta-pair", type=int, default=0, choices=[0, 1, 2],
+                    help="grouped GEMMs that run as their own kernels: 0 library default (pair tiles but for "
+                         "dgrad2), 1 one CTA per tile, 2 two-CTA pair tiles")
     ap.add_argument("--profile", action="store_true",
                     help="run the warm-up steps and one more step only (for ncu captures)")
     ap.add_argument("--part", default="step", choices=["step", "plan"],

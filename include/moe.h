@@ -98,15 +98,21 @@ typedef struct {
 /* Options (may be NULL for defaults). */
 typedef struct {
   int32_t grid;     /* CTAs of the persistent kernels; 0 = one per SM.  Results do not depend on it. */
-  int32_t schedule; /* 0 (default): the forward's gather, GEMM1 and GEMM2 run as one persistent
-                       kernel with a task cursor and per-tile readiness counters; the backward's
-                       four GEMMs run as four persistent kernels.
-                       1: one launch per phase in both passes.
-                       2: as 0, and the backward's four GEMMs also run as one persistent kernel.
+  int32_t schedule; /* 0 (default): one persistent launch per phase in both passes (gather,
+                       GEMM1, GEMM2; the backward's four GEMMs), the fastest measured on GB300.
+                       1: the forward's gather, GEMM1 and GEMM2 run as one persistent kernel with
+                       a task cursor and per-tile readiness counters (single-CTA tiles).
+                       2: as 1, and the backward's four GEMMs also run as one persistent kernel.
                        All three give the same bits. */
   void **events;    /* optional: 2*n_events cudaEvent_t recorded around each kernel of the call */
   int32_t n_events; /* capacity of events/2; kernels beyond it are not timed */
-  int32_t reserved2;
+  int32_t cta_pair; /* tile shape of the grouped GEMMs that run as their own kernels:
+                       1: one CTA per 128 x 256 tile (tcgen05 cta_group::1);
+                       2: a cluster of two CTAs per 256 x 256 tile (cta_group::2, each SM holding
+                       its 128 rows of A and half of B);
+                       0 (default): 2 for every GEMM but the dgrad GEMM with the SwiGLU backward
+                       epilogue, which measured faster with 1.  Both shapes give the same bits.
+                       The fused persistent kernels of schedules 1 and 2 use single-CTA tiles. */
 } moe_opts;
 
 /* ---- sizes ------------------------------------------------------------------ */
@@ -204,7 +210,7 @@ MOE_API int32_t moe_version(void);
 /* Number of kernels this library has launched in this process. */
 MOE_API uint64_t moe_launch_count(void);
 /* Name of the i-th kernel a call launches (call: 0 plan, 1 forward, 2 backward, 3 forward with
- * schedule = 1, 4 backward with schedule = 2); NULL past the end. */
+ * schedule 1 or 2, 4 backward with schedule = 2); NULL past the end. */
 MOE_API const char *moe_kernel_name(int32_t call, int32_t i);
 
 #ifdef __cplusplus

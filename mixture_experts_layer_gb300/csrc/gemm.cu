@@ -80,6 +80,7 @@ struct Maps {
 struct GemmParams {
   int H, F, E, R;
   const int32_t* tiles;
+  const int32_t* pairs;  // first 256-row pair tile of each expert (E + 1)
   const int32_t* offsets;
   const int32_t* counts;
   __nv_bfloat16* out0;
@@ -579,6 +580,371 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// ---------------------------------------------------------------------------
+// Two-SM pair tiles (tcgen05 cta_group::2).
+//
+// A cluster of two CTAs owns one 256 x N output tile: CTA r of the pair holds
+// its 128 rows of A (the 128-row tile 2 pi + r of the expert, or rows
+// m0 + 128 r of a weight gradient) and half of B (columns r N/2 .. of the
+// tile; for the paired W1|W3 and dG|dU tiles, CTA 0 holds the W1 / dG half and
+// CTA 1 the W3 / dU half).  One thread of the even CTA issues the MMAs, which
+// read both CTAs' shared memory and write both CTAs' tensor memory (each CTA
+// holds its own 128 rows x N of the accumulator), so each SM moves half of B
+// into shared memory and reads a third less shared memory per MMA than a
+// 128 x 256 single-CTA tile.
+//
+// Synchronisation per stage: each CTA's TMA loads complete on its own `full`
+// barrier; the odd CTA's warp 1 waits for it (and clears a weight-gradient
+// K tail in its own shared memory) and arrives on the even CTA's `pfull`; the
+// even CTA's warp 1 waits for its own `full`, clears its own tail, waits on
+// `pfull` and issues the MMAs.  MMA completion arrives on `empty` (stage free)
+// and, after a tile's last k-block, on `tfull` in both CTAs (multicast commit).
+// Both CTAs' epilogue warps arrive on the even CTA's `tempty` when they have
+// read their accumulator.  Tile order and arithmetic are those of the
+// single-CTA kernels, so results do not depend on the grid size either.
+// ---------------------------------------------------------------------------
+constexpr int kPairBHalfBytes = 128 * BK * 2;  // half of a 256-wide B tile
+constexpr int kPairStageBytes = kABytes + kPairBHalfBytes;
+
+template <int MODE>
+struct PairTraits {
+  static constexpr bool wgrad = ModeTraits<MODE>::wgrad;
+  static constexpr int kStages = wgrad ? 4 : 6;
+  static constexpr int kStagingBytes = wgrad ? kEpiWarps * kOutBoxes * kStageOutBytes : 0;
+  static constexpr int kSmemBytes = kStages * kPairStageBytes + kStagingBytes + 1024 /*align*/ + 512 /*barriers*/;
+};
+// Shared memory of the staged per-expert tables (4 arrays of E + 1 ints).
+inline size_t pair_table_bytes(int E) { return 4 * (static_cast<size_t>(E) + 1) * 4; }
+
+template <int MODE>
+__device__ __forceinline__ int pair_n_tiles(const GemmParams& p, const int* pairs) {
+  const int nn = n_ntiles<MODE>(p);
+  if (MODE == kWgrad13) return p.E * ((p.H + 255) / 256) * nn;
+  if (MODE == kWgrad2) return p.E * ((p.F + 255) / 256) * nn;
+  return pairs[p.E] * nn;
+}
+
+// This CTA's part of pair tile `tile`: row0 / nrows of its 128-row tile
+// (forward, dgrad; nrows = 0 for the missing half of an expert's last pair) or
+// its 128-row slice m0 of the weight gradient (m0 >= the extent: no rows).
+// Per-expert tables of the pair kernels, staged in shared memory at launch.
+struct ExpertTables {
+  const int* pairs;   // [E + 1] first pair tile
+  const int* counts;  // [E]
+  const int* offsets; // [E]
+  const int* tstart;  // [E]     first 128-row tile
+};
+
+template <int MODE>
+__device__ __forceinline__ Tile pair_decode(const GemmParams& p, const ExpertTables& x, int tile, uint32_t rank) {
+  Tile t;
+  const int nn = n_ntiles<MODE>(p);
+  int nt;
+  if (ModeTraits<MODE>::wgrad) {
+    const int MT2 = ((MODE == kWgrad13 ? p.H : p.F) + 255) / 256;
+    t.e = tile / (MT2 * nn);
+    const int rem = tile - t.e * MT2 * nn;
+    nt = rem / MT2;
+    t.m0 = (rem - nt * MT2) * 256 + 128 * static_cast<int>(rank);
+    t.row0 = x.offsets[t.e];
+    t.nrows = x.counts[t.e];
+    t.kblocks = (t.nrows + BK - 1) / BK;
+    t.mt = -1;
+  } else {
+    // Expert: the last e with pairs[e] * nn <= tile (empty experts own no pairs).
+    int lo = 0, hi = p.E;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (x.pairs[mid] * nn <= tile)
+        lo = mid;
+      else
+        hi = mid;
+    }
+    const int e = lo;
+    const int first = x.pairs[e];
+    const int cnt = x.pairs[e + 1] - first;
+    const int local = tile - nn * first;
+    nt = local / cnt;
+    const int j = 2 * (local - nt * cnt) + static_cast<int>(rank);  // this CTA's 128-row tile of the expert
+    const int n_e = x.counts[e];
+    t.e = e;
+    t.row0 = x.offsets[e] + kTileRows * j;
+    t.nrows = max(0, min(kTileRows, n_e - kTileRows * j));
+    t.m0 = 0;
+    t.mt = x.tstart[e] + j;
+    const int K = (MODE == kFwd1 || MODE == kDgrad2) ? p.H : (MODE == kFwd2) ? p.F : 2 * p.F;
+    t.kblocks = K / BK;
+  }
+  if (ModeTraits<MODE>::paired) {
+    t.n0 = nt * 128;
+    t.nw = 256;
+  } else {
+    t.n0 = nt * BN;
+    t.nw = min(BN, n_extent<MODE>(p) - t.n0);
+  }
+  return t;
+}
+
+// TMA loads of one k-block of this CTA's half: A (its 128 rows) into sA, its
+// half of B into sB.
+template <int MODE>
+__device__ __forceinline__ void load_kblock_pair(const GemmParams& p, const Maps& m, const Tile& t, int kb,
+                                                 uint8_t* sA, uint8_t* sB, uint64_t* bar, uint32_t rank) {
+  const int k0 = kb * BK;
+  const int hb = t.nw / 2;  // B columns of this CTA
+  const int r = static_cast<int>(rank);
+  if (MODE == kFwd1) {
+    tma_load_2d(sA, &m.a, bar, k0, t.row0);
+    const int y = t.e * p.H + k0;
+    const CUtensorMap* w = r ? &m.b1 : &m.b0;  // W1 (G columns) on CTA 0, W3 (U columns) on CTA 1
+    tma_load_2d(sB, w, bar, t.n0, y);
+    tma_load_2d(sB + kPanelBytes, w, bar, t.n0 + 64, y);
+  } else if (MODE == kFwd2) {
+    tma_load_2d(sA, &m.a, bar, k0, t.row0);
+    const int y = t.e * p.F + k0;
+    for (int q = 0; q < hb / 64; ++q) tma_load_2d(sB + q * kPanelBytes, &m.b0, bar, t.n0 + r * hb + 64 * q, y);
+  } else if (MODE == kDgrad2) {
+    tma_load_2d(sA, &m.a, bar, k0, t.row0);
+    tma_load_2d(sB, hb == 128 ? &m.b0 : &m.b2, bar, k0, t.e * p.F + t.n0 + r * hb);
+  } else if (MODE == kDgrad1) {
+    tma_load_2d(sA, &m.a, bar, k0, t.row0);
+    const int yb = t.e * p.H + t.n0 + r * hb;
+    if (k0 < p.F)
+      tma_load_2d(sB, hb == 128 ? &m.b0 : &m.b2, bar, k0, yb);
+    else
+      tma_load_2d(sB, hb == 128 ? &m.b1 : &m.b3, bar, k0 - p.F, yb);
+  } else if (MODE == kWgrad13) {
+    const int y = t.row0 + k0;
+    tma_load_2d(sA, &m.a, bar, t.m0, y);
+    tma_load_2d(sA + kPanelBytes, &m.a, bar, t.m0 + 64, y);
+    const int c = r ? p.F + t.n0 : t.n0;  // dG half on CTA 0, dU half on CTA 1
+    tma_load_2d(sB, &m.b0, bar, c, y);
+    tma_load_2d(sB + kPanelBytes, &m.b0, bar, c + 64, y);
+  } else {  // kWgrad2
+    const int y = t.row0 + k0;
+    tma_load_2d(sA, &m.a, bar, t.m0, y);
+    tma_load_2d(sA + kPanelBytes, &m.a, bar, t.m0 + 64, y);
+    for (int q = 0; q < hb / 64; ++q) tma_load_2d(sB + q * kPanelBytes, &m.b0, bar, t.n0 + r * hb + 64 * q, y);
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_constant__ Maps maps,
+                                                                const GemmParams p) {
+  using TR = ModeTraits<MODE>;
+  constexpr int S = PairTraits<MODE>::kStages;
+  constexpr uint32_t kAStep = TR::a_mn ? 2048u : 32u;
+  constexpr uint32_t kBStep = TR::b_mn ? 2048u : 32u;
+  constexpr uint32_t kIdesc256 = idesc_bf16_f32(256, 256, TR::a_mn, TR::b_mn);
+  constexpr uint32_t kIdesc128 = idesc_bf16_f32(256, 128, TR::a_mn, TR::b_mn);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* staging = smem + S * kPairStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + PairTraits<MODE>::kStagingBytes);
+  uint64_t* empty = full + S;
+  uint64_t* pfull = empty + S;
+  uint64_t* tfull = pfull + S;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* tab = reinterpret_cast<int*>(smem + S * kPairStageBytes + PairTraits<MODE>::kStagingBytes + 512);
+  ExpertTables xt;
+  xt.pairs = tab;
+  xt.counts = tab + (p.E + 1);
+  xt.offsets = tab + 2 * (p.E + 1);
+  xt.tstart = tab + 3 * (p.E + 1);
+  for (int e = threadIdx.x; e <= p.E; e += blockDim.x) {
+    tab[e] = TR::wgrad ? 0 : __ldg(p.pairs + e);
+    tab[(p.E + 1) + e] = e < p.E ? __ldg(p.counts + e) : 0;
+    tab[2 * (p.E + 1) + e] = __ldg(p.offsets + e);
+    tab[3 * (p.E + 1) + e] = __ldg(p.tiles + 1 + e);
+  }
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = (rank == 0);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+      mbar_init(&pfull[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 2 * kEpiWarps);
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&maps.a);
+    tma_prefetch_desc(&maps.b0);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int ntiles = pair_n_tiles<MODE>(p, xt.pairs);
+  const int npairs = gridDim.x >> 1;
+  const int pid = blockIdx.x >> 1;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (both CTAs)
+    int s = 0;
+    uint32_t ph = 0;
+    uint32_t issued = 0, last_parity = 0;
+    bool ok = true;
+    for (int tile = pid; tile < ntiles && ok; tile += npairs) {
+      const Tile t = pair_decode<MODE>(p, xt, tile, rank);
+      for (int kb = 0; kb < t.kblocks; ++kb) {
+        if (!mbar_wait_cluster(&empty[s], ph ^ 1u, p.ws, 200 + MODE, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (elect_one()) {
+          mbar_arrive_expect_tx(&full[s], kABytes + t.nw * 64);
+          uint8_t* sA = smem + s * kPairStageBytes;
+          load_kblock_pair<MODE>(p, maps, t, kb, sA, sA + kABytes, &full[s], rank);
+        }
+        __syncwarp();
+        issued |= 1u << s;
+        last_parity = (last_parity & ~(1u << s)) | (ph << s);
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+    for (int i = 0; i < S; ++i)
+      if ((issued >> i) & 1u) mbar_wait(&full[i], (last_parity >> i) & 1u, p.ws, 210 + MODE, nullptr);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA) / relay (odd CTA)
+    int s = 0;
+    uint32_t ph = 0;
+    int acc = 0;
+    uint32_t acc_ph = 0;
+    bool ok = true;
+    const uint32_t pfull_leader = mapa_shared(smem_u32(pfull), 0);
+    for (int tile = pid; tile < ntiles && ok; tile += npairs) {
+      const Tile t = pair_decode<MODE>(p, xt, tile, rank);
+      if (t.kblocks == 0) continue;  // empty expert (weight gradients): the epilogue writes zeros
+      if (leader) {
+        if (!mbar_wait_cluster(&tempty[acc], acc_ph ^ 1u, p.ws, 220 + MODE, abort_flag)) break;
+        tc_fence_after();
+      }
+      const uint32_t d_tmem = tmem_base + acc * kAccStride;
+      const uint32_t idesc = (t.nw == 256) ? kIdesc256 : kIdesc128;
+      for (int kb = 0; kb < t.kblocks; ++kb) {
+        if (!mbar_wait(&full[s], ph, p.ws, 230 + MODE, abort_flag)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sA = smem + s * kPairStageBytes;
+        uint8_t* sB = sA + kABytes;
+        int nkk = BK / 16;
+        if (TR::wgrad) {
+          const int valid = t.nrows - kb * BK;
+          if (valid < BK) nkk = clear_k_tail(sA, sB, valid, t.nw / 2, lane);
+        }
+        __syncwarp();
+        if (!leader) {
+          if (lane == 0) mbar_arrive_cluster(pfull_leader + s * 8);
+          __syncwarp();
+        } else {
+          if (!mbar_wait_cluster(&pfull[s], ph, p.ws, 240 + MODE, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (elect_one()) {
+            const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              if (kk < nkk) {
+                const uint64_t ad = smem_desc_sw128(a0 + kk * kAStep, TR::a_mn ? kPanelBytes : 16, 1024);
+                const uint64_t bd = smem_desc_sw128(b0 + kk * kBStep, TR::b_mn ? kPanelBytes : 16, 1024);
+                tc_mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+              }
+            }
+            tc_commit_pair(&empty[s]);
+          }
+          __syncwarp();
+        }
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (leader) {
+        if (elect_one()) tc_commit_pair(&tfull[acc]);
+        __syncwarp();
+      }
+      acc ^= 1;
+      if (acc == 0) acc_ph ^= 1u;
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs, own rows)
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int row = q * 32 + lane;
+    const int mext = (MODE == kWgrad13) ? p.H : p.F;
+    OutStager st;
+    st.buf = staging + (warp - 2) * kOutBoxes * kStageOutBytes;
+    const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), 0);
+    int acc = 0;
+    uint32_t acc_ph = 0;
+    for (int tile = pid; tile < ntiles; tile += npairs) {
+      const Tile t = pair_decode<MODE>(p, xt, tile, rank);
+      const bool mine = TR::wgrad ? (t.m0 < mext) : (t.nrows > 0);
+      if (t.kblocks == 0) {
+        if (TR::wgrad && mine) {
+          const int NCall = (MODE == kWgrad13) ? 128 : t.nw;
+          const int c_lo = half * (NCall / 2), c_hi = c_lo + NCall / 2;
+          float* d0 = (MODE == kWgrad13) ? p.f0 + (static_cast<size_t>(t.e) * p.H + t.m0 + row) * p.F + t.n0
+                                         : p.f0 + (static_cast<size_t>(t.e) * p.F + t.m0 + row) * p.H + t.n0;
+          for (int c = c_lo; c < c_hi; c += 32) store_zero_f32(d0 + c);
+          if (MODE == kWgrad13) {
+            float* d1 = p.f1 + (static_cast<size_t>(t.e) * p.H + t.m0 + row) * p.F + t.n0;
+            for (int c = c_lo; c < c_hi; c += 32) store_zero_f32(d1 + c);
+          }
+        }
+        continue;
+      }
+      if (!mbar_wait_cluster(&tfull[acc], acc_ph, p.ws, 250 + MODE, abort_flag)) break;
+      tc_fence_after();
+      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccStride;
+      if (mine) epilogue<MODE>(p, maps, t, tacc, q, half, lane, st);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader)
+          mbar_arrive(&tempty[acc]);
+        else
+          mbar_arrive_cluster(tempty_leader + acc * 8);
+      }
+      acc ^= 1;
+      if (acc == 0) acc_ph ^= 1u;
+    }
+    if (TR::wgrad && lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no CTA leaves while its pair may still use its shared or tensor memory
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
 }
 
 // ---------------------------------------------------------------------------
@@ -1261,6 +1627,70 @@ cudaError_t launch_mode(const GemmLaunch& L, const Maps& maps, const GemmParams&
   return cudaGetLastError();
 }
 
+template <int MODE>
+cudaError_t launch_pair_mode(const GemmLaunch& L, const Maps& maps, const GemmParams& p, cudaStream_t s,
+                             LaunchHook& hook) {
+  const int kSmem = PairTraits<MODE>::kSmemBytes + static_cast<int>(pair_table_bytes(L.E));
+  auto kern = pair_gemm_kernel<MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // At most as many pairs as can be resident at once (a persistent grid).
+  static int max_pairs = -1, max_pairs_smem = -1;
+  if (max_pairs < 0 || max_pairs_smem != kSmem) {
+    max_pairs_smem = kSmem;
+    cfg.gridDim = dim3(2, 1, 1);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      n = 0;
+    }
+    max_pairs = n;
+  }
+  int pairs = L.grid / 2;
+  if (pairs < 1) pairs = 1;
+  if (max_pairs > 0 && pairs > max_pairs) pairs = max_pairs;
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  hook.before(s);
+  e = cudaLaunchKernelEx(&cfg, kern, maps, p);
+  hook.after(s);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+// Tensor maps of the pair kernels: as the single-CTA ones, except that K-major
+// B boxes are half a tile high (128 rows, or 64 for a 128-wide tail tile).
+cudaError_t launch_gemm_pair(GemmMode mode, const GemmLaunch& L, Maps& m, const GemmParams& p, cudaStream_t s,
+                             LaunchHook& hook) {
+  const uint64_t H = L.H, F = L.F, E = L.E;
+  bool ok = true;
+  if (mode == kDgrad2)
+    ok = make_map(&m.b0, L.W2, H, E * F, 64, 128) && make_map(&m.b2, L.W2, H, E * F, 64, 64);
+  else if (mode == kDgrad1)
+    ok = make_map(&m.b0, L.W1, F, E * H, 64, 128) && make_map(&m.b1, L.W3, F, E * H, 64, 128) &&
+         make_map(&m.b2, L.W1, F, E * H, 64, 64) && make_map(&m.b3, L.W3, F, E * H, 64, 64);
+  if (!ok) return cudaErrorInvalidValue;
+  switch (mode) {
+    case kFwd1: return launch_pair_mode<kFwd1>(L, m, p, s, hook);
+    case kFwd2: return launch_pair_mode<kFwd2>(L, m, p, s, hook);
+    case kDgrad2: return launch_pair_mode<kDgrad2>(L, m, p, s, hook);
+    case kDgrad1: return launch_pair_mode<kDgrad1>(L, m, p, s, hook);
+    case kWgrad13: return launch_pair_mode<kWgrad13>(L, m, p, s, hook);
+    case kWgrad2: return launch_pair_mode<kWgrad2>(L, m, p, s, hook);
+  }
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 bool tensor_map_encoder_ready() { return encoder() != nullptr; }
@@ -1286,6 +1716,7 @@ cudaError_t launch_fused_backward(const GemmLaunch& L, int32_t* cursor, int32_t*
   p.E = L.E;
   p.R = L.R;
   p.tiles = L.tiles;
+  p.pairs = L.pairs;
   p.offsets = L.offsets;
   p.counts = L.counts;
   p.ws = L.ws;
@@ -1328,6 +1759,7 @@ cudaError_t launch_fused_forward(const GemmLaunch& L, const void* x, const int32
   p.E = L.E;
   p.R = L.R;
   p.tiles = L.tiles;
+  p.pairs = L.pairs;
   p.offsets = L.offsets;
   p.counts = L.counts;
   p.ws = L.ws;
@@ -1362,6 +1794,7 @@ cudaError_t launch_gemm(GemmMode mode, const GemmLaunch& L, cudaStream_t s, Laun
   p.E = L.E;
   p.R = L.R;
   p.tiles = L.tiles;
+  p.pairs = L.pairs;
   p.offsets = L.offsets;
   p.counts = L.counts;
   p.ws = L.ws;
@@ -1402,6 +1835,7 @@ cudaError_t launch_gemm(GemmMode mode, const GemmLaunch& L, cudaStream_t s, Laun
       break;
   }
   if (!ok) return cudaErrorInvalidValue;
+  if (L.pair) return launch_gemm_pair(mode, L, m, p, s, hook);
   switch (mode) {
     case kFwd1: return launch_mode<kFwd1>(L, m, p, s, hook);
     case kFwd2: return launch_mode<kFwd2>(L, m, p, s, hook);

@@ -13,10 +13,17 @@ constexpr int kTileRows = 128;            // rows of a GEMM tile (the tcgen05 M)
 
 // Layout of moe_plan_t.tiles (int32): [0] number of 128-row tiles; [1 + e]
 // first tile of expert e (E + 1 entries); then, from tiles_entry_base(E),
-// one int4 {expert, first row, rows, 0} per tile in expert order.
+// one int4 {expert, first row, rows, 0} per tile in expert order; then, from
+// tiles_pair_base(R, E), the first 256-row pair of each expert (E + 1 entries).
 __host__ __device__ inline int tiles_entry_base(int E) { return ((E + 2) + 3) & ~3; }
 
 __host__ __device__ inline long long tiles_capacity(long long R, int E) { return R / kTileRows + E + 1; }
+
+// After the entries: E + 1 ints, the first 256-row pair tile of each expert
+// (exclusive prefix of ceil(n_e / 256)), used by the two-SM GEMMs.
+__host__ __device__ inline long long tiles_pair_base(long long R, int E) {
+  return tiles_entry_base(E) + 4 * tiles_capacity(R, E);
+}
 
 extern std::atomic<unsigned long long> g_launches;
 
@@ -52,6 +59,7 @@ struct PlanLaunch {
   int32_t* counts;
   int32_t* offsets;
   int32_t* tiles;
+  int32_t* pairs;  // tiles + tiles_pair_base(R, E)
   int32_t* dest;
   int32_t* row_src;
   uint8_t* row_slot;
@@ -89,8 +97,10 @@ enum GemmMode : int {
 struct GemmLaunch {
   int T, H, F, E, k, R;
   int grid;
-  int bn;  // N of one tile: 256, or 128 when the N extent is not a multiple of 256
+  int bn;    // N of one tile: 256, or 128 when the N extent is not a multiple of 256
+  int pair;  // 1: two-SM pair tiles (cta_group::2), 0: one CTA per 128-row tile
   const int32_t* tiles;
+  const int32_t* pairs;  // first 256-row pair of each expert (tiles + tiles_pair_base)
   const int32_t* offsets;
   const int32_t* counts;
   // operands (bf16)

@@ -120,9 +120,19 @@ int grid_for(const moe_opts* o, int sms) {
 
 int finish(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH; }
 
+// Tile shape of a grouped GEMM launched on its own: the two-CTA pair tile
+// wherever it measured faster (every mode but the dgrad GEMM with the SwiGLU
+// backward epilogue), unless the caller asks for one shape everywhere.
+int use_pair(const moe_opts* o, GemmMode m) {
+  const int c = (o != nullptr) ? o->cta_pair : 0;
+  if (c == 1) return 0;
+  if (c == 2) return 1;
+  return m != kDgrad2;
+}
+
 const char* const kPlanKernels[] = {"route_topk", "route_scan", "route_rank", nullptr};
-const char* const kFwdKernels[] = {"fused_forward", "combine", nullptr};
-const char* const kFwdKernelsPhased[] = {"gather_rows", "gemm_fwd1_swiglu", "gemm_fwd2", "combine", nullptr};
+const char* const kFwdKernelsFused[] = {"fused_forward", "combine", nullptr};
+const char* const kFwdKernels[] = {"gather_rows", "gemm_fwd1_swiglu", "gemm_fwd2", "combine", nullptr};
 const char* const kBwdKernels[] = {"combine_bwd", "gemm_dgrad2_swiglu_bwd", "gemm_dgrad1", "gemm_wgrad13",
                                    "gemm_wgrad2", "unpermute", nullptr};
 const char* const kBwdKernelsFused[] = {"combine_bwd", "fused_backward", "unpermute", nullptr};
@@ -137,6 +147,7 @@ GemmLaunch gemm_common(const moe_dims& d, const moe_plan_t* plan, WsHeader* ws, 
   g.R = d.T * d.k;
   g.grid = grid;
   g.tiles = plan->tiles;
+  g.pairs = plan->tiles + tiles_pair_base(static_cast<long long>(d.T) * d.k, d.E);
   g.offsets = plan->offsets;
   g.counts = plan->counts;
   g.ws = ws;
@@ -157,8 +168,7 @@ size_t moe_workspace_bytes(moe_dims d) {
 
 size_t moe_plan_tiles_elems(moe_dims d) {
   if (check_dims(d) != MOE_OK) return 0;
-  return static_cast<size_t>(tiles_entry_base(d.E)) +
-         4 * static_cast<size_t>(tiles_capacity(static_cast<long long>(d.T) * d.k, d.E));
+  return static_cast<size_t>(tiles_pair_base(static_cast<long long>(d.T) * d.k, d.E)) + d.E + 1;
 }
 
 int moe_plan(moe_dims d, const float* logits, const moe_plan_t* plan, void* ws, size_t ws_bytes, void* stream) {
@@ -186,6 +196,7 @@ int moe_plan(moe_dims d, const float* logits, const moe_plan_t* plan, void* ws, 
   p.counts = plan->counts;
   p.offsets = plan->offsets;
   p.tiles = plan->tiles;
+  p.pairs = plan->tiles + tiles_pair_base(static_cast<long long>(d.T) * d.k, d.E);
   p.dest = plan->dest;
   p.row_src = plan->row_src;
   p.row_slot = plan->row_slot;
@@ -200,7 +211,9 @@ int moe_forward(moe_dims d, const void* x, const void* W1, const void* W3, const
   int rc = check_dims(d);
   if (rc) return rc;
   if ((rc = check_ws(d, ws, ws_bytes))) return rc;
-  if (opts != nullptr && (opts->schedule < 0 || opts->schedule > 2 || opts->grid < 0)) return MOE_ERR_ARG;
+  if (opts != nullptr && (opts->schedule < 0 || opts->schedule > 2 || opts->grid < 0 || opts->cta_pair < 0 ||
+                          opts->cta_pair > 2))
+    return MOE_ERR_ARG;
   if (d.T == 0) return MOE_OK;
   if ((rc = check_plan(plan))) return rc;
   if (saved == nullptr) return MOE_ERR_ARG;
@@ -224,7 +237,7 @@ int moe_forward(moe_dims d, const void* x, const void* W1, const void* W3, const
   g.h = saved->h;
   g.out_Y = saved->Y;
   cudaError_t e;
-  if (opts == nullptr || opts->schedule != 1) {
+  if (opts != nullptr && opts->schedule != 0) {
     const WsLayout L = ws_layout(d);
     uint8_t* sched = static_cast<uint8_t*>(ws) + L.sched;
     if (cudaMemsetAsync(sched, 0, L.sched_bytes, s) != cudaSuccess) return MOE_ERR_LAUNCH;
@@ -237,8 +250,10 @@ int moe_forward(moe_dims d, const void* x, const void* W1, const void* W3, const
     e = launch_gather(r, x, saved->Xp, s, hook);
     if (e != cudaSuccess) return MOE_ERR_LAUNCH;
     g.bn = 256;
+    g.pair = use_pair(opts, kFwd1);
     if ((e = launch_gemm(kFwd1, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
     g.bn = (d.H % 256 == 0) ? 256 : 128;
+    g.pair = use_pair(opts, kFwd2);
     if ((e = launch_gemm(kFwd2, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
   }
   return finish(launch_combine(r, saved->Y, out, s, hook));
@@ -251,7 +266,9 @@ int moe_backward(moe_dims d, const void* dout, const void* W1, const void* W3, c
   int rc = check_dims(d);
   if (rc) return rc;
   if ((rc = check_ws(d, ws, ws_bytes))) return rc;
-  if (opts != nullptr && (opts->schedule < 0 || opts->schedule > 2 || opts->grid < 0)) return MOE_ERR_ARG;
+  if (opts != nullptr && (opts->schedule < 0 || opts->schedule > 2 || opts->grid < 0 || opts->cta_pair < 0 ||
+                          opts->cta_pair > 2))
+    return MOE_ERR_ARG;
   if ((rc = check_ptrs({dW1, dW3, dW2}))) return rc;
   if (d.T > 0) {
     if ((rc = check_plan(plan))) return rc;
@@ -304,12 +321,16 @@ int moe_backward(moe_dims d, const void* dout, const void* W1, const void* W3, c
     if ((e = launch_fused_backward(g, cursor, cnt_d2, cnt_e, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
   } else {
     g.bn = (d.F % 256 == 0) ? 256 : 128;
+    g.pair = use_pair(opts, kDgrad2);
     if ((e = launch_gemm(kDgrad2, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
     g.bn = (d.H % 256 == 0) ? 256 : 128;
+    g.pair = use_pair(opts, kDgrad1);
     if ((e = launch_gemm(kDgrad1, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
     g.bn = 256;
+    g.pair = use_pair(opts, kWgrad13);
     if ((e = launch_gemm(kWgrad13, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
     g.bn = (d.H % 256 == 0) ? 256 : 128;
+    g.pair = use_pair(opts, kWgrad2);
     if ((e = launch_gemm(kWgrad2, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
   }
   return finish(launch_unpermute(r, grads->dXp, dx, s, hook));
@@ -363,7 +384,7 @@ const char* moe_kernel_name(int32_t call, int32_t i) {
   const char* const* t = call == 0   ? kPlanKernels
                          : call == 1 ? kFwdKernels
                          : call == 2 ? kBwdKernels
-                         : call == 3 ? kFwdKernelsPhased
+                         : call == 3 ? kFwdKernelsFused
                          : call == 4 ? kBwdKernelsFused
                                      : nullptr;
   if (t == nullptr || i < 0) return nullptr;

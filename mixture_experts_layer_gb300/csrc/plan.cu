@@ -402,9 +402,10 @@ __global__ void __launch_bounds__(32 * kScanWarps) route_scan_kernel(const int32
                                                                      int nchunks, int E, int32_t* __restrict__ cbase,
                                                                      int32_t* __restrict__ counts,
                                                                      int32_t* __restrict__ offsets,
-                                                                     int32_t* __restrict__ tiles, int32_t* ticket) {
+                                                                     int32_t* __restrict__ tiles,
+                                                                     int32_t* __restrict__ pairs, int32_t* ticket) {
   __shared__ int s_last;
-  __shared__ int s_wsum_n[32], s_wsum_m[32];
+  __shared__ int s_wsum_n[32], s_wsum_m[32], s_wsum_p[32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * kScanWarps + warp;
   if (e < E) {
@@ -442,34 +443,39 @@ __global__ void __launch_bounds__(32 * kScanWarps) route_scan_kernel(const int32
   // 128-row tile counts.  Thread i takes experts [i * per, (i + 1) * per).
   const int per = (E + blockDim.x - 1) / blockDim.x;
   const int e0 = threadIdx.x * per;
-  int my_n = 0, my_m = 0;
+  int my_n = 0, my_m = 0, my_p = 0;
   for (int i = 0; i < per; ++i) {
     const int ee = e0 + i;
     if (ee < E) {
       const int n = __ldcg(counts + ee);
       my_n += n;
       my_m += (n + kTileRows - 1) / kTileRows;
+      my_p += (n + 2 * kTileRows - 1) / (2 * kTileRows);
     }
   }
-  int in_n = my_n, in_m = my_m;
+  int in_n = my_n, in_m = my_m, in_p = my_p;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
     const int yn = __shfl_up_sync(0xffffffffu, in_n, off);
     const int ym = __shfl_up_sync(0xffffffffu, in_m, off);
+    const int yp = __shfl_up_sync(0xffffffffu, in_p, off);
     if (lane >= off) {
       in_n += yn;
       in_m += ym;
+      in_p += yp;
     }
   }
   if (lane == 31) {
     s_wsum_n[warp] = in_n;
     s_wsum_m[warp] = in_m;
+    s_wsum_p[warp] = in_p;
   }
   __syncthreads();
-  int run_n = in_n - my_n, run_m = in_m - my_m;
+  int run_n = in_n - my_n, run_m = in_m - my_m, run_p = in_p - my_p;
   for (int w = 0; w < warp; ++w) {
     run_n += s_wsum_n[w];
     run_m += s_wsum_m[w];
+    run_p += s_wsum_p[w];
   }
   for (int i = 0; i < per; ++i) {
     const int ee = e0 + i;
@@ -477,12 +483,15 @@ __global__ void __launch_bounds__(32 * kScanWarps) route_scan_kernel(const int32
     const int n = __ldcg(counts + ee);
     offsets[ee] = run_n;
     tiles[1 + ee] = run_m;
+    pairs[ee] = run_p;
     run_n += n;
     run_m += (n + kTileRows - 1) / kTileRows;
+    run_p += (n + 2 * kTileRows - 1) / (2 * kTileRows);
     if (ee == E - 1) {
       offsets[E] = run_n;
       tiles[1 + E] = run_m;
       tiles[0] = run_m;
+      pairs[E] = run_p;
     }
   }
 }
@@ -684,7 +693,7 @@ cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t s, LaunchHook& hook) {
   if (err != cudaSuccess) return err;
   hook.before(s);
   route_scan_kernel<<<(p.E + kScanWarps - 1) / kScanWarps, 32 * kScanWarps, 0, s>>>(
-      p.ccount, nchunks, p.E, p.cbase, p.counts, p.offsets, p.tiles, p.ticket);
+      p.ccount, nchunks, p.E, p.cbase, p.counts, p.offsets, p.tiles, p.pairs, p.ticket);
   hook.after(s);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
@@ -792,6 +801,7 @@ extern "C" int moe_plan_noalloc(moe_dims d, const float* logits, const moe_plan_
   p.counts = plan->counts;
   p.offsets = plan->offsets;
   p.tiles = plan->tiles;
+  p.pairs = plan->tiles + tiles_pair_base(static_cast<long long>(d.T) * d.k, d.E);
   p.dest = plan->dest;
   p.row_src = plan->row_src;
   p.row_slot = plan->row_slot;
