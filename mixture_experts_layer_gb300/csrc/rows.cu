@@ -1,6 +1,7 @@
-// Row-wise, HBM-bound steps of the layer: dispatch (row gather), gated
-// combine, combine backward, dispatch backward.  One warp per row or token,
-// 16-byte vector loads and stores, grid-stride over the rows.
+// Row-wise, HBM-bound steps of the layer: dispatch (a gather by grouped row,
+// or a scatter of each token's row to its k grouped rows when x is large),
+// gated combine, combine backward, dispatch backward.  One warp per row or
+// token, 16-byte vector loads and stores, grid-stride.
 //
 // Sources: "UniEP: Unified Expert-Parallel MoE MegaKernel for LLM Training",
 // section 3.1 (Comm-Worker: one warp per token, 128-bit vector loads) and
@@ -43,6 +44,9 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
   return v;
 }
 
+// Dispatch as a gather, one warp per grouped row: Xp[r] = x[row_src[r]].
+// Used while x fits comfortably in L2 (its re-reads are L2 hits), where the
+// R rows give more parallelism than the T tokens.
 __global__ void __launch_bounds__(kThreads) gather_rows_kernel(const uint4* __restrict__ x,
                                                                  const int32_t* __restrict__ row_src,
                                                                  uint4* __restrict__ Xp, int R, int T, int hv,
@@ -70,6 +74,18 @@ __global__ void __launch_bounds__(kThreads) gather_rows_kernel(const uint4* __re
   }
 }
 
+// Dispatch as a scatter, one warp per token: x[t] is read once and written to
+// its k grouped rows Xp[dest[t, j]] (the Comm-Worker of "UniEP", section 3.1:
+// one warp per token, 128-bit vector loads; "MoonEP": zero-copy dispatch into
+// the expert-grouped layout).  Reading each token once keeps the HBM traffic at
+// 2TH + 2RH even when x does not fit in L2, which a gather over the grouped
+// rows (x re-read once per slot) would not.
+template <int K>
+__global__ void __launch_bounds__(kThreads) scatter_rows_kernel(const uint4* __restrict__ x,
+                                                                  const int32_t* __restrict__ dest,
+                                                                  uint4* __restrict__ Xp, int T, int k, int R,
+                                                                  int hv, WsHeader* ws);
+
 // The k (row, weight) pairs of token t, held in registers by every lane
 // (K = compile-time bound on k).  Returns false (and reports) if a row index is
 // out of range.
@@ -93,6 +109,42 @@ __device__ __forceinline__ bool token_rows(const int32_t* dest, const float* w, 
     ws_[j] = __shfl_sync(0xffffffffu, my_w, j);
   }
   return true;
+}
+
+template <int K>
+__global__ void __launch_bounds__(kThreads) scatter_rows_kernel(const uint4* __restrict__ x,
+                                                                  const int32_t* __restrict__ dest,
+                                                                  uint4* __restrict__ Xp, int T, int k, int R,
+                                                                  int hv, WsHeader* ws) {
+  const int lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * (kThreads / 32);
+  for (int t = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); t < T; t += nwarps) {
+    int rows[K];
+    float unused[K];
+    if (!token_rows<K>(dest, nullptr, t, k, R, lane, rows, unused, ws, 10)) continue;
+    const uint4* src = x + static_cast<size_t>(t) * hv;
+    int v = lane;
+    for (; v + 96 < hv; v += 128) {
+      const uint4 a = ldg_nc(src + v), b = ldg_nc(src + v + 32), c = ldg_nc(src + v + 64),
+                  d = ldg_nc(src + v + 96);
+#pragma unroll
+      for (int j = 0; j < K; ++j) {
+        if (j < k) {
+          uint4* dst = Xp + static_cast<size_t>(rows[j]) * hv;
+          dst[v] = a;
+          dst[v + 32] = b;
+          dst[v + 64] = c;
+          dst[v + 96] = d;
+        }
+      }
+    }
+    for (; v < hv; v += 32) {
+      const uint4 a = ldg_nc(src + v);
+#pragma unroll
+      for (int j = 0; j < K; ++j)
+        if (j < k) Xp[static_cast<size_t>(rows[j]) * hv + v] = a;
+    }
+  }
 }
 
 // out[t] = bf16(sum_j w[t,j] Y[dest[t,j]]), slots in ascending order.
@@ -213,8 +265,16 @@ __global__ void __launch_bounds__(kThreads) unpermute_kernel(const uint4* __rest
 
 cudaError_t launch_gather(const RowsLaunch& p, const void* x, void* Xp, cudaStream_t s, LaunchHook& hook) {
   hook.before(s);
-  gather_rows_kernel<<<p.grid, kThreads, 0, s>>>(static_cast<const uint4*>(x), p.row_src, static_cast<uint4*>(Xp),
-                                                  p.R, p.T, p.H / 8, p.ws);
+  // x up to 32 MB: gather by grouped row (re-reads hit L2); larger: scatter by token.
+  if (static_cast<size_t>(p.T) * p.H * 2 <= (size_t(32) << 20))
+    gather_rows_kernel<<<p.grid, kThreads, 0, s>>>(static_cast<const uint4*>(x), p.row_src,
+                                                    static_cast<uint4*>(Xp), p.R, p.T, p.H / 8, p.ws);
+  else if (p.k <= 8)
+    scatter_rows_kernel<8><<<p.grid, kThreads, 0, s>>>(static_cast<const uint4*>(x), p.dest,
+                                                        static_cast<uint4*>(Xp), p.T, p.k, p.R, p.H / 8, p.ws);
+  else
+    scatter_rows_kernel<kMaxK><<<p.grid, kThreads, 0, s>>>(static_cast<const uint4*>(x), p.dest,
+                                                            static_cast<uint4*>(Xp), p.T, p.k, p.R, p.H / 8, p.ws);
   hook.after(s);
   return cudaGetLastError();
 }

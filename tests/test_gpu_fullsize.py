@@ -57,6 +57,9 @@ def _sampled(idx, n_tokens, experts_fn):
 
     W = lambda e: (f64(inp["W1"][e]), f64(inp["W3"][e]), f64(inp["W2"][e]))
     rng = np.random.default_rng(1000 + idx)
+    # Dispatched rows: a copy, bit-exact (sampled rows of Xp against x[row_src]).
+    rs = torch.as_tensor(rng.choice(layer.R, size=min(layer.R, 4096), replace=False), device="cuda")
+    assert torch.equal(layer.Xp[rs], inp["x"][torch.as_tensor(perm.row_src, device="cuda")[rs]]), "Xp rows"
     toks = sorted(rng.choice(shape.T, size=n_tokens, replace=False).tolist())
     tk = torch.tensor(toks, device="cuda")
     s = O.token_rows(toks, f64(inp["x"][tk]), f64(inp["dout"][tk]), ids, w, W, mirror=True)

@@ -22,6 +22,8 @@ CASES = {
     "E_eq_k": (S.LayerShape(130, 128, 256, 4, 4), 14, None),
     "one_token": (S.LayerShape(1, 256, 128, 6, 2), 15, None),
     "empty_experts": (S.LayerShape(512, 256, 256, 32, 4), 16, "skew"),
+    # x of 34 MB: the dispatch runs as a scatter by token instead of a gather by row
+    "scatter_dispatch": (S.LayerShape(2100, 8192, 128, 8, 2), 19, None),
 }
 
 
