@@ -20,8 +20,8 @@
 //              half of the tile's columns: tcgen05.ld of the fp32 accumulator
 //              (the next chunk's load in flight while this one is stored),
 //              fused elementwise work (SwiGLU forward or backward), stores.  The
-//              fp32 weight gradients go out through swizzled shared-memory
-//              staging and TMA bulk stores, one 32x32 box per warp at a time.
+//              fp32 weight gradients go out through a swizzled shared-memory
+//              box per warp, re-read row-wise for coalesced 16-byte stores.
 // The accumulator is double-buffered in tensor memory (2 x 256 columns), so the
 // epilogue of one tile overlaps the main loop of the next.
 //
@@ -53,7 +53,6 @@ constexpr int kABytes = BM * BK * 2;
 constexpr int kBBytesMax = BN * BK * 2;
 constexpr int kStageBytes = kABytes + kBBytesMax;
 constexpr int kStageOutBytes = 32 * 128;  // one warp's 32x32 fp32 staging box
-constexpr int kOutBoxes = 2;              // staging boxes per epilogue warp (stores in flight)
 
 template <int MODE>
 struct ModeTraits {
@@ -62,8 +61,8 @@ struct ModeTraits {
   static constexpr bool b_mn = (MODE == kFwd1 || MODE == kFwd2 || wgrad);
   // Output columns per tile are 2 x 128 (two weights side by side) or up to 256.
   static constexpr bool paired = (MODE == kFwd1 || MODE == kWgrad13);
-  static constexpr int kStages = wgrad ? 3 : 4;
-  static constexpr int kStagingBytes = wgrad ? kEpiWarps * kOutBoxes * kStageOutBytes : 0;
+  static constexpr int kStages = 4;
+  static constexpr int kStagingBytes = wgrad ? kEpiWarps * kStageOutBytes : 0;
   static constexpr int kSmemBytes = kStages * kStageBytes + kStagingBytes + 1024 /*align*/ + 256 /*barriers*/;
 };
 
@@ -73,8 +72,6 @@ struct Maps {
   CUtensorMap b1;  // second B tensor (W3), full-width box
   CUtensorMap b2;  // B, 128-row box for a 128-wide tail tile (K-major B only)
   CUtensorMap b3;  // W3, 128-row box
-  CUtensorMap o0;  // fp32 output (weight gradients), 32x32 box
-  CUtensorMap o1;
 };
 
 struct GemmParams {
@@ -226,28 +223,33 @@ __device__ __forceinline__ void store_zero_f32(float* dst) {
   for (int i = 0; i < 32; i += 4) st_v4(dst + i, 0u, 0u, 0u, 0u);
 }
 
-// One warp's fp32 output path: its 32 rows x 32 columns go to a 128B-swizzled
-// staging box in shared memory, then one lane issues a TMA bulk store.  The
-// warp cycles through kOutBoxes boxes, so that many stores are in flight; a box
-// is reused only after its previous store has finished reading shared memory.
+// One warp's fp32 output path (weight gradients): its 32 rows x 32 columns go
+// to a 128B-swizzled 4 KB box in shared memory, are read back row-wise (8 lanes
+// per 128-byte row, conflict-free) and written with plain 16-byte stores, each
+// store instruction covering 4 whole rows.  (TMA bulk stores of the same boxes
+// measured slower: one 4 KB bulk store at a time kept each SM near 16 B/clk.)
 struct OutStager {
-  uint8_t* buf;  // kOutBoxes boxes of 4 KB, 1024-byte aligned
-  int next = 0;
-  __device__ __forceinline__ void put(const CUtensorMap* map, const uint32_t (&r)[32], int x, int y, int lane) {
-    uint8_t* box = buf + next * kStageOutBytes;
-    if (lane == 0) bulk_wait_read<kOutBoxes - 1>();
-    __syncwarp();
-    const uint32_t row = smem_u32(box) + lane * 128;
+  uint8_t* buf;  // one 4 KB box, 1024-byte aligned
+  // dst points at the block's first element; ld is the row stride in floats.
+  __device__ __forceinline__ void put(float* dst, size_t ld, const uint32_t (&r)[32], int lane) {
+    const uint32_t base = smem_u32(buf);
+    const uint32_t row = base + lane * 128;
 #pragma unroll
     for (int j = 0; j < 8; ++j)
       st_shared_v4(row + ((j ^ (lane & 7)) << 4), r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
-    fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) {
-      tma_store_2d(map, box, x, y);
-      bulk_commit();
+    const int j = lane & 7;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int rr = 4 * i + (lane >> 3);
+      uint32_t a, b, c, d;
+      asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+                   : "r"(base + rr * 128 + ((j ^ (rr & 7)) << 4)));
+      float* q = dst + static_cast<size_t>(rr) * ld + 4 * j;
+      asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(q), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
     }
-    next = (next + 1 == kOutBoxes) ? 0 : next + 1;
+    __syncwarp();
   }
 };
 
@@ -280,9 +282,10 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, const Maps& m, con
   const int c_lo = half * (NCall / 2), c_hi = c_lo + NCall / 2;
   if (ModeTraits<MODE>::wgrad) {
     const int y = (MODE == kWgrad13) ? t.e * p.H + t.m0 + q * 32 : t.e * p.F + t.m0 + q * 32;
+    const size_t ld = (MODE == kWgrad13) ? p.F : p.H;
 #pragma unroll 1
     for (int out = 0; out < ((MODE == kWgrad13) ? 2 : 1); ++out) {
-      const CUtensorMap* map = out ? &m.o1 : &m.o0;
+      float* obase = (out ? p.f1 : p.f0) + static_cast<size_t>(y) * ld;
       const uint32_t tbase = tacc + (out ? 128 : 0);
       uint32_t a[32];
       tc_ld_32x32b_x32(tbase + c_lo, a);
@@ -292,7 +295,7 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, const Maps& m, con
         const bool more = c + 32 < c_hi;
         uint32_t b[32];
         if (more) tc_ld_32x32b_x32(tbase + c + 32, b);  // next chunk in flight during this chunk's stores
-        st.put(map, a, t.n0 + c, y, lane);
+        st.put(obase + t.n0 + c, ld, a, lane);
         if (more) {
           tc_wait_ld();
 #pragma unroll
@@ -542,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     const int half = (warp - 2) >> 2;    // which half of the columns
     const int row = q * 32 + lane;
     OutStager st;
-    st.buf = staging + (warp - 2) * kOutBoxes * kStageOutBytes;
+    st.buf = staging + (warp - 2) * kStageOutBytes;
     int acc = 0;
     uint32_t acc_ph = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
@@ -611,8 +614,8 @@ constexpr int kPairStageBytes = kABytes + kPairBHalfBytes;
 template <int MODE>
 struct PairTraits {
   static constexpr bool wgrad = ModeTraits<MODE>::wgrad;
-  static constexpr int kStages = wgrad ? 4 : 6;
-  static constexpr int kStagingBytes = wgrad ? kEpiWarps * kOutBoxes * kStageOutBytes : 0;
+  static constexpr int kStages = 6;
+  static constexpr int kStagingBytes = wgrad ? kEpiWarps * kStageOutBytes : 0;
   static constexpr int kSmemBytes = kStages * kPairStageBytes + kStagingBytes + 1024 /*align*/ + 512 /*barriers*/;
 };
 // Shared memory of the staged per-expert tables (4 arrays of E + 1 ints).
@@ -643,13 +646,16 @@ __device__ __forceinline__ Tile pair_decode(const GemmParams& p, const ExpertTab
   const int nn = n_ntiles<MODE>(p);
   int nt;
   if (ModeTraits<MODE>::wgrad) {
+    // Order (expert, M pair, N tile), N fastest: the pairs running side by side
+    // write whole rows of dW (long contiguous DRAM runs) and share A.
     const int MT2 = ((MODE == kWgrad13 ? p.H : p.F) + 255) / 256;
     t.e = tile / (MT2 * nn);
     const int rem = tile - t.e * MT2 * nn;
-    nt = rem / MT2;
-    t.m0 = (rem - nt * MT2) * 256 + 128 * static_cast<int>(rank);
-    t.row0 = x.offsets[t.e];
-    t.nrows = x.counts[t.e];
+    const int mp = rem / nn;
+    nt = rem - mp * nn;
+    t.m0 = mp * 256 + 128 * static_cast<int>(rank);
+    t.row0 = __ldg(p.offsets + t.e);  // weight gradients: no staged tables (their shared memory holds store boxes)
+    t.nrows = __ldg(p.counts + t.e);
     t.kblocks = (t.nrows + BK - 1) / BK;
     t.mt = -1;
   } else {
@@ -756,8 +762,8 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
   xt.counts = tab + (p.E + 1);
   xt.offsets = tab + 2 * (p.E + 1);
   xt.tstart = tab + 3 * (p.E + 1);
-  for (int e = threadIdx.x; e <= p.E; e += blockDim.x) {
-    tab[e] = TR::wgrad ? 0 : __ldg(p.pairs + e);
+  for (int e = threadIdx.x; e <= p.E && !TR::wgrad; e += blockDim.x) {
+    tab[e] = __ldg(p.pairs + e);
     tab[(p.E + 1) + e] = e < p.E ? __ldg(p.counts + e) : 0;
     tab[2 * (p.E + 1) + e] = __ldg(p.offsets + e);
     tab[3 * (p.E + 1) + e] = __ldg(p.tiles + 1 + e);
@@ -900,7 +906,7 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
     const int row = q * 32 + lane;
     const int mext = (MODE == kWgrad13) ? p.H : p.F;
     OutStager st;
-    st.buf = staging + (warp - 2) * kOutBoxes * kStageOutBytes;
+    st.buf = staging + (warp - 2) * kStageOutBytes;
     const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), 0);
     int acc = 0;
     uint32_t acc_ph = 0;
@@ -1264,7 +1270,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_forward_kernel(const __grid
 // producer fetches its next task id one task ahead (still in increasing order).
 // ---------------------------------------------------------------------------
 constexpr int kBwdSkew = 2;
-constexpr int kBwdStages = 3;
+constexpr int kBwdStages = 4;
 
 struct FusedBwdParams {
   GemmParams d2;   // out0 = dGU, aux = GU
@@ -1346,7 +1352,7 @@ __device__ __forceinline__ uint32_t bwd_idesc(int kind, int nw) {
 __global__ void __launch_bounds__(kThreads, 1) fused_backward_kernel(const __grid_constant__ FusedBwdMaps maps,
                                                                      const FusedBwdParams f) {
   constexpr int S = kBwdStages;
-  constexpr int kStaging = kEpiWarps * kOutBoxes * kStageOutBytes;
+  constexpr int kStaging = kEpiWarps * kStageOutBytes;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1523,7 +1529,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_backward_kernel(const __gri
     const int half = ew >> 2;
     const int row = q * 32 + lane;
     OutStager st;
-    st.buf = staging + ew * kOutBoxes * kStageOutBytes;
+    st.buf = staging + ew * kStageOutBytes;
     int slot = 0, acc = 0;
     uint32_t rph = 0, acc_ph = 0;
     while (true) {
@@ -1599,19 +1605,18 @@ EncodeFn encoder() {
   return fn;
 }
 
-// 2-D tensor [outer, inner] (inner contiguous), box {box_inner, box_outer}, 128-byte swizzle.
+// 2-D bf16 tensor [outer, inner] (inner contiguous), box {box_inner, box_outer}, 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
-              uint32_t box_outer, bool f32 = false) {
+              uint32_t box_outer) {
   EncodeFn enc = encoder();
   if (!enc) return false;
-  const uint64_t esz = f32 ? 4 : 2;
   const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {inner * esz};
+  const cuuint64_t strides[1] = {inner * 2};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
-  return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
-             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int MODE>
@@ -1630,7 +1635,7 @@ cudaError_t launch_mode(const GemmLaunch& L, const Maps& maps, const GemmParams&
 template <int MODE>
 cudaError_t launch_pair_mode(const GemmLaunch& L, const Maps& maps, const GemmParams& p, cudaStream_t s,
                              LaunchHook& hook) {
-  const int kSmem = PairTraits<MODE>::kSmemBytes + static_cast<int>(pair_table_bytes(L.E));
+  const int kSmem = PairTraits<MODE>::kSmemBytes + (ModeTraits<MODE>::wgrad ? 0 : static_cast<int>(pair_table_bytes(L.E)));
   auto kern = pair_gemm_kernel<MODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
@@ -1705,10 +1710,8 @@ cudaError_t launch_fused_backward(const GemmLaunch& L, int32_t* cursor, int32_t*
   ok = ok && make_map(&m.d1.a, L.dGU, 2 * F, R, 64, BM) && make_map(&m.d1.b0, L.W1, F, E * H, 64, BN) &&
        make_map(&m.d1.b1, L.W3, F, E * H, 64, BN) && make_map(&m.d1.b2, L.W1, F, E * H, 64, 128) &&
        make_map(&m.d1.b3, L.W3, F, E * H, 64, 128);
-  ok = ok && make_map(&m.w13.a, L.Xp, H, R, 64, 64) && make_map(&m.w13.b0, L.dGU, 2 * F, R, 64, 64) &&
-       make_map(&m.w13.o0, L.dW1, F, E * H, 32, 32, true) && make_map(&m.w13.o1, L.dW3, F, E * H, 32, 32, true);
-  ok = ok && make_map(&m.w2.a, L.h, F, R, 64, 64) && make_map(&m.w2.b0, L.dY, H, R, 64, 64) &&
-       make_map(&m.w2.o0, L.dW2, H, E * F, 32, 32, true);
+  ok = ok && make_map(&m.w13.a, L.Xp, H, R, 64, 64) && make_map(&m.w13.b0, L.dGU, 2 * F, R, 64, 64);
+  ok = ok && make_map(&m.w2.a, L.h, F, R, 64, 64) && make_map(&m.w2.b0, L.dY, H, R, 64, 64);
   if (!ok) return cudaErrorInvalidValue;
   GemmParams p{};
   p.H = L.H;
@@ -1734,7 +1737,7 @@ cudaError_t launch_fused_backward(const GemmLaunch& L, int32_t* cursor, int32_t*
   f.cursor = cursor;
   f.cnt_d2 = cnt_d2;
   f.cnt_e = cnt_e;
-  constexpr int kSmem = kBwdStages * kStageBytes + kEpiWarps * kOutBoxes * kStageOutBytes + 1024 + 512;
+  constexpr int kSmem = kBwdStages * kStageBytes + kEpiWarps * kStageOutBytes + 1024 + 512;
   cudaError_t e = cudaFuncSetAttribute(fused_backward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   hook.before(s);
@@ -1823,14 +1826,12 @@ cudaError_t launch_gemm(GemmMode mode, const GemmLaunch& L, cudaStream_t s, Laun
       p.out0 = static_cast<__nv_bfloat16*>(L.out_dXp);
       break;
     case kWgrad13:
-      ok = make_map(&m.a, L.Xp, H, R, 64, 64) && make_map(&m.b0, L.dGU, 2 * F, R, 64, 64) &&
-           make_map(&m.o0, L.dW1, F, E * H, 32, 32, true) && make_map(&m.o1, L.dW3, F, E * H, 32, 32, true);
+      ok = make_map(&m.a, L.Xp, H, R, 64, 64) && make_map(&m.b0, L.dGU, 2 * F, R, 64, 64);
       p.f0 = L.dW1;
       p.f1 = L.dW3;
       break;
     case kWgrad2:
-      ok = make_map(&m.a, L.h, F, R, 64, 64) && make_map(&m.b0, L.dY, H, R, 64, 64) &&
-           make_map(&m.o0, L.dW2, H, E * F, 32, 32, true);
+      ok = make_map(&m.a, L.h, F, R, 64, 64) && make_map(&m.b0, L.dY, H, R, 64, 64);
       p.f0 = L.dW2;
       break;
   }
