@@ -37,6 +37,9 @@ What it computes (sources are named by page title and section):
   The router is outside the timed layer (UniEP, section 6, Figure 4 "excluding
   gating"), so routing is held fixed and the gate weights w are an input whose
   gradient dgate is returned.
+* Router (optional, ``router_logits`` / ``router_grads`` / ``layer_step_router``):
+  logits = x Wr and the gradient through the renormalised top-k softmax with
+  routing held fixed: dlogits, dWr = x^T dlogits and the router's share of dx.
 
 Precision policy.  ``mirror=True`` rounds where the layer stores a tensor:
 bf16 (round to nearest even) for Xp, G, U, h, Y, out, dY, dG, dU, dXp, dx and
@@ -309,6 +312,81 @@ def layer_step(x, logits, dout, W, k: int, E: int, mirror=True) -> dict:
     fwd = forward(x, W, ids, w, perm, mirror)
     bwd = backward(dout, W, fwd, w, perm, mirror)
     return {"ids": ids, "w": w, "perm": perm, **fwd, **bwd}
+
+
+# --------------------------------------------------------------------------
+# the router (gating) forward and backward
+# --------------------------------------------------------------------------
+def router_logits(x, Wr, mirror=True) -> np.ndarray:
+    """l[t,e] = sum_h x[t,h] Wr[h,e]: the router's score of token t for expert e
+    (UniEP, background, Forward Propagation: the router maps each token to a
+    distribution over the experts).  Stored as float32."""
+    x = np.asarray(x, dtype=np.float64)
+    Wr = np.asarray(Wr, dtype=np.float64)
+    return _store_f32(x @ Wr, mirror)
+
+
+def router_grads(x, Wr, ids, w, dgate, E: int, mirror=True) -> dict:
+    """Gradient of the loss through the gating, routing held fixed.
+
+    With w_j = exp(l_j) / sum_{i in top-k} exp(l_i) (softmax over the experts,
+    renormalised over the k chosen ones), dw_j / dl_m = w_j (delta_jm - w_m) for
+    m among the chosen experts and 0 otherwise (the choice is piecewise
+    constant in l), so
+        dl_m = w_m (dgate_m - sum_j w_j dgate_j)   for the k chosen experts,
+        dl_m = 0                                  for the others.
+    dWr = x^T dl and the router's share of dx is dl Wr^T.
+
+    Rounding points of the layer (mirror=True): dl in float32 (``dlogits``);
+    the weight gradient dWr (float32) is formed from dl rounded to bf16, the
+    stored row gradient the tensor cores read; the router's dx share is
+    returned unrounded and is added to the experts' share before dx's single
+    bf16 rounding.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    Wr = np.asarray(Wr, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    dgate = np.asarray(dgate, dtype=np.float64)
+    ids = np.asarray(ids)
+    T, k = ids.shape
+    s = np.zeros(T)
+    for j in range(k):
+        s += w[:, j] * dgate[:, j]
+    dl_slot = _store_f32(w * (dgate - s[:, None]), mirror)
+    dlogits = np.zeros((T, E))
+    for j in range(k):
+        dlogits[np.arange(T), ids[:, j]] = dl_slot[:, j]
+    dl_gemm = _store_bf16(dlogits, mirror)
+    dWr = _store_f32(x.T @ dl_gemm, mirror)
+    dx_router = dlogits @ Wr.T
+    return {"dl_slot": dl_slot, "dlogits": dlogits, "dWr": dWr, "dx_router": dx_router}
+
+
+def layer_step_router(x, Wr, dout, W, k: int, E: int, mirror=True) -> dict:
+    """One step with the router on the path: logits = x Wr, then plan, forward
+    and backward as in layer_step; dx gains the router's share (one bf16
+    rounding of the sum of both shares).
+
+    The experts are chosen on the float32 logits as in ``route``; the gate
+    weights come from the float32 logits in mirror mode (as the layer stores
+    them) and from the float64 logits otherwise."""
+    logits = router_logits(x, Wr, mirror)
+    ids, w = route(logits, k)
+    if not mirror:
+        sel = np.take_along_axis(np.asarray(logits, dtype=np.float64), ids.astype(np.int64), axis=1)
+        ex = np.exp(sel - sel[:, :1])
+        w = ex / ex.sum(axis=1, keepdims=True)
+    perm = permutation(ids, E)
+    fwd = forward(x, W, ids, w, perm, mirror)
+    bwd = backward(dout, W, fwd, w, perm, mirror)
+    r = router_grads(x, Wr, ids, w, bwd["dgate"], E, mirror)
+    dx_experts = unpermute_sum(bwd["dXp"], perm.dest, mirror=False)
+    step = {"ids": ids, "w": w, "perm": perm, **fwd, **bwd}
+    step["logits"] = logits
+    step["dlogits"] = r["dlogits"]
+    step["dWr"] = r["dWr"]
+    step["dx"] = _store_bf16(dx_experts + r["dx_router"], mirror)
+    return step
 
 
 # --------------------------------------------------------------------------
