@@ -40,6 +40,8 @@ FWD_KERNELS = ["gather_rows", "gemm_fwd1_swiglu", "gemm_fwd2", "combine"]
 FWD_KERNELS_FUSED = ["fused_forward", "combine"]
 BWD_KERNELS = ["combine_bwd", "gemm_dgrad2_swiglu_bwd", "gemm_dgrad1", "gemm_wgrad13", "gemm_wgrad2", "unpermute"]
 BWD_KERNELS_FUSED = ["combine_bwd", "fused_backward", "unpermute"]
+BWD_KERNELS_ROUTER = ["router_transpose", "combine_bwd", "gemm_dgrad2_swiglu_bwd", "gemm_dgrad1", "gemm_wgrad13",
+                      "gemm_wgrad2", "gemm_router_wgrad", "router_reduce", "unpermute"]
 N_PLAN_KERNELS = 3
 
 
@@ -64,7 +66,16 @@ def work_per_kernel(T, H, F, E, k):
     # Fused backward: reads dY, GU, Xp, h and every weight once; writes dGU, dXp and dW1, dW3, dW2 (fp32).
     b["fused_backward"] = (2 * R * H + 4 * R * F + 2 * R * H + 2 * R * F + 6 * E * H * F
                            + 4 * R * F + 2 * R * H + 12 * E * H * F)
+    # The router (--router): logits GEMM; Wr^T; dWr GEMM over token splits (dense
+    # in the experts) and the fixed-order reduction of its partials.
+    sp = router_splits(T, H, E)
+    b["gemm_router_fwd"] = 2 * T * H + 2 * H * E + 4 * T * E
+    b["router_transpose"] = 4 * H * E
+    b["gemm_router_wgrad"] = 2 * T * H + 2 * T * E + 4 * sp * H * E
+    b["router_reduce"] = 4 * sp * H * E + 4 * H * E
     f = {
+        "gemm_router_fwd": 2 * T * H * E,
+        "gemm_router_wgrad": 2 * T * H * E,
         "fused_forward": 6 * R * H * F,
         "fused_backward": 12 * R * H * F,
         "gemm_fwd1_swiglu": 4 * R * H * F,
@@ -75,6 +86,15 @@ def work_per_kernel(T, H, F, E, k):
         "gemm_wgrad2": 2 * R * H * F,
     }
     return f, b
+
+
+def router_splits(T, H, E):
+    """Token splits of the router's dWr GEMM (the library's rule: ~304 tiles, a function of the dims)."""
+    tiles = (H // 128) * ((E + 255) // 256)
+    nkb = (T + 63) // 64
+    sp = max(1, min(nkb, (304 + tiles - 1) // tiles))
+    ks = ((nkb + sp - 1) // sp) * 64
+    return max(1, (T + ks - 1) // ks)
 
 
 def load_peaks():
@@ -310,23 +330,30 @@ def run_ours(args):
                               "kernels_per_step": N_PLAN_KERNELS}), flush=True)
         return
     inp = S.layer_inputs(shape, seed, device=dev)
-    layer = MoELayer(T, H, F, E, k, device=dev)
+    layer = MoELayer(T, H, F, E, k, device=dev, with_router=args.router)
     stream = torch.cuda.current_stream(dev)
     fwd_names = FWD_KERNELS_FUSED if args.schedule in (1, 2) else FWD_KERNELS
     bwd_names = BWD_KERNELS_FUSED if args.schedule == 2 else BWD_KERNELS
+    if args.router:
+        if args.schedule == 2:
+            raise SystemExit("--router is measured with schedules 0 and 1")
+        bwd_names = BWD_KERNELS_ROUTER
     nf, nb = len(fwd_names), len(bwd_names)
+    router_arg = (inp["x"], inp["Wr"]) if args.router else None
     base_opts = layer.opts(schedule=args.schedule, cta_pair=args.cta_pair)
 
-    def step(opts_f=None, opts_b=None, ev_plan=None):
+    def step(opts_f=None, opts_b=None, ev_plan=None, opts_r=None):
         opts_f = opts_f if opts_f is not None else base_opts
         opts_b = opts_b if opts_b is not None else base_opts
+        if args.router:
+            layer.router_forward(inp["x"], inp["Wr"], opts=opts_r if opts_r is not None else base_opts)
         if ev_plan is not None:
             ev_plan[0].record(stream)
-        layer.plan(inp["logits"])
+        layer.plan(layer.logits if args.router else inp["logits"])
         if ev_plan is not None:
             ev_plan[1].record(stream)
         layer.forward(inp["x"], inp["W1"], inp["W3"], inp["W2"], opts=opts_f)
-        layer.backward(inp["dout"], inp["W1"], inp["W3"], inp["W2"], opts=opts_b)
+        layer.backward(inp["dout"], inp["W1"], inp["W3"], inp["W2"], opts=opts_b, router=router_arg)
 
     for _ in range(args.warmup):
         step()
@@ -350,7 +377,8 @@ def run_ours(args):
     evs_f = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nf)] for _ in range(args.steps)]
     evs_b = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nb)] for _ in range(args.steps)]
     evs_p = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    for e in [e for row in evs_f + evs_b + evs_p for e in row]:
+    evs_r = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for e in [e for row in evs_f + evs_b + evs_p + evs_r for e in row]:
         e.record(stream)  # torch creates the CUDA event on first record
     torch.cuda.synchronize()
     opts_f = []
@@ -364,6 +392,11 @@ def run_ours(args):
         o = layer.opts(events=e, schedule=args.schedule, cta_pair=args.cta_pair)
         keep.append(layer._ev_keep)
         opts_b.append(o)
+    opts_r = []
+    for e in evs_r:
+        o = layer.opts(events=e, schedule=args.schedule, cta_pair=args.cta_pair)
+        keep.append(layer._ev_keep)
+        opts_r.append(o)
 
     clocks = ClockSampler(local)
     barrier(world)
@@ -375,7 +408,7 @@ def run_ours(args):
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for i in range(args.steps):
-        step(opts_f[i], opts_b[i], evs_p[i])
+        step(opts_f[i], opts_b[i], evs_p[i], opts_r[i])
     t_end.record(stream)
     torch.cuda.synchronize()
     launches = M.moe_launch_count() - l0
@@ -388,9 +421,11 @@ def run_ours(args):
         raise RuntimeError(f"device status {st}")
 
     # Per-kernel average durations.
-    names = ["plan"] + fwd_names + bwd_names
+    names = (["gemm_router_fwd"] if args.router else []) + ["plan"] + fwd_names + bwd_names
     per = {n: 0.0 for n in names}
     for i in range(args.steps):
+        if args.router:
+            per["gemm_router_fwd"] += evs_r[i][0].elapsed_time(evs_r[i][1])
         per["plan"] += evs_p[i][0].elapsed_time(evs_p[i][1])
         for j, n in enumerate(fwd_names):
             per[n] += evs_f[i][2 * j].elapsed_time(evs_f[i][2 * j + 1])
@@ -443,11 +478,15 @@ def run_ours(args):
 
     def e2e_step():
         d_x.copy_(h_x, non_blocking=True)
-        d_lg.copy_(h_lg, non_blocking=True)
+        if not args.router:
+            d_lg.copy_(h_lg, non_blocking=True)
         d_do.copy_(h_do, non_blocking=True)
-        layer.plan(d_lg)
+        if args.router:
+            layer.router_forward(d_x, inp["Wr"], opts=base_opts)
+        layer.plan(layer.logits if args.router else d_lg)
         layer.forward(d_x, inp["W1"], inp["W3"], inp["W2"], opts=base_opts)
-        layer.backward(d_do, inp["W1"], inp["W3"], inp["W2"], opts=base_opts)
+        layer.backward(d_do, inp["W1"], inp["W3"], inp["W2"], opts=base_opts,
+                       router=(d_x, inp["Wr"]) if args.router else None)
         h_out.copy_(layer.out, non_blocking=True)
         h_dx.copy_(layer.dx, non_blocking=True)
 
@@ -463,7 +502,7 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
-    h2d = h_x.numel() * 2 + h_lg.numel() * 4 + h_do.numel() * 2
+    h2d = h_x.numel() * 2 + (0 if args.router else h_lg.numel() * 4) + h_do.numel() * 2
     d2h = h_out.numel() * 2 + h_dx.numel() * 2
 
     ms_step = ms_total / args.steps
@@ -477,14 +516,18 @@ def run_ours(args):
                                  2: "fused forward, fused backward"}[args.schedule],
                        gemm_tiles={0: "two-CTA 256x256 pair tiles (cta_group::2) except dgrad2: 128x256 single-CTA",
                                    1: "single-CTA 128x256 tiles (cta_group::1)",
-                                   2: "two-CTA 256x256 pair tiles (cta_group::2)"}[args.cta_pair]),
+                                   2: "two-CTA 256x256 pair tiles (cta_group::2)"}[args.cta_pair],
+                       router="on the path: logits = x Wr on the GPU, gradient through the gating (dlogits, dWr, "
+                              "dx share)" if args.router else "off (logits given; the pages time the layer "
+                                                               "excluding gating)"),
         "roofline": roof,
         "e2e": {"value": round(world * T * args.steps / (e2e_ms * 1e-3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),
         "clocks": clk,
         "kernels": kern,
-        "step_gemm_tflops": round(18 * T * k * H * F / (ms_step * 1e-3) / 1e12, 1),
+        "step_gemm_tflops": round((18 * T * k * H * F + (4 * T * H * E if args.router else 0))
+                                  / (ms_step * 1e-3) / 1e12, 1),
     }
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -527,6 +570,8 @@ def main():
     ap.add_argument("--cta-pair", type=int, default=0, choices=[0, 1, 2],
                     help="grouped GEMMs that run as their own kernels: 0 library default (pair tiles but for "
                          "dgrad2), 1 one CTA per tile, 2 two-CTA pair tiles")
+    ap.add_argument("--router", action="store_true",
+                    help="put the router on the timed path: logits = x Wr on the GPU and its backward")
     ap.add_argument("--profile", action="store_true",
                     help="run the warm-up steps and one more step only (for ncu captures)")
     ap.add_argument("--part", default="step", choices=["step", "plan"],

@@ -95,6 +95,22 @@ typedef struct {
   void *dXp; /* [R,H]   gradient of the dispatched rows */
 } moe_grads_t;
 
+/* The router's backward, requested from moe_backward (NULL: routing is held
+ * fixed and only dgate is returned, as the pages time the layer).  With it, the
+ * gradient flows on through the renormalised top-k softmax, routing held fixed
+ * (the selection is piecewise constant in the logits):
+ *   dl[t,m] = w[t,m] (dgate[t,m] - sum_j w[t,j] dgate[t,j]) for the k chosen m, 0 otherwise,
+ *   dWr = x^T dl (fp32; dl rounded to bf16 for the tensor cores; a fixed number
+ *   of token splits reduced in a fixed order, so bitwise reproducible),
+ *   and dx gains sum_j dl[t,j] Wr[:, ids[t,j]] (one bf16 rounding of the sum
+ *   of both shares).  E must be a multiple of 8. */
+typedef struct {
+  const void *x;  /* [T,H] bf16: the layer input (the router's input) */
+  const void *Wr; /* [H,E] bf16: router weight */
+  float *dlogits; /* [T,E] out: dL/dlogits, zero outside each token's k experts */
+  float *dWr;     /* [H,E] out */
+} moe_router_t;
+
 /* Options (may be NULL for defaults). */
 typedef struct {
   int32_t grid;     /* CTAs of the persistent kernels; 0 = one per SM.  Results do not depend on it. */
@@ -119,7 +135,8 @@ typedef struct {
 
 /* Bytes of the scratch workspace every call of one step needs (status word,
  * per-chunk counts and bitmaps of the routing, task cursor and per-tile
- * readiness counters of the persistent kernels).  Caller-allocated;
+ * readiness counters of the persistent kernels, and the router backward's
+ * Wr^T, per-slot and bf16 logit gradients and token-split partials of dWr).  Caller-allocated;
  * pass the same workspace to moe_plan, moe_forward and moe_backward of a step.
  * Returns 0 for invalid dims. */
 MOE_API size_t moe_workspace_bytes(moe_dims d);
@@ -160,7 +177,18 @@ MOE_API int moe_forward(moe_dims d, const void *x, const void *W1, const void *W
  *   dx [T,H] bf16; dW1, dW3 [E,H,F], dW2 [E,F,H], dgate [T,k]: fp32, device. */
 MOE_API int moe_backward(moe_dims d, const void *dout, const void *W1, const void *W3, const void *W2, const moe_plan_t *plan,
                  const moe_saved_t *saved, const moe_grads_t *grads, void *dx, float *dW1, float *dW3, float *dW2,
-                 float *dgate, void *ws, size_t ws_bytes, const moe_opts *opts, void *stream);
+                 float *dgate, void *ws, size_t ws_bytes, const moe_opts *opts, void *stream,
+                 const moe_router_t *router);
+
+/* ---- the router (gating) ----------------------------------------------------- */
+
+/* Router logits on the tensor cores: logits[t,e] = sum_h x[t,h] Wr[h,e]
+ * (bf16 in, fp32 accumulate and out).  [UniEP] background, Forward Propagation:
+ * the router scores each token against every expert; the scores feed moe_plan.
+ *   x [T,H] bf16, Wr [H,E] bf16, logits [T,E] fp32: device, caller-owned.
+ *   E must be a multiple of 8 (16-byte rows of Wr).  T = 0 is a no-op. */
+MOE_API int moe_router_forward(moe_dims d, const void *x, const void *Wr, float *logits, void *ws, size_t ws_bytes,
+                               const moe_opts *opts, void *stream);
 
 /* Synchronises `stream`, copies the status word out of the workspace and clears it.
  * device_status: 0 or a positive MOE_ERR_* code; where/detail: which kernel/task
@@ -210,7 +238,8 @@ MOE_API int32_t moe_version(void);
 /* Number of kernels this library has launched in this process. */
 MOE_API uint64_t moe_launch_count(void);
 /* Name of the i-th kernel a call launches (call: 0 plan, 1 forward, 2 backward, 3 forward with
- * schedule 1 or 2, 4 backward with schedule = 2); NULL past the end. */
+ * schedule 1 or 2, 4 backward with schedule = 2, 5 backward with the router (schedule 0 or 1),
+ * 6 moe_router_forward); NULL past the end. */
 MOE_API const char *moe_kernel_name(int32_t call, int32_t i);
 
 #ifdef __cplusplus

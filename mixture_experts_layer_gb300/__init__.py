@@ -17,7 +17,7 @@ __all__ = [
     "moe_dims", "moe_plan_t", "moe_saved_t", "moe_grads_t", "moe_opts", "MoeError",
     "moe_workspace_bytes", "moe_plan_tiles_elems", "moe_plan", "moe_forward", "moe_backward",
     "moe_get_status", "moe_clear_status", "moe_strerror", "moe_version", "moe_launch_count",
-    "moe_kernel_name", "moe_plan_noalloc", "check", "lib", "lib_path",
+    "moe_kernel_name", "moe_plan_noalloc", "moe_router_t", "moe_router_forward", "check", "lib", "lib_path",
 ]
 
 MOE_OK = 0
@@ -49,6 +49,10 @@ class moe_saved_t(Structure):
 
 class moe_grads_t(Structure):
     _fields_ = [("dY", c_void_p), ("dGU", c_void_p), ("dXp", c_void_p)]
+
+
+class moe_router_t(Structure):
+    _fields_ = [("x", c_void_p), ("Wr", c_void_p), ("dlogits", c_void_p), ("dWr", c_void_p)]
 
 
 class moe_opts(Structure):
@@ -90,7 +94,8 @@ def lib() -> ctypes.CDLL:
                                         c_size_t, POINTER(moe_opts), vp]),
                 "moe_backward": (c_int, [moe_dims, vp, vp, vp, vp, POINTER(moe_plan_t), POINTER(moe_saved_t),
                                          POINTER(moe_grads_t), vp, vp, vp, vp, vp, vp, c_size_t, POINTER(moe_opts),
-                                         vp]),
+                                         vp, POINTER(moe_router_t)]),
+                "moe_router_forward": (c_int, [moe_dims, vp, vp, vp, vp, c_size_t, POINTER(moe_opts), vp]),
                 "moe_get_status": (c_int, [vp, vp, POINTER(c_int32), POINTER(c_int32), POINTER(c_int32)]),
                 "moe_clear_status": (c_int, [vp, vp]),
                 "moe_strerror": (c_char_p, [c_int]),
@@ -134,10 +139,16 @@ def moe_forward(d, x, W1, W3, W2, plan, saved, out, ws, ws_bytes, opts=None, str
 
 
 def moe_backward(d, dout, W1, W3, W2, plan, saved, grads, dx, dW1, dW3, dW2, dgate, ws, ws_bytes, opts=None,
-                 stream=0) -> int:
+                 stream=0, router=None) -> int:
     return lib().moe_backward(d, _p(dout), _p(W1), _p(W3), _p(W2), byref(plan), byref(saved), byref(grads), _p(dx),
                               _p(dW1), _p(dW3), _p(dW2), _p(dgate), _p(ws), ws_bytes,
-                              byref(opts) if opts is not None else None, _p(stream))
+                              byref(opts) if opts is not None else None, _p(stream),
+                              byref(router) if router is not None else None)
+
+
+def moe_router_forward(d, x, Wr, logits, ws, ws_bytes, opts=None, stream=0) -> int:
+    return lib().moe_router_forward(d, _p(x), _p(Wr), _p(logits), _p(ws), ws_bytes,
+                                     byref(opts) if opts is not None else None, _p(stream))
 
 
 def moe_get_status(ws, stream=0):

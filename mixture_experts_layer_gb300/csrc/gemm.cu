@@ -57,8 +57,9 @@ constexpr int kStageOutBytes = 32 * 128;  // one warp's 32x32 fp32 staging box
 template <int MODE>
 struct ModeTraits {
   static constexpr bool wgrad = (MODE == kWgrad13 || MODE == kWgrad2);
-  static constexpr bool a_mn = wgrad;
-  static constexpr bool b_mn = (MODE == kFwd1 || MODE == kFwd2 || wgrad);
+  static constexpr bool router = (MODE == kRfwd || MODE == kRwgrad);
+  static constexpr bool a_mn = wgrad || MODE == kRwgrad;
+  static constexpr bool b_mn = (MODE == kFwd1 || MODE == kFwd2 || wgrad || router);
   // Output columns per tile are 2 x 128 (two weights side by side) or up to 256.
   static constexpr bool paired = (MODE == kFwd1 || MODE == kWgrad13);
   static constexpr int kStages = 4;
@@ -76,6 +77,7 @@ struct Maps {
 
 struct GemmParams {
   int H, F, E, R;
+  int T, splits, ks;  // router modes: tokens, token splits of the weight gradient, tokens per split
   const int32_t* tiles;
   const int32_t* pairs;  // first 256-row pair tile of each expert (E + 1)
   const int32_t* offsets;
@@ -101,7 +103,19 @@ struct Tile {
 
 template <int MODE>
 __device__ __forceinline__ int n_extent(const GemmParams& p) {
+  if (ModeTraits<MODE>::router) return p.E;
   return (MODE == kFwd2 || MODE == kDgrad1 || MODE == kWgrad2) ? p.H : p.F;
+}
+
+// MMA N of a router tile: the remaining expert columns rounded up to 16 (the
+// B columns past E are zero-filled by TMA), at most 256.
+__device__ __forceinline__ int router_nw(int E, int n0) { return min(BN, (E - n0 + 15) & ~15); }
+
+// Bytes one k-block's TMA loads bring into a stage (the A box plus B).
+template <int MODE>
+__device__ __forceinline__ uint32_t stage_tx_bytes(int nw) {
+  if (ModeTraits<MODE>::router) return kABytes + ((nw + 63) / 64) * kPanelBytes;
+  return kABytes + nw * 128;
 }
 
 template <int MODE>
@@ -113,6 +127,8 @@ __device__ __forceinline__ int n_ntiles(const GemmParams& p) {
 template <int MODE>
 __device__ __forceinline__ int n_tiles(const GemmParams& p) {
   const int nn = n_ntiles<MODE>(p);
+  if (MODE == kRfwd) return ((p.T + BM - 1) / BM) * nn;
+  if (MODE == kRwgrad) return p.splits * (p.H / BM) * nn;
   if (MODE == kWgrad13) return p.E * (p.H / BM) * nn;
   if (MODE == kWgrad2) return p.E * (p.F / BM) * nn;
   return __ldg(p.tiles) * nn;
@@ -123,6 +139,35 @@ __device__ __forceinline__ Tile decode(const GemmParams& p, int tile) {
   Tile t;
   const int nn = n_ntiles<MODE>(p);
   int nt;
+  if (MODE == kRfwd) {  // 128 token rows x up to 256 experts; K = H
+    const int mt = tile / nn;
+    nt = tile - mt * nn;
+    t.e = 0;
+    t.row0 = mt * BM;
+    t.nrows = min(BM, p.T - t.row0);
+    t.m0 = 0;
+    t.mt = -1;
+    t.kblocks = p.H / BK;
+    t.n0 = nt * BN;
+    t.nw = router_nw(p.E, t.n0);
+    return t;
+  }
+  if (MODE == kRwgrad) {  // 128 rows of H x up to 256 experts; K = the tokens of split s
+    const int MT = p.H / BM;
+    const int sp = tile / (MT * nn);
+    const int rem = tile - sp * MT * nn;
+    const int mt = rem / nn;
+    nt = rem - mt * nn;
+    t.e = sp;  // the split (partial buffer index)
+    t.row0 = sp * p.ks;
+    t.nrows = min(p.ks, p.T - t.row0);
+    t.m0 = mt * BM;
+    t.mt = -1;
+    t.kblocks = (t.nrows + BK - 1) / BK;
+    t.n0 = nt * BN;
+    t.nw = router_nw(p.E, t.n0);
+    return t;
+  }
   if (ModeTraits<MODE>::wgrad) {
     const int MT = (MODE == kWgrad13) ? p.H / BM : p.F / BM;
     t.e = tile / (MT * nn);
@@ -198,11 +243,19 @@ __device__ __forceinline__ void load_kblock(const GemmParams& p, const Maps& m, 
     tma_load_2d(sB + 1 * kPanelBytes, &m.b0, bar, t.n0 + 64, y);
     tma_load_2d(sB + 2 * kPanelBytes, &m.b0, bar, p.F + t.n0, y);
     tma_load_2d(sB + 3 * kPanelBytes, &m.b0, bar, p.F + t.n0 + 64, y);
-  } else {  // kWgrad2
+  } else if (MODE == kWgrad2) {
     const int y = t.row0 + k0;
     tma_load_2d(sA, &m.a, bar, t.m0, y);
     tma_load_2d(sA + kPanelBytes, &m.a, bar, t.m0 + 64, y);
     for (int q = 0; q < t.nw / 64; ++q) tma_load_2d(sB + q * kPanelBytes, &m.b0, bar, t.n0 + 64 * q, y);
+  } else if (MODE == kRfwd) {  // A = x rows (K-major), B = Wr [H, E] panels (MN-major)
+    tma_load_2d(sA, &m.a, bar, k0, t.row0);
+    for (int q = 0; q < (t.nw + 63) / 64; ++q) tma_load_2d(sB + q * kPanelBytes, &m.b0, bar, t.n0 + 64 * q, k0);
+  } else {  // kRwgrad: A = x^T (MN-major panels of H), B = dl [T, E] panels; rows past T read as zeros
+    const int y = t.row0 + k0;
+    tma_load_2d(sA, &m.a, bar, t.m0, y);
+    tma_load_2d(sA + kPanelBytes, &m.a, bar, t.m0 + 64, y);
+    for (int q = 0; q < (t.nw + 63) / 64; ++q) tma_load_2d(sB + q * kPanelBytes, &m.b0, bar, t.n0 + 64 * q, y);
   }
 }
 
@@ -277,6 +330,34 @@ template <int MODE>
 __device__ __forceinline__ void epilogue(const GemmParams& p, const Maps& m, const Tile& t, uint32_t tacc, int q,
                                          int half, int lane, OutStager& st) {
   const int row = q * 32 + lane;
+  if (ModeTraits<MODE>::router) {
+    // fp32 rows of the output (logits [T, E], or the split's dWr partial
+    // [H, E]); this warp takes every other 32-column chunk, columns >= E skipped.
+    float* orow;
+    bool ok;
+    if (MODE == kRfwd) {
+      ok = row < t.nrows;
+      orow = p.f0 + static_cast<size_t>(t.row0 + row) * p.E + t.n0;
+    } else {
+      ok = true;
+      orow = p.f0 + (static_cast<size_t>(t.e) * p.H + t.m0 + row) * p.E + t.n0;
+    }
+    const int ncol = min(t.nw, p.E - t.n0);
+#pragma unroll 1
+    for (int c = 32 * half; c < t.nw; c += 64) {
+      uint32_t d[32];
+      tc_ld_32x32b_x32(tacc + c, d);
+      tc_wait_ld();
+      if (!ok) continue;
+      if (c + 32 <= ncol) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) st_v4(orow + c + i, d[i], d[i + 1], d[i + 2], d[i + 3]);
+      } else {
+        for (int i = 0; i < 32 && c + i < ncol; ++i) orow[c + i] = __uint_as_float(d[i]);
+      }
+    }
+    return;
+  }
   // This warp's columns: [c_lo, c_hi) of each output (NC / 2 is a multiple of 32).
   const int NCall = ModeTraits<MODE>::paired ? 128 : t.nw;
   const int c_lo = half * (NCall / 2), c_hi = c_lo + NCall / 2;
@@ -469,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
           break;
         }
         if (elect_one()) {
-          mbar_arrive_expect_tx(&full[s], kABytes + t.nw * 128);
+          mbar_arrive_expect_tx(&full[s], stage_tx_bytes<MODE>(t.nw));
           uint8_t* sA = smem + s * kStageBytes;
           load_kblock<MODE>(p, maps, t, kb, sA, sA + kABytes, &full[s]);
         }
@@ -498,7 +579,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       if (!mbar_wait(&tempty[acc], acc_ph ^ 1u, p.ws, 120 + MODE, abort_flag)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * kAccStride;
-      const uint32_t idesc = (t.nw == 256) ? kIdesc256 : kIdesc128;
+      const uint32_t idesc = TR::router ? idesc_bf16_f32(BM, t.nw, TR::a_mn, TR::b_mn)
+                                       : (t.nw == 256) ? kIdesc256 : kIdesc128;
       for (int kb = 0; kb < t.kblocks; ++kb) {
         if (!mbar_wait(&full[s], ph, p.ws, 130 + MODE, abort_flag)) {
           ok = false;
@@ -1834,10 +1916,24 @@ cudaError_t launch_gemm(GemmMode mode, const GemmLaunch& L, cudaStream_t s, Laun
       ok = make_map(&m.a, L.h, F, R, 64, 64) && make_map(&m.b0, L.dY, H, R, 64, 64);
       p.f0 = L.dW2;
       break;
+    case kRfwd:
+      ok = make_map(&m.a, L.x, H, static_cast<uint64_t>(L.T), 64, BM) && make_map(&m.b0, L.Wr, E, H, 64, 64);
+      p.f0 = L.logits;
+      break;
+    case kRwgrad:
+      ok = make_map(&m.a, L.x, H, static_cast<uint64_t>(L.T), 64, 64) &&
+           make_map(&m.b0, L.dl, E, static_cast<uint64_t>(L.T), 64, 64);
+      p.f0 = L.dwr_part;
+      break;
   }
+  p.T = L.T;
+  p.splits = L.splits;
+  p.ks = L.ks;
   if (!ok) return cudaErrorInvalidValue;
-  if (L.pair) return launch_gemm_pair(mode, L, m, p, s, hook);
+  if (L.pair && mode != kRfwd && mode != kRwgrad) return launch_gemm_pair(mode, L, m, p, s, hook);
   switch (mode) {
+    case kRfwd: return launch_mode<kRfwd>(L, m, p, s, hook);
+    case kRwgrad: return launch_mode<kRwgrad>(L, m, p, s, hook);
     case kFwd1: return launch_mode<kFwd1>(L, m, p, s, hook);
     case kFwd2: return launch_mode<kFwd2>(L, m, p, s, hook);
     case kDgrad2: return launch_mode<kDgrad2>(L, m, p, s, hook);

@@ -67,6 +67,16 @@ struct PlanLaunch {
 };
 cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t s, LaunchHook& hook);
 
+// Router buffers of the row kernels (all null when the router is not on the path).
+struct RouterRows {
+  const int32_t* ids;         // [T,k] chosen experts
+  float* dl_slot;             // [T,k] dl of each chosen logit (combine_bwd writes, unpermute reads)
+  float* dlogits;             // [T,E] fp32 out (combine_bwd)
+  __nv_bfloat16* dl_bf16;     // [T,E] bf16 copy for the dWr GEMM (combine_bwd)
+  const uint4* WrT;           // [E,H] bf16 rows of Wr^T (unpermute)
+  int E;
+};
+
 struct RowsLaunch {
   int T, H, k, R;
   int grid;  // CTAs (256 threads each)
@@ -74,6 +84,7 @@ struct RowsLaunch {
   const int32_t* row_src;
   const float* w;
   WsHeader* ws;
+  RouterRows rt;
 };
 // Xp[r] = x[row_src[r]]
 cudaError_t launch_gather(const RowsLaunch& p, const void* x, void* Xp, cudaStream_t s, LaunchHook& hook);
@@ -82,8 +93,13 @@ cudaError_t launch_combine(const RowsLaunch& p, const void* Y, void* out, cudaSt
 // dY[dest[t,j]] = bf16(w[t,j] dout[t]); dgate[t,j] = <dout[t], Y[dest[t,j]]>
 cudaError_t launch_combine_bwd(const RowsLaunch& p, const void* dout, const void* Y, void* dY, float* dgate,
                                cudaStream_t s, LaunchHook& hook);
-// dx[t] = bf16(sum_j dXp[dest[t,j]])
+// dx[t] = bf16(sum_j dXp[dest[t,j]] (+ sum_j dl[t,j] WrT[ids[t,j]] with the router))
 cudaError_t launch_unpermute(const RowsLaunch& p, const void* dXp, void* dx, cudaStream_t s, LaunchHook& hook);
+// WrT = Wr^T (bf16 [H,E] -> [E,H])
+cudaError_t launch_transpose_wr(const void* Wr, void* WrT, int H, int E, cudaStream_t s, LaunchHook& hook);
+// out[i] = sum_s part[s][i] over `splits` partial buffers of n floats (n % 4 == 0)
+cudaError_t launch_reduce_splits(const float* part, float* out, size_t n, int splits, int grid, cudaStream_t s,
+                                 LaunchHook& hook);
 
 enum GemmMode : int {
   kFwd1 = 0,    // [G|U] = Xp [W1|W3], h = silu(G) U           (A K-major, B MN-major)
@@ -92,6 +108,8 @@ enum GemmMode : int {
   kDgrad1 = 3,  // dXp = [dG dU] [W1 W3]^T                      (A K-major, B K-major)
   kWgrad13 = 4, // dW1 = Xp^T dG, dW3 = Xp^T dU per expert      (A MN-major, B MN-major)
   kWgrad2 = 5,  // dW2 = h^T dY per expert                      (A MN-major, B MN-major)
+  kRfwd = 6,    // router logits = x Wr (fp32 out)              (A K-major, B MN-major)
+  kRwgrad = 7,  // router dWr partial = x^T dl over a token split (A MN-major, B MN-major)
 };
 
 struct GemmLaunch {
@@ -121,6 +139,13 @@ struct GemmLaunch {
   float* dW1;     // kWgrad13
   float* dW3;     // kWgrad13
   float* dW2;     // kWgrad2
+  // router
+  const void* x;       // [T,H] bf16
+  const void* Wr;      // [H,E] bf16
+  const void* dl;      // [T,E] bf16 router logit gradient (kRwgrad B operand)
+  float* logits;       // kRfwd out [T,E]
+  float* dwr_part;     // kRwgrad out [splits][H][E] (or dWr itself when splits = 1)
+  int splits, ks;      // token splits of kRwgrad and tokens per split (a multiple of 64)
   WsHeader* ws;
 };
 cudaError_t launch_gemm(GemmMode mode, const GemmLaunch& p, cudaStream_t s, LaunchHook& hook);

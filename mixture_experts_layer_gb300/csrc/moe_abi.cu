@@ -58,7 +58,23 @@ int check_dims(const moe_dims& d) {
 struct WsLayout {
   size_t ccount, cbase, gbm, sched, sched_bytes, total;
   size_t cap;  // capacity of the 128-row tile table
+  size_t wrT, dl_slot, dl_bf16, dwr_part;  // router backward
+  int splits, ks;                          // token splits of the dWr GEMM and tokens per split
 };
+
+// Token splits of the router's weight-gradient GEMM (K = the tokens): enough
+// tiles for ~2 per SM, a function of the dims alone (so the reduction order,
+// and the bits, do not depend on the GPU or the grid).
+void router_splits(const moe_dims& d, int* splits, int* ks) {
+  const long long tiles = static_cast<long long>(d.H / 128) * ((d.E + 255) / 256);
+  const long long nkb = (static_cast<long long>(d.T) + 63) / 64;
+  long long sp = (304 + tiles - 1) / tiles;
+  if (sp > nkb) sp = nkb;
+  if (sp < 1) sp = 1;
+  const long long kb_per = (nkb + sp - 1) / sp;
+  *ks = static_cast<int>(kb_per * 64);
+  *splits = static_cast<int>(d.T > 0 ? (d.T + *ks - 1) / *ks : 1);
+}
 
 WsLayout ws_layout(const moe_dims& d) {
   const size_t nchunks = (static_cast<size_t>(d.T) + kChunk - 1) / kChunk;
@@ -76,6 +92,15 @@ WsLayout ws_layout(const moe_dims& d) {
   L.sched = off;
   L.sched_bytes = 64 + 2 * L.cap * 4;
   off = align256(off + L.sched_bytes);
+  router_splits(d, &L.splits, &L.ks);
+  L.wrT = off;
+  off = align256(off + static_cast<size_t>(d.E) * d.H * 2);
+  L.dl_slot = off;
+  off = align256(off + static_cast<size_t>(d.T) * d.k * 4);
+  L.dl_bf16 = off;
+  off = align256(off + static_cast<size_t>(d.T) * d.E * 2);
+  L.dwr_part = off;
+  off = align256(off + static_cast<size_t>(L.splits) * d.H * d.E * 4);
   L.total = off;
   return L;
 }
@@ -136,6 +161,10 @@ const char* const kFwdKernels[] = {"gather_rows", "gemm_fwd1_swiglu", "gemm_fwd2
 const char* const kBwdKernels[] = {"combine_bwd", "gemm_dgrad2_swiglu_bwd", "gemm_dgrad1", "gemm_wgrad13",
                                    "gemm_wgrad2", "unpermute", nullptr};
 const char* const kBwdKernelsFused[] = {"combine_bwd", "fused_backward", "unpermute", nullptr};
+const char* const kBwdKernelsRouter[] = {"router_transpose", "combine_bwd", "gemm_dgrad2_swiglu_bwd", "gemm_dgrad1",
+                                         "gemm_wgrad13", "gemm_wgrad2", "gemm_router_wgrad", "router_reduce",
+                                         "unpermute", nullptr};
+const char* const kRouterFwdKernels[] = {"gemm_router_fwd", nullptr};
 
 GemmLaunch gemm_common(const moe_dims& d, const moe_plan_t* plan, WsHeader* ws, int grid) {
   GemmLaunch g{};
@@ -262,7 +291,7 @@ int moe_forward(moe_dims d, const void* x, const void* W1, const void* W3, const
 int moe_backward(moe_dims d, const void* dout, const void* W1, const void* W3, const void* W2,
                  const moe_plan_t* plan, const moe_saved_t* saved, const moe_grads_t* grads, void* dx, float* dW1,
                  float* dW3, float* dW2, float* dgate, void* ws, size_t ws_bytes, const moe_opts* opts,
-                 void* stream) {
+                 void* stream, const moe_router_t* router) {
   int rc = check_dims(d);
   if (rc) return rc;
   if ((rc = check_ws(d, ws, ws_bytes))) return rc;
@@ -270,6 +299,10 @@ int moe_backward(moe_dims d, const void* dout, const void* W1, const void* W3, c
                           opts->cta_pair > 2))
     return MOE_ERR_ARG;
   if ((rc = check_ptrs({dW1, dW3, dW2}))) return rc;
+  if (router != nullptr) {
+    if (d.E % 8 != 0) return MOE_ERR_SHAPE;
+    if ((rc = check_ptrs({router->x, router->Wr, router->dlogits, router->dWr}))) return rc;
+  }
   if (d.T > 0) {
     if ((rc = check_plan(plan))) return rc;
     if (saved == nullptr || grads == nullptr) return MOE_ERR_ARG;
@@ -286,6 +319,9 @@ int moe_backward(moe_dims d, const void* dout, const void* W1, const void* W3, c
     if (cudaMemsetAsync(dW1, 0, n, s) != cudaSuccess || cudaMemsetAsync(dW3, 0, n, s) != cudaSuccess ||
         cudaMemsetAsync(dW2, 0, n, s) != cudaSuccess)
       return MOE_ERR_LAUNCH;
+    if (router != nullptr &&
+        cudaMemsetAsync(router->dWr, 0, static_cast<size_t>(d.H) * d.E * sizeof(float), s) != cudaSuccess)
+      return MOE_ERR_LAUNCH;
     return MOE_OK;
   }
   if (!tensor_map_encoder_ready()) return MOE_ERR_LAUNCH;
@@ -293,8 +329,19 @@ int moe_backward(moe_dims d, const void* dout, const void* W1, const void* W3, c
   const int grid = grid_for(opts, sms);
   LaunchHook hook = make_hook(opts);
 
-  RowsLaunch r{d.T, d.H, d.k, d.T * d.k, grid * 8, plan->dest, plan->row_src, plan->topk_w, wsh};
-  cudaError_t e = launch_combine_bwd(r, dout, saved->Y, grads->dY, dgate, s, hook);
+  RowsLaunch r{d.T, d.H, d.k, d.T * d.k, grid * 8, plan->dest, plan->row_src, plan->topk_w, wsh, RouterRows{}};
+  const WsLayout WL = ws_layout(d);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  cudaError_t e;
+  if (router != nullptr) {
+    r.rt.ids = plan->topk_ids;
+    r.rt.dl_slot = reinterpret_cast<float*>(wsb + WL.dl_slot);
+    r.rt.dlogits = router->dlogits;
+    r.rt.dl_bf16 = reinterpret_cast<__nv_bfloat16*>(wsb + WL.dl_bf16);
+    r.rt.E = d.E;
+    if ((e = launch_transpose_wr(router->Wr, wsb + WL.wrT, d.H, d.E, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
+  }
+  e = launch_combine_bwd(r, dout, saved->Y, grads->dY, dgate, s, hook);
   if (e != cudaSuccess) return MOE_ERR_LAUNCH;
 
   GemmLaunch g = gemm_common(d, plan, wsh, grid);
@@ -333,7 +380,49 @@ int moe_backward(moe_dims d, const void* dout, const void* W1, const void* W3, c
     g.pair = use_pair(opts, kWgrad2);
     if ((e = launch_gemm(kWgrad2, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
   }
+  if (router != nullptr) {
+    // dWr = x^T dl over a fixed number of token splits, reduced in split order.
+    GemmLaunch rg = gemm_common(d, plan, wsh, grid);
+    rg.x = router->x;
+    rg.dl = wsb + WL.dl_bf16;
+    rg.dwr_part = reinterpret_cast<float*>(wsb + WL.dwr_part);
+    rg.splits = WL.splits;
+    rg.ks = WL.ks;
+    if ((e = launch_gemm(kRwgrad, rg, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
+    if ((e = launch_reduce_splits(rg.dwr_part, router->dWr, static_cast<size_t>(d.H) * d.E, WL.splits, grid * 4, s,
+                                  hook)) != cudaSuccess)
+      return MOE_ERR_LAUNCH;
+    r.rt.WrT = reinterpret_cast<const uint4*>(wsb + WL.wrT);
+  }
   return finish(launch_unpermute(r, grads->dXp, dx, s, hook));
+}
+
+int moe_router_forward(moe_dims d, const void* x, const void* Wr, float* logits, void* ws, size_t ws_bytes,
+                       const moe_opts* opts, void* stream) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (d.E % 8 != 0) return MOE_ERR_SHAPE;
+  if ((rc = check_ws(d, ws, ws_bytes))) return rc;
+  if (opts != nullptr && opts->grid < 0) return MOE_ERR_ARG;
+  if (d.T == 0) return MOE_OK;
+  if ((rc = check_ptrs({x, Wr, logits}))) return rc;
+  int sms = 0;
+  if ((rc = device_info(&sms))) return rc;
+  if (!tensor_map_encoder_ready()) return MOE_ERR_LAUNCH;
+  GemmLaunch g{};
+  g.T = d.T;
+  g.H = d.H;
+  g.F = d.F;
+  g.E = d.E;
+  g.k = d.k;
+  g.R = d.T * d.k;
+  g.grid = grid_for(opts, sms);
+  g.ws = static_cast<WsHeader*>(ws);
+  g.x = x;
+  g.Wr = Wr;
+  g.logits = logits;
+  LaunchHook hook = make_hook(opts);
+  return finish(launch_gemm(kRfwd, g, static_cast<cudaStream_t>(stream), hook));
 }
 
 int moe_get_status(void* ws, void* stream, int32_t* device_status, int32_t* where, int32_t* detail) {
@@ -386,6 +475,8 @@ const char* moe_kernel_name(int32_t call, int32_t i) {
                          : call == 2 ? kBwdKernels
                          : call == 3 ? kFwdKernelsFused
                          : call == 4 ? kBwdKernelsFused
+                         : call == 5 ? kBwdKernelsRouter
+                         : call == 6 ? kRouterFwdKernels
                                      : nullptr;
   if (t == nullptr || i < 0) return nullptr;
   for (int j = 0; j <= i; ++j)

@@ -188,7 +188,8 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(const uint4* __re
                                                                  const int32_t* __restrict__ dest,
                                                                  const float* __restrict__ w,
                                                                  uint4* __restrict__ dY, float* __restrict__ dgate,
-                                                                 int T, int k, int R, int hv, WsHeader* ws) {
+                                                                 int T, int k, int R, int hv, WsHeader* ws,
+                                                                 RouterRows rt) {
   const int lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * (kThreads / 32);
   for (int t = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); t < T; t += nwarps) {
@@ -219,28 +220,78 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(const uint4* __re
         }
       }
     }
+    float dg[K];
 #pragma unroll
     for (int j = 0; j < K; ++j) {
       float s = part[j];
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      dg[j] = s;
       if (j < k && lane == 0) dgate[static_cast<size_t>(t) * k + j] = s;
+    }
+    if (rt.dlogits != nullptr) {
+      // Gradient through the renormalised top-k softmax (routing fixed):
+      // dl_j = w_j (dgate_j - sum_i w_i dgate_i), slots in ascending order;
+      // the logits of the other experts get 0.
+      float sw = 0.f;
+#pragma unroll
+      for (int j = 0; j < K; ++j)
+        if (j < k) sw = fmaf(wj[j], dg[j], sw);
+      int ej[K];
+      float dl[K];
+      const int my_e = (lane < k) ? rt.ids[static_cast<size_t>(t) * k + lane] : -1;
+#pragma unroll
+      for (int j = 0; j < K; ++j) {
+        ej[j] = __shfl_sync(0xffffffffu, my_e, j);
+        dl[j] = wj[j] * (dg[j] - sw);
+        if (j < k && lane == 0) rt.dl_slot[static_cast<size_t>(t) * k + j] = dl[j];
+      }
+      float* drow = rt.dlogits + static_cast<size_t>(t) * rt.E;
+      __nv_bfloat16* brow = rt.dl_bf16 + static_cast<size_t>(t) * rt.E;
+      for (int e = lane; e < rt.E; e += 32) {
+        float v = 0.f;
+#pragma unroll
+        for (int j = 0; j < K; ++j)
+          if (j < k && ej[j] == e) v = dl[j];
+        drow[e] = v;
+        brow[e] = __float2bfloat16_rn(v);
+      }
     }
   }
 }
 
 // dx[t] = bf16(sum_j dXp[dest[t,j]]), slots in ascending order.
+// With the router on the path, dx[t] also gains the router's share
+// sum_j dl[t,j] Wr[:, ids[t,j]] (only the k chosen logits have a gradient), read
+// from rows of Wr^T; both shares are summed in fp32 and rounded once.
 template <int K>
 __global__ void __launch_bounds__(kThreads) unpermute_kernel(const uint4* __restrict__ dXp,
                                                                const int32_t* __restrict__ dest,
                                                                uint4* __restrict__ dx, int T, int k, int R, int hv,
-                                                               WsHeader* ws) {
+                                                               WsHeader* ws, RouterRows rt) {
   const int lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * (kThreads / 32);
+  const bool router = rt.WrT != nullptr;
   for (int t = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); t < T; t += nwarps) {
     int rows[K];
     float wj[K];
     if (!token_rows<K>(dest, nullptr, t, k, R, lane, rows, wj, ws, 13)) continue;
+    int ej[K];
+    float dl[K];
+    if (router) {
+      const int my_e = (lane < k) ? rt.ids[static_cast<size_t>(t) * k + lane] : 0;
+      const float my_d = (lane < k) ? rt.dl_slot[static_cast<size_t>(t) * k + lane] : 0.f;
+      const bool bad = lane < k && (my_e < 0 || my_e >= rt.E);
+      if (__any_sync(0xffffffffu, bad)) {
+        if (lane == 0) report(ws, MOE_ERR_BOUNDS, 14, t);
+        continue;
+      }
+#pragma unroll
+      for (int j = 0; j < K; ++j) {
+        ej[j] = __shfl_sync(0xffffffffu, my_e, j);
+        dl[j] = __shfl_sync(0xffffffffu, my_d, j);
+      }
+    }
     for (int v = lane; v < hv; v += 32) {
       uint4 y[K];
 #pragma unroll
@@ -256,8 +307,53 @@ __global__ void __launch_bounds__(kThreads) unpermute_kernel(const uint4* __rest
           for (int i = 0; i < 8; ++i) acc[i] += f[i];
         }
       }
+      if (router) {
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+          if (j < k) {
+            float f[8];
+            unpack8(ldg_nc(rt.WrT + static_cast<size_t>(ej[j]) * hv + v), f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = fmaf(dl[j], f[i], acc[i]);
+          }
+        }
+      }
       dx[static_cast<size_t>(t) * hv + v] = pack8(acc);
     }
+  }
+}
+
+// WrT[e, h] = Wr[h, e] (bf16), through 32 x 32 tiles in shared memory.
+__global__ void __launch_bounds__(256) transpose_wr_kernel(const __nv_bfloat16* __restrict__ Wr,
+                                                             __nv_bfloat16* __restrict__ WrT, int H, int E) {
+  __shared__ __nv_bfloat16 tile[32][33];
+  const int h0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+  for (int r = ty; r < 32; r += 8) {
+    const int h = h0 + r, e = e0 + tx;
+    if (h < H && e < E) tile[r][tx] = Wr[static_cast<size_t>(h) * E + e];
+  }
+  __syncthreads();
+  for (int r = ty; r < 32; r += 8) {
+    const int e = e0 + r, h = h0 + tx;
+    if (h < H && e < E) WrT[static_cast<size_t>(e) * H + h] = tile[tx][r];
+  }
+}
+
+// dWr[i] = sum_s part[s][i], s ascending (a fixed order: the same bits for any grid).
+__global__ void __launch_bounds__(256) reduce_splits_kernel(const float4* __restrict__ part, float4* __restrict__ out,
+                                                              size_t n4, int splits) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    float4 a = part[i];
+    for (int sp = 1; sp < splits; ++sp) {
+      const float4 b = part[static_cast<size_t>(sp) * n4 + i];
+      a.x += b.x;
+      a.y += b.y;
+      a.z += b.z;
+      a.w += b.w;
+    }
+    out[i] = a;
   }
 }
 
@@ -297,12 +393,12 @@ cudaError_t launch_combine_bwd(const RowsLaunch& p, const void* dout, const void
   if (p.k <= 8)
     combine_bwd_kernel<8><<<p.grid, kThreads, 0, s>>>(static_cast<const uint4*>(dout), static_cast<const uint4*>(Y),
                                                        p.dest, p.w, static_cast<uint4*>(dY), dgate, p.T, p.k, p.R,
-                                                       p.H / 8, p.ws);
+                                                       p.H / 8, p.ws, p.rt);
   else
     combine_bwd_kernel<kMaxK><<<p.grid, kThreads, 0, s>>>(static_cast<const uint4*>(dout),
                                                            static_cast<const uint4*>(Y), p.dest, p.w,
                                                            static_cast<uint4*>(dY), dgate, p.T, p.k, p.R, p.H / 8,
-                                                           p.ws);
+                                                           p.ws, p.rt);
   hook.after(s);
   return cudaGetLastError();
 }
@@ -311,10 +407,28 @@ cudaError_t launch_unpermute(const RowsLaunch& p, const void* dXp, void* dx, cud
   hook.before(s);
   if (p.k <= 8)
     unpermute_kernel<8><<<p.grid, kThreads, 0, s>>>(static_cast<const uint4*>(dXp), p.dest,
-                                                     static_cast<uint4*>(dx), p.T, p.k, p.R, p.H / 8, p.ws);
+                                                     static_cast<uint4*>(dx), p.T, p.k, p.R, p.H / 8, p.ws, p.rt);
   else
     unpermute_kernel<kMaxK><<<p.grid, kThreads, 0, s>>>(static_cast<const uint4*>(dXp), p.dest,
-                                                         static_cast<uint4*>(dx), p.T, p.k, p.R, p.H / 8, p.ws);
+                                                         static_cast<uint4*>(dx), p.T, p.k, p.R, p.H / 8, p.ws,
+                                                         p.rt);
+  hook.after(s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_wr(const void* Wr, void* WrT, int H, int E, cudaStream_t s, LaunchHook& hook) {
+  hook.before(s);
+  transpose_wr_kernel<<<dim3((H + 31) / 32, (E + 31) / 32), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(Wr), static_cast<__nv_bfloat16*>(WrT), H, E);
+  hook.after(s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_splits(const float* part, float* out, size_t n, int splits, int grid, cudaStream_t s,
+                                 LaunchHook& hook) {
+  hook.before(s);
+  reduce_splits_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const float4*>(part), reinterpret_cast<float4*>(out),
+                                            n / 4, splits);
   hook.after(s);
   return cudaGetLastError();
 }

@@ -8,7 +8,7 @@ from __future__ import annotations
 import torch
 
 from . import (check, moe_backward, moe_dims, moe_forward, moe_get_status, moe_grads_t, moe_opts, moe_plan,
-               moe_plan_t, moe_plan_tiles_elems, moe_saved_t, moe_workspace_bytes)
+               moe_plan_t, moe_plan_tiles_elems, moe_router_forward, moe_router_t, moe_saved_t, moe_workspace_bytes)
 
 
 def _empty(shape, dtype, device):
@@ -22,7 +22,7 @@ def _empty(shape, dtype, device):
 class MoELayer:
     """Buffers of plan, forward and backward for fixed (T, H, F, E, k)."""
 
-    def __init__(self, T, H, F, E, k, device="cuda", with_backward=True, plan_only=False):
+    def __init__(self, T, H, F, E, k, device="cuda", with_backward=True, plan_only=False, with_router=False):
         self.dims = moe_dims(T, H, F, E, k)
         self.T, self.H, self.F, self.E, self.k = T, H, F, E, k
         R = T * k
@@ -47,6 +47,10 @@ class MoELayer:
         self.plan_s = moe_plan_t(self.ids.data_ptr(), self.w.data_ptr(), self.counts.data_ptr(),
                                  self.offsets.data_ptr(), self.dest.data_ptr(), self.row_src.data_ptr(),
                                  self.row_slot.data_ptr(), self.tiles.data_ptr())
+        if with_router:  # the router on the path: logits from x Wr, and their gradients
+            self.logits = _empty((T, E), f32, dev)
+            self.dlogits = _empty((T, E), f32, dev)
+            self.dWr = torch.empty((H, E), dtype=f32, device=dev)
         if plan_only:  # routing tables only (profiling the routing kernels)
             return
         self.Xp = _empty((R, H), bf, dev)
@@ -94,12 +98,23 @@ class MoELayer:
                           self._stream(stream)), "moe_forward")
         return self.out
 
-    def backward(self, dout, W1, W3, W2, opts=None, stream=None):
+    def backward(self, dout, W1, W3, W2, opts=None, stream=None, router=None):
+        """router: (x, Wr) to carry the gradient on through the gating (dlogits, dWr, dx's router share)."""
+        r = None
+        if router is not None:
+            x, Wr = router
+            r = moe_router_t(x.data_ptr(), Wr.data_ptr(), self.dlogits.data_ptr(), self.dWr.data_ptr())
         check(moe_backward(self.dims, dout.data_ptr(), W1.data_ptr(), W3.data_ptr(), W2.data_ptr(), self.plan_s,
                            self.saved, self.grads, self.dx.data_ptr(), self.dW1.data_ptr(), self.dW3.data_ptr(),
                            self.dW2.data_ptr(), self.dgate.data_ptr(), self.ws.data_ptr(), self.ws_bytes, opts,
-                           self._stream(stream)), "moe_backward")
+                           self._stream(stream), r), "moe_backward")
         return self.dx
+
+    def router_forward(self, x, Wr, opts=None, stream=None):
+        """logits = x Wr (fp32) into self.logits."""
+        check(moe_router_forward(self.dims, x.data_ptr(), Wr.data_ptr(), self.logits.data_ptr(), self.ws.data_ptr(),
+                                 self.ws_bytes, opts, self._stream(stream)), "moe_router_forward")
+        return self.logits
 
     def status(self, stream=None):
         rc, st, where, detail = moe_get_status(self.ws.data_ptr(), self._stream(stream))
