@@ -38,10 +38,10 @@ UNIT = "tokens/s"
 
 FWD_KERNELS = ["gather_rows", "gemm_fwd1_swiglu", "gemm_fwd2", "combine"]
 FWD_KERNELS_FUSED = ["fused_forward", "combine"]
-BWD_KERNELS = ["combine_bwd", "gemm_dgrad2_swiglu_bwd", "gemm_dgrad1", "gemm_wgrad13", "gemm_wgrad2", "unpermute"]
+BWD_KERNELS = ["combine_bwd", "gemm_dgrad2_swiglu_bwd", "gemm_dgrad1", "unpermute", "gemm_wgrad13", "gemm_wgrad2"]
 BWD_KERNELS_FUSED = ["combine_bwd", "fused_backward", "unpermute"]
-BWD_KERNELS_ROUTER = ["router_transpose", "combine_bwd", "gemm_dgrad2_swiglu_bwd", "gemm_dgrad1", "gemm_wgrad13",
-                      "gemm_wgrad2", "gemm_router_wgrad", "router_reduce", "unpermute"]
+BWD_KERNELS_ROUTER = ["router_transpose", "combine_bwd", "gemm_dgrad2_swiglu_bwd", "gemm_dgrad1", "gemm_router_wgrad",
+                      "router_reduce", "unpermute", "gemm_wgrad13", "gemm_wgrad2"]
 N_PLAN_KERNELS = 3
 
 

@@ -353,7 +353,9 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, const Maps& m, con
 #pragma unroll
         for (int i = 0; i < 32; i += 4) st_v4(orow + c + i, d[i], d[i + 1], d[i + 2], d[i + 3]);
       } else {
-        for (int i = 0; i < 32 && c + i < ncol; ++i) orow[c + i] = __uint_as_float(d[i]);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (c + i < ncol) orow[c + i] = __uint_as_float(d[i]);
       }
     }
     return;

@@ -158,12 +158,12 @@ int use_pair(const moe_opts* o, GemmMode m) {
 const char* const kPlanKernels[] = {"route_topk", "route_scan", "route_rank", nullptr};
 const char* const kFwdKernelsFused[] = {"fused_forward", "combine", nullptr};
 const char* const kFwdKernels[] = {"gather_rows", "gemm_fwd1_swiglu", "gemm_fwd2", "combine", nullptr};
-const char* const kBwdKernels[] = {"combine_bwd", "gemm_dgrad2_swiglu_bwd", "gemm_dgrad1", "gemm_wgrad13",
-                                   "gemm_wgrad2", "unpermute", nullptr};
+const char* const kBwdKernels[] = {"combine_bwd", "gemm_dgrad2_swiglu_bwd", "gemm_dgrad1", "unpermute",
+                                   "gemm_wgrad13", "gemm_wgrad2", nullptr};
 const char* const kBwdKernelsFused[] = {"combine_bwd", "fused_backward", "unpermute", nullptr};
 const char* const kBwdKernelsRouter[] = {"router_transpose", "combine_bwd", "gemm_dgrad2_swiglu_bwd", "gemm_dgrad1",
-                                         "gemm_wgrad13", "gemm_wgrad2", "gemm_router_wgrad", "router_reduce",
-                                         "unpermute", nullptr};
+                                         "gemm_router_wgrad", "router_reduce", "unpermute", "gemm_wgrad13",
+                                         "gemm_wgrad2", nullptr};
 const char* const kRouterFwdKernels[] = {"gemm_router_fwd", nullptr};
 
 GemmLaunch gemm_common(const moe_dims& d, const moe_plan_t* plan, WsHeader* ws, int grid) {
@@ -181,6 +181,28 @@ GemmLaunch gemm_common(const moe_dims& d, const moe_plan_t* plan, WsHeader* ws, 
   g.counts = plan->counts;
   g.ws = ws;
   return g;
+}
+
+// The router's weight gradient (when the router is on the path) and the
+// dispatch backward dx[t] = sum_j dXp[dest[t,j]] (+ the router's share).
+int router_wgrad_and_unpermute(const moe_dims& d, const moe_plan_t* plan, WsHeader* wsh, int grid, const WsLayout& WL,
+                               uint8_t* wsb, const moe_router_t* router, RowsLaunch& r, const void* dXp, void* dx,
+                               cudaStream_t s, LaunchHook& hook) {
+  if (router != nullptr) {
+    // dWr = x^T dl over a fixed number of token splits, reduced in split order.
+    GemmLaunch rg = gemm_common(d, plan, wsh, grid);
+    rg.x = router->x;
+    rg.dl = wsb + WL.dl_bf16;
+    rg.dwr_part = reinterpret_cast<float*>(wsb + WL.dwr_part);
+    rg.splits = WL.splits;
+    rg.ks = WL.ks;
+    if (launch_gemm(kRwgrad, rg, s, hook) != cudaSuccess) return MOE_ERR_LAUNCH;
+    if (launch_reduce_splits(rg.dwr_part, router->dWr, static_cast<size_t>(d.H) * d.E, WL.splits, grid * 4, s,
+                             hook) != cudaSuccess)
+      return MOE_ERR_LAUNCH;
+    r.rt.WrT = reinterpret_cast<const uint4*>(wsb + WL.wrT);
+  }
+  return finish(launch_unpermute(r, dXp, dx, s, hook));
 }
 
 }  // namespace
@@ -373,28 +395,18 @@ int moe_backward(moe_dims d, const void* dout, const void* W1, const void* W3, c
     g.bn = (d.H % 256 == 0) ? 256 : 128;
     g.pair = use_pair(opts, kDgrad1);
     if ((e = launch_gemm(kDgrad1, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
+    // The dispatch backward right after dgrad1, while dXp is still in L2; the
+    // weight gradients, which read Xp / h / dY / dGU, follow.
+    if ((rc = router_wgrad_and_unpermute(d, plan, wsh, grid, WL, wsb, router, r, grads->dXp, dx, s, hook))) return rc;
     g.bn = 256;
     g.pair = use_pair(opts, kWgrad13);
     if ((e = launch_gemm(kWgrad13, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
     g.bn = (d.H % 256 == 0) ? 256 : 128;
     g.pair = use_pair(opts, kWgrad2);
     if ((e = launch_gemm(kWgrad2, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
+    return MOE_OK;
   }
-  if (router != nullptr) {
-    // dWr = x^T dl over a fixed number of token splits, reduced in split order.
-    GemmLaunch rg = gemm_common(d, plan, wsh, grid);
-    rg.x = router->x;
-    rg.dl = wsb + WL.dl_bf16;
-    rg.dwr_part = reinterpret_cast<float*>(wsb + WL.dwr_part);
-    rg.splits = WL.splits;
-    rg.ks = WL.ks;
-    if ((e = launch_gemm(kRwgrad, rg, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
-    if ((e = launch_reduce_splits(rg.dwr_part, router->dWr, static_cast<size_t>(d.H) * d.E, WL.splits, grid * 4, s,
-                                  hook)) != cudaSuccess)
-      return MOE_ERR_LAUNCH;
-    r.rt.WrT = reinterpret_cast<const uint4*>(wsb + WL.wrT);
-  }
-  return finish(launch_unpermute(r, grads->dXp, dx, s, hook));
+  return router_wgrad_and_unpermute(d, plan, wsh, grid, WL, wsb, router, r, grads->dXp, dx, s, hook);
 }
 
 int moe_router_forward(moe_dims d, const void* x, const void* Wr, float* logits, void* ws, size_t ws_bytes,

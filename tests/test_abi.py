@@ -26,7 +26,7 @@ def test_every_declared_symbol_is_exported():
     assert M.moe_version() >= 1
     assert M.moe_kernel_name(1, 1) == "gemm_fwd1_swiglu"
     assert M.moe_kernel_name(3, 0) == "fused_forward"
-    assert M.moe_kernel_name(2, 4) == "gemm_wgrad2"
+    assert M.moe_kernel_name(2, 5) == "gemm_wgrad2"
     assert M.moe_kernel_name(2, 6) is None
     assert M.moe_kernel_name(4, 1) == "fused_backward"
 
