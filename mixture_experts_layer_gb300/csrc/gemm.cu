@@ -1124,14 +1124,14 @@ __device__ __forceinline__ void gather_rows_task(const FusedFwdParams& f, const 
     }
     const uint4* src = f.x + static_cast<size_t>(tok) * hv;
     uint4* dst = f.Xp + static_cast<size_t>(r) * hv;
+    // 8 x 16 B in flight per lane (a 4 KB row per pass over the warp).
     int v = lane;
-    for (; v + 96 < hv; v += 128) {
-      const uint4 a = ld_nc_v4(src + v), b = ld_nc_v4(src + v + 32), c = ld_nc_v4(src + v + 64),
-                  d = ld_nc_v4(src + v + 96);
-      dst[v] = a;
-      dst[v + 32] = b;
-      dst[v + 64] = c;
-      dst[v + 96] = d;
+    for (; v + 224 < hv; v += 256) {
+      uint4 a[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) a[u] = ld_nc_v4(src + v + 32 * u);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) dst[v + 32 * u] = a[u];
     }
     for (; v < hv; v += 32) dst[v] = ld_nc_v4(src + v);
   }
@@ -1336,6 +1336,332 @@ __global__ void __launch_bounds__(kThreads, 1) fused_forward_kernel(const __grid
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// ---------------------------------------------------------------------------
+// Fused persistent forward on two-SM pair tiles: the same task space as
+// fused_forward_kernel -- dispatch gathers, then GEMM1 (+SwiGLU) tiles, then
+// GEMM2 tiles, expert-ascending -- with a task of each kind covering one
+// 256-row pair of 128-row tiles, and the pair-tile pipeline of
+// pair_gemm_kernel for the GEMM tasks.
+//
+// The even CTA's producer warp takes the task ids from the global cursor and
+// writes each into the task rings of both CTAs (a shared::cluster store into
+// the odd CTA's ring, released with the arrive on its `rfull`).  Every other
+// role warp of both CTAs reads its own ring and releases the slot on the even
+// CTA's `rempty` (count 9 + 10).  A gather task has each CTA gather the rows
+// of its own 128-row tile; a GEMM task has each CTA's producer wait on the
+// scoreboard counters of its own rows ("UniEP", section 3, Scoreboard-based
+// Synchronization: a GEMM1 tile once its rows are gathered, a GEMM2 tile once
+// every GEMM1 tile of its rows has stored h).  Tasks wait only on smaller task
+// indices, so progress needs no more pairs than the ones resident.
+// ---------------------------------------------------------------------------
+constexpr int kFusedPairStages = 6;
+
+struct PairFwdTask {
+  int kind;  // kTaskGather, kFwd1, kFwd2 or kTaskEnd
+  Tile t;    // this CTA's part
+};
+
+// Task order: the gathers of every pair first, then the GEMM1 tiles, then the
+// GEMM2 tiles, each in ascending expert order ("UniEP", section 4: dispatch
+// before computation).  (Interleaving an expert's gathers with the previous
+// experts' GEMM tiles measured slower: the GEMM tiles then wait on gathers
+// still in flight.)
+__device__ __forceinline__ PairFwdTask fwd_pair_decode(const FusedFwdParams& f, const ExpertTables& x, int task,
+                                                       uint32_t rank) {
+  const int P = x.pairs[f.p1.E];
+  const int nn1 = f.p1.F / 128;
+  PairFwdTask k;
+  if (task < P) {  // gather of pair `task`: this CTA's 128-row tile of it
+    int lo = 0, hi = f.p1.E;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (x.pairs[mid] <= task)
+        lo = mid;
+      else
+        hi = mid;
+    }
+    const int e = lo;
+    const int j = 2 * (task - x.pairs[e]) + static_cast<int>(rank);
+    k.kind = kTaskGather;
+    k.t.e = e;
+    k.t.row0 = x.offsets[e] + kTileRows * j;
+    k.t.nrows = max(0, min(kTileRows, x.counts[e] - kTileRows * j));
+    k.t.mt = x.tstart[e] + j;
+    k.t.m0 = k.t.n0 = k.t.nw = k.t.kblocks = 0;
+  } else if (task < P * (1 + nn1)) {
+    k.kind = kFwd1;
+    k.t = pair_decode<kFwd1>(f.p1, x, task - P, rank);
+  } else {
+    k.kind = kFwd2;
+    k.t = pair_decode<kFwd2>(f.p2, x, task - P * (1 + nn1), rank);
+  }
+  return k;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) fused_forward_pair_kernel(const __grid_constant__ FusedFwdMaps maps,
+                                                                         const FusedFwdParams f) {
+  constexpr int S = kFusedPairStages;
+  constexpr uint32_t kIdesc256 = idesc_bf16_f32(256, 256, false, true);
+  constexpr uint32_t kIdesc128 = idesc_bf16_f32(256, 128, false, true);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * kPairStageBytes);
+  uint64_t* empty = full + S;
+  uint64_t* pfull = empty + S;
+  uint64_t* tfull = pfull + S;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* rfull = tempty + 2;
+  uint64_t* rempty = rfull + kTaskRing;
+  volatile int* ring = reinterpret_cast<volatile int*>(rempty + kTaskRing);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(ring) + kTaskRing);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* tab = reinterpret_cast<int*>(smem + S * kPairStageBytes + 512);
+  const int E = f.p1.E;
+  ExpertTables xt;
+  xt.pairs = tab;
+  xt.counts = tab + (E + 1);
+  xt.offsets = tab + 2 * (E + 1);
+  xt.tstart = tab + 3 * (E + 1);
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    tab[e] = __ldg(f.p1.pairs + e);
+    tab[(E + 1) + e] = e < E ? __ldg(f.p1.counts + e) : 0;
+    tab[2 * (E + 1) + e] = __ldg(f.p1.offsets + e);
+    tab[3 * (E + 1) + e] = __ldg(f.p1.tiles + 1 + e);
+  }
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = (rank == 0);
+  WsHeader* ws = f.p1.ws;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+      mbar_init(&pfull[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 2 * kEpiWarps);
+    }
+    for (int i = 0; i < kTaskRing; ++i) {
+      mbar_init(&rfull[i], 1);
+      mbar_init(&rempty[i], (1 + kEpiWarps) + (2 + kEpiWarps));  // even CTA: MMA + epilogue; odd: all role warps
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int P = xt.pairs[E];
+  const int nn1 = f.p1.F / 128;
+  const int nn2 = (f.p1.H + BN - 1) / BN;
+  const int total = P * (1 + nn1 + nn2);
+  const uint32_t rempty_leader = mapa_shared(smem_u32(rempty), 0);
+
+  // Next task of the ring: the even CTA's producer fills slots, every other role
+  // warp of both CTAs consumes them.  Returns kTaskEnd when done or aborted.
+  auto consume = [&](int& slot, uint32_t& rph, int where) -> int {
+    const bool ok = leader ? mbar_wait(&rfull[slot], rph, ws, where, abort_flag)
+                           : mbar_wait_acq_cluster(&rfull[slot], rph, ws, where, abort_flag);
+    int task = kTaskEnd;
+    if (ok) task = ring[slot];
+    __syncwarp();
+    if (ok && lane == 0) {
+      if (leader)
+        mbar_arrive(&rempty[slot]);
+      else
+        mbar_arrive_cluster(rempty_leader + slot * 8);
+    }
+    if (++slot == kTaskRing) {
+      slot = 0;
+      rph ^= 1u;
+    }
+    return task;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ task fetch (even CTA) + producer (both)
+    int s = 0, slot = 0;
+    uint32_t ph = 0, rph = 0;
+    uint32_t issued = 0, last_parity = 0;
+    const uint32_t ring_peer = mapa_shared(smem_u32(const_cast<int*>(ring)), 1);
+    const uint32_t rfull_peer = mapa_shared(smem_u32(rfull), 1);
+    int next = (leader && lane == 0) ? atomicAdd(f.cursor, 1) : 0;
+    while (true) {
+      int task;
+      if (leader) {
+        if (!mbar_wait(&rempty[slot], rph ^ 1u, ws, 180, abort_flag)) break;
+        task = 0;
+        if (lane == 0) {
+          task = next;
+          if (task >= total || *abort_flag) task = kTaskEnd;
+          if (task != kTaskEnd) next = atomicAdd(f.cursor, 1);
+          ring[slot] = task;
+          st_shared_cluster_u32(ring_peer + slot * 4, static_cast<uint32_t>(task));
+        }
+        task = __shfl_sync(0xffffffffu, task, 0);
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&rfull[slot]);
+          mbar_arrive_release_cluster(rfull_peer + slot * 8);
+        }
+        if (++slot == kTaskRing) {
+          slot = 0;
+          rph ^= 1u;
+        }
+      } else {
+        task = consume(slot, rph, 181);
+      }
+      if (task == kTaskEnd) break;
+      const PairFwdTask k = fwd_pair_decode(f, xt, task, rank);
+      if (k.kind == kTaskGather) continue;
+      const bool g1 = (k.kind == kFwd1);
+      // Scoreboard: this CTA's input rows must be complete.
+      if (k.t.nrows > 0) {
+        if (!wait_counter(g1 ? f.cnt_gather + k.t.mt : f.cnt_g1 + k.t.mt, g1 ? kEpiWarps : nn1 * kEpiWarps, ws,
+                          g1 ? 182 : 183, abort_flag))
+          continue;
+        fence_proxy_async_global();
+      }
+      for (int kb = 0; kb < k.t.kblocks; ++kb) {
+        if (!mbar_wait_cluster(&empty[s], ph ^ 1u, ws, 184, abort_flag)) break;
+        if (elect_one()) {
+          mbar_arrive_expect_tx(&full[s], kABytes + k.t.nw * 64);
+          uint8_t* sA = smem + s * kPairStageBytes;
+          if (g1)
+            load_kblock_pair<kFwd1>(f.p1, maps.g1, k.t, kb, sA, sA + kABytes, &full[s], rank);
+          else
+            load_kblock_pair<kFwd2>(f.p2, maps.g2, k.t, kb, sA, sA + kABytes, &full[s], rank);
+        }
+        __syncwarp();
+        issued |= 1u << s;
+        last_parity = (last_parity & ~(1u << s)) | (ph << s);
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+    for (int i = 0; i < S; ++i)
+      if ((issued >> i) & 1u) mbar_wait(&full[i], (last_parity >> i) & 1u, ws, 185, nullptr);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA) / relay (odd CTA)
+    int s = 0, slot = 0, acc = 0;
+    uint32_t ph = 0, rph = 0, acc_ph = 0;
+    bool ok = true;
+    const uint32_t pfull_leader = mapa_shared(smem_u32(pfull), 0);
+    while (ok) {
+      const int task = consume(slot, rph, 186);
+      if (task == kTaskEnd) break;
+      const PairFwdTask k = fwd_pair_decode(f, xt, task, rank);
+      if (k.kind == kTaskGather) continue;
+      if (leader) {
+        if (!mbar_wait_cluster(&tempty[acc], acc_ph ^ 1u, ws, 187, abort_flag)) break;
+        tc_fence_after();
+      }
+      const uint32_t d_tmem = tmem_base + acc * kAccStride;
+      const uint32_t idesc = (k.t.nw == 256) ? kIdesc256 : kIdesc128;
+      for (int kb = 0; kb < k.t.kblocks; ++kb) {
+        if (!mbar_wait(&full[s], ph, ws, 188, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (!leader) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(pfull_leader + s * 8);
+          __syncwarp();
+        } else {
+          if (!mbar_wait_cluster(&pfull[s], ph, ws, 189, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (elect_one()) {
+            const uint32_t a0 = smem_u32(smem + s * kPairStageBytes), b0 = a0 + kABytes;
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint64_t ad = smem_desc_sw128(a0 + kk * 32u, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(b0 + kk * 2048u, kPanelBytes, 1024);
+              tc_mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+            }
+            tc_commit_pair(&empty[s]);
+          }
+          __syncwarp();
+        }
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (leader) {
+        if (elect_one()) tc_commit_pair(&tfull[acc]);
+        __syncwarp();
+      }
+      acc ^= 1;
+      if (acc == 0) acc_ph ^= 1u;
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue + gathers (both CTAs)
+    const int ew = warp - 2;
+    const int q = warp & 3;
+    const int half = ew >> 2;
+    OutStager st;  // unused by the forward modes
+    st.buf = nullptr;
+    const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), 0);
+    int slot = 0, acc = 0;
+    uint32_t rph = 0, acc_ph = 0;
+    while (true) {
+      const int task = consume(slot, rph, 190);
+      if (task == kTaskEnd) break;
+      const PairFwdTask k = fwd_pair_decode(f, xt, task, rank);
+      if (k.kind == kTaskGather) {
+        if (k.t.nrows > 0) {
+          gather_rows_task(f, k.t, ew, lane);
+          signal_counter(f.cnt_gather + k.t.mt, lane);
+        }
+        continue;
+      }
+      if (!mbar_wait_cluster(&tfull[acc], acc_ph, ws, 191, abort_flag)) break;
+      tc_fence_after();
+      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccStride;
+      if (k.t.nrows > 0) {
+        if (k.kind == kFwd1)
+          epilogue<kFwd1>(f.p1, maps.g1, k.t, tacc, q, half, lane, st);
+        else
+          epilogue<kFwd2>(f.p2, maps.g2, k.t, tacc, q, half, lane, st);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader)
+          mbar_arrive(&tempty[acc]);
+        else
+          mbar_arrive_cluster(tempty_leader + acc * 8);
+      }
+      acc ^= 1;
+      if (acc == 0) acc_ph ^= 1u;
+      if (k.kind == kFwd1 && k.t.nrows > 0) signal_counter(f.cnt_g1 + k.t.mt, lane);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
 }
 
 // ---------------------------------------------------------------------------
@@ -1868,6 +2194,75 @@ cudaError_t launch_fused_forward(const GemmLaunch& L, const void* x, const int32
   hook.before(s);
   fused_forward_kernel<<<L.grid, kThreads, kSmem, s>>>(m, f);
   hook.after(s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fused_forward_pair(const GemmLaunch& L, const void* x, const int32_t* row_src, int32_t* cursor,
+                                      int32_t* cnt_gather, int32_t* cnt_g1, cudaStream_t s, LaunchHook& hook) {
+  const uint64_t R = L.R, H = L.H, F = L.F, E = L.E;
+  FusedFwdMaps m;
+  memset(&m, 0, sizeof(m));
+  if (!(make_map(&m.g1.a, L.Xp, H, R, 64, BM) && make_map(&m.g1.b0, L.W1, F, E * H, 64, 64) &&
+        make_map(&m.g1.b1, L.W3, F, E * H, 64, 64) && make_map(&m.g2.a, L.out_h, F, R, 64, BM) &&
+        make_map(&m.g2.b0, L.W2, H, E * F, 64, 64)))
+    return cudaErrorInvalidValue;
+  FusedFwdParams f{};
+  GemmParams p{};
+  p.H = L.H;
+  p.F = L.F;
+  p.E = L.E;
+  p.R = L.R;
+  p.tiles = L.tiles;
+  p.pairs = L.pairs;
+  p.offsets = L.offsets;
+  p.counts = L.counts;
+  p.ws = L.ws;
+  f.p1 = p;
+  f.p1.out0 = static_cast<__nv_bfloat16*>(L.out_h);
+  f.p1.out1 = static_cast<__nv_bfloat16*>(L.out_GU);
+  f.p2 = p;
+  f.p2.out0 = static_cast<__nv_bfloat16*>(L.out_Y);
+  f.x = static_cast<const uint4*>(x);
+  f.Xp = static_cast<uint4*>(const_cast<void*>(L.Xp));
+  f.row_src = row_src;
+  f.T = L.T;
+  f.cursor = cursor;
+  f.cnt_gather = cnt_gather;
+  f.cnt_g1 = cnt_g1;
+  const int kSmem = kFusedPairStages * kPairStageBytes + 1024 + 512 + static_cast<int>(pair_table_bytes(L.E));
+  auto kern = fused_forward_pair_kernel;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  static int max_pairs = -1, max_pairs_smem = -1;
+  if (max_pairs < 0 || max_pairs_smem != kSmem) {
+    max_pairs_smem = kSmem;
+    cfg.gridDim = dim3(2, 1, 1);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      n = 0;
+    }
+    max_pairs = n;
+  }
+  int pairs = L.grid / 2;
+  if (pairs < 1) pairs = 1;
+  if (max_pairs > 0 && pairs > max_pairs) pairs = max_pairs;
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  hook.before(s);
+  e = cudaLaunchKernelEx(&cfg, kern, m, f);
+  hook.after(s);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

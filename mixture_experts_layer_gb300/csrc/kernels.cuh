@@ -155,6 +155,10 @@ cudaError_t launch_gemm(GemmMode mode, const GemmLaunch& p, cudaStream_t s, Laun
 cudaError_t launch_fused_forward(const GemmLaunch& L, const void* x, const int32_t* row_src, int32_t* cursor,
                                  int32_t* cnt_gather, int32_t* cnt_g1, cudaStream_t s, LaunchHook& hook);
 
+// The same on two-SM pair tiles (clusters of two CTAs; counters per 128-row tile).
+cudaError_t launch_fused_forward_pair(const GemmLaunch& L, const void* x, const int32_t* row_src, int32_t* cursor,
+                                      int32_t* cnt_gather, int32_t* cnt_g1, cudaStream_t s, LaunchHook& hook);
+
 // dgrad2, dgrad1 and both weight-gradient GEMMs as one persistent kernel
 // (task cursor and per-tile counters must be zero at launch).
 cudaError_t launch_fused_backward(const GemmLaunch& L, int32_t* cursor, int32_t* cnt_d2, int32_t* cnt_e,

@@ -295,7 +295,8 @@ int moe_forward(moe_dims d, const void* x, const void* W1, const void* W3, const
     int32_t* cursor = reinterpret_cast<int32_t*>(sched);
     int32_t* cnt_gather = reinterpret_cast<int32_t*>(sched + 64);
     int32_t* cnt_g1 = cnt_gather + L.cap;
-    e = launch_fused_forward(g, x, plan->row_src, cursor, cnt_gather, cnt_g1, s, hook);
+    e = use_pair(opts, kFwd1) ? launch_fused_forward_pair(g, x, plan->row_src, cursor, cnt_gather, cnt_g1, s, hook)
+                              : launch_fused_forward(g, x, plan->row_src, cursor, cnt_gather, cnt_g1, s, hook);
     if (e != cudaSuccess) return MOE_ERR_LAUNCH;
   } else {
     e = launch_gather(r, x, saved->Xp, s, hook);

@@ -82,3 +82,28 @@ def test_pair_tiles_give_the_bits_of_single_tiles(shape, seed):
     for n in OUTS:
         md, frac = _diff(getattr(a, n), getattr(b, n))
         assert md == 0 and frac == 0, f"{n}: max_diff={md} non-bw={frac:.2%}"
+
+
+@pytest.mark.parametrize("shape,seed", [(S.CONFIGS[1], S.config_seed(1)), (S.LayerShape(700, 384, 640, 6, 2), 44),
+                                        (S.LayerShape(900, 256, 256, 24, 4), 45)])
+def test_fused_forward_pair_tiles_bitwise(shape, seed):
+    """The fused persistent forward on pair tiles (task ring shared by a CTA pair)
+    gives the bits of the phased pair-tile forward, over grids of 2, 74 and one
+    CTA per SM, and of the single-CTA fused forward."""
+    from mixture_experts_layer_gb300.layer import MoELayer
+    inp = shape_inputs(shape, seed)
+    if shape.E == 24:
+        inp["logits"][:, :5] -= 40.0  # a few empty experts
+    ref = MoELayer(shape.T, shape.H, shape.F, shape.E, shape.k)
+    run_gpu(ref, inp, opts=ref.opts(schedule=0))
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    L = MoELayer(shape.T, shape.H, shape.F, shape.E, shape.k)
+    for g, pair in ((0, 2), (2, 2), (74, 2), (sms, 2), (0, 1)):
+        for n in ("Xp", "GU", "h", "Y", "out"):
+            getattr(L, n).fill_(float("nan"))
+        run_gpu(L, inp, opts=L.opts(grid=g, schedule=1, cta_pair=pair))
+        for n in ("Xp", "GU", "h", "Y", "out", "dx", "dW1"):
+            a, b = getattr(L, n), getattr(ref, n)
+            if n in ("Xp", "GU", "h", "Y"):
+                a, b = a[: L.R], b[: L.R]
+            assert torch.equal(a, b), f"{n} differs (grid {g}, cta_pair {pair})"
