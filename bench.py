@@ -37,6 +37,7 @@ METRIC = "MoE-layer tokens/s fwd+bwd; GEMM % BF16 peak; permute GB/s % HBM"
 UNIT = "tokens/s"
 
 FWD_KERNELS = ["gather_rows", "gemm_fwd1_swiglu", "gemm_fwd2", "combine"]
+FWD_KERNELS_COMBINE_FUSED = ["gather_rows", "gemm_fwd1_swiglu", "gemm_fwd2_combine"]
 FWD_KERNELS_FUSED = ["fused_forward", "combine"]
 BWD_KERNELS = ["combine_bwd", "gemm_dgrad2_swiglu_bwd", "gemm_dgrad1", "unpermute", "gemm_wgrad13", "gemm_wgrad2"]
 BWD_KERNELS_FUSED = ["combine_bwd", "fused_backward", "unpermute"]
@@ -61,6 +62,8 @@ def work_per_kernel(T, H, F, E, k):
         "gemm_wgrad2": 2 * R * F + 2 * R * H + 4 * E * H * F,
         "unpermute": 2 * R * H + 2 * T * H + 4 * R,
     }
+    # GEMM2 with the gated combine in its epilogue: also reads the k rows of Y per token and writes out.
+    b["gemm_fwd2_combine"] = b["gemm_fwd2"] + b["combine"]
     # Fused forward: reads x, row_src and every weight once; writes Xp, GU, h and Y.
     b["fused_forward"] = 2 * T * H + 4 * R + 6 * E * H * F + 2 * R * H + 6 * R * F + 2 * R * H
     # Fused backward: reads dY, GU, Xp, h and every weight once; writes dGU, dXp and dW1, dW3, dW2 (fp32).
@@ -80,6 +83,7 @@ def work_per_kernel(T, H, F, E, k):
         "fused_backward": 12 * R * H * F,
         "gemm_fwd1_swiglu": 4 * R * H * F,
         "gemm_fwd2": 2 * R * H * F,
+        "gemm_fwd2_combine": 2 * R * H * F,
         "gemm_dgrad2_swiglu_bwd": 2 * R * H * F,
         "gemm_dgrad1": 4 * R * H * F,
         "gemm_wgrad13": 4 * R * H * F,
@@ -332,7 +336,8 @@ def run_ours(args):
     inp = S.layer_inputs(shape, seed, device=dev)
     layer = MoELayer(T, H, F, E, k, device=dev, with_router=args.router)
     stream = torch.cuda.current_stream(dev)
-    fwd_names = FWD_KERNELS_FUSED if args.schedule in (1, 2) else FWD_KERNELS
+    fwd_names = (FWD_KERNELS_FUSED if args.schedule in (1, 2)
+                 else FWD_KERNELS_COMBINE_FUSED if args.combine == 1 else FWD_KERNELS)
     bwd_names = BWD_KERNELS_FUSED if args.schedule == 2 else BWD_KERNELS
     if args.router:
         if args.schedule == 2:
@@ -340,7 +345,7 @@ def run_ours(args):
         bwd_names = BWD_KERNELS_ROUTER
     nf, nb = len(fwd_names), len(bwd_names)
     router_arg = (inp["x"], inp["Wr"]) if args.router else None
-    base_opts = layer.opts(schedule=args.schedule, cta_pair=args.cta_pair)
+    base_opts = layer.opts(schedule=args.schedule, cta_pair=args.cta_pair, combine=args.combine)
 
     def step(opts_f=None, opts_b=None, ev_plan=None, opts_r=None):
         opts_f = opts_f if opts_f is not None else base_opts
@@ -384,17 +389,17 @@ def run_ours(args):
     opts_f = []
     keep = []
     for e in evs_f:
-        o = layer.opts(events=e, schedule=args.schedule, cta_pair=args.cta_pair)
+        o = layer.opts(events=e, schedule=args.schedule, cta_pair=args.cta_pair, combine=args.combine)
         keep.append(layer._ev_keep)
         opts_f.append(o)
     opts_b = []
     for e in evs_b:
-        o = layer.opts(events=e, schedule=args.schedule, cta_pair=args.cta_pair)
+        o = layer.opts(events=e, schedule=args.schedule, cta_pair=args.cta_pair, combine=args.combine)
         keep.append(layer._ev_keep)
         opts_b.append(o)
     opts_r = []
     for e in evs_r:
-        o = layer.opts(events=e, schedule=args.schedule, cta_pair=args.cta_pair)
+        o = layer.opts(events=e, schedule=args.schedule, cta_pair=args.cta_pair, combine=args.combine)
         keep.append(layer._ev_keep)
         opts_r.append(o)
 
@@ -570,6 +575,8 @@ def main():
     ap.add_argument("--cta-pair", type=int, default=0, choices=[0, 1, 2],
                     help="grouped GEMMs that run as their own kernels: 0 library default (pair tiles but for "
                          "dgrad2), 1 one CTA per tile, 2 two-CTA pair tiles")
+    ap.add_argument("--combine", type=int, default=0, choices=[0, 1],
+                    help="schedule 0: 0 a separate gated-combine kernel, 1 the combine in GEMM2's epilogue")
     ap.add_argument("--router", action="store_true",
                     help="put the router on the timed path: logits = x Wr on the GPU and its backward")
     ap.add_argument("--profile", action="store_true",

@@ -129,6 +129,11 @@ typedef struct {
                        0 (default): 2 for every GEMM but the dgrad GEMM with the SwiGLU backward
                        epilogue, which measured faster with 1.  Both shapes give the same bits.
                        The fused persistent kernels of schedules 1 and 2 use single-CTA tiles. */
+  int32_t combine;  /* schedule 0 only.  0 (default): a separate gated-combine kernel.
+                       1: the combine runs in GEMM2's epilogue (per-token arrival counters; the
+                       warp that completes a token's k rows sums them, in slot order).  Same
+                       bits; measured slower on GB300 (the fence and the combine work in the
+                       epilogue hold the accumulator and stall the tensor pipe). */
 } moe_opts;
 
 /* ---- sizes ------------------------------------------------------------------ */
@@ -239,7 +244,7 @@ MOE_API int32_t moe_version(void);
 MOE_API uint64_t moe_launch_count(void);
 /* Name of the i-th kernel a call launches (call: 0 plan, 1 forward, 2 backward, 3 forward with
  * schedule 1 or 2, 4 backward with schedule = 2, 5 backward with the router (schedule 0 or 1),
- * 6 moe_router_forward); NULL past the end. */
+ * 6 moe_router_forward, 7 forward with schedule 0 and combine = 1 (combine in GEMM2's epilogue)); NULL past the end. */
 MOE_API const char *moe_kernel_name(int32_t call, int32_t i);
 
 #ifdef __cplusplus

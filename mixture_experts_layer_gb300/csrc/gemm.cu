@@ -75,9 +75,20 @@ struct Maps {
   CUtensorMap b3;  // W3, 128-row box
 };
 
+// The gated combine fused into GEMM2's epilogue (null cnt: not fused).
+struct CombineParams {
+  int32_t* cnt;            // [T][N tiles][2] arrivals of (token, 256-column tile, column half); zero at launch
+  const int32_t* row_src;  // [R] token of each grouped row
+  const int32_t* dest;     // [T,k]
+  const float* w;          // [T,k]
+  __nv_bfloat16* out;      // [T,H]
+  int k;
+};
+
 struct GemmParams {
   int H, F, E, R;
   int T, splits, ks;  // router modes: tokens, token splits of the weight gradient, tokens per split
+  CombineParams cmb;
   const int32_t* tiles;
   const int32_t* pairs;  // first 256-row pair tile of each expert (E + 1)
   const int32_t* offsets;
@@ -326,6 +337,121 @@ __device__ __forceinline__ int clear_k_tail(uint8_t* sA, uint8_t* sB, int valid,
   return nkk;
 }
 
+// The gated combine in GEMM2's epilogue ("UniEP", section 3, Top-k
+// accumulation constraint, and section 5, Reduce Workers: a token's output is
+// summed only when all k of its expert rows are ready, in a fixed order).  Each
+// thread has just stored columns [c_lo, c_hi) of the 256-column tile for its
+// row; it counts that half-row done for its token (release: a fence before the
+// atomic).  The thread whose count completes the token's k rows flags it, and
+// the warp then writes out[t] for those columns for every flagged token:
+// out = bf16(sum_j w[t,j] Y[dest[t,j]]) in slot order, the arithmetic of the
+// separate combine kernel, so both give the same bits.
+__device__ __forceinline__ void combine_in_epilogue(const GemmParams& p, const Tile& t, size_t grow, bool valid,
+                                                    int half, int c_lo, int c_hi, int lane) {
+  const CombineParams& c = p.cmb;
+  const int nn = (p.H + BN - 1) / BN;
+  __threadfence();
+  int tok = -1, done = 0;
+  if (valid) {
+    tok = __ldg(c.row_src + grow);
+    if (tok < 0 || tok >= p.T) {
+      report(p.ws, MOE_ERR_BOUNDS, 30, static_cast<int>(grow));
+    } else {
+      const int old = atomicAdd(c.cnt + (static_cast<size_t>(tok) * nn + t.n0 / BN) * 2 + half, 1);
+      done = (old == c.k - 1);
+    }
+  }
+  uint32_t m = __ballot_sync(0xffffffffu, done);
+  if (m == 0) return;
+  __threadfence();  // acquire: the other rows' Y stores are visible to this warp
+  // Lane groups of nvec lanes (one 16-byte vector each) take one completed token
+  // apiece; every slot's row is loaded before any is summed.
+  const int nvec = (c_hi - c_lo) / 8;  // 8 or 16
+  const int per = 32 / nvec;
+  const int grp = lane / nvec, l = lane % nvec;
+  const int hv = p.H / 8;
+  const int v = (t.n0 + c_lo) / 8 + l;
+  while (m) {
+    int src = -1;
+    for (int i = 0; i < per; ++i) {
+      const int f = m ? __ffs(m) - 1 : -1;
+      if (i == grp) src = f;
+      if (m) m &= m - 1;
+    }
+    const int tt = __shfl_sync(0xffffffffu, tok, src < 0 ? 0 : src);
+    if (src < 0) continue;
+    constexpr int K = 8;
+    if (c.k <= K) {
+      int r[K];
+      float wj[K];
+      uint4 y[K];
+#pragma unroll
+      for (int j = 0; j < K; ++j) {
+        r[j] = j < c.k ? __ldg(c.dest + static_cast<size_t>(tt) * c.k + j) : 0;
+        wj[j] = j < c.k ? __ldg(c.w + static_cast<size_t>(tt) * c.k + j) : 0.f;
+      }
+      bool bad = false;
+#pragma unroll
+      for (int j = 0; j < K; ++j) {
+        if (j < c.k) {
+          if (r[j] < 0 || r[j] >= p.R) {
+            bad = true;
+            r[j] = 0;
+          }
+          asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(y[j].x), "=r"(y[j].y), "=r"(y[j].z), "=r"(y[j].w)
+                       : "l"(reinterpret_cast<const uint4*>(p.out0) + static_cast<size_t>(r[j]) * hv + v));
+        }
+      }
+      if (bad) {
+        report(p.ws, MOE_ERR_BOUNDS, 31, tt);
+        continue;
+      }
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < K; ++j) {
+        if (j < c.k) {
+          const uint32_t yw[4] = {y[j].x, y[j].y, y[j].z, y[j].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc[2 * i] = fmaf(wj[j], bf16lo(yw[i]), acc[2 * i]);
+            acc[2 * i + 1] = fmaf(wj[j], bf16hi(yw[i]), acc[2 * i + 1]);
+          }
+        }
+      }
+      st_v4(reinterpret_cast<uint4*>(c.out) + static_cast<size_t>(tt) * hv + v, pack_bf16x2(acc[0], acc[1]),
+            pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+    } else {
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      bool bad = false;
+      for (int j = 0; j < c.k; ++j) {
+        const int rj = __ldg(c.dest + static_cast<size_t>(tt) * c.k + j);
+        const float wjj = __ldg(c.w + static_cast<size_t>(tt) * c.k + j);
+        if (rj < 0 || rj >= p.R) {
+          bad = true;
+          break;
+        }
+        uint4 y;
+        asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(y.x), "=r"(y.y), "=r"(y.z), "=r"(y.w)
+                     : "l"(reinterpret_cast<const uint4*>(p.out0) + static_cast<size_t>(rj) * hv + v));
+        const uint32_t yw[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[2 * i] = fmaf(wjj, bf16lo(yw[i]), acc[2 * i]);
+          acc[2 * i + 1] = fmaf(wjj, bf16hi(yw[i]), acc[2 * i + 1]);
+        }
+      }
+      if (bad) {
+        report(p.ws, MOE_ERR_BOUNDS, 31, tt);
+        continue;
+      }
+      st_v4(reinterpret_cast<uint4*>(c.out) + static_cast<size_t>(tt) * hv + v, pack_bf16x2(acc[0], acc[1]),
+            pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+    }
+  }
+}
+
 template <int MODE>
 __device__ __forceinline__ void epilogue(const GemmParams& p, const Maps& m, const Tile& t, uint32_t tacc, int q,
                                          int half, int lane, OutStager& st) {
@@ -486,6 +612,7 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, const Maps& m, con
       }
     }
   }
+  if (MODE == kFwd2 && p.cmb.cnt != nullptr) combine_in_epilogue(p, t, grow, valid, half, c_lo, c_hi, lane);
 }
 
 template <int MODE>
@@ -2291,6 +2418,8 @@ cudaError_t launch_gemm(GemmMode mode, const GemmLaunch& L, cudaStream_t s, Laun
     case kFwd2:
       ok = make_map(&m.a, L.h, F, R, 64, BM) && make_map(&m.b0, L.W2, H, E * F, 64, 64);
       p.out0 = static_cast<__nv_bfloat16*>(L.out_Y);
+      p.cmb = CombineParams{L.cmb.cnt, L.cmb.row_src, L.cmb.dest, L.cmb.w,
+                            static_cast<__nv_bfloat16*>(L.cmb.out), L.cmb.k};
       break;
     case kDgrad2:
       ok = make_map(&m.a, L.dY, H, R, 64, BM) && make_map(&m.b0, L.W2, H, E * F, 64, BN) &&
@@ -2326,6 +2455,7 @@ cudaError_t launch_gemm(GemmMode mode, const GemmLaunch& L, cudaStream_t s, Laun
   p.T = L.T;
   p.splits = L.splits;
   p.ks = L.ks;
+  if (mode != kFwd2) p.cmb = CombineParams{};
   if (!ok) return cudaErrorInvalidValue;
   if (L.pair && mode != kRfwd && mode != kRwgrad) return launch_gemm_pair(mode, L, m, p, s, hook);
   switch (mode) {

@@ -112,6 +112,16 @@ enum GemmMode : int {
   kRwgrad = 7,  // router dWr partial = x^T dl over a token split (A MN-major, B MN-major)
 };
 
+// The gated combine fused into GEMM2's epilogue (kFwd2; cnt = null: not fused).
+struct CombineLaunch {
+  int32_t* cnt;            // [T][ceil(H/256)][2], zeroed before the launch
+  const int32_t* row_src;
+  const int32_t* dest;
+  const float* w;
+  void* out;               // [T,H] bf16
+  int k;
+};
+
 struct GemmLaunch {
   int T, H, F, E, k, R;
   int grid;
@@ -146,6 +156,7 @@ struct GemmLaunch {
   float* logits;       // kRfwd out [T,E]
   float* dwr_part;     // kRwgrad out [splits][H][E] (or dWr itself when splits = 1)
   int splits, ks;      // token splits of kRwgrad and tokens per split (a multiple of 64)
+  CombineLaunch cmb;   // kFwd2
   WsHeader* ws;
 };
 cudaError_t launch_gemm(GemmMode mode, const GemmLaunch& p, cudaStream_t s, LaunchHook& hook);

@@ -59,6 +59,7 @@ struct WsLayout {
   size_t ccount, cbase, gbm, sched, sched_bytes, total;
   size_t cap;  // capacity of the 128-row tile table
   size_t wrT, dl_slot, dl_bf16, dwr_part;  // router backward
+  size_t cmb_cnt, cmb_bytes;               // arrivals of the combine fused into GEMM2
   int splits, ks;                          // token splits of the dWr GEMM and tokens per split
 };
 
@@ -101,6 +102,9 @@ WsLayout ws_layout(const moe_dims& d) {
   off = align256(off + static_cast<size_t>(d.T) * d.E * 2);
   L.dwr_part = off;
   off = align256(off + static_cast<size_t>(L.splits) * d.H * d.E * 4);
+  L.cmb_cnt = off;
+  L.cmb_bytes = static_cast<size_t>(d.T) * ((d.H + 255) / 256) * 2 * 4;
+  off = align256(off + L.cmb_bytes);
   L.total = off;
   return L;
 }
@@ -158,6 +162,7 @@ int use_pair(const moe_opts* o, GemmMode m) {
 const char* const kPlanKernels[] = {"route_topk", "route_scan", "route_rank", nullptr};
 const char* const kFwdKernelsFused[] = {"fused_forward", "combine", nullptr};
 const char* const kFwdKernels[] = {"gather_rows", "gemm_fwd1_swiglu", "gemm_fwd2", "combine", nullptr};
+const char* const kFwdKernelsCombineFused[] = {"gather_rows", "gemm_fwd1_swiglu", "gemm_fwd2_combine", nullptr};
 const char* const kBwdKernels[] = {"combine_bwd", "gemm_dgrad2_swiglu_bwd", "gemm_dgrad1", "unpermute",
                                    "gemm_wgrad13", "gemm_wgrad2", nullptr};
 const char* const kBwdKernelsFused[] = {"combine_bwd", "fused_backward", "unpermute", nullptr};
@@ -263,7 +268,7 @@ int moe_forward(moe_dims d, const void* x, const void* W1, const void* W3, const
   if (rc) return rc;
   if ((rc = check_ws(d, ws, ws_bytes))) return rc;
   if (opts != nullptr && (opts->schedule < 0 || opts->schedule > 2 || opts->grid < 0 || opts->cta_pair < 0 ||
-                          opts->cta_pair > 2))
+                          opts->cta_pair > 2 || opts->combine < 0 || opts->combine > 1))
     return MOE_ERR_ARG;
   if (d.T == 0) return MOE_OK;
   if ((rc = check_plan(plan))) return rc;
@@ -306,7 +311,15 @@ int moe_forward(moe_dims d, const void* x, const void* W1, const void* W3, const
     if ((e = launch_gemm(kFwd1, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
     g.bn = (d.H % 256 == 0) ? 256 : 128;
     g.pair = use_pair(opts, kFwd2);
+    const bool fuse = (opts != nullptr && opts->combine == 1);
+    if (fuse) {
+      const WsLayout L = ws_layout(d);
+      int32_t* cnt = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + L.cmb_cnt);
+      if (cudaMemsetAsync(cnt, 0, L.cmb_bytes, s) != cudaSuccess) return MOE_ERR_LAUNCH;
+      g.cmb = CombineLaunch{cnt, plan->row_src, plan->dest, plan->topk_w, out, d.k};
+    }
     if ((e = launch_gemm(kFwd2, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
+    if (fuse) return MOE_OK;
   }
   return finish(launch_combine(r, saved->Y, out, s, hook));
 }
@@ -319,7 +332,7 @@ int moe_backward(moe_dims d, const void* dout, const void* W1, const void* W3, c
   if (rc) return rc;
   if ((rc = check_ws(d, ws, ws_bytes))) return rc;
   if (opts != nullptr && (opts->schedule < 0 || opts->schedule > 2 || opts->grid < 0 || opts->cta_pair < 0 ||
-                          opts->cta_pair > 2))
+                          opts->cta_pair > 2 || opts->combine < 0 || opts->combine > 1))
     return MOE_ERR_ARG;
   if ((rc = check_ptrs({dW1, dW3, dW2}))) return rc;
   if (router != nullptr) {
@@ -490,6 +503,7 @@ const char* moe_kernel_name(int32_t call, int32_t i) {
                          : call == 4 ? kBwdKernelsFused
                          : call == 5 ? kBwdKernelsRouter
                          : call == 6 ? kRouterFwdKernels
+                         : call == 7 ? kFwdKernelsCombineFused
                                      : nullptr;
   if (t == nullptr || i < 0) return nullptr;
   for (int j = 0; j <= i; ++j)

@@ -25,6 +25,8 @@ def test_every_declared_symbol_is_exported():
         assert hasattr(M, n), f"binding lacks {n}"
     assert M.moe_version() >= 1
     assert M.moe_kernel_name(1, 1) == "gemm_fwd1_swiglu"
+    assert M.moe_kernel_name(1, 2) == "gemm_fwd2"
+    assert M.moe_kernel_name(7, 2) == "gemm_fwd2_combine"
     assert M.moe_kernel_name(3, 0) == "fused_forward"
     assert M.moe_kernel_name(2, 5) == "gemm_wgrad2"
     assert M.moe_kernel_name(2, 6) is None

@@ -74,3 +74,21 @@ def test_schedules_give_the_same_bits(shape, seed):
         assert not torch.isnan(ref.float()).any(), n
         for L in layers[1:]:
             assert torch.equal(getattr(L, n)[: L.R if n in rows else None], ref), n
+
+
+@pytest.mark.parametrize("shape,seed", [(S.CONFIGS[1], S.config_seed(1)), (S.LayerShape(700, 384, 640, 6, 2), 35),
+                                        (S.LayerShape(300, 256, 128, 4, 4), 36), (S.LayerShape(200, 128, 128, 8, 1), 37)])
+def test_combine_in_gemm2_epilogue_is_bitwise(shape, seed):
+    """The gated combine run in GEMM2's epilogue (per-token arrival counters,
+    the warp completing a token sums its k rows in slot order) gives the bits of
+    the separate combine kernel, over runs and grids."""
+    from mixture_experts_layer_gb300.layer import MoELayer
+    inp = shape_inputs(shape, seed)
+    ref = MoELayer(shape.T, shape.H, shape.F, shape.E, shape.k)
+    run_gpu(ref, inp, opts=ref.opts(combine=0))
+    L = MoELayer(shape.T, shape.H, shape.F, shape.E, shape.k)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for g in (0, 0, 74, sms, 2):
+        L.out.fill_(float("nan"))
+        run_gpu(L, inp, opts=L.opts(grid=g, combine=1))
+        assert torch.equal(L.out, ref.out), f"out differs at grid {g}"
