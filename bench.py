@@ -424,6 +424,8 @@ def run_ours(args):
     st = layer.status()
     if st[0] != 0:
         raise RuntimeError(f"device status {st}")
+    # Load imbalance of the routed batch: the busiest expert's rows over the mean, minus one.
+    maxvio = float(layer.counts.max().item()) / (T * k / E) - 1.0
 
     # Per-kernel average durations.
     names = (["gemm_router_fwd"] if args.router else []) + ["plan"] + fwd_names + bwd_names
@@ -524,7 +526,8 @@ def run_ours(args):
                                    2: "two-CTA 256x256 pair tiles (cta_group::2)"}[args.cta_pair],
                        router="on the path: logits = x Wr on the GPU, gradient through the gating (dlogits, dWr, "
                               "dx share)" if args.router else "off (logits given; the pages time the layer "
-                                                               "excluding gating)"),
+                                                               "excluding gating)",
+                       maxvio=round(maxvio, 4)),
         "roofline": roof,
         "e2e": {"value": round(world * T * args.steps / (e2e_ms * 1e-3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

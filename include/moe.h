@@ -134,6 +134,11 @@ typedef struct {
                        warp that completes a token's k rows sums them, in slot order).  Same
                        bits; measured slower on GB300 (the fence and the combine work in the
                        epilogue hold the accumulator and stall the tensor pipe). */
+  int32_t debug_drop_task; /* failure injection, for tests of the bounded waits: with schedule 1
+                       or 2, the fused forward withholds the completion signal of its gather task
+                       number debug_drop_task - 1, so the GEMM tile that needs those rows waits
+                       out its bound (2 s), the kernel records MOE_ERR_TIMEOUT in the status word
+                       and returns; the outputs are then undefined.  0 (default): off. */
 } moe_opts;
 
 /* ---- sizes ------------------------------------------------------------------ */

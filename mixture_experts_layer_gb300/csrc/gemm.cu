@@ -1196,6 +1196,7 @@ struct FusedFwdParams {
   int32_t* cursor;
   int32_t* cnt_gather;  // per 128-row tile: epilogue warps done gathering its rows
   int32_t* cnt_g1;      // per 128-row tile: GEMM1 epilogue warps done storing h
+  int drop_task;        // failure injection: task + 1 whose gather signal is withheld (0: none)
 };
 
 struct FusedFwdMaps {
@@ -1440,7 +1441,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_forward_kernel(const __grid
       const FwdTask k = fwd_decode(f, task);
       if (k.kind == kTaskGather) {
         gather_rows_task(f, k.t, ew, lane);
-        signal_counter(f.cnt_gather + k.t.mt, lane);
+        if (task + 1 != f.drop_task) signal_counter(f.cnt_gather + k.t.mt, lane);
         continue;
       }
       if (!mbar_wait(&tfull[acc], acc_ph, ws, 159, abort_flag)) break;
@@ -1757,7 +1758,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_forward_pair_kernel(const _
       if (k.kind == kTaskGather) {
         if (k.t.nrows > 0) {
           gather_rows_task(f, k.t, ew, lane);
-          signal_counter(f.cnt_gather + k.t.mt, lane);
+          if (task + 1 != f.drop_task) signal_counter(f.cnt_gather + k.t.mt, lane);
         }
         continue;
       }
@@ -2315,6 +2316,7 @@ cudaError_t launch_fused_forward(const GemmLaunch& L, const void* x, const int32
   f.cursor = cursor;
   f.cnt_gather = cnt_gather;
   f.cnt_g1 = cnt_g1;
+  f.drop_task = L.drop_task;
   constexpr int kSmem = 4 * kStageBytes + 1024 + 512;
   cudaError_t e = cudaFuncSetAttribute(fused_forward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
@@ -2356,6 +2358,7 @@ cudaError_t launch_fused_forward_pair(const GemmLaunch& L, const void* x, const 
   f.cursor = cursor;
   f.cnt_gather = cnt_gather;
   f.cnt_g1 = cnt_g1;
+  f.drop_task = L.drop_task;
   const int kSmem = kFusedPairStages * kPairStageBytes + 1024 + 512 + static_cast<int>(pair_table_bytes(L.E));
   auto kern = fused_forward_pair_kernel;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);

@@ -157,6 +157,7 @@ struct GemmLaunch {
   float* dwr_part;     // kRwgrad out [splits][H][E] (or dWr itself when splits = 1)
   int splits, ks;      // token splits of kRwgrad and tokens per split (a multiple of 64)
   CombineLaunch cmb;   // kFwd2
+  int drop_task;       // fused forward: failure injection (task + 1 whose gather signal is withheld; 0 none)
   WsHeader* ws;
 };
 cudaError_t launch_gemm(GemmMode mode, const GemmLaunch& p, cudaStream_t s, LaunchHook& hook);

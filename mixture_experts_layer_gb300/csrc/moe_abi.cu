@@ -268,7 +268,7 @@ int moe_forward(moe_dims d, const void* x, const void* W1, const void* W3, const
   if (rc) return rc;
   if ((rc = check_ws(d, ws, ws_bytes))) return rc;
   if (opts != nullptr && (opts->schedule < 0 || opts->schedule > 2 || opts->grid < 0 || opts->cta_pair < 0 ||
-                          opts->cta_pair > 2 || opts->combine < 0 || opts->combine > 1))
+                          opts->cta_pair > 2 || opts->combine < 0 || opts->combine > 1 || opts->debug_drop_task < 0))
     return MOE_ERR_ARG;
   if (d.T == 0) return MOE_OK;
   if ((rc = check_plan(plan))) return rc;
@@ -300,6 +300,7 @@ int moe_forward(moe_dims d, const void* x, const void* W1, const void* W3, const
     int32_t* cursor = reinterpret_cast<int32_t*>(sched);
     int32_t* cnt_gather = reinterpret_cast<int32_t*>(sched + 64);
     int32_t* cnt_g1 = cnt_gather + L.cap;
+    g.drop_task = (opts != nullptr && opts->debug_drop_task > 0) ? opts->debug_drop_task : 0;
     e = use_pair(opts, kFwd1) ? launch_fused_forward_pair(g, x, plan->row_src, cursor, cnt_gather, cnt_g1, s, hook)
                               : launch_fused_forward(g, x, plan->row_src, cursor, cnt_gather, cnt_g1, s, hook);
     if (e != cudaSuccess) return MOE_ERR_LAUNCH;
@@ -332,7 +333,7 @@ int moe_backward(moe_dims d, const void* dout, const void* W1, const void* W3, c
   if (rc) return rc;
   if ((rc = check_ws(d, ws, ws_bytes))) return rc;
   if (opts != nullptr && (opts->schedule < 0 || opts->schedule > 2 || opts->grid < 0 || opts->cta_pair < 0 ||
-                          opts->cta_pair > 2 || opts->combine < 0 || opts->combine > 1))
+                          opts->cta_pair > 2 || opts->combine < 0 || opts->combine > 1 || opts->debug_drop_task < 0))
     return MOE_ERR_ARG;
   if ((rc = check_ptrs({dW1, dW3, dW2}))) return rc;
   if (router != nullptr) {
