@@ -43,6 +43,11 @@ BWD_KERNELS = ["combine_bwd", "gemm_dgrad2_swiglu_bwd", "gemm_dgrad1", "unpermut
 BWD_KERNELS_FUSED = ["combine_bwd", "fused_backward", "unpermute"]
 BWD_KERNELS_ROUTER = ["router_transpose", "combine_bwd", "gemm_dgrad2_swiglu_bwd", "gemm_dgrad1", "gemm_router_wgrad",
                       "router_reduce", "unpermute", "gemm_wgrad13", "gemm_wgrad2"]
+# The non-bitwise weight-gradient variant (--wgrad-subbatches 2): each weight
+# gradient GEMM runs once per token sub-batch, the second adding onto the first.
+NB_TAIL = ["subbatch_rows", "gemm_wgrad13_sb0", "gemm_wgrad2_sb0", "gemm_wgrad13_sb1", "gemm_wgrad2_sb1"]
+BWD_KERNELS_NB = BWD_KERNELS[:4] + NB_TAIL
+BWD_KERNELS_ROUTER_NB = BWD_KERNELS_ROUTER[:7] + NB_TAIL
 N_PLAN_KERNELS = 3
 
 
@@ -76,6 +81,14 @@ def work_per_kernel(T, H, F, E, k):
     b["router_transpose"] = 4 * H * E
     b["gemm_router_wgrad"] = 2 * T * H + 2 * T * E + 4 * sp * H * E
     b["router_reduce"] = 4 * sp * H * E + 4 * H * E
+    # NB sub-batch passes: sub-batch 0 writes dW, sub-batch 1 reads it back and adds.
+    R0 = k * ((T + 1) // 2)
+    R1 = R - R0
+    b["subbatch_rows"] = 12 * E
+    b["gemm_wgrad13_sb0"] = 2 * R0 * H + 4 * R0 * F + 8 * E * H * F
+    b["gemm_wgrad2_sb0"] = 2 * R0 * F + 2 * R0 * H + 4 * E * H * F
+    b["gemm_wgrad13_sb1"] = 2 * R1 * H + 4 * R1 * F + 16 * E * H * F
+    b["gemm_wgrad2_sb1"] = 2 * R1 * F + 2 * R1 * H + 8 * E * H * F
     f = {
         "gemm_router_fwd": 2 * T * H * E,
         "gemm_router_wgrad": 2 * T * H * E,
@@ -88,6 +101,10 @@ def work_per_kernel(T, H, F, E, k):
         "gemm_dgrad1": 4 * R * H * F,
         "gemm_wgrad13": 4 * R * H * F,
         "gemm_wgrad2": 2 * R * H * F,
+        "gemm_wgrad13_sb0": 4 * R0 * H * F,
+        "gemm_wgrad2_sb0": 2 * R0 * H * F,
+        "gemm_wgrad13_sb1": 4 * R1 * H * F,
+        "gemm_wgrad2_sb1": 2 * R1 * H * F,
     }
     return f, b
 
@@ -338,14 +355,19 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     fwd_names = (FWD_KERNELS_FUSED if args.schedule in (1, 2)
                  else FWD_KERNELS_COMBINE_FUSED if args.combine == 1 else FWD_KERNELS)
-    bwd_names = BWD_KERNELS_FUSED if args.schedule == 2 else BWD_KERNELS
+    nb_variant = args.wgrad_subbatches == 2
+    if nb_variant and args.schedule == 2:
+        raise SystemExit("--wgrad-subbatches 2 runs with schedules 0 and 1")
+    bwd_names = BWD_KERNELS_FUSED if args.schedule == 2 else BWD_KERNELS_NB if nb_variant else BWD_KERNELS
     if args.router:
         if args.schedule == 2:
             raise SystemExit("--router is measured with schedules 0 and 1")
-        bwd_names = BWD_KERNELS_ROUTER
+        bwd_names = BWD_KERNELS_ROUTER_NB if nb_variant else BWD_KERNELS_ROUTER
     nf, nb = len(fwd_names), len(bwd_names)
     router_arg = (inp["x"], inp["Wr"]) if args.router else None
-    base_opts = layer.opts(schedule=args.schedule, cta_pair=args.cta_pair, combine=args.combine)
+    opt_kw = dict(schedule=args.schedule, cta_pair=args.cta_pair, combine=args.combine,
+                  wgrad_subbatches=args.wgrad_subbatches)
+    base_opts = layer.opts(**opt_kw)
 
     def step(opts_f=None, opts_b=None, ev_plan=None, opts_r=None):
         opts_f = opts_f if opts_f is not None else base_opts
@@ -389,17 +411,17 @@ def run_ours(args):
     opts_f = []
     keep = []
     for e in evs_f:
-        o = layer.opts(events=e, schedule=args.schedule, cta_pair=args.cta_pair, combine=args.combine)
+        o = layer.opts(events=e, **opt_kw)
         keep.append(layer._ev_keep)
         opts_f.append(o)
     opts_b = []
     for e in evs_b:
-        o = layer.opts(events=e, schedule=args.schedule, cta_pair=args.cta_pair, combine=args.combine)
+        o = layer.opts(events=e, **opt_kw)
         keep.append(layer._ev_keep)
         opts_b.append(o)
     opts_r = []
     for e in evs_r:
-        o = layer.opts(events=e, schedule=args.schedule, cta_pair=args.cta_pair, combine=args.combine)
+        o = layer.opts(events=e, **opt_kw)
         keep.append(layer._ev_keep)
         opts_r.append(o)
 
@@ -527,6 +549,8 @@ def run_ours(args):
                        router="on the path: logits = x Wr on the GPU, gradient through the gating (dlogits, dWr, "
                               "dx share)" if args.router else "off (logits given; the pages time the layer "
                                                                "excluding gating)",
+                       weight_gradients="non-bitwise: two token sub-batches, the second added onto the first"
+                       if args.wgrad_subbatches == 2 else "bitwise-reproducible: one reduction chain per tile",
                        maxvio=round(maxvio, 4)),
         "roofline": roof,
         "e2e": {"value": round(world * T * args.steps / (e2e_ms * 1e-3), 1), "unit": UNIT,
@@ -580,6 +604,9 @@ def main():
                          "dgrad2), 1 one CTA per tile, 2 two-CTA pair tiles")
     ap.add_argument("--combine", type=int, default=0, choices=[0, 1],
                     help="schedule 0: 0 a separate gated-combine kernel, 1 the combine in GEMM2's epilogue")
+    ap.add_argument("--wgrad-subbatches", type=int, default=0, choices=[0, 2],
+                    help="0: bitwise-reproducible weight gradients (one reduction chain); 2: the non-bitwise "
+                         "variant (two token sub-batches, the second added onto the first)")
     ap.add_argument("--router", action="store_true",
                     help="put the router on the timed path: logits = x Wr on the GPU and its backward")
     ap.add_argument("--profile", action="store_true",

@@ -117,8 +117,9 @@ typedef struct {
   int32_t schedule; /* 0 (default): one persistent launch per phase in both passes (gather,
                        GEMM1, GEMM2; the backward's four GEMMs), the fastest measured on GB300.
                        1: the forward's gather, GEMM1 and GEMM2 run as one persistent kernel with
-                       a task cursor and per-tile readiness counters (single-CTA tiles).
-                       2: as 1, and the backward's four GEMMs also run as one persistent kernel.
+                       a task cursor and per-tile readiness counters (tile shape per cta_pair).
+                       2: as 1, and the backward's four GEMMs also run as one persistent kernel
+                       (single-CTA tiles).
                        All three give the same bits. */
   void **events;    /* optional: 2*n_events cudaEvent_t recorded around each kernel of the call */
   int32_t n_events; /* capacity of events/2; kernels beyond it are not timed */
@@ -128,7 +129,8 @@ typedef struct {
                        its 128 rows of A and half of B);
                        0 (default): 2 for every GEMM but the dgrad GEMM with the SwiGLU backward
                        epilogue, which measured faster with 1.  Both shapes give the same bits.
-                       The fused persistent kernels of schedules 1 and 2 use single-CTA tiles. */
+                       The fused forward (schedules 1, 2) takes pair tiles unless cta_pair = 1;
+                       the fused backward (schedule 2) always uses single-CTA tiles. */
   int32_t combine;  /* schedule 0 only.  0 (default): a separate gated-combine kernel.
                        1: the combine runs in GEMM2's epilogue (per-token arrival counters; the
                        warp that completes a token's k rows sums them, in slot order).  Same
@@ -139,6 +141,16 @@ typedef struct {
                        number debug_drop_task - 1, so the GEMM tile that needs those rows waits
                        out its bound (2 s), the kernel records MOE_ERR_TIMEOUT in the status word
                        and returns; the outputs are then undefined.  0 (default): off. */
+  int32_t wgrad_subbatches; /* reduction order of the weight gradients ([UniEP] section 6,
+                       Performance Cost of Bitwise Reproducibility).  0 or 1 (default): one
+                       accumulation chain over each expert's rows in ascending row order, the
+                       bitwise-reproducible (BW) variant.  2: the non-bitwise (NB) variant: the
+                       tokens form two sub-batches, [0, ceil(T/2)) and the rest; each weight
+                       gradient is the sum of the two sub-batches' own reductions, the second
+                       added onto the first by a float32 reduction in the L2 (dW = fl32(dW_0 +
+                       dW_1); such reductions may flush subnormal values to zero).  NB results are
+                       reproducible from run to run but differ in the last bits from BW; every
+                       other output is identical.  Not with schedule 2 (MOE_ERR_ARG). */
 } moe_opts;
 
 /* ---- sizes ------------------------------------------------------------------ */
@@ -249,7 +261,8 @@ MOE_API int32_t moe_version(void);
 MOE_API uint64_t moe_launch_count(void);
 /* Name of the i-th kernel a call launches (call: 0 plan, 1 forward, 2 backward, 3 forward with
  * schedule 1 or 2, 4 backward with schedule = 2, 5 backward with the router (schedule 0 or 1),
- * 6 moe_router_forward, 7 forward with schedule 0 and combine = 1 (combine in GEMM2's epilogue)); NULL past the end. */
+ * 6 moe_router_forward, 7 forward with schedule 0 and combine = 1 (combine in GEMM2's epilogue),
+ * 8 backward with wgrad_subbatches = 2, 9 the same with the router); NULL past the end. */
 MOE_API const char *moe_kernel_name(int32_t call, int32_t i);
 
 #ifdef __cplusplus

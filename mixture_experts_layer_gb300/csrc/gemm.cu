@@ -98,8 +98,26 @@ struct GemmParams {
   const __nv_bfloat16* aux;
   float* f0;
   float* f1;
+  // Weight gradients reduced as two token sub-batches: 0 one chain over all of
+  // an expert's rows; 1 the first sb_rows[e] rows (stored); 2 the rest, added
+  // onto the stored values.
+  int sb;
+  const int32_t* sb_rows;
   WsHeader* ws;
 };
+
+// Restricts a weight-gradient tile's K range (the expert's rows) to one token
+// sub-batch.  Rows of an expert are in token order, so sub-batch 0 is a prefix.
+__device__ __forceinline__ void subbatch_range(const GemmParams& p, int e, int& row0, int& nrows) {
+  if (p.sb == 0) return;
+  const int m = __ldg(p.sb_rows + e);
+  if (p.sb == 1) {
+    nrows = m;
+  } else {
+    row0 += m;
+    nrows -= m;
+  }
+}
 
 struct Tile {
   int e;      // expert
@@ -187,6 +205,7 @@ __device__ __forceinline__ Tile decode(const GemmParams& p, int tile) {
     t.m0 = (rem - nt * MT) * BM;
     t.row0 = __ldg(p.offsets + t.e);
     t.nrows = __ldg(p.counts + t.e);
+    subbatch_range(p, t.e, t.row0, t.nrows);
     t.kblocks = (t.nrows + BK - 1) / BK;
     t.mt = -1;
   } else {
@@ -295,6 +314,8 @@ __device__ __forceinline__ void store_zero_f32(float* dst) {
 struct OutStager {
   uint8_t* buf;  // one 4 KB box, 1024-byte aligned
   // dst points at the block's first element; ld is the row stride in floats.
+  // ACC: add the values already stored there (the second sub-batch's partial).
+  template <bool ACC = false>
   __device__ __forceinline__ void put(float* dst, size_t ld, const uint32_t (&r)[32], int lane) {
     const uint32_t base = smem_u32(buf);
     const uint32_t row = base + lane * 128;
@@ -311,7 +332,12 @@ struct OutStager {
                    : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
                    : "r"(base + rr * 128 + ((j ^ (rr & 7)) << 4)));
       float* q = dst + static_cast<size_t>(rr) * ld + 4 * j;
-      asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(q), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+      if (ACC)  // the L2 adds (one add per element onto the stored value: no ordering question)
+        asm volatile("red.global.add.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(q), "f"(__uint_as_float(a)),
+                     "f"(__uint_as_float(b)), "f"(__uint_as_float(c)), "f"(__uint_as_float(d))
+                     : "memory");
+      else
+        asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(q), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
     }
     __syncwarp();
   }
@@ -504,7 +530,10 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, const Maps& m, con
         const bool more = c + 32 < c_hi;
         uint32_t b[32];
         if (more) tc_ld_32x32b_x32(tbase + c + 32, b);  // next chunk in flight during this chunk's stores
-        st.put(obase + t.n0 + c, ld, a, lane);
+        if (p.sb == 2)
+          st.put<true>(obase + t.n0 + c, ld, a, lane);
+        else
+          st.put(obase + t.n0 + c, ld, a, lane);
         if (more) {
           tc_wait_ld();
 #pragma unroll
@@ -762,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
       const Tile t = decode<MODE>(p, tile);
       if (t.kblocks == 0) {
-        if (TR::wgrad) {
+        if (TR::wgrad && p.sb != 2) {  // an empty second sub-batch leaves the first one's values
           const int NCall = (MODE == kWgrad13) ? 128 : t.nw;
           const int c_lo = half * (NCall / 2), c_hi = c_lo + NCall / 2;
           float* d0 = (MODE == kWgrad13) ? p.f0 + (static_cast<size_t>(t.e) * p.H + t.m0 + row) * p.F + t.n0
@@ -867,6 +896,7 @@ __device__ __forceinline__ Tile pair_decode(const GemmParams& p, const ExpertTab
     t.m0 = mp * 256 + 128 * static_cast<int>(rank);
     t.row0 = __ldg(p.offsets + t.e);  // weight gradients: no staged tables (their shared memory holds store boxes)
     t.nrows = __ldg(p.counts + t.e);
+    subbatch_range(p, t.e, t.row0, t.nrows);
     t.kblocks = (t.nrows + BK - 1) / BK;
     t.mt = -1;
   } else {
@@ -1125,7 +1155,7 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
       const Tile t = pair_decode<MODE>(p, xt, tile, rank);
       const bool mine = TR::wgrad ? (t.m0 < mext) : (t.nrows > 0);
       if (t.kblocks == 0) {
-        if (TR::wgrad && mine) {
+        if (TR::wgrad && mine && p.sb != 2) {  // an empty second sub-batch leaves the first one's values
           const int NCall = (MODE == kWgrad13) ? 128 : t.nw;
           const int c_lo = half * (NCall / 2), c_hi = c_lo + NCall / 2;
           float* d0 = (MODE == kWgrad13) ? p.f0 + (static_cast<size_t>(t.e) * p.H + t.m0 + row) * p.F + t.n0
@@ -2458,6 +2488,10 @@ cudaError_t launch_gemm(GemmMode mode, const GemmLaunch& L, cudaStream_t s, Laun
   p.T = L.T;
   p.splits = L.splits;
   p.ks = L.ks;
+  if (mode == kWgrad13 || mode == kWgrad2) {
+    p.sb = L.sb;
+    p.sb_rows = L.sb_rows;
+  }
   if (mode != kFwd2) p.cmb = CombineParams{};
   if (!ok) return cudaErrorInvalidValue;
   if (L.pair && mode != kRfwd && mode != kRwgrad) return launch_gemm_pair(mode, L, m, p, s, hook);

@@ -97,6 +97,9 @@ cudaError_t launch_combine_bwd(const RowsLaunch& p, const void* dout, const void
 cudaError_t launch_unpermute(const RowsLaunch& p, const void* dXp, void* dx, cudaStream_t s, LaunchHook& hook);
 // WrT = Wr^T (bf16 [H,E] -> [E,H])
 cudaError_t launch_transpose_wr(const void* Wr, void* WrT, int H, int E, cudaStream_t s, LaunchHook& hook);
+// sb_rows[e] = rows of expert e whose token is below t_split (a prefix of its segment)
+cudaError_t launch_subbatch_rows(const int32_t* offsets, const int32_t* counts, const int32_t* row_src, int E,
+                                 int t_split, int32_t* sb_rows, cudaStream_t s, LaunchHook& hook);
 // out[i] = sum_s part[s][i] over `splits` partial buffers of n floats (n % 4 == 0)
 cudaError_t launch_reduce_splits(const float* part, float* out, size_t n, int splits, int grid, cudaStream_t s,
                                  LaunchHook& hook);
@@ -158,6 +161,8 @@ struct GemmLaunch {
   int splits, ks;      // token splits of kRwgrad and tokens per split (a multiple of 64)
   CombineLaunch cmb;   // kFwd2
   int drop_task;       // fused forward: failure injection (task + 1 whose gather signal is withheld; 0 none)
+  int sb;                  // weight gradients: 0 one chain; 1 / 2 token sub-batch 0 (stored) / 1 (added)
+  const int32_t* sb_rows;  // [E] rows of each expert that belong to token sub-batch 0
   WsHeader* ws;
 };
 cudaError_t launch_gemm(GemmMode mode, const GemmLaunch& p, cudaStream_t s, LaunchHook& hook);

@@ -60,6 +60,7 @@ struct WsLayout {
   size_t cap;  // capacity of the 128-row tile table
   size_t wrT, dl_slot, dl_bf16, dwr_part;  // router backward
   size_t cmb_cnt, cmb_bytes;               // arrivals of the combine fused into GEMM2
+  size_t sb_rows;                          // [E] rows of each expert in token sub-batch 0
   int splits, ks;                          // token splits of the dWr GEMM and tokens per split
 };
 
@@ -105,6 +106,8 @@ WsLayout ws_layout(const moe_dims& d) {
   L.cmb_cnt = off;
   L.cmb_bytes = static_cast<size_t>(d.T) * ((d.H + 255) / 256) * 2 * 4;
   off = align256(off + L.cmb_bytes);
+  L.sb_rows = off;
+  off = align256(off + static_cast<size_t>(d.E) * 4);
   L.total = off;
   return L;
 }
@@ -170,6 +173,15 @@ const char* const kBwdKernelsRouter[] = {"router_transpose", "combine_bwd", "gem
                                          "gemm_router_wgrad", "router_reduce", "unpermute", "gemm_wgrad13",
                                          "gemm_wgrad2", nullptr};
 const char* const kRouterFwdKernels[] = {"gemm_router_fwd", nullptr};
+const char* const kBwdKernelsNB[] = {"combine_bwd",      "gemm_dgrad2_swiglu_bwd", "gemm_dgrad1",
+                                     "unpermute",        "subbatch_rows",          "gemm_wgrad13_sb0",
+                                     "gemm_wgrad2_sb0",  "gemm_wgrad13_sb1",       "gemm_wgrad2_sb1",
+                                     nullptr};
+const char* const kBwdKernelsRouterNB[] = {"router_transpose", "combine_bwd",      "gemm_dgrad2_swiglu_bwd",
+                                           "gemm_dgrad1",      "gemm_router_wgrad", "router_reduce",
+                                           "unpermute",        "subbatch_rows",    "gemm_wgrad13_sb0",
+                                           "gemm_wgrad2_sb0",  "gemm_wgrad13_sb1", "gemm_wgrad2_sb1",
+                                           nullptr};
 
 GemmLaunch gemm_common(const moe_dims& d, const moe_plan_t* plan, WsHeader* ws, int grid) {
   GemmLaunch g{};
@@ -333,7 +345,9 @@ int moe_backward(moe_dims d, const void* dout, const void* W1, const void* W3, c
   if (rc) return rc;
   if ((rc = check_ws(d, ws, ws_bytes))) return rc;
   if (opts != nullptr && (opts->schedule < 0 || opts->schedule > 2 || opts->grid < 0 || opts->cta_pair < 0 ||
-                          opts->cta_pair > 2 || opts->combine < 0 || opts->combine > 1 || opts->debug_drop_task < 0))
+                          opts->cta_pair > 2 || opts->combine < 0 || opts->combine > 1 || opts->debug_drop_task < 0 ||
+                          opts->wgrad_subbatches < 0 || opts->wgrad_subbatches > 2 ||
+                          (opts->wgrad_subbatches == 2 && opts->schedule == 2)))
     return MOE_ERR_ARG;
   if ((rc = check_ptrs({dW1, dW3, dW2}))) return rc;
   if (router != nullptr) {
@@ -413,12 +427,24 @@ int moe_backward(moe_dims d, const void* dout, const void* W1, const void* W3, c
     // The dispatch backward right after dgrad1, while dXp is still in L2; the
     // weight gradients, which read Xp / h / dY / dGU, follow.
     if ((rc = router_wgrad_and_unpermute(d, plan, wsh, grid, WL, wsb, router, r, grads->dXp, dx, s, hook))) return rc;
-    g.bn = 256;
-    g.pair = use_pair(opts, kWgrad13);
-    if ((e = launch_gemm(kWgrad13, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
-    g.bn = (d.H % 256 == 0) ? 256 : 128;
-    g.pair = use_pair(opts, kWgrad2);
-    if ((e = launch_gemm(kWgrad2, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
+    const bool nb = opts != nullptr && opts->wgrad_subbatches == 2;
+    if (nb) {
+      int32_t* sb_rows = reinterpret_cast<int32_t*>(wsb + WL.sb_rows);
+      if (launch_subbatch_rows(plan->offsets, plan->counts, plan->row_src, d.E, (d.T + 1) / 2, sb_rows, s, hook) !=
+          cudaSuccess)
+        return MOE_ERR_LAUNCH;
+      g.sb_rows = sb_rows;
+    }
+    // BW: one pass (sb 0).  NB: sub-batch 0 stored (sb 1), then sub-batch 1 added (sb 2).
+    for (int sb = nb ? 1 : 0; sb <= (nb ? 2 : 0); ++sb) {
+      g.sb = sb;
+      g.bn = 256;
+      g.pair = use_pair(opts, kWgrad13);
+      if ((e = launch_gemm(kWgrad13, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
+      g.bn = (d.H % 256 == 0) ? 256 : 128;
+      g.pair = use_pair(opts, kWgrad2);
+      if ((e = launch_gemm(kWgrad2, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
+    }
     return MOE_OK;
   }
   return router_wgrad_and_unpermute(d, plan, wsh, grid, WL, wsb, router, r, grads->dXp, dx, s, hook);
@@ -505,6 +531,8 @@ const char* moe_kernel_name(int32_t call, int32_t i) {
                          : call == 5 ? kBwdKernelsRouter
                          : call == 6 ? kRouterFwdKernels
                          : call == 7 ? kFwdKernelsCombineFused
+                         : call == 8 ? kBwdKernelsNB
+                         : call == 9 ? kBwdKernelsRouterNB
                                      : nullptr;
   if (t == nullptr || i < 0) return nullptr;
   for (int j = 0; j <= i; ++j)

@@ -357,7 +357,47 @@ __global__ void __launch_bounds__(256) reduce_splits_kernel(const float4* __rest
   }
 }
 
+// Rows of each expert that belong to token sub-batch 0 (tokens below t_split):
+// an expert's rows are in token order, so this is the length of the prefix of
+// its segment with row_src < t_split.  One warp per expert, 32-way search: the
+// lanes probe 32 evenly spaced rows of the remaining interval [lo, hi] and the
+// ballot narrows it to one gap between probes.
+__global__ void __launch_bounds__(256) subbatch_rows_kernel(const int32_t* __restrict__ offsets,
+                                                              const int32_t* __restrict__ counts,
+                                                              const int32_t* __restrict__ row_src, int E, int t_split,
+                                                              int32_t* __restrict__ sb_rows) {
+  const int lane = threadIdx.x & 31;
+  const int e = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (e >= E) return;
+  const int32_t* seg = row_src + offsets[e];
+  int lo = 0, hi = counts[e];  // the answer m lies in [lo, hi]: rows below m are in sub-batch 0
+  while (lo < hi) {
+    const long long span = hi - lo;
+    const int i = lo + static_cast<int>(((lane + 1) * span - 1) / 32);  // in [lo, hi - 1], ascending in lane
+    const unsigned below = __ballot_sync(0xffffffffu, seg[i] < t_split);
+    const int c = __popc(below);  // probes 0 .. c-1 are in sub-batch 0
+    const int i0 = __shfl_sync(0xffffffffu, i, 0);
+    const int ilast = __shfl_sync(0xffffffffu, i, c > 0 ? c - 1 : 0);
+    const int inext = __shfl_sync(0xffffffffu, i, c < 32 ? c : 31);
+    if (c == 0) {
+      hi = i0;
+    } else {
+      lo = ilast + 1;
+      if (c < 32) hi = inext;
+    }
+  }
+  if (lane == 0) sb_rows[e] = lo;
+}
+
 }  // namespace
+
+cudaError_t launch_subbatch_rows(const int32_t* offsets, const int32_t* counts, const int32_t* row_src, int E,
+                                 int t_split, int32_t* sb_rows, cudaStream_t s, LaunchHook& hook) {
+  hook.before(s);
+  subbatch_rows_kernel<<<(E + 7) / 8, 256, 0, s>>>(offsets, counts, row_src, E, t_split, sb_rows);
+  hook.after(s);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gather(const RowsLaunch& p, const void* x, void* Xp, cudaStream_t s, LaunchHook& hook) {
   hook.before(s);

@@ -37,6 +37,9 @@ What it computes (sources are named by page title and section):
   The router is outside the timed layer (UniEP, section 6, Figure 4 "excluding
   gating"), so routing is held fixed and the gate weights w are an input whose
   gradient dgate is returned.
+* Non-bitwise variant (``layer_step_subbatches``) -- UniEP, section 6,
+  Performance Cost of Bitwise Reproducibility: two token sub-batches, weight
+  gradients summed over them.
 * Router (optional, ``router_logits`` / ``router_grads`` / ``layer_step_router``):
   logits = x Wr and the gradient through the renormalised top-k softmax with
   routing held fixed: dlogits, dWr = x^T dlogits and the router's share of dx.
@@ -312,6 +315,25 @@ def layer_step(x, logits, dout, W, k: int, E: int, mirror=True) -> dict:
     fwd = forward(x, W, ids, w, perm, mirror)
     bwd = backward(dout, W, fwd, w, perm, mirror)
     return {"ids": ids, "w": w, "perm": perm, **fwd, **bwd}
+
+
+def layer_step_subbatches(x, logits, dout, W, k: int, E: int, mirror=True) -> dict:
+    """The non-bitwise (NB) variant of one step: the tokens form two sub-batches,
+    [0, ceil(T/2)) and [ceil(T/2), T), each runs the whole step on its own, and
+    the weight gradients are the sum of the two sub-batches' gradients, the
+    second added onto the first in float32 (UniEP, section 6, Performance Cost of
+    Bitwise Reproducibility: splitting the tokens into two sub-batches changes
+    the accumulation order of the weight-gradient reduction).  Every other output
+    is per token, so it is the two sub-batches' rows in token order."""
+    x = np.asarray(x)
+    T = x.shape[0]
+    t0 = (T + 1) // 2
+    parts = [layer_step(x[a:b], logits[a:b], dout[a:b], W, k, E, mirror) for a, b in ((0, t0), (t0, T)) if b > a]
+    res = {n: np.concatenate([q[n] for q in parts]) for n in ("ids", "w", "out", "dx", "dgate")}
+    for n in ("dW1", "dW3", "dW2"):
+        res[n] = _store_f32(sum(q[n] for q in parts), mirror)  # one sub-batch (T = 1): its own gradient
+    res["parts"] = parts
+    return res
 
 
 # --------------------------------------------------------------------------

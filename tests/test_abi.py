@@ -31,6 +31,10 @@ def test_every_declared_symbol_is_exported():
     assert M.moe_kernel_name(2, 5) == "gemm_wgrad2"
     assert M.moe_kernel_name(2, 6) is None
     assert M.moe_kernel_name(4, 1) == "fused_backward"
+    assert M.moe_kernel_name(8, 4) == "subbatch_rows"
+    assert M.moe_kernel_name(8, 8) == "gemm_wgrad2_sb1"
+    assert M.moe_kernel_name(8, 9) is None
+    assert M.moe_kernel_name(9, 11) == "gemm_wgrad2_sb1"
 
 
 def test_workspace_sizes():
@@ -59,3 +63,10 @@ def test_host_side_rejections():
     assert M.moe_plan(bad, aligned, plan, aligned, n) == M.MOE_ERR_ARG
     assert M.moe_plan(M.moe_dims(16, 96, 128, 4, 2), aligned, plan, aligned, n) == M.MOE_ERR_SHAPE
     assert "aligned" in M.moe_strerror(M.MOE_ERR_ALIGN)
+    # option checks of moe_backward come before any device work
+    args = (d, aligned, aligned, aligned, aligned, M.moe_plan_t(), M.moe_saved_t(), M.moe_grads_t(), aligned, aligned,
+            aligned, aligned, aligned, aligned, n)
+    for sched, sb in ((2, 2), (0, 3), (0, -1)):
+        o = M.moe_opts()
+        o.schedule, o.wgrad_subbatches = sched, sb
+        assert M.moe_backward(*args, opts=o) == M.MOE_ERR_ARG, (sched, sb)
