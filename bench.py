@@ -339,7 +339,7 @@ def run_ours(args):
     if args.profile and args.part == "plan":
         # Routing only: the logits and the plan's tables are all that is allocated.
         lg = S.layer_inputs(shape, seed, device=dev, with_weights=False)["logits"]
-        layer = MoELayer(T, H, F, E, k, device=dev, plan_only=True)
+        layer = MoELayer(T, H, F, E, k, device=dev, plan_only=True, pad=args.pad)
         for _ in range(args.warmup + 1):
             layer.plan(lg)
         torch.cuda.synchronize()
@@ -351,7 +351,7 @@ def run_ours(args):
                               "kernels_per_step": N_PLAN_KERNELS}), flush=True)
         return
     inp = S.layer_inputs(shape, seed, device=dev)
-    layer = MoELayer(T, H, F, E, k, device=dev, with_router=args.router)
+    layer = MoELayer(T, H, F, E, k, device=dev, with_router=args.router, pad=args.pad)
     stream = torch.cuda.current_stream(dev)
     fwd_names = (FWD_KERNELS_FUSED if args.schedule in (1, 2)
                  else FWD_KERNELS_COMBINE_FUSED if args.combine == 1 else FWD_KERNELS)
@@ -549,6 +549,10 @@ def run_ours(args):
                        router="on the path: logits = x Wr on the GPU, gradient through the gating (dlogits, dWr, "
                               "dx share)" if args.router else "off (logits given; the pages time the layer "
                                                                "excluding gating)",
+                       rows=("padding-free GroupGEMM (R = T*k rows)" if args.pad <= 1 else
+                             f"static-shape: each expert's rows padded to a multiple of {args.pad} "
+                             f"({int(layer.offsets[-1].item())} rows in use of {layer.R}; the algorithmic "
+                             "work counts the T*k routed rows)"),
                        weight_gradients="non-bitwise: two token sub-batches, the second added onto the first"
                        if args.wgrad_subbatches == 2 else "bitwise-reproducible: one reduction chain per tile",
                        maxvio=round(maxvio, 4)),
@@ -607,6 +611,9 @@ def main():
     ap.add_argument("--wgrad-subbatches", type=int, default=0, choices=[0, 2],
                     help="0: bitwise-reproducible weight gradients (one reduction chain); 2: the non-bitwise "
                          "variant (two token sub-batches, the second added onto the first)")
+    ap.add_argument("--pad", type=int, default=0,
+                    help="token padding granule: 0 padding-free (default); P >= 2 pads every expert's rows to a "
+                         "multiple of P (static-shape variant)")
     ap.add_argument("--router", action="store_true",
                     help="put the router on the timed path: logits = x Wr on the GPU and its backward")
     ap.add_argument("--profile", action="store_true",

@@ -16,7 +16,7 @@
  *
  * Conventions for every entry point
  *   - Dimensions: T tokens, H hidden, F per-expert FFN width, E experts, k
- *     experts per token, R = T*k grouped rows.
+ *     experts per token, R = moe_rows(d) grouped rows (T*k without padding).
  *   - Every pointer argument is a DEVICE pointer owned by the caller, except
  *     the structs passed by address (host memory) and the host outputs of
  *     moe_get_status.  The library never allocates or frees memory and never
@@ -49,7 +49,7 @@ extern "C" {
 
 /* ---- error codes ---------------------------------------------------------- */
 #define MOE_OK 0
-#define MOE_ERR_ARG (-1)     /* null pointer, non-positive dimension, k > E, k > 32, R >= 2^31 */
+#define MOE_ERR_ARG (-1)     /* null pointer, non-positive dimension, k > E, k > 32, pad outside [0, 4096], R >= 2^31 */
 #define MOE_ERR_ALIGN (-2)   /* a pointer is not 16-byte aligned */
 #define MOE_ERR_WS (-3)      /* workspace smaller than moe_workspace_bytes() */
 #define MOE_ERR_LAUNCH (-4)  /* a CUDA launch or API call failed */
@@ -63,6 +63,14 @@ extern "C" {
 /* ---- shapes and tables ------------------------------------------------------ */
 typedef struct {
   int32_t T, H, F, E, k;
+  int32_t pad; /* token padding granule P.  0 or 1 (default): padding-free, the grouped
+                  buffers hold exactly R = T*k rows ([UniEP] section 3, padding-free
+                  GroupGEMM).  P >= 2: static-shape variant ([MoonEP] "The Buffer API",
+                  token_padding): every expert's rows are rounded up to a multiple of P with
+                  padding rows (row_src = -1, row_slot = 255, zero in Xp, GU, h, Y, dY, dGU,
+                  dXp), and the buffers hold R = T*k + min(E, T*k)*(P-1) rows, a bound that
+                  does not depend on the routing.  Results are the same bits as without
+                  padding.  Pass the same dims to every call of a step. */
 } moe_dims;
 
 /* Routing state of one step.  Filled by moe_plan, read unchanged by
@@ -72,11 +80,12 @@ typedef struct {
 typedef struct {
   int32_t *topk_ids; /* [T,k]  expert of slot j of token t; descending logit, ties to the lower id */
   float *topk_w;     /* [T,k]  renormalised gate weight of that slot (fp32) */
-  int32_t *counts;   /* [E]    rows per expert n_e */
-  int32_t *offsets;  /* [E+1]  exclusive prefix of counts; offsets[E] = R */
+  int32_t *counts;   /* [E]    rows per expert n_e (tokens routed to e; padding not counted) */
+  int32_t *offsets;  /* [E+1]  first row of each expert's segment: exclusive prefix of the counts
+                                (of the counts rounded up to P with padding); offsets[E] = rows in use */
   int32_t *dest;     /* [T,k]  grouped row of slot (t,j): offsets[e] + #{t' < t routed to e} */
-  int32_t *row_src;  /* [R]    token of each grouped row (inverse of dest) */
-  uint8_t *row_slot; /* [R]    slot j of each grouped row */
+  int32_t *row_src;  /* [R]    token of each grouped row (inverse of dest); -1 on padding rows */
+  uint8_t *row_slot; /* [R]    slot j of each grouped row; 255 on padding rows */
   int32_t *tiles;    /* [moe_plan_tiles_elems(d)]  128-row GEMM tiles of the grouped buffer (internal) */
 } moe_plan_t;
 
@@ -165,6 +174,11 @@ MOE_API size_t moe_workspace_bytes(moe_dims d);
 
 /* int32 elements of moe_plan_t.tiles.  Returns 0 for invalid dims. */
 MOE_API size_t moe_plan_tiles_elems(moe_dims d);
+
+/* R: rows of every grouped buffer (row_src, row_slot, Xp, GU, h, Y, dY, dGU, dXp):
+ * T*k, or T*k + min(E, T*k)*(P-1) with a padding granule P = d.pad >= 2.
+ * Returns 0 for invalid dims. */
+MOE_API size_t moe_rows(moe_dims d);
 
 /* ---- the layer -------------------------------------------------------------- */
 

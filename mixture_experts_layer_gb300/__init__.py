@@ -15,7 +15,7 @@ from ctypes import POINTER, Structure, byref, c_char_p, c_int, c_int32, c_size_t
 
 __all__ = [
     "moe_dims", "moe_plan_t", "moe_saved_t", "moe_grads_t", "moe_opts", "MoeError",
-    "moe_workspace_bytes", "moe_plan_tiles_elems", "moe_plan", "moe_forward", "moe_backward",
+    "moe_workspace_bytes", "moe_plan_tiles_elems", "moe_rows", "moe_plan", "moe_forward", "moe_backward",
     "moe_get_status", "moe_clear_status", "moe_strerror", "moe_version", "moe_launch_count",
     "moe_kernel_name", "moe_plan_noalloc", "moe_router_t", "moe_router_forward", "check", "lib", "lib_path",
 ]
@@ -35,7 +35,7 @@ MOE_ERR_BOUNDS = 3
 
 
 class moe_dims(Structure):
-    _fields_ = [("T", c_int32), ("H", c_int32), ("F", c_int32), ("E", c_int32), ("k", c_int32)]
+    _fields_ = [("T", c_int32), ("H", c_int32), ("F", c_int32), ("E", c_int32), ("k", c_int32), ("pad", c_int32)]
 
 
 class moe_plan_t(Structure):
@@ -90,6 +90,7 @@ def lib() -> ctypes.CDLL:
             sig = {
                 "moe_workspace_bytes": (c_size_t, [moe_dims]),
                 "moe_plan_tiles_elems": (c_size_t, [moe_dims]),
+                "moe_rows": (c_size_t, [moe_dims]),
                 "moe_plan": (c_int, [moe_dims, vp, POINTER(moe_plan_t), vp, c_size_t, vp]),
                 "moe_forward": (c_int, [moe_dims, vp, vp, vp, vp, POINTER(moe_plan_t), POINTER(moe_saved_t), vp, vp,
                                         c_size_t, POINTER(moe_opts), vp]),
@@ -128,6 +129,10 @@ def moe_workspace_bytes(d: moe_dims) -> int:
 
 def moe_plan_tiles_elems(d: moe_dims) -> int:
     return lib().moe_plan_tiles_elems(d)
+
+
+def moe_rows(d: moe_dims) -> int:
+    return lib().moe_rows(d)
 
 
 def moe_plan(d, logits, plan, ws, ws_bytes, stream=0) -> int:

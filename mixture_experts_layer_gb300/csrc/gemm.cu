@@ -380,7 +380,9 @@ __device__ __forceinline__ void combine_in_epilogue(const GemmParams& p, const T
   int tok = -1, done = 0;
   if (valid) {
     tok = __ldg(c.row_src + grow);
-    if (tok < 0 || tok >= p.T) {
+    if (tok == -1) {
+      // a padding row: no token to combine
+    } else if (tok < 0 || tok >= p.T) {
       report(p.ws, MOE_ERR_BOUNDS, 30, static_cast<int>(grow));
     } else {
       const int old = atomicAdd(c.cnt + (static_cast<size_t>(tok) * nn + t.n0 / BN) * 2 + half, 1);
@@ -1270,12 +1272,18 @@ __device__ __forceinline__ uint4 ld_nc_v4(const uint4* p) {
 }
 
 // Dispatch of one 128-row tile by one epilogue warp (rows ew, ew+8, ...):
-// Xp[r] = x[row_src[r]] ("MoonEP": zero-copy dispatch into the expert-grouped layout).
+// Xp[r] = x[row_src[r]] ("MoonEP": zero-copy dispatch into the expert-grouped
+// layout); a padding row (row_src = -1) is written as zeros.
 __device__ __forceinline__ void gather_rows_task(const FusedFwdParams& f, const Tile& t, int ew, int lane) {
   const int hv = f.p1.H / 8;
   for (int i = ew; i < t.nrows; i += kEpiWarps) {
     const int r = t.row0 + i;
     const int tok = __ldg(f.row_src + r);
+    if (tok == -1) {
+      uint4* dst = f.Xp + static_cast<size_t>(r) * hv;
+      for (int v = lane; v < hv; v += 32) dst[v] = make_uint4(0u, 0u, 0u, 0u);
+      continue;
+    }
     if (tok < 0 || tok >= f.T) {
       if (lane == 0) report(f.p1.ws, MOE_ERR_BOUNDS, 20, r);
       continue;

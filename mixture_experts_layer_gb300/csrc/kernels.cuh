@@ -10,11 +10,23 @@ namespace moe {
 constexpr int kChunk = 256;               // tokens per routing chunk (one "source" of the mapping)
 constexpr int kChunkWords = kChunk / 32;  // bitmap words per expert and chunk
 constexpr int kTileRows = 128;            // rows of a GEMM tile (the tcgen05 M)
+constexpr int kMaxPad = 4096;             // largest padding granule of an expert's rows
+
+// Grouped rows the [R, ...] buffers hold.  Padding-free (pad 0 or 1): T*k.
+// With a padding granule pad >= 2 every expert's rows are rounded up to a
+// multiple of pad, which adds at most pad - 1 rows to each non-empty expert: a
+// bound that does not depend on the routing (static shapes).
+__host__ __device__ inline long long grouped_rows(long long T, int k, int E, int pad) {
+  const long long R = T * k;
+  return pad > 1 ? R + (R < E ? R : static_cast<long long>(E)) * (pad - 1) : R;
+}
 
 // Layout of moe_plan_t.tiles (int32): [0] number of 128-row tiles; [1 + e]
 // first tile of expert e (E + 1 entries); then, from tiles_entry_base(E),
 // one int4 {expert, first row, rows, 0} per tile in expert order; then, from
-// tiles_pair_base(R, E), the first 256-row pair of each expert (E + 1 entries).
+// tiles_pair_base(R, E), the first 256-row pair of each expert (E + 1 entries);
+// then, from tiles_gcount_base(R, E), the rows the GEMMs run for each expert
+// (E entries: n_e rounded up to the padding granule).  R = grouped_rows.
 __host__ __device__ inline int tiles_entry_base(int E) { return ((E + 2) + 3) & ~3; }
 
 __host__ __device__ inline long long tiles_capacity(long long R, int E) { return R / kTileRows + E + 1; }
@@ -24,6 +36,8 @@ __host__ __device__ inline long long tiles_capacity(long long R, int E) { return
 __host__ __device__ inline long long tiles_pair_base(long long R, int E) {
   return tiles_entry_base(E) + 4 * tiles_capacity(R, E);
 }
+__host__ __device__ inline long long tiles_gcount_base(long long R, int E) { return tiles_pair_base(R, E) + E + 1; }
+__host__ __device__ inline long long tiles_elems(long long R, int E) { return tiles_gcount_base(R, E) + E; }
 
 extern std::atomic<unsigned long long> g_launches;
 
@@ -50,6 +64,8 @@ struct LaunchHook {
 struct PlanLaunch {
   const float* logits;
   int T, E, k;
+  int pad;          // padding granule of each expert's rows (0 or 1: none)
+  int R;            // grouped_rows(T, k, E, pad)
   int32_t* ids;
   float* w;
   uint32_t* gbm;
@@ -60,6 +76,7 @@ struct PlanLaunch {
   int32_t* offsets;
   int32_t* tiles;
   int32_t* pairs;  // tiles + tiles_pair_base(R, E)
+  int32_t* gcounts;  // tiles + tiles_gcount_base(R, E)
   int32_t* dest;
   int32_t* row_src;
   uint8_t* row_slot;
@@ -85,6 +102,8 @@ struct RowsLaunch {
   const float* w;
   WsHeader* ws;
   RouterRows rt;
+  const int32_t* rows_used;  // device count of the grouped rows in use (the plan's offsets[E])
+  int pad;                   // padding granule (>= 2: the padding rows of Xp and dY are written as zeros)
 };
 // Xp[r] = x[row_src[r]]
 cudaError_t launch_gather(const RowsLaunch& p, const void* x, void* Xp, cudaStream_t s, LaunchHook& hook);

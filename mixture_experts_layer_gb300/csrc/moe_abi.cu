@@ -45,10 +45,14 @@ int device_info(int* sms) {
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
+// Grouped rows of the [R, ...] buffers (padding rows included).
+long long rows_of(const moe_dims& d) { return grouped_rows(d.T, d.k, d.E, d.pad); }
+
 int check_dims(const moe_dims& d) {
   if (d.T < 0 || d.H <= 0 || d.F <= 0 || d.E <= 0 || d.k <= 0) return MOE_ERR_ARG;
   if (d.k > d.E || d.k > 32) return MOE_ERR_ARG;
-  if (static_cast<long long>(d.T) * d.k >= (1ll << 31)) return MOE_ERR_ARG;
+  if (d.pad < 0 || d.pad > kMaxPad) return MOE_ERR_ARG;
+  if (rows_of(d) >= (1ll << 31)) return MOE_ERR_ARG;
   if (d.H % 128 != 0 || d.F % 128 != 0 || d.E > 1024) return MOE_ERR_SHAPE;
   if (static_cast<long long>(d.E) * d.H >= (1ll << 31) || static_cast<long long>(d.E) * d.F >= (1ll << 31))
     return MOE_ERR_SHAPE;
@@ -90,7 +94,7 @@ WsLayout ws_layout(const moe_dims& d) {
   off = align256(off + nchunks * d.E * kChunkWords * 4);
   // Scheduling words of the persistent kernels: a task cursor (padded to 64 B)
   // and two counters per 128-row tile.
-  L.cap = static_cast<size_t>(tiles_capacity(static_cast<long long>(d.T) * d.k, d.E));
+  L.cap = static_cast<size_t>(tiles_capacity(rows_of(d), d.E));
   L.sched = off;
   L.sched_bytes = 64 + 2 * L.cap * 4;
   off = align256(off + L.sched_bytes);
@@ -190,12 +194,12 @@ GemmLaunch gemm_common(const moe_dims& d, const moe_plan_t* plan, WsHeader* ws, 
   g.F = d.F;
   g.E = d.E;
   g.k = d.k;
-  g.R = d.T * d.k;
+  g.R = static_cast<int>(rows_of(d));
   g.grid = grid;
   g.tiles = plan->tiles;
-  g.pairs = plan->tiles + tiles_pair_base(static_cast<long long>(d.T) * d.k, d.E);
+  g.pairs = plan->tiles + tiles_pair_base(rows_of(d), d.E);
   g.offsets = plan->offsets;
-  g.counts = plan->counts;
+  g.counts = plan->tiles + tiles_gcount_base(rows_of(d), d.E);  // rows the GEMMs run (padded counts)
   g.ws = ws;
   return g;
 }
@@ -236,7 +240,12 @@ size_t moe_workspace_bytes(moe_dims d) {
 
 size_t moe_plan_tiles_elems(moe_dims d) {
   if (check_dims(d) != MOE_OK) return 0;
-  return static_cast<size_t>(tiles_pair_base(static_cast<long long>(d.T) * d.k, d.E)) + d.E + 1;
+  return static_cast<size_t>(tiles_elems(rows_of(d), d.E));
+}
+
+size_t moe_rows(moe_dims d) {
+  if (check_dims(d) != MOE_OK) return 0;
+  return static_cast<size_t>(rows_of(d));
 }
 
 int moe_plan(moe_dims d, const float* logits, const moe_plan_t* plan, void* ws, size_t ws_bytes, void* stream) {
@@ -255,6 +264,8 @@ int moe_plan(moe_dims d, const float* logits, const moe_plan_t* plan, void* ws, 
   p.T = d.T;
   p.E = d.E;
   p.k = d.k;
+  p.pad = d.pad;
+  p.R = static_cast<int>(rows_of(d));
   p.ids = plan->topk_ids;
   p.w = plan->topk_w;
   p.gbm = reinterpret_cast<uint32_t*>(w + L.gbm);
@@ -264,7 +275,8 @@ int moe_plan(moe_dims d, const float* logits, const moe_plan_t* plan, void* ws, 
   p.counts = plan->counts;
   p.offsets = plan->offsets;
   p.tiles = plan->tiles;
-  p.pairs = plan->tiles + tiles_pair_base(static_cast<long long>(d.T) * d.k, d.E);
+  p.pairs = plan->tiles + tiles_pair_base(rows_of(d), d.E);
+  p.gcounts = plan->tiles + tiles_gcount_base(rows_of(d), d.E);
   p.dest = plan->dest;
   p.row_src = plan->row_src;
   p.row_slot = plan->row_slot;
@@ -294,7 +306,9 @@ int moe_forward(moe_dims d, const void* x, const void* W1, const void* W3, const
   const int grid = grid_for(opts, sms);
   LaunchHook hook = make_hook(opts);
 
-  RowsLaunch r{d.T, d.H, d.k, d.T * d.k, grid * 8, plan->dest, plan->row_src, plan->topk_w, wsh};
+  RowsLaunch r{d.T, d.H, d.k, static_cast<int>(rows_of(d)), grid * 8, plan->dest, plan->row_src, plan->topk_w, wsh};
+  r.rows_used = plan->offsets + d.E;
+  r.pad = d.pad;
   GemmLaunch g = gemm_common(d, plan, wsh, grid);
   g.Xp = saved->Xp;
   g.W1 = W1;
@@ -380,7 +394,10 @@ int moe_backward(moe_dims d, const void* dout, const void* W1, const void* W3, c
   const int grid = grid_for(opts, sms);
   LaunchHook hook = make_hook(opts);
 
-  RowsLaunch r{d.T, d.H, d.k, d.T * d.k, grid * 8, plan->dest, plan->row_src, plan->topk_w, wsh, RouterRows{}};
+  RowsLaunch r{d.T, d.H, d.k, static_cast<int>(rows_of(d)), grid * 8, plan->dest, plan->row_src, plan->topk_w, wsh,
+               RouterRows{}};
+  r.rows_used = plan->offsets + d.E;
+  r.pad = d.pad;
   const WsLayout WL = ws_layout(d);
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   cudaError_t e;
@@ -468,7 +485,7 @@ int moe_router_forward(moe_dims d, const void* x, const void* Wr, float* logits,
   g.F = d.F;
   g.E = d.E;
   g.k = d.k;
-  g.R = d.T * d.k;
+  g.R = static_cast<int>(rows_of(d));
   g.grid = grid_for(opts, sms);
   g.ws = static_cast<WsHeader*>(ws);
   g.x = x;

@@ -397,13 +397,19 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk4_kernel(const float* 
 // chunks -- the O_all of Algorithm 1 -- and the expert's row count.  The last
 // CTA to finish (ticket) then takes the prefix over experts of the row counts
 // (offsets) and of the 128-row tile counts (first tile of each expert); the
-// tile entries themselves are written by route_rank.
+// tile entries themselves are written by route_rank.  With a padding granule
+// (pad >= 2) each expert's segment is its count rounded up to a multiple of
+// pad: offsets, tiles and pairs count the padded rows, gcounts holds them, and
+// the padding rows get row_src = -1, row_slot = 255.
 __global__ void __launch_bounds__(32 * kScanWarps) route_scan_kernel(const int32_t* __restrict__ ccount,
                                                                      int nchunks, int E, int32_t* __restrict__ cbase,
                                                                      int32_t* __restrict__ counts,
                                                                      int32_t* __restrict__ offsets,
                                                                      int32_t* __restrict__ tiles,
-                                                                     int32_t* __restrict__ pairs, int32_t* ticket) {
+                                                                     int32_t* __restrict__ pairs, int32_t* ticket,
+                                                                     int pad, int R, int32_t* __restrict__ gcounts,
+                                                                     int32_t* __restrict__ row_src,
+                                                                     uint8_t* __restrict__ row_slot, WsHeader* ws) {
   __shared__ int s_last;
   __shared__ int s_wsum_n[32], s_wsum_m[32], s_wsum_p[32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -443,11 +449,12 @@ __global__ void __launch_bounds__(32 * kScanWarps) route_scan_kernel(const int32
   // 128-row tile counts.  Thread i takes experts [i * per, (i + 1) * per).
   const int per = (E + blockDim.x - 1) / blockDim.x;
   const int e0 = threadIdx.x * per;
+  auto padded = [pad](int n) { return pad > 1 ? (n + pad - 1) / pad * pad : n; };
   int my_n = 0, my_m = 0, my_p = 0;
   for (int i = 0; i < per; ++i) {
     const int ee = e0 + i;
     if (ee < E) {
-      const int n = __ldcg(counts + ee);
+      const int n = padded(__ldcg(counts + ee));
       my_n += n;
       my_m += (n + kTileRows - 1) / kTileRows;
       my_p += (n + 2 * kTileRows - 1) / (2 * kTileRows);
@@ -480,7 +487,17 @@ __global__ void __launch_bounds__(32 * kScanWarps) route_scan_kernel(const int32
   for (int i = 0; i < per; ++i) {
     const int ee = e0 + i;
     if (ee >= E) break;
-    const int n = __ldcg(counts + ee);
+    const int real = __ldcg(counts + ee);
+    const int n = padded(real);
+    gcounts[ee] = n;
+    for (int r = run_n + real; r < run_n + n; ++r) {  // the padding rows of expert ee
+      if (r < 0 || r >= R) {
+        report(ws, MOE_ERR_BOUNDS, 1, r);
+        break;
+      }
+      row_src[r] = -1;
+      row_slot[r] = 255;
+    }
     offsets[ee] = run_n;
     tiles[1 + ee] = run_m;
     pairs[ee] = run_p;
@@ -508,7 +525,7 @@ __global__ void __launch_bounds__(256) route_rank_kernel(const int32_t* __restri
                                                          const uint32_t* __restrict__ gbm,
                                                          const int32_t* __restrict__ cbase,
                                                          const int32_t* __restrict__ offsets,
-                                                         const int32_t* __restrict__ counts,
+                                                         const int32_t* __restrict__ gcounts,
                                                          int32_t* __restrict__ tiles, int T, int E, int k, int R,
                                                          int32_t* __restrict__ dest, int32_t* __restrict__ row_src,
                                                          uint8_t* __restrict__ row_slot, WsHeader* ws) {
@@ -635,7 +652,7 @@ __global__ void __launch_bounds__(256) route_rank_kernel(const int32_t* __restri
         hi = mid;
     }
     const int j = m - tstart[lo];
-    const int n = __ldg(counts + lo);
+    const int n = __ldg(gcounts + lo);  // rows the GEMMs run: n_e, padded
     ent[m] = make_int4(lo, __ldg(offsets + lo) + kTileRows * j, min(kTileRows, n - kTileRows * j), 0);
   }
 }
@@ -693,7 +710,8 @@ cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t s, LaunchHook& hook) {
   if (err != cudaSuccess) return err;
   hook.before(s);
   route_scan_kernel<<<(p.E + kScanWarps - 1) / kScanWarps, 32 * kScanWarps, 0, s>>>(
-      p.ccount, nchunks, p.E, p.cbase, p.counts, p.offsets, p.tiles, p.pairs, p.ticket);
+      p.ccount, nchunks, p.E, p.cbase, p.counts, p.offsets, p.tiles, p.pairs, p.ticket, p.pad, p.R, p.gcounts,
+      p.row_src, p.row_slot, p.ws);
   hook.after(s);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
@@ -705,8 +723,8 @@ cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t s, LaunchHook& hook) {
                                static_cast<int>(rank_smem));
     if (err != cudaSuccess) return err;
   }
-  route_rank_kernel<<<nchunks, 256, rank_smem, s>>>(p.ids, p.gbm, p.cbase, p.offsets, p.counts, p.tiles, p.T, p.E,
-                                                    p.k, p.T * p.k, p.dest, p.row_src, p.row_slot, p.ws);
+  route_rank_kernel<<<nchunks, 256, rank_smem, s>>>(p.ids, p.gbm, p.cbase, p.offsets, p.gcounts, p.tiles, p.T,
+                                                    p.E, p.k, p.R, p.dest, p.row_src, p.row_slot, p.ws);
   hook.after(s);
   return cudaGetLastError();
 }
@@ -765,8 +783,8 @@ bool na_ok_ptr(const void* p) { return p != nullptr && (reinterpret_cast<uintptr
 extern "C" int moe_plan_noalloc(moe_dims d, const float* logits, const moe_plan_t* plan, int32_t* status,
                                 void* stream) {
   using namespace moe;
-  if (d.T < 0 || d.H <= 0 || d.F <= 0 || d.E <= 0 || d.k <= 0 || d.k > d.E || d.k > 32 ||
-      static_cast<long long>(d.T) * d.k >= (1ll << 31))
+  if (d.T < 0 || d.H <= 0 || d.F <= 0 || d.E <= 0 || d.k <= 0 || d.k > d.E || d.k > 32 || d.pad < 0 ||
+      d.pad > kMaxPad || grouped_rows(d.T, d.k, d.E, d.pad) >= (1ll << 31))
     return MOE_ERR_ARG;
   if (d.H % 128 != 0 || d.F % 128 != 0 || d.E > 1024) return MOE_ERR_SHAPE;
   const size_t nchunks = (static_cast<size_t>(d.T) + kChunk - 1) / kChunk;
@@ -792,6 +810,9 @@ extern "C" int moe_plan_noalloc(moe_dims d, const float* logits, const moe_plan_
   p.T = d.T;
   p.E = d.E;
   p.k = d.k;
+  p.pad = d.pad;
+  const long long R = grouped_rows(d.T, d.k, d.E, d.pad);
+  p.R = static_cast<int>(R);
   p.ids = plan->topk_ids;
   p.w = plan->topk_w;
   p.ticket = reinterpret_cast<int32_t*>(w + ccount);
@@ -801,7 +822,8 @@ extern "C" int moe_plan_noalloc(moe_dims d, const float* logits, const moe_plan_
   p.counts = plan->counts;
   p.offsets = plan->offsets;
   p.tiles = plan->tiles;
-  p.pairs = plan->tiles + tiles_pair_base(static_cast<long long>(d.T) * d.k, d.E);
+  p.pairs = plan->tiles + tiles_pair_base(R, d.E);
+  p.gcounts = plan->tiles + tiles_gcount_base(R, d.E);
   p.dest = plan->dest;
   p.row_src = plan->row_src;
   p.row_slot = plan->row_slot;

@@ -44,17 +44,50 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
   return v;
 }
 
-// Dispatch as a gather, one warp per grouped row: Xp[r] = x[row_src[r]].
-// Used while x fits comfortably in L2 (its re-reads are L2 hits), where the
-// R rows give more parallelism than the T tokens.
+// Grouped rows in use: the plan's offsets[E] (R itself without padding).
+__device__ __forceinline__ int rows_in_use(const int32_t* rows_used, int R, WsHeader* ws, int where) {
+  const int n = __ldg(rows_used);
+  if (n < 0 || n > R) {
+    if ((threadIdx.x & 31) == 0) report(ws, MOE_ERR_BOUNDS, where, n);
+    return 0;
+  }
+  return n;
+}
+
+// The padding rows (row_src = -1) of a grouped buffer are written as zeros.  A
+// warp tests 32 rows at a time and clears the padding rows among them.
+__device__ __forceinline__ void zero_padding_rows(const int32_t* __restrict__ row_src, int n, uint4* __restrict__ buf,
+                                                  int hv, int gwarp, int nwarps, int lane) {
+  for (int r0 = gwarp * 32; r0 < n; r0 += nwarps * 32) {
+    const int r = r0 + lane;
+    unsigned m = __ballot_sync(0xffffffffu, r < n && row_src[r] == -1);
+    while (m != 0u) {
+      const int b = __ffs(m) - 1;
+      m &= m - 1u;
+      uint4* dst = buf + static_cast<size_t>(r0 + b) * hv;
+      for (int v = lane; v < hv; v += 32) dst[v] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+}
+
+// Dispatch as a gather, one warp per grouped row: Xp[r] = x[row_src[r]], zeros
+// for a padding row.  Used while x fits comfortably in L2 (its re-reads are L2
+// hits), where the R rows give more parallelism than the T tokens.
 __global__ void __launch_bounds__(kThreads) gather_rows_kernel(const uint4* __restrict__ x,
                                                                  const int32_t* __restrict__ row_src,
+                                                                 const int32_t* __restrict__ rows_used,
                                                                  uint4* __restrict__ Xp, int R, int T, int hv,
                                                                  WsHeader* ws) {
   const int lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * (kThreads / 32);
-  for (int r = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); r < R; r += nwarps) {
+  const int n = rows_in_use(rows_used, R, ws, 10);
+  for (int r = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); r < n; r += nwarps) {
     const int t = row_src[r];
+    if (t == -1) {
+      uint4* dst = Xp + static_cast<size_t>(r) * hv;
+      for (int v = lane; v < hv; v += 32) dst[v] = make_uint4(0u, 0u, 0u, 0u);
+      continue;
+    }
     if (t < 0 || t >= T) {
       if (lane == 0) report(ws, MOE_ERR_BOUNDS, 10, r);
       continue;
@@ -84,7 +117,8 @@ template <int K>
 __global__ void __launch_bounds__(kThreads) scatter_rows_kernel(const uint4* __restrict__ x,
                                                                   const int32_t* __restrict__ dest,
                                                                   uint4* __restrict__ Xp, int T, int k, int R,
-                                                                  int hv, WsHeader* ws);
+                                                                  int hv, WsHeader* ws, const int32_t* row_src,
+                                                                  const int32_t* rows_used);
 
 // The k (row, weight) pairs of token t, held in registers by every lane
 // (K = compile-time bound on k).  Returns false (and reports) if a row index is
@@ -111,11 +145,13 @@ __device__ __forceinline__ bool token_rows(const int32_t* dest, const float* w, 
   return true;
 }
 
+// With padding (rows_used != nullptr) the padding rows are cleared after the tokens.
 template <int K>
 __global__ void __launch_bounds__(kThreads) scatter_rows_kernel(const uint4* __restrict__ x,
                                                                   const int32_t* __restrict__ dest,
                                                                   uint4* __restrict__ Xp, int T, int k, int R,
-                                                                  int hv, WsHeader* ws) {
+                                                                  int hv, WsHeader* ws, const int32_t* row_src,
+                                                                  const int32_t* rows_used) {
   const int lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * (kThreads / 32);
   for (int t = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); t < T; t += nwarps) {
@@ -145,6 +181,9 @@ __global__ void __launch_bounds__(kThreads) scatter_rows_kernel(const uint4* __r
         if (j < k) Xp[static_cast<size_t>(rows[j]) * hv + v] = a;
     }
   }
+  if (rows_used != nullptr)
+    zero_padding_rows(row_src, rows_in_use(rows_used, R, ws, 10), Xp, hv,
+                      blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5), nwarps, lane);
 }
 
 // out[t] = bf16(sum_j w[t,j] Y[dest[t,j]]), slots in ascending order.
@@ -189,7 +228,8 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(const uint4* __re
                                                                  const float* __restrict__ w,
                                                                  uint4* __restrict__ dY, float* __restrict__ dgate,
                                                                  int T, int k, int R, int hv, WsHeader* ws,
-                                                                 RouterRows rt) {
+                                                                 RouterRows rt, const int32_t* row_src,
+                                                                 const int32_t* rows_used) {
   const int lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * (kThreads / 32);
   for (int t = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); t < T; t += nwarps) {
@@ -258,6 +298,9 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(const uint4* __re
       }
     }
   }
+  if (rows_used != nullptr)  // padding rows of dY: zero, so the GEMMs that read them add nothing
+    zero_padding_rows(row_src, rows_in_use(rows_used, R, ws, 12), dY, hv,
+                      blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5), nwarps, lane);
 }
 
 // dx[t] = bf16(sum_j dXp[dest[t,j]]), slots in ascending order.
@@ -403,14 +446,16 @@ cudaError_t launch_gather(const RowsLaunch& p, const void* x, void* Xp, cudaStre
   hook.before(s);
   // x up to 32 MB: gather by grouped row (re-reads hit L2); larger: scatter by token.
   if (static_cast<size_t>(p.T) * p.H * 2 <= (size_t(32) << 20))
-    gather_rows_kernel<<<p.grid, kThreads, 0, s>>>(static_cast<const uint4*>(x), p.row_src,
+    gather_rows_kernel<<<p.grid, kThreads, 0, s>>>(static_cast<const uint4*>(x), p.row_src, p.rows_used,
                                                     static_cast<uint4*>(Xp), p.R, p.T, p.H / 8, p.ws);
   else if (p.k <= 8)
     scatter_rows_kernel<8><<<p.grid, kThreads, 0, s>>>(static_cast<const uint4*>(x), p.dest,
-                                                        static_cast<uint4*>(Xp), p.T, p.k, p.R, p.H / 8, p.ws);
+                                                        static_cast<uint4*>(Xp), p.T, p.k, p.R, p.H / 8, p.ws,
+                                                        p.row_src, p.pad > 1 ? p.rows_used : nullptr);
   else
     scatter_rows_kernel<kMaxK><<<p.grid, kThreads, 0, s>>>(static_cast<const uint4*>(x), p.dest,
-                                                            static_cast<uint4*>(Xp), p.T, p.k, p.R, p.H / 8, p.ws);
+                                                            static_cast<uint4*>(Xp), p.T, p.k, p.R, p.H / 8, p.ws,
+                                                            p.row_src, p.pad > 1 ? p.rows_used : nullptr);
   hook.after(s);
   return cudaGetLastError();
 }
@@ -433,12 +478,12 @@ cudaError_t launch_combine_bwd(const RowsLaunch& p, const void* dout, const void
   if (p.k <= 8)
     combine_bwd_kernel<8><<<p.grid, kThreads, 0, s>>>(static_cast<const uint4*>(dout), static_cast<const uint4*>(Y),
                                                        p.dest, p.w, static_cast<uint4*>(dY), dgate, p.T, p.k, p.R,
-                                                       p.H / 8, p.ws, p.rt);
+                                                       p.H / 8, p.ws, p.rt, p.row_src, p.pad > 1 ? p.rows_used : nullptr);
   else
     combine_bwd_kernel<kMaxK><<<p.grid, kThreads, 0, s>>>(static_cast<const uint4*>(dout),
                                                            static_cast<const uint4*>(Y), p.dest, p.w,
                                                            static_cast<uint4*>(dY), dgate, p.T, p.k, p.R, p.H / 8,
-                                                           p.ws, p.rt);
+                                                           p.ws, p.rt, p.row_src, p.pad > 1 ? p.rows_used : nullptr);
   hook.after(s);
   return cudaGetLastError();
 }

@@ -8,7 +8,8 @@ from __future__ import annotations
 import torch
 
 from . import (check, moe_backward, moe_dims, moe_forward, moe_get_status, moe_grads_t, moe_opts, moe_plan,
-               moe_plan_t, moe_plan_tiles_elems, moe_router_forward, moe_router_t, moe_saved_t, moe_workspace_bytes)
+               moe_plan_t, moe_plan_tiles_elems, moe_router_forward, moe_router_t, moe_rows, moe_saved_t,
+               moe_workspace_bytes)
 
 
 def _empty(shape, dtype, device):
@@ -20,12 +21,17 @@ def _empty(shape, dtype, device):
 
 
 class MoELayer:
-    """Buffers of plan, forward and backward for fixed (T, H, F, E, k)."""
+    """Buffers of plan, forward and backward for fixed (T, H, F, E, k).
 
-    def __init__(self, T, H, F, E, k, device="cuda", with_backward=True, plan_only=False, with_router=False):
-        self.dims = moe_dims(T, H, F, E, k)
-        self.T, self.H, self.F, self.E, self.k = T, H, F, E, k
-        R = T * k
+    pad >= 2 selects the static-shape variant: every expert's rows are padded to
+    a multiple of pad, and the grouped buffers hold moe_rows(dims) rows."""
+
+    def __init__(self, T, H, F, E, k, device="cuda", with_backward=True, plan_only=False, with_router=False, pad=0):
+        self.dims = moe_dims(T, H, F, E, k, pad)
+        self.T, self.H, self.F, self.E, self.k, self.pad = T, H, F, E, k, pad
+        R = moe_rows(self.dims)
+        if R == 0 and T * k > 0:
+            raise ValueError("invalid layer dimensions")
         self.R = R
         dev = torch.device(device)
         self.device = dev

@@ -137,24 +137,31 @@ class Permutation:
     row_slot: np.ndarray  # int64 [R]    slot j of each grouped row
 
 
-def permutation(ids, E: int) -> Permutation:
+def permutation(ids, E: int, pad: int = 0) -> Permutation:
     """Stable counting sort of the (token, slot) pairs by expert.
 
     Histogram, exclusive scan, then one pass over tokens in order (slots in
     order) handing out consecutive rows of each expert's segment.
+
+    pad >= 2 is the static-shape layout ("MoonEP: Balanced Expert Parallelism
+    for MoE Training via Dynamic Redundant Experts", The Buffer API, the
+    token_padding parameter): each expert's segment is its count rounded up to
+    a multiple of pad; the rows past the count are padding rows, marked with
+    row_src = -1 and row_slot = 255.  counts stay the routed rows.
     """
     ids = np.asarray(ids)
     T, k = ids.shape
     counts = np.zeros(E, dtype=np.int64)
     for e in ids.reshape(-1).tolist():
         counts[e] += 1
+    seg = -(-counts // pad) * pad if pad > 1 else counts
     offsets = np.zeros(E + 1, dtype=np.int64)
-    offsets[1:] = np.cumsum(counts)
+    offsets[1:] = np.cumsum(seg)
     cursor = offsets[:-1].copy()
-    R = T * k
+    R = int(offsets[E])
     dest = np.empty((T, k), dtype=np.int64)
-    row_src = np.empty(R, dtype=np.int64)
-    row_slot = np.empty(R, dtype=np.int64)
+    row_src = np.full(R, -1, dtype=np.int64)
+    row_slot = np.full(R, 255, dtype=np.int64)
     idl = ids.tolist()
     for t in range(T):
         for j in range(k):
@@ -168,8 +175,12 @@ def permutation(ids, E: int) -> Permutation:
 
 
 def gather(x, row_src) -> np.ndarray:
-    """Dispatch: Xp[r] = x[row_src[r]] (a copy; exact)."""
-    return np.asarray(x, dtype=np.float64)[np.asarray(row_src)]
+    """Dispatch: Xp[r] = x[row_src[r]] (a copy; exact); padding rows (row_src = -1) are zero."""
+    row_src = np.asarray(row_src)
+    real = row_src >= 0
+    Xp = np.zeros((row_src.shape[0], np.asarray(x).shape[1]), dtype=np.float64)
+    Xp[real] = np.asarray(x, dtype=np.float64)[row_src[real]]
+    return Xp
 
 
 def combine(Y, w, dest, mirror=True) -> np.ndarray:
@@ -237,10 +248,14 @@ def expert_wgrad(X, h, dY, dG, dU, mirror=True):
 
 
 def dispatch_grad(dout, w, row_src, row_slot, mirror=True):
-    """dY[r] = w[t,j] * dout[t] for the grouped row r of slot (t, j)."""
+    """dY[r] = w[t,j] * dout[t] for the grouped row r of slot (t, j); zero on padding rows."""
     dout = np.asarray(dout, dtype=np.float64)
     w = np.asarray(w, dtype=np.float64)
-    return _store_bf16(w[row_src, row_slot][:, None] * dout[row_src], mirror)
+    row_src, row_slot = np.asarray(row_src), np.asarray(row_slot)
+    real = row_src >= 0
+    dY = np.zeros((row_src.shape[0], dout.shape[1]), dtype=np.float64)
+    dY[real] = w[row_src[real], row_slot[real]][:, None] * dout[row_src[real]]
+    return _store_bf16(dY, mirror)
 
 
 def gate_grad(dout, Y, dest, mirror=True):
@@ -308,10 +323,11 @@ def backward(dout, W, fwd: dict, w, perm: Permutation, mirror=True) -> dict:
             "dW1": dW1, "dW3": dW3, "dW2": dW2}
 
 
-def layer_step(x, logits, dout, W, k: int, E: int, mirror=True) -> dict:
-    """Plan, forward and backward of one step (everything the layer computes)."""
+def layer_step(x, logits, dout, W, k: int, E: int, mirror=True, pad: int = 0) -> dict:
+    """Plan, forward and backward of one step (everything the layer computes);
+    pad >= 2: the static-shape layout with padded expert segments."""
     ids, w = route(logits, k)
-    perm = permutation(ids, E)
+    perm = permutation(ids, E, pad)
     fwd = forward(x, W, ids, w, perm, mirror)
     bwd = backward(dout, W, fwd, w, perm, mirror)
     return {"ids": ids, "w": w, "perm": perm, **fwd, **bwd}

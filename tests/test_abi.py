@@ -46,6 +46,16 @@ def test_workspace_sizes():
     assert M.moe_workspace_bytes(M.moe_dims(16, 100, 128, 4, 2)) == 0   # H % 128
     assert M.moe_workspace_bytes(M.moe_dims(16, 128, 128, 2048, 2)) == 0  # E too large
     assert M.moe_workspace_bytes(M.moe_dims(16, 128, 128, 64, 33)) == 0   # k > 32
+    # grouped rows: T*k, or with padding granule P, T*k + min(E, T*k) * (P - 1)
+    assert M.moe_rows(M.moe_dims(4096, 2048, 1408, 64, 6)) == 4096 * 6
+    assert M.moe_rows(M.moe_dims(4096, 2048, 1408, 64, 6, 1)) == 4096 * 6
+    assert M.moe_rows(M.moe_dims(4096, 2048, 1408, 64, 6, 128)) == 4096 * 6 + 64 * 127
+    assert M.moe_rows(M.moe_dims(1, 128, 128, 8, 2, 16)) == 2 + 2 * 15
+    assert M.moe_rows(M.moe_dims(16, 128, 128, 4, 2, -1)) == 0
+    assert M.moe_rows(M.moe_dims(16, 128, 128, 4, 2, 4097)) == 0
+    for pad in (0, 128):
+        d = M.moe_dims(4096, 2048, 1408, 64, 6, pad)
+        assert M.moe_plan_tiles_elems(d) >= M.moe_rows(d) // 128 * 4 + 2 * 64
 
 
 def test_host_side_rejections():
