@@ -39,6 +39,8 @@ UNIT = "tokens/s"
 FWD_KERNELS = ["gather_rows", "gemm_fwd1_swiglu", "gemm_fwd2", "combine"]
 FWD_KERNELS_COMBINE_FUSED = ["gather_rows", "gemm_fwd1_swiglu", "gemm_fwd2_combine"]
 FWD_KERNELS_FUSED = ["fused_forward", "combine"]
+FWD_KERNELS_GATHER = ["gemm_fwd1_gather_swiglu", "gemm_fwd2", "combine"]
+FWD_KERNELS_GATHER_COMBINE = ["gemm_fwd1_gather_swiglu", "gemm_fwd2_combine"]
 BWD_KERNELS = ["combine_bwd", "gemm_dgrad2_swiglu_bwd", "gemm_dgrad1", "unpermute", "gemm_wgrad13", "gemm_wgrad2"]
 BWD_KERNELS_FUSED = ["combine_bwd", "fused_backward", "unpermute"]
 BWD_KERNELS_ROUTER = ["router_transpose", "combine_bwd", "gemm_dgrad2_swiglu_bwd", "gemm_dgrad1", "gemm_router_wgrad",
@@ -67,6 +69,8 @@ def work_per_kernel(T, H, F, E, k):
         "gemm_wgrad2": 2 * R * F + 2 * R * H + 4 * E * H * F,
         "unpermute": 2 * R * H + 2 * T * H + 4 * R,
     }
+    # GEMM1 with the dispatch in its A-operand load: reads x (and row_src) instead of Xp, writes Xp.
+    b["gemm_fwd1_gather_swiglu"] = 2 * T * H + 4 * R + 2 * R * H + 4 * E * H * F + 6 * R * F
     # GEMM2 with the gated combine in its epilogue: also reads the k rows of Y per token and writes out.
     b["gemm_fwd2_combine"] = b["gemm_fwd2"] + b["combine"]
     # Fused forward: reads x, row_src and every weight once; writes Xp, GU, h and Y.
@@ -95,6 +99,7 @@ def work_per_kernel(T, H, F, E, k):
         "fused_forward": 6 * R * H * F,
         "fused_backward": 12 * R * H * F,
         "gemm_fwd1_swiglu": 4 * R * H * F,
+        "gemm_fwd1_gather_swiglu": 4 * R * H * F,
         "gemm_fwd2": 2 * R * H * F,
         "gemm_fwd2_combine": 2 * R * H * F,
         "gemm_dgrad2_swiglu_bwd": 2 * R * H * F,
@@ -353,8 +358,12 @@ def run_ours(args):
     inp = S.layer_inputs(shape, seed, device=dev)
     layer = MoELayer(T, H, F, E, k, device=dev, with_router=args.router, pad=args.pad)
     stream = torch.cuda.current_stream(dev)
-    fwd_names = (FWD_KERNELS_FUSED if args.schedule in (1, 2)
-                 else FWD_KERNELS_COMBINE_FUSED if args.combine == 1 else FWD_KERNELS)
+    gather_fused = args.dispatch == 2 and args.schedule == 0 and args.cta_pair != 1 and args.pad <= 1
+    if gather_fused:
+        fwd_names = FWD_KERNELS_GATHER_COMBINE if args.combine == 1 else FWD_KERNELS_GATHER
+    else:
+        fwd_names = (FWD_KERNELS_FUSED if args.schedule in (1, 2)
+                     else FWD_KERNELS_COMBINE_FUSED if args.combine == 1 else FWD_KERNELS)
     nb_variant = args.wgrad_subbatches == 2
     if nb_variant and args.schedule == 2:
         raise SystemExit("--wgrad-subbatches 2 runs with schedules 0 and 1")
@@ -366,7 +375,7 @@ def run_ours(args):
     nf, nb = len(fwd_names), len(bwd_names)
     router_arg = (inp["x"], inp["Wr"]) if args.router else None
     opt_kw = dict(schedule=args.schedule, cta_pair=args.cta_pair, combine=args.combine,
-                  wgrad_subbatches=args.wgrad_subbatches)
+                  wgrad_subbatches=args.wgrad_subbatches, dispatch=args.dispatch)
     base_opts = layer.opts(**opt_kw)
 
     def step(opts_f=None, opts_b=None, ev_plan=None, opts_r=None):
@@ -549,6 +558,9 @@ def run_ours(args):
                        router="on the path: logits = x Wr on the GPU, gradient through the gating (dlogits, dWr, "
                               "dx share)" if args.router else "off (logits given; the pages time the layer "
                                                                "excluding gating)",
+                       dispatch=("inside GEMM1's A-operand load (TMA row gathers, Xp stored from the stages)"
+                                 if gather_fused else "its own kernel" if args.schedule == 0
+                                 else "gather tasks of the fused forward"),
                        rows=("padding-free GroupGEMM (R = T*k rows)" if args.pad <= 1 else
                              f"static-shape: each expert's rows padded to a multiple of {args.pad} "
                              f"({int(layer.offsets[-1].item())} rows in use of {layer.R}; the algorithmic "
@@ -608,6 +620,9 @@ def main():
                          "dgrad2), 1 one CTA per tile, 2 two-CTA pair tiles")
     ap.add_argument("--combine", type=int, default=0, choices=[0, 1],
                     help="schedule 0: 0 a separate gated-combine kernel, 1 the combine in GEMM2's epilogue")
+    ap.add_argument("--dispatch", type=int, default=0, choices=[0, 1, 2],
+                    help="schedule 0: 0 library default, 1 a dispatch kernel, 2 the dispatch inside GEMM1's "
+                         "A-operand load (TMA row gathers)")
     ap.add_argument("--wgrad-subbatches", type=int, default=0, choices=[0, 2],
                     help="0: bitwise-reproducible weight gradients (one reduction chain); 2: the non-bitwise "
                          "variant (two token sub-batches, the second added onto the first)")

@@ -150,6 +150,14 @@ typedef struct {
                        number debug_drop_task - 1, so the GEMM tile that needs those rows waits
                        out its bound (2 s), the kernel records MOE_ERR_TIMEOUT in the status word
                        and returns; the outputs are then undefined.  0 (default): off. */
+  int32_t dispatch; /* schedule 0: where the row dispatch Xp = x[row_src] runs.  0 (default) or
+                       1: its own kernel (gather by row, or scatter by token when x is large).
+                       2: inside GEMM1's A-operand load: the producer warp gathers the tile's
+                       rows of x with TMA row gathers (four rows per instruction), and the
+                       first N tile of each row block stores the gathered rows to Xp for the
+                       backward ([UniEP] section 3: the dispatch workers write the GEMM's
+                       operand rows).  Needs pair tiles for GEMM1 and the padding-free layout;
+                       otherwise 1 is used.  Same bits. */
   int32_t wgrad_subbatches; /* reduction order of the weight gradients ([UniEP] section 6,
                        Performance Cost of Bitwise Reproducibility).  0 or 1 (default): one
                        accumulation chain over each expert's rows in ascending row order, the
@@ -276,7 +284,8 @@ MOE_API uint64_t moe_launch_count(void);
 /* Name of the i-th kernel a call launches (call: 0 plan, 1 forward, 2 backward, 3 forward with
  * schedule 1 or 2, 4 backward with schedule = 2, 5 backward with the router (schedule 0 or 1),
  * 6 moe_router_forward, 7 forward with schedule 0 and combine = 1 (combine in GEMM2's epilogue),
- * 8 backward with wgrad_subbatches = 2, 9 the same with the router); NULL past the end. */
+ * 8 backward with wgrad_subbatches = 2, 9 the same with the router, 10 forward with dispatch = 2,
+ * 11 forward with dispatch = 2 and combine = 1); NULL past the end. */
 MOE_API const char *moe_kernel_name(int32_t call, int32_t i);
 
 #ifdef __cplusplus

@@ -58,7 +58,7 @@ class moe_router_t(Structure):
 class moe_opts(Structure):
     _fields_ = [("grid", c_int32), ("schedule", c_int32), ("events", POINTER(c_void_p)), ("n_events", c_int32),
                 ("cta_pair", c_int32), ("combine", c_int32), ("debug_drop_task", c_int32),
-                ("wgrad_subbatches", c_int32)]
+                ("dispatch", c_int32), ("wgrad_subbatches", c_int32)]
 
 
 class MoeError(RuntimeError):

@@ -73,6 +73,7 @@ struct Maps {
   CUtensorMap b1;  // second B tensor (W3), full-width box
   CUtensorMap b2;  // B, 128-row box for a 128-wide tail tile (K-major B only)
   CUtensorMap b3;  // W3, 128-row box
+  CUtensorMap gx;  // x [T, H], 64 x 1 box: the rows GEMM1 gathers for its A operand
 };
 
 // The gated combine fused into GEMM2's epilogue (null cnt: not fused).
@@ -103,6 +104,10 @@ struct GemmParams {
   // onto the stored values.
   int sb;
   const int32_t* sb_rows;
+  // GEMM1 with the dispatch in its A-operand load: A rows are gathered from x by
+  // row_src (TMA gather4) and the first N tile of each row block stores them to Xp.
+  int gather;
+  const int32_t* row_src;
   WsHeader* ws;
 };
 
@@ -945,7 +950,7 @@ __device__ __forceinline__ void load_kblock_pair(const GemmParams& p, const Maps
   const int hb = t.nw / 2;  // B columns of this CTA
   const int r = static_cast<int>(rank);
   if (MODE == kFwd1) {
-    tma_load_2d(sA, &m.a, bar, k0, t.row0);
+    if (sA != nullptr) tma_load_2d(sA, &m.a, bar, k0, t.row0);  // null: A is gathered from x
     const int y = t.e * p.H + k0;
     const CUtensorMap* w = r ? &m.b1 : &m.b0;  // W1 (G columns) on CTA 0, W3 (U columns) on CTA 1
     tma_load_2d(sB, w, bar, t.n0, y);
@@ -1055,14 +1060,32 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
     bool ok = true;
     for (int tile = pid; tile < ntiles && ok; tile += npairs) {
       const Tile t = pair_decode<MODE>(p, xt, tile, rank);
+      const bool gather = (MODE == kFwd1) && p.gather;
+      int src[4] = {0, 0, 0, 0};  // gather: tokens of this lane's 4 rows (rows past R read token 0, never stored)
+      if (gather) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = t.row0 + 4 * lane + j;
+          const int tok = r < p.R ? __ldg(p.row_src + r) : 0;
+          src[j] = (tok >= 0 && tok < p.T) ? tok : 0;
+        }
+      }
       for (int kb = 0; kb < t.kblocks; ++kb) {
         if (!mbar_wait_cluster(&empty[s], ph ^ 1u, p.ws, 200 + MODE, abort_flag)) {
           ok = false;
           break;
         }
-        if (elect_one()) {
+        uint8_t* sA = smem + s * kPairStageBytes;
+        if (gather) {
+          if (elect_one()) {
+            mbar_arrive_expect_tx(&full[s], kABytes + t.nw * 64);
+            load_kblock_pair<MODE>(p, maps, t, kb, nullptr, sA + kABytes, &full[s], rank);  // B only
+          }
+          __syncwarp();
+          // A: the warp's 32 lanes gather the tile's 128 rows of x, 4 rows each.
+          tma_gather4(sA + lane * 4 * 128, &maps.gx, &full[s], kb * BK, src[0], src[1], src[2], src[3]);
+        } else if (elect_one()) {
           mbar_arrive_expect_tx(&full[s], kABytes + t.nw * 64);
-          uint8_t* sA = smem + s * kPairStageBytes;
           load_kblock_pair<MODE>(p, maps, t, kb, sA, sA + kABytes, &full[s], rank);
         }
         __syncwarp();
@@ -1105,9 +1128,19 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
           const int valid = t.nrows - kb * BK;
           if (valid < BK) nkk = clear_k_tail(sA, sB, valid, t.nw / 2, lane);
         }
+        // Gathered A rows of a row block's first N tile go out to Xp (the backward
+        // reads them); the store reads the stage before the stage is released.
+        const bool store_xp = (MODE == kFwd1) && p.gather && t.n0 == 0 && t.nrows > 0;
+        if (store_xp && lane == 0) {
+          tma_store_2d(&maps.a, sA, kb * BK, t.row0);
+          bulk_commit();
+        }
         __syncwarp();
         if (!leader) {
-          if (lane == 0) mbar_arrive_cluster(pfull_leader + s * 8);
+          if (lane == 0) {
+            if (store_xp) bulk_wait_read<0>();
+            mbar_arrive_cluster(pfull_leader + s * 8);
+          }
           __syncwarp();
         } else {
           if (!mbar_wait_cluster(&pfull[s], ph, p.ws, 240 + MODE, abort_flag)) {
@@ -1115,7 +1148,9 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
             break;
           }
           tc_fence_after();
-          if (elect_one()) {
+          // One thread (lane 0) issues the MMAs, the Xp store and the commits, so
+          // each commit tracks that thread's MMAs and the store's bulk group.
+          if (lane == 0) {
             const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
@@ -1125,6 +1160,7 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
                 tc_mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0);
               }
             }
+            if (store_xp) bulk_wait_read<0>();
             tc_commit_pair(&empty[s]);
           }
           __syncwarp();
@@ -1136,12 +1172,14 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
       }
       if (!ok) break;
       if (leader) {
-        if (elect_one()) tc_commit_pair(&tfull[acc]);
+        if (lane == 0) tc_commit_pair(&tfull[acc]);
         __syncwarp();
       }
       acc ^= 1;
       if (acc == 0) acc_ph ^= 1u;
     }
+    if ((MODE == kFwd1) && p.gather && lane == 0) bulk_wait_all();  // Xp stores complete before exit
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs, own rows)
     const int q = warp & 3;
@@ -2455,6 +2493,12 @@ cudaError_t launch_gemm(GemmMode mode, const GemmLaunch& L, cudaStream_t s, Laun
            make_map(&m.b1, L.W3, F, E * H, 64, 64);
       p.out0 = static_cast<__nv_bfloat16*>(L.out_h);
       p.out1 = static_cast<__nv_bfloat16*>(L.out_GU);
+      if (L.gather) {  // pair tiles only: the A rows come from x, one row per box
+        if (!L.pair) return cudaErrorInvalidValue;
+        ok = ok && make_map(&m.gx, L.x, H, static_cast<uint64_t>(L.T), 64, 1);
+        p.gather = 1;
+        p.row_src = L.row_src;
+      }
       break;
     case kFwd2:
       ok = make_map(&m.a, L.h, F, R, 64, BM) && make_map(&m.b0, L.W2, H, E * F, 64, 64);

@@ -180,6 +180,8 @@ struct GemmLaunch {
   int splits, ks;      // token splits of kRwgrad and tokens per split (a multiple of 64)
   CombineLaunch cmb;   // kFwd2
   int drop_task;       // fused forward: failure injection (task + 1 whose gather signal is withheld; 0 none)
+  int gather;              // kFwd1 on pair tiles: A rows gathered from x by row_src, Xp stored from the stages
+  const int32_t* row_src;  // [R] (gather)
   int sb;                  // weight gradients: 0 one chain; 1 / 2 token sub-batch 0 (stored) / 1 (added)
   const int32_t* sb_rows;  // [E] rows of each expert that belong to token sub-batch 0
   WsHeader* ws;

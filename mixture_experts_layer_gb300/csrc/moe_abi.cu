@@ -156,6 +156,14 @@ int grid_for(const moe_opts* o, int sms) {
 
 int finish(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH; }
 
+// Whether the phased forward runs the dispatch inside GEMM1's A-operand load
+// (moe_opts.dispatch = 2; pair tiles, padding-free layout) instead of as its own
+// kernel (1).  Default (0): its own kernel.
+bool dispatch_in_gemm1(const moe_dims& d, const moe_opts* o, int pair) {
+  const int mode = o != nullptr ? o->dispatch : 0;
+  return mode == 2 && pair && d.pad <= 1;
+}
+
 // CTAs of the weight-gradient GEMMs.  When the experts are short (at most 256
 // rows on average) each tile is a few k-blocks followed by 256 KB of fp32 dW
 // stores, and the kernels are bound by DRAM writes; fewer concurrent writers
@@ -185,6 +193,8 @@ const char* const kPlanKernels[] = {"route_topk", "route_scan", "route_rank", nu
 const char* const kFwdKernelsFused[] = {"fused_forward", "combine", nullptr};
 const char* const kFwdKernels[] = {"gather_rows", "gemm_fwd1_swiglu", "gemm_fwd2", "combine", nullptr};
 const char* const kFwdKernelsCombineFused[] = {"gather_rows", "gemm_fwd1_swiglu", "gemm_fwd2_combine", nullptr};
+const char* const kFwdKernelsGather[] = {"gemm_fwd1_gather_swiglu", "gemm_fwd2", "combine", nullptr};
+const char* const kFwdKernelsGatherCombine[] = {"gemm_fwd1_gather_swiglu", "gemm_fwd2_combine", nullptr};
 const char* const kBwdKernels[] = {"combine_bwd", "gemm_dgrad2_swiglu_bwd", "gemm_dgrad1", "unpermute",
                                    "gemm_wgrad13", "gemm_wgrad2", nullptr};
 const char* const kBwdKernelsFused[] = {"combine_bwd", "fused_backward", "unpermute", nullptr};
@@ -307,7 +317,8 @@ int moe_forward(moe_dims d, const void* x, const void* W1, const void* W3, const
   if (rc) return rc;
   if ((rc = check_ws(d, ws, ws_bytes))) return rc;
   if (opts != nullptr && (opts->schedule < 0 || opts->schedule > 2 || opts->grid < 0 || opts->cta_pair < 0 ||
-                          opts->cta_pair > 2 || opts->combine < 0 || opts->combine > 1 || opts->debug_drop_task < 0))
+                          opts->cta_pair > 2 || opts->combine < 0 || opts->combine > 1 || opts->debug_drop_task < 0 ||
+                          opts->dispatch < 0 || opts->dispatch > 2))
     return MOE_ERR_ARG;
   if (d.T == 0) return MOE_OK;
   if ((rc = check_plan(plan))) return rc;
@@ -346,11 +357,18 @@ int moe_forward(moe_dims d, const void* x, const void* W1, const void* W3, const
                               : launch_fused_forward(g, x, plan->row_src, cursor, cnt_gather, cnt_g1, s, hook);
     if (e != cudaSuccess) return MOE_ERR_LAUNCH;
   } else {
-    e = launch_gather(r, x, saved->Xp, s, hook);
-    if (e != cudaSuccess) return MOE_ERR_LAUNCH;
     g.bn = 256;
     g.pair = use_pair(opts, kFwd1);
+    if (dispatch_in_gemm1(d, opts, g.pair)) {  // GEMM1 gathers its A rows from x and stores Xp
+      g.gather = 1;
+      g.x = x;
+      g.row_src = plan->row_src;
+    } else {
+      e = launch_gather(r, x, saved->Xp, s, hook);
+      if (e != cudaSuccess) return MOE_ERR_LAUNCH;
+    }
     if ((e = launch_gemm(kFwd1, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
+    g.gather = 0;
     g.bn = (d.H % 256 == 0) ? 256 : 128;
     g.pair = use_pair(opts, kFwd2);
     const bool fuse = (opts != nullptr && opts->combine == 1);
@@ -566,6 +584,8 @@ const char* moe_kernel_name(int32_t call, int32_t i) {
                          : call == 7 ? kFwdKernelsCombineFused
                          : call == 8 ? kBwdKernelsNB
                          : call == 9 ? kBwdKernelsRouterNB
+                         : call == 10 ? kFwdKernelsGather
+                         : call == 11 ? kFwdKernelsGatherCombine
                                      : nullptr;
   if (t == nullptr || i < 0) return nullptr;
   for (int j = 0; j <= i; ++j)

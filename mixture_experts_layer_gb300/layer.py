@@ -82,7 +82,8 @@ class MoELayer:
             stream = torch.cuda.current_stream()
         return stream.cuda_stream
 
-    def opts(self, grid=0, events=None, schedule=0, cta_pair=0, combine=0, debug_drop_task=0, wgrad_subbatches=0):
+    def opts(self, grid=0, events=None, schedule=0, cta_pair=0, combine=0, debug_drop_task=0, wgrad_subbatches=0,
+             dispatch=0):
         o = moe_opts()
         o.grid = grid
         o.schedule = schedule
@@ -90,6 +91,7 @@ class MoELayer:
         o.combine = combine
         o.debug_drop_task = debug_drop_task
         o.wgrad_subbatches = wgrad_subbatches
+        o.dispatch = dispatch
         if events:
             arr = (ctypes_void_p_array(len(events)))(*[e.cuda_event for e in events])
             self._ev_keep = arr

@@ -35,6 +35,9 @@ def test_every_declared_symbol_is_exported():
     assert M.moe_kernel_name(8, 8) == "gemm_wgrad2_sb1"
     assert M.moe_kernel_name(8, 9) is None
     assert M.moe_kernel_name(9, 11) == "gemm_wgrad2_sb1"
+    assert M.moe_kernel_name(10, 0) == "gemm_fwd1_gather_swiglu"
+    assert M.moe_kernel_name(11, 1) == "gemm_fwd2_combine"
+    assert M.moe_kernel_name(11, 2) is None
 
 
 def test_workspace_sizes():
