@@ -554,7 +554,9 @@ def run_ours(args):
                                  2: "fused forward, fused backward"}[args.schedule],
                        gemm_tiles={0: "two-CTA 256x256 pair tiles (cta_group::2) except dgrad2: 128x256 single-CTA",
                                    1: "single-CTA 128x256 tiles (cta_group::1)",
-                                   2: "two-CTA 256x256 pair tiles (cta_group::2)"}[args.cta_pair],
+                                   2: "two-CTA 256x256 pair tiles (cta_group::2)",
+                                   4: "pair tiles; forward and dgrad GEMM1 in 4-CTA clusters sharing A by TMA "
+                                      "multicast; dgrad2: 128x256 single-CTA"}[args.cta_pair],
                        router="on the path: logits = x Wr on the GPU, gradient through the gating (dlogits, dWr, "
                               "dx share)" if args.router else "off (logits given; the pages time the layer "
                                                                "excluding gating)",
@@ -615,7 +617,7 @@ def main():
     ap.add_argument("--schedule", type=int, default=0, choices=[0, 1, 2],
                     help="0: one persistent launch per phase; 1: fused persistent forward, one persistent "
                          "kernel per backward GEMM; 2: fused forward and fused backward")
-    ap.add_argument("--cta-pair", type=int, default=0, choices=[0, 1, 2],
+    ap.add_argument("--cta-pair", type=int, default=0, choices=[0, 1, 2, 4],
                     help="grouped GEMMs that run as their own kernels: 0 library default (pair tiles but for "
                          "dgrad2), 1 one CTA per tile, 2 two-CTA pair tiles")
     ap.add_argument("--combine", type=int, default=0, choices=[0, 1],

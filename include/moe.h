@@ -138,6 +138,10 @@ typedef struct {
                        its 128 rows of A and half of B);
                        0 (default): 2 for every GEMM but the dgrad GEMM with the SwiGLU backward
                        epilogue, which measured faster with 1.  Both shapes give the same bits.
+                       4: as 0, and the pair-tile forward GEMMs and dgrad GEMM1 run in clusters
+                       of four CTAs: two pairs on the same 256 rows and neighbouring N tiles,
+                       each CTA loading half of its A rows and multicasting them to its
+                       counterpart in the other pair (a quarter less L2-to-SM traffic).
                        The fused forward (schedules 1, 2) takes pair tiles unless cta_pair = 1;
                        the fused backward (schedule 2) always uses single-CTA tiles. */
   int32_t combine;  /* schedule 0 only.  0 (default): a separate gated-combine kernel.

@@ -74,6 +74,7 @@ struct Maps {
   CUtensorMap b2;  // B, 128-row box for a 128-wide tail tile (K-major B only)
   CUtensorMap b3;  // W3, 128-row box
   CUtensorMap gx;  // x [T, H], 64 x 1 box: the rows GEMM1 gathers for its A operand
+  CUtensorMap a64; // A operand, 64-row box: each CTA of a 4-CTA cluster loads half of a shared A block
 };
 
 // The gated combine fused into GEMM2's epilogue (null cnt: not fused).
@@ -956,14 +957,14 @@ __device__ __forceinline__ void load_kblock_pair(const GemmParams& p, const Maps
     tma_load_2d(sB, w, bar, t.n0, y);
     tma_load_2d(sB + kPanelBytes, w, bar, t.n0 + 64, y);
   } else if (MODE == kFwd2) {
-    tma_load_2d(sA, &m.a, bar, k0, t.row0);
+    if (sA != nullptr) tma_load_2d(sA, &m.a, bar, k0, t.row0);
     const int y = t.e * p.F + k0;
     for (int q = 0; q < hb / 64; ++q) tma_load_2d(sB + q * kPanelBytes, &m.b0, bar, t.n0 + r * hb + 64 * q, y);
   } else if (MODE == kDgrad2) {
-    tma_load_2d(sA, &m.a, bar, k0, t.row0);
+    if (sA != nullptr) tma_load_2d(sA, &m.a, bar, k0, t.row0);
     tma_load_2d(sB, hb == 128 ? &m.b0 : &m.b2, bar, k0, t.e * p.F + t.n0 + r * hb);
   } else if (MODE == kDgrad1) {
-    tma_load_2d(sA, &m.a, bar, k0, t.row0);
+    if (sA != nullptr) tma_load_2d(sA, &m.a, bar, k0, t.row0);
     const int yb = t.e * p.H + t.n0 + r * hb;
     if (k0 < p.F)
       tma_load_2d(sB, hb == 128 ? &m.b0 : &m.b2, bar, k0, yb);
@@ -984,9 +985,49 @@ __device__ __forceinline__ void load_kblock_pair(const GemmParams& p, const Maps
   }
 }
 
-template <int MODE>
+// Clusters of four CTAs (CL = 4): two pairs that share the A rows of a
+// super-tile, the same 256 rows of one expert, with pair 0 on N tile 2j and
+// pair 1 on N tile 2j + 1.  Each CTA loads half of its 128 A rows and the TMA
+// multicast delivers them to the CTA with the same rows in the other pair, so
+// the L2 -> SM traffic per MMA drops by a quarter.  With an odd number of N
+// tiles, pair 1 repeats N tile 2j of the last super-tile and stores nothing.
+template <int MODE, int CL>
+__device__ __forceinline__ int cl_n_tiles(const GemmParams& p, const int* pairs) {
+  if (CL == 2) return pair_n_tiles<MODE>(p, pairs);
+  return pairs[p.E] * ((n_ntiles<MODE>(p) + 1) / 2);
+}
+
+template <int MODE, int CL>
+__device__ __forceinline__ Tile cl_decode(const GemmParams& p, const ExpertTables& x, int tile, uint32_t rank,
+                                          bool& dummy) {
+  dummy = false;
+  if (CL == 2) return pair_decode<MODE>(p, x, tile, rank);
+  const int nn = n_ntiles<MODE>(p), nn2 = (nn + 1) / 2;
+  int lo = 0, hi = p.E;  // the last e with pairs[e] * nn2 <= tile (empty experts own no super-tiles)
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (x.pairs[mid] * nn2 <= tile)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  const int first = x.pairs[lo];
+  const int cnt = x.pairs[lo + 1] - first;
+  const int local = tile - nn2 * first;
+  const int j = local / cnt;
+  const int mp = local - j * cnt;  // M pairs fastest, as in the pair order
+  int nt = 2 * j + static_cast<int>(rank >> 1);
+  if (nt >= nn) {
+    nt = 2 * j;
+    dummy = true;
+  }
+  return pair_decode<MODE>(p, x, nn * first + nt * cnt + mp, rank & 1u);
+}
+
+template <int MODE, int CL>
 __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_constant__ Maps maps,
                                                                 const GemmParams p) {
+  static_assert(CL == 2 || (CL == 4 && !ModeTraits<MODE>::wgrad), "4-CTA clusters: forward and dgrad modes");
   using TR = ModeTraits<MODE>;
   constexpr int S = PairTraits<MODE>::kStages;
   constexpr uint32_t kAStep = TR::a_mn ? 2048u : 32u;
@@ -1019,13 +1060,19 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
+  const uint32_t crank = cluster_ctarank();  // rank in the cluster
+  const uint32_t rank = crank & 1u;           // rank in the pair
   const bool leader = (rank == 0);
+  const uint32_t pair_leader = crank & ~1u;
+  // A stage is free once every pair that reads it has committed: with CL = 4 the
+  // A rows arrive by multicast in both pairs, so both leaders' commits count.
+  constexpr uint16_t kEmptyMask = CL == 4 ? 0xF : 0x3;
+  const uint16_t tfull_mask = static_cast<uint16_t>(0x3u << pair_leader);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&empty[i], CL / 2);
       mbar_init(&pfull[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -1048,19 +1095,20 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
   cluster_sync();  // both CTAs' barriers exist before any remote arrive
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int ntiles = pair_n_tiles<MODE>(p, xt.pairs);
-  const int npairs = gridDim.x >> 1;
-  const int pid = blockIdx.x >> 1;
+  const int ntiles = cl_n_tiles<MODE, CL>(p, xt.pairs);
+  const int npairs = gridDim.x / CL;  // clusters
+  const int pid = blockIdx.x / CL;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer (both CTAs)
+    // ------------------------------------------------------------ producer (every CTA)
     int s = 0;
     uint32_t ph = 0;
     uint32_t issued = 0, last_parity = 0;
     bool ok = true;
     for (int tile = pid; tile < ntiles && ok; tile += npairs) {
-      const Tile t = pair_decode<MODE>(p, xt, tile, rank);
-      const bool gather = (MODE == kFwd1) && p.gather;
+      bool dummy;
+      const Tile t = cl_decode<MODE, CL>(p, xt, tile, crank, dummy);
+      const bool gather = (MODE == kFwd1) && CL == 2 && p.gather;
       int src[4] = {0, 0, 0, 0};  // gather: tokens of this lane's 4 rows (rows past R read token 0, never stored)
       if (gather) {
 #pragma unroll
@@ -1076,7 +1124,17 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
           break;
         }
         uint8_t* sA = smem + s * kPairStageBytes;
-        if (gather) {
+        if (CL == 4) {
+          // Half of this CTA's 128 A rows, multicast to the CTA with the same rows in
+          // the other pair; B (this pair's N tile) as usual.
+          if (elect_one()) {
+            mbar_arrive_expect_tx(&full[s], kABytes + t.nw * 64);
+            const int hv = static_cast<int>(crank >> 1);
+            tma_load_2d_mc(sA + hv * (kABytes / 2), &maps.a64, &full[s], kb * BK, t.row0 + 64 * hv,
+                           static_cast<uint16_t>(0x5u << rank));
+            load_kblock_pair<MODE>(p, maps, t, kb, nullptr, sA + kABytes, &full[s], rank);
+          }
+        } else if (gather) {
           if (elect_one()) {
             mbar_arrive_expect_tx(&full[s], kABytes + t.nw * 64);
             load_kblock_pair<MODE>(p, maps, t, kb, nullptr, sA + kABytes, &full[s], rank);  // B only
@@ -1106,9 +1164,10 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
     int acc = 0;
     uint32_t acc_ph = 0;
     bool ok = true;
-    const uint32_t pfull_leader = mapa_shared(smem_u32(pfull), 0);
+    const uint32_t pfull_leader = mapa_shared(smem_u32(pfull), pair_leader);
     for (int tile = pid; tile < ntiles && ok; tile += npairs) {
-      const Tile t = pair_decode<MODE>(p, xt, tile, rank);
+      bool dummy;
+      const Tile t = cl_decode<MODE, CL>(p, xt, tile, crank, dummy);
       if (t.kblocks == 0) continue;  // empty expert (weight gradients): the epilogue writes zeros
       if (leader) {
         if (!mbar_wait_cluster(&tempty[acc], acc_ph ^ 1u, p.ws, 220 + MODE, abort_flag)) break;
@@ -1130,15 +1189,15 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
         }
         // Gathered A rows of a row block's first N tile go out to Xp (the backward
         // reads them); the store reads the stage before the stage is released.
-        const bool store_xp = (MODE == kFwd1) && p.gather && t.n0 == 0 && t.nrows > 0;
-        if (store_xp && lane == 0) {
-          tma_store_2d(&maps.a, sA, kb * BK, t.row0);
-          bulk_commit();
-        }
+        const bool store_xp = (MODE == kFwd1) && CL == 2 && p.gather && t.n0 == 0 && t.nrows > 0;
         __syncwarp();
         if (!leader) {
           if (lane == 0) {
-            if (store_xp) bulk_wait_read<0>();
+            if (store_xp) {
+              tma_store_2d(&maps.a, sA, kb * BK, t.row0);
+              bulk_commit();
+              bulk_wait_read<0>();
+            }
             mbar_arrive_cluster(pfull_leader + s * 8);
           }
           __syncwarp();
@@ -1148,9 +1207,13 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
             break;
           }
           tc_fence_after();
-          // One thread (lane 0) issues the MMAs, the Xp store and the commits, so
-          // each commit tracks that thread's MMAs and the store's bulk group.
-          if (lane == 0) {
+          // One elected thread issues the Xp store, the MMAs and the commits, so each
+          // commit tracks that thread's MMAs and the store's bulk group.
+          if (elect_one()) {
+            if (store_xp) {
+              tma_store_2d(&maps.a, sA, kb * BK, t.row0);
+              bulk_commit();
+            }
             const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
@@ -1161,7 +1224,7 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
               }
             }
             if (store_xp) bulk_wait_read<0>();
-            tc_commit_pair(&empty[s]);
+            tc_commit_pair(&empty[s], kEmptyMask);
           }
           __syncwarp();
         }
@@ -1172,13 +1235,13 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
       }
       if (!ok) break;
       if (leader) {
-        if (lane == 0) tc_commit_pair(&tfull[acc]);
+        if (elect_one()) tc_commit_pair(&tfull[acc], tfull_mask);
         __syncwarp();
       }
       acc ^= 1;
       if (acc == 0) acc_ph ^= 1u;
     }
-    if ((MODE == kFwd1) && p.gather && lane == 0) bulk_wait_all();  // Xp stores complete before exit
+    if ((MODE == kFwd1) && CL == 2 && p.gather) bulk_wait_all();  // Xp stores complete before exit (any lane)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs, own rows)
@@ -1188,12 +1251,13 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
     const int mext = (MODE == kWgrad13) ? p.H : p.F;
     OutStager st;
     st.buf = staging + (warp - 2) * kStageOutBytes;
-    const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), 0);
+    const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), pair_leader);
     int acc = 0;
     uint32_t acc_ph = 0;
     for (int tile = pid; tile < ntiles; tile += npairs) {
-      const Tile t = pair_decode<MODE>(p, xt, tile, rank);
-      const bool mine = TR::wgrad ? (t.m0 < mext) : (t.nrows > 0);
+      bool dummy;
+      const Tile t = cl_decode<MODE, CL>(p, xt, tile, crank, dummy);
+      const bool mine = TR::wgrad ? (t.m0 < mext) : (t.nrows > 0 && !dummy);
       if (t.kblocks == 0) {
         if (TR::wgrad && mine && p.sb != 2) {  // an empty second sub-batch leaves the first one's values
           const int NCall = (MODE == kWgrad13) ? 128 : t.nw;
@@ -2246,17 +2310,17 @@ cudaError_t launch_mode(const GemmLaunch& L, const Maps& maps, const GemmParams&
   return cudaGetLastError();
 }
 
-template <int MODE>
+template <int MODE, int CL = 2>
 cudaError_t launch_pair_mode(const GemmLaunch& L, const Maps& maps, const GemmParams& p, cudaStream_t s,
                              LaunchHook& hook) {
   const int kSmem = PairTraits<MODE>::kSmemBytes + (ModeTraits<MODE>::wgrad ? 0 : static_cast<int>(pair_table_bytes(L.E)));
-  auto kern = pair_gemm_kernel<MODE>;
+  auto kern = pair_gemm_kernel<MODE, CL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = CL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -2264,11 +2328,11 @@ cudaError_t launch_pair_mode(const GemmLaunch& L, const Maps& maps, const GemmPa
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // At most as many pairs as can be resident at once (a persistent grid).
+  // At most as many clusters as can be resident at once (a persistent grid).
   static int max_pairs = -1, max_pairs_smem = -1;
   if (max_pairs < 0 || max_pairs_smem != kSmem) {
     max_pairs_smem = kSmem;
-    cfg.gridDim = dim3(2, 1, 1);
+    cfg.gridDim = dim3(CL, 1, 1);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
       (void)cudaGetLastError();
@@ -2276,10 +2340,10 @@ cudaError_t launch_pair_mode(const GemmLaunch& L, const Maps& maps, const GemmPa
     }
     max_pairs = n;
   }
-  int pairs = L.grid / 2;
+  int pairs = L.grid / CL;
   if (pairs < 1) pairs = 1;
   if (max_pairs > 0 && pairs > max_pairs) pairs = max_pairs;
-  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.gridDim = dim3(CL * pairs, 1, 1);
   hook.before(s);
   e = cudaLaunchKernelEx(&cfg, kern, maps, p);
   hook.after(s);
@@ -2299,6 +2363,20 @@ cudaError_t launch_gemm_pair(GemmMode mode, const GemmLaunch& L, Maps& m, const 
     ok = make_map(&m.b0, L.W1, F, E * H, 64, 128) && make_map(&m.b1, L.W3, F, E * H, 64, 128) &&
          make_map(&m.b2, L.W1, F, E * H, 64, 64) && make_map(&m.b3, L.W3, F, E * H, 64, 64);
   if (!ok) return cudaErrorInvalidValue;
+  // Clusters of two pairs sharing A by multicast (not with the gather-fused A).
+  const bool quad = L.quad && !(mode == kFwd1 && L.gather) && mode != kWgrad13 && mode != kWgrad2;
+  if (quad) {
+    const void* a = mode == kFwd1 ? L.Xp : mode == kFwd2 ? L.h : mode == kDgrad2 ? L.dY : L.dGU;
+    const uint64_t K = mode == kFwd1 || mode == kDgrad2 ? H : mode == kFwd2 ? F : 2 * F;
+    if (!make_map(&m.a64, a, K, static_cast<uint64_t>(L.R), 64, 64)) return cudaErrorInvalidValue;
+    switch (mode) {
+      case kFwd1: return launch_pair_mode<kFwd1, 4>(L, m, p, s, hook);
+      case kFwd2: return launch_pair_mode<kFwd2, 4>(L, m, p, s, hook);
+      case kDgrad2: return launch_pair_mode<kDgrad2, 4>(L, m, p, s, hook);
+      case kDgrad1: return launch_pair_mode<kDgrad1, 4>(L, m, p, s, hook);
+      default: break;
+    }
+  }
   switch (mode) {
     case kFwd1: return launch_pair_mode<kFwd1>(L, m, p, s, hook);
     case kFwd2: return launch_pair_mode<kFwd2>(L, m, p, s, hook);
