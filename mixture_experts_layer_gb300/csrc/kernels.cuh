@@ -147,7 +147,6 @@ struct CombineLaunch {
 struct GemmLaunch {
   int T, H, F, E, k, R;
   int grid;
-  int bn;    // N of one tile: 256, or 128 when the N extent is not a multiple of 256
   int pair;  // 1: two-SM pair tiles (cta_group::2), 0: one CTA per 128-row tile
   int quad;  // with pair: clusters of two pairs sharing the A rows by TMA multicast (forward and dgrad modes)
   const int32_t* tiles;

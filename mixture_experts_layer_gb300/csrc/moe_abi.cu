@@ -362,7 +362,6 @@ int moe_forward(moe_dims d, const void* x, const void* W1, const void* W3, const
                               : launch_fused_forward(g, x, plan->row_src, cursor, cnt_gather, cnt_g1, s, hook);
     if (e != cudaSuccess) return MOE_ERR_LAUNCH;
   } else {
-    g.bn = 256;
     g.pair = use_pair(opts, kFwd1);
     if (dispatch_in_gemm1(d, opts, g.pair)) {  // GEMM1 gathers its A rows from x and stores Xp
       g.gather = 1;
@@ -374,7 +373,6 @@ int moe_forward(moe_dims d, const void* x, const void* W1, const void* W3, const
     }
     if ((e = launch_gemm(kFwd1, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
     g.gather = 0;
-    g.bn = (d.H % 256 == 0) ? 256 : 128;
     g.pair = use_pair(opts, kFwd2);
     const bool fuse = (opts != nullptr && opts->combine == 1);
     if (fuse) {
@@ -474,10 +472,8 @@ int moe_backward(moe_dims d, const void* dout, const void* W1, const void* W3, c
     int32_t* cnt_e = cnt_d2 + L.cap;
     if ((e = launch_fused_backward(g, cursor, cnt_d2, cnt_e, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
   } else {
-    g.bn = (d.F % 256 == 0) ? 256 : 128;
     g.pair = use_pair(opts, kDgrad2);
     if ((e = launch_gemm(kDgrad2, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
-    g.bn = (d.H % 256 == 0) ? 256 : 128;
     g.pair = use_pair(opts, kDgrad1);
     if ((e = launch_gemm(kDgrad1, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
     // The dispatch backward right after dgrad1, while dXp is still in L2; the
@@ -495,10 +491,8 @@ int moe_backward(moe_dims d, const void* dout, const void* W1, const void* W3, c
     g.grid = wgrad_grid(d, opts, sms);
     for (int sb = nb ? 1 : 0; sb <= (nb ? 2 : 0); ++sb) {
       g.sb = sb;
-      g.bn = 256;
       g.pair = use_pair(opts, kWgrad13);
       if ((e = launch_gemm(kWgrad13, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
-      g.bn = (d.H % 256 == 0) ? 256 : 128;
       g.pair = use_pair(opts, kWgrad2);
       if ((e = launch_gemm(kWgrad2, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
     }
