@@ -137,7 +137,8 @@ typedef struct {
                        2: a cluster of two CTAs per 256 x 256 tile (cta_group::2, each SM holding
                        its 128 rows of A and half of B);
                        0 (default): 2 for every GEMM but the dgrad GEMM with the SwiGLU backward
-                       epilogue, which measured faster with 1.  Both shapes give the same bits.
+                       epilogue, which measured faster with 1 unless the experts average at least
+                       2048 rows (T*k >= 2048*E).  Both shapes give the same bits.
                        4: as 0, and the pair-tile forward GEMMs and dgrad GEMM1 run in clusters
                        of four CTAs: two pairs on the same 256 rows and neighbouring N tiles,
                        each CTA loading half of its A rows and multicasting them to its

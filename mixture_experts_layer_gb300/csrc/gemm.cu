@@ -53,6 +53,15 @@ constexpr int kABytes = BM * BK * 2;
 constexpr int kBBytesMax = BN * BK * 2;
 constexpr int kStageBytes = kABytes + kBBytesMax;
 constexpr int kStageOutBytes = 32 * 128;  // one warp's 32x32 fp32 staging box
+constexpr int kEpiRing = 2;                // dgrad2 epilogue: G/U chunk boxes in flight per warp
+constexpr int kEpiRingBytes = kEpiRing * 2048;
+
+// Per-warp epilogue staging of a mode: fp32 store boxes (weight gradients) or
+// the G/U chunk ring (dgrad2).
+template <int MODE>
+__host__ __device__ constexpr int epi_stage_bytes() {
+  return MODE == kDgrad2 ? kEpiRingBytes : (MODE == kWgrad13 || MODE == kWgrad2) ? kStageOutBytes : 0;
+}
 
 template <int MODE>
 struct ModeTraits {
@@ -63,8 +72,8 @@ struct ModeTraits {
   // Output columns per tile are 2 x 128 (two weights side by side) or up to 256.
   static constexpr bool paired = (MODE == kFwd1 || MODE == kWgrad13);
   static constexpr int kStages = 4;
-  static constexpr int kStagingBytes = wgrad ? kEpiWarps * kStageOutBytes : 0;
-  static constexpr int kSmemBytes = kStages * kStageBytes + kStagingBytes + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int kStagingBytes = kEpiWarps * epi_stage_bytes<MODE>();
+  static constexpr int kSmemBytes = kStages * kStageBytes + kStagingBytes + 1024 /*align*/ + 512 /*barriers*/;
 };
 
 struct Maps {
@@ -75,6 +84,7 @@ struct Maps {
   CUtensorMap b3;  // W3, 128-row box
   CUtensorMap gx;  // x [T, H], 64 x 1 box: the rows GEMM1 gathers for its A operand
   CUtensorMap a64; // A operand, 64-row box: each CTA of a 4-CTA cluster loads half of a shared A block
+  CUtensorMap gu;  // dgrad2 epilogue: GU [R, 2F], 16-column x 32-row boxes, 32-byte swizzle
 };
 
 // The gated combine fused into GEMM2's epilogue (null cnt: not fused).
@@ -319,6 +329,22 @@ __device__ __forceinline__ void store_zero_f32(float* dst) {
 // measured slower: one 4 KB bulk store at a time kept each SM near 16 B/clk.)
 struct OutStager {
   uint8_t* buf;  // one 4 KB box, 1024-byte aligned
+  // dgrad2: buf holds a ring of kEpiRing 2 KB slots, each a (G, U) pair of
+  // 16-column x 32-row boxes filled by TMA; ebar[kEpiRing] their barriers (null:
+  // G and U are read directly from global memory); eph the parity each barrier
+  // waits for next.
+  uint64_t* ebar = nullptr;
+  uint32_t eph = 0;
+  uint32_t pending = 0;  // slots whose load was issued and not yet consumed
+  // Before the CTA exits (also after an abort): wait (bounded) for loads still in flight.
+  __device__ __forceinline__ void drain(WsHeader* ws) {
+    for (int s = 0; s < kEpiRing && ebar != nullptr; ++s)
+      if ((pending >> s) & 1u) {
+        mbar_wait(&ebar[s], (eph >> s) & 1u, ws, 271, nullptr);
+        eph ^= 1u << s;
+      }
+    pending = 0;
+  }
   // dst points at the block's first element; ld is the row stride in floats.
   // ACC: add the values already stored there (the second sub-batch's partial).
   template <bool ACC = false>
@@ -486,6 +512,111 @@ __device__ __forceinline__ void combine_in_epilogue(const GemmParams& p, const T
   }
 }
 
+// SwiGLU backward of one element, with every rounding step spelled out so that
+// each epilogue that uses it gives the same bits: s = sigmoid(G),
+// dG = dH U s (1 + G (1 - s)), dU = dH G s.
+__device__ __forceinline__ void swiglu_bwd(float G, float U, float dh, float& dg, float& du) {
+  const float sg = __frcp_rn(__fadd_rn(1.0f, expf(-G)));
+  const float tt = __fmaf_rn(G, __fsub_rn(1.0f, sg), 1.0f);
+  dg = __fmul_rn(__fmul_rn(__fmul_rn(dh, U), sg), tt);
+  du = __fmul_rn(__fmul_rn(dh, G), sg);
+}
+
+// dgrad2 epilogue with staged operands: this warp's 32 rows x [c_lo, c_hi)
+// columns in 16-column chunks.  The G and U blocks of a chunk (32 rows x 16
+// columns, 32-byte swizzle) arrive by TMA into a ring of kEpiRing slots: the
+// first kEpiRing are requested before the accumulator is ready
+// (dgrad2_prefetch), each later one as soon as its slot is free.  Each lane
+// reads its row, writes dG and dU back in place, and the warp then stores the
+// two blocks with row-contiguous 32-byte segments (16 rows per instruction),
+// skipping the rows past the tile's valid rows.
+__device__ __forceinline__ void dgrad2_cols(const Tile& t, int half, int& c_lo, int& c_hi) {
+  c_lo = half * (t.nw / 2);
+  c_hi = c_lo + t.nw / 2;
+}
+
+__device__ __forceinline__ void dgrad2_issue(const GemmParams& p, const Maps& m, const Tile& t, int q, int c_lo, int k,
+                                             int lane, OutStager& st) {
+  const int slot = k % kEpiRing;
+  __syncwarp();
+  if (lane == 0) {
+    fence_proxy_async_smem();  // this warp's earlier reads and writes of the slot come first
+    mbar_arrive_expect_tx(&st.ebar[slot], 2048);
+    const int col = t.n0 + c_lo + 16 * k;
+    tma_load_2d(st.buf + slot * 2048, &m.gu, &st.ebar[slot], col, t.row0 + 32 * q);
+    tma_load_2d(st.buf + slot * 2048 + 1024, &m.gu, &st.ebar[slot], p.F + col, t.row0 + 32 * q);
+  }
+  st.pending |= 1u << slot;
+}
+
+__device__ __forceinline__ void dgrad2_prefetch(const GemmParams& p, const Maps& m, const Tile& t, int q, int half,
+                                                int lane, OutStager& st) {
+  int c_lo, c_hi;
+  dgrad2_cols(t, half, c_lo, c_hi);
+  const int nch = (c_hi - c_lo) / 16;
+  for (int k = 0; k < nch && k < kEpiRing; ++k) dgrad2_issue(p, m, t, q, c_lo, k, lane, st);
+}
+
+__device__ __forceinline__ void dgrad2_epilogue_staged(const GemmParams& p, const Maps& m, const Tile& t, uint32_t tacc,
+                                                       int q, int c_lo, int c_hi, int lane, OutStager& st) {
+  const int y0 = t.row0 + 32 * q;
+  const int nch = (c_hi - c_lo) / 16;
+  const uint32_t base = smem_u32(st.buf);
+  // Byte offset of 16-byte chunk j of row r in a 32-byte-swizzled box.
+  auto sw = [](int r, int j) { return static_cast<uint32_t>(r * 32 + ((j ^ ((r >> 2) & 1)) << 4)); };
+#pragma unroll 1
+  for (int k = 0; k < nch; ++k) {
+    const int slot = k % kEpiRing;
+    uint32_t d[16];
+    tc_ld_32x32b_x16(tacc + c_lo + 16 * k, d);
+    mbar_wait(&st.ebar[slot], (st.eph >> slot) & 1u, p.ws, 270, nullptr);
+    st.eph ^= 1u << slot;
+    st.pending &= ~(1u << slot);
+    tc_wait_ld();
+    const uint32_t gbox = base + slot * 2048, ubox = gbox + 1024;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      uint32_t g0, g1, g2, g3, u0, u1, u2, u3;
+      asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(g0), "=r"(g1), "=r"(g2), "=r"(g3)
+                   : "r"(gbox + sw(lane, j)));
+      asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(u0), "=r"(u1), "=r"(u2), "=r"(u3)
+                   : "r"(ubox + sw(lane, j)));
+      const uint32_t gw[4] = {g0, g1, g2, g3}, uw[4] = {u0, u1, u2, u3};
+      uint32_t dgw[4], duw[4];
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) {
+        float dg0, du0, dg1, du1;
+        swiglu_bwd(bf16lo(gw[qq]), bf16lo(uw[qq]), __uint_as_float(d[8 * j + 2 * qq]), dg0, du0);
+        swiglu_bwd(bf16hi(gw[qq]), bf16hi(uw[qq]), __uint_as_float(d[8 * j + 2 * qq + 1]), dg1, du1);
+        dgw[qq] = pack_bf16x2(dg0, dg1);
+        duw[qq] = pack_bf16x2(du0, du1);
+      }
+      st_shared_v4(gbox + sw(lane, j), dgw[0], dgw[1], dgw[2], dgw[3]);
+      st_shared_v4(ubox + sw(lane, j), duw[0], duw[1], duw[2], duw[3]);
+    }
+    __syncwarp();
+    // Row-contiguous stores: lane l covers row 16 i + l / 2, 16-byte chunk l % 2.
+    const int j = lane & 1;
+    const int col = t.n0 + c_lo + 16 * k + 8 * j;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int rr = 16 * i + (lane >> 1);
+      if (32 * q + rr < t.nrows) {
+        uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                     : "r"(gbox + sw(rr, j)));
+        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(b0), "=r"(b1), "=r"(b2), "=r"(b3)
+                     : "r"(ubox + sw(rr, j)));
+        __nv_bfloat16* dst = p.out0 + static_cast<size_t>(y0 + rr) * (2 * p.F) + col;
+        st_v4(dst, a0, a1, a2, a3);
+        st_v4(dst + p.F, b0, b1, b2, b3);
+      }
+    }
+    if (k + kEpiRing < nch) dgrad2_issue(p, m, t, q, c_lo, k + kEpiRing, lane, st);  // the slot is free again
+  }
+  __syncwarp();
+}
+
 template <int MODE>
 __device__ __forceinline__ void epilogue(const GemmParams& p, const Maps& m, const Tile& t, uint32_t tacc, int q,
                                          int half, int lane, OutStager& st) {
@@ -549,6 +680,10 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, const Maps& m, con
         }
       }
     }
+    return;
+  }
+  if (MODE == kDgrad2 && st.ebar != nullptr) {
+    dgrad2_epilogue_staged(p, m, t, tacc, q, c_lo, c_hi, lane, st);
     return;
   }
   const bool valid = row < t.nrows;
@@ -617,10 +752,7 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, const Maps& m, con
             for (int hbit = 0; hbit < 2; ++hbit) {
               const float G = hbit ? bf16hi(gw[qq]) : bf16lo(gw[qq]);
               const float U = hbit ? bf16hi(uw[qq]) : bf16lo(uw[qq]);
-              const float dh = __uint_as_float(d[8 * i + 2 * qq + hbit]);
-              const float sg = __frcp_rn(1.0f + expf(-G));
-              dg2[hbit] = dh * U * sg * (1.0f + G * (1.0f - sg));
-              du2[hbit] = dh * G * sg;
+              swiglu_bwd(G, U, __uint_as_float(d[8 * i + 2 * qq + hbit]), dg2[hbit], du2[hbit]);
             }
             dgw[qq] = pack_bf16x2(dg2[0], dg2[1]);
             duw[qq] = pack_bf16x2(du2[0], du2[1]);
@@ -671,6 +803,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint64_t* ebar = tempty + 3;  // dgrad2: kEpiRing G/U chunk barriers per epilogue warp
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -684,6 +817,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], kEpiWarps);
     }
+    for (int i = 0; i < kEpiRing * kEpiWarps && MODE == kDgrad2; ++i) mbar_init(&ebar[i], 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -793,7 +927,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     const int half = (warp - 2) >> 2;    // which half of the columns
     const int row = q * 32 + lane;
     OutStager st;
-    st.buf = staging + (warp - 2) * kStageOutBytes;
+    st.buf = staging + (warp - 2) * epi_stage_bytes<MODE>();
+    if (MODE == kDgrad2) st.ebar = ebar + kEpiRing * (warp - 2);
     int acc = 0;
     uint32_t acc_ph = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
@@ -812,6 +947,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         }
         continue;
       }
+      if (MODE == kDgrad2) dgrad2_prefetch(p, maps, t, q, half, lane, st);  // G/U need no accumulator
       if (!mbar_wait(&tfull[acc], acc_ph, p.ws, 140 + MODE, abort_flag)) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccStride;
@@ -824,6 +960,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     }
     // Bulk stores must finish reading shared memory (and land) before the CTA exits.
     if (TR::wgrad && lane == 0) bulk_wait_all();
+    if (MODE == kDgrad2) st.drain(p.ws);  // no G/U load may land after the CTA is gone
     __syncwarp();
   }
 
@@ -862,8 +999,8 @@ constexpr int kPairStageBytes = kABytes + kPairBHalfBytes;
 template <int MODE>
 struct PairTraits {
   static constexpr bool wgrad = ModeTraits<MODE>::wgrad;
-  static constexpr int kStages = 6;
-  static constexpr int kStagingBytes = wgrad ? kEpiWarps * kStageOutBytes : 0;
+  static constexpr int kStages = MODE == kDgrad2 ? 5 : 6;  // dgrad2 gives a stage to its G/U chunk ring
+  static constexpr int kStagingBytes = kEpiWarps * epi_stage_bytes<MODE>();
   static constexpr int kSmemBytes = kStages * kPairStageBytes + kStagingBytes + 1024 /*align*/ + 512 /*barriers*/;
 };
 // Shared memory of the staged per-expert tables (4 arrays of E + 1 ints).
@@ -1045,6 +1182,7 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint64_t* ebar = tempty + 3;  // dgrad2: kEpiRing G/U chunk barriers per epilogue warp
   int* tab = reinterpret_cast<int*>(smem + S * kPairStageBytes + PairTraits<MODE>::kStagingBytes + 512);
   ExpertTables xt;
   xt.pairs = tab;
@@ -1079,6 +1217,7 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], 2 * kEpiWarps);
     }
+    for (int i = 0; i < kEpiRing * kEpiWarps && MODE == kDgrad2; ++i) mbar_init(&ebar[i], 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -1250,7 +1389,8 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
     const int row = q * 32 + lane;
     const int mext = (MODE == kWgrad13) ? p.H : p.F;
     OutStager st;
-    st.buf = staging + (warp - 2) * kStageOutBytes;
+    st.buf = staging + (warp - 2) * epi_stage_bytes<MODE>();
+    if (MODE == kDgrad2) st.ebar = ebar + kEpiRing * (warp - 2);
     const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), pair_leader);
     int acc = 0;
     uint32_t acc_ph = 0;
@@ -1272,6 +1412,7 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
         }
         continue;
       }
+      if (MODE == kDgrad2 && mine) dgrad2_prefetch(p, maps, t, q, half, lane, st);  // G/U need no accumulator
       if (!mbar_wait_cluster(&tfull[acc], acc_ph, p.ws, 250 + MODE, abort_flag)) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccStride;
@@ -1288,6 +1429,7 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
       if (acc == 0) acc_ph ^= 1u;
     }
     if (TR::wgrad && lane == 0) bulk_wait_all();
+    if (MODE == kDgrad2) st.drain(p.ws);  // no G/U load may land after the CTA is gone
     __syncwarp();
   }
 
@@ -2285,7 +2427,7 @@ EncodeFn encoder() {
 
 // 2-D bf16 tensor [outer, inner] (inner contiguous), box {box_inner, box_outer}, 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
-              uint32_t box_outer) {
+              uint32_t box_outer, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeFn enc = encoder();
   if (!enc) return false;
   const cuuint64_t dims[2] = {inner, outer};
@@ -2293,7 +2435,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, 
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -2589,6 +2731,7 @@ cudaError_t launch_gemm(GemmMode mode, const GemmLaunch& L, cudaStream_t s, Laun
            make_map(&m.b2, L.W2, H, E * F, 64, 128);
       p.out0 = static_cast<__nv_bfloat16*>(L.out_dGU);
       p.aux = static_cast<const __nv_bfloat16*>(L.GU);
+      ok = ok && make_map(&m.gu, L.GU, 2 * F, R, 16, 32, CU_TENSOR_MAP_SWIZZLE_32B);  // epilogue G/U boxes
       break;
     case kDgrad1:
       ok = make_map(&m.a, L.dGU, 2 * F, R, 64, BM) && make_map(&m.b0, L.W1, F, E * H, 64, BN) &&

@@ -182,11 +182,15 @@ int wgrad_grid(const moe_dims& d, const moe_opts* o, int sms) {
 // Tile shape of a grouped GEMM launched on its own: the two-CTA pair tile
 // wherever it measured faster (every mode but the dgrad GEMM with the SwiGLU
 // backward epilogue), unless the caller asks for one shape everywhere.
-int use_pair(const moe_opts* o, GemmMode m) {
+int use_pair(const moe_opts* o, GemmMode m, const moe_dims& d) {
   const int c = (o != nullptr) ? o->cta_pair : 0;
   if (c == 1) return 0;
   if (c == 2) return 1;
-  return m != kDgrad2;
+  // dgrad2 (SwiGLU backward epilogue) measured faster on single-CTA tiles unless the
+  // experts are long (long-seq, 8192 rows each: 9.8 against 10.9 ms), where the pair
+  // tiles' 256-row granularity wastes nothing.
+  if (m == kDgrad2) return static_cast<long long>(d.T) * d.k >= 2048ll * d.E;
+  return 1;
 }
 
 // cta_pair = 4: the pair-tile forward and dgrad GEMMs run in clusters of two
@@ -358,11 +362,11 @@ int moe_forward(moe_dims d, const void* x, const void* W1, const void* W3, const
     int32_t* cnt_gather = reinterpret_cast<int32_t*>(sched + 64);
     int32_t* cnt_g1 = cnt_gather + L.cap;
     g.drop_task = (opts != nullptr && opts->debug_drop_task > 0) ? opts->debug_drop_task : 0;
-    e = use_pair(opts, kFwd1) ? launch_fused_forward_pair(g, x, plan->row_src, cursor, cnt_gather, cnt_g1, s, hook)
+    e = use_pair(opts, kFwd1, d) ? launch_fused_forward_pair(g, x, plan->row_src, cursor, cnt_gather, cnt_g1, s, hook)
                               : launch_fused_forward(g, x, plan->row_src, cursor, cnt_gather, cnt_g1, s, hook);
     if (e != cudaSuccess) return MOE_ERR_LAUNCH;
   } else {
-    g.pair = use_pair(opts, kFwd1);
+    g.pair = use_pair(opts, kFwd1, d);
     if (dispatch_in_gemm1(d, opts, g.pair)) {  // GEMM1 gathers its A rows from x and stores Xp
       g.gather = 1;
       g.x = x;
@@ -373,7 +377,7 @@ int moe_forward(moe_dims d, const void* x, const void* W1, const void* W3, const
     }
     if ((e = launch_gemm(kFwd1, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
     g.gather = 0;
-    g.pair = use_pair(opts, kFwd2);
+    g.pair = use_pair(opts, kFwd2, d);
     const bool fuse = (opts != nullptr && opts->combine == 1);
     if (fuse) {
       const WsLayout L = ws_layout(d);
@@ -472,9 +476,9 @@ int moe_backward(moe_dims d, const void* dout, const void* W1, const void* W3, c
     int32_t* cnt_e = cnt_d2 + L.cap;
     if ((e = launch_fused_backward(g, cursor, cnt_d2, cnt_e, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
   } else {
-    g.pair = use_pair(opts, kDgrad2);
+    g.pair = use_pair(opts, kDgrad2, d);
     if ((e = launch_gemm(kDgrad2, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
-    g.pair = use_pair(opts, kDgrad1);
+    g.pair = use_pair(opts, kDgrad1, d);
     if ((e = launch_gemm(kDgrad1, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
     // The dispatch backward right after dgrad1, while dXp is still in L2; the
     // weight gradients, which read Xp / h / dY / dGU, follow.
@@ -491,9 +495,9 @@ int moe_backward(moe_dims d, const void* dout, const void* W1, const void* W3, c
     g.grid = wgrad_grid(d, opts, sms);
     for (int sb = nb ? 1 : 0; sb <= (nb ? 2 : 0); ++sb) {
       g.sb = sb;
-      g.pair = use_pair(opts, kWgrad13);
+      g.pair = use_pair(opts, kWgrad13, d);
       if ((e = launch_gemm(kWgrad13, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
-      g.pair = use_pair(opts, kWgrad2);
+      g.pair = use_pair(opts, kWgrad2, d);
       if ((e = launch_gemm(kWgrad2, g, s, hook)) != cudaSuccess) return MOE_ERR_LAUNCH;
     }
     return MOE_OK;
