@@ -70,7 +70,7 @@ struct PlanLaunch {
   float* w;
   uint32_t* gbm;
   int32_t* ticket;  // 16 words, then ccount; both cleared by launch_plan
-  int32_t* ccount;  // [nchunks][E] = ticket + 16
+  int32_t* ccount;  // [E][nchunks] (expert-major) = ticket + 16
   int32_t* cbase;
   int32_t* counts;
   int32_t* offsets;

@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float* _
   uint32_t* out = gbm + static_cast<size_t>(chunk) * E * kChunkWords;
   for (int i = threadIdx.x; i < 2 * E; i += blockDim.x) out[(i >> 1) * kChunkWords + w0 + (i & 1)] = bm[i];
   for (int e = threadIdx.x; e < E; e += blockDim.x)
-    if (cnt[e] != 0) atomicAdd(&ccount[static_cast<size_t>(chunk) * E + e], cnt[e]);
+    if (cnt[e] != 0) atomicAdd(&ccount[static_cast<size_t>(e) * ((T + kChunk - 1) / kChunk) + chunk], cnt[e]);
 }
 
 // Fast path of the same selection for E % 4 == 0, E <= 256 and k <= 8: four
@@ -390,7 +390,7 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk4_kernel(const float* 
   uint32_t* out = gbm + static_cast<size_t>(chunk) * E * kChunkWords;
   for (int i = threadIdx.x; i < 2 * E; i += blockDim.x) out[(i >> 1) * kChunkWords + w0 + (i & 1)] = bm[i];
   for (int e = threadIdx.x; e < E; e += blockDim.x)
-    if (cnt[e] != 0) atomicAdd(&ccount[static_cast<size_t>(chunk) * E + e], cnt[e]);
+    if (cnt[e] != 0) atomicAdd(&ccount[static_cast<size_t>(e) * ((T + kChunk - 1) / kChunk) + chunk], cnt[e]);
 }
 
 // Per expert (one warp each): exclusive prefix of the chunk counts over the
@@ -422,7 +422,7 @@ __global__ void __launch_bounds__(32 * kScanWarps) route_scan_kernel(const int32
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int c = c0 + 32 * u + lane;
-        v[u] = (c < nchunks) ? ccount[static_cast<size_t>(c) * E + e] : 0;
+        v[u] = (c < nchunks) ? ccount[static_cast<size_t>(e) * nchunks + c] : 0;  // expert-major: coalesced
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
