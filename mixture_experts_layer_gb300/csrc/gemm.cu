@@ -724,8 +724,9 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, const Maps& m, con
         for (int i = 0; i < 16; i += 4) st_v4(gdst + p.F + 2 * i, u[i], u[i + 1], u[i + 2], u[i + 3]);
       }
     } else if (MODE == kDgrad2) {
-      // G and U of this row are read from global memory; the loads of the
-      // next 32 columns are issued before this chunk's arithmetic.
+      // Without staging boxes (the fused backward): G and U of this row are read
+      // from global memory; the loads of the next 32 columns are issued before
+      // this chunk's arithmetic.
       uint32_t d[32];
       tc_ld_32x32b_x32(tacc + c, d);
       uint4 gn[4], un[4];

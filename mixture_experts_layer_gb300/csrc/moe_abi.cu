@@ -180,8 +180,7 @@ int wgrad_grid(const moe_dims& d, const moe_opts* o, int sms) {
 }
 
 // Tile shape of a grouped GEMM launched on its own: the two-CTA pair tile
-// wherever it measured faster (every mode but the dgrad GEMM with the SwiGLU
-// backward epilogue), unless the caller asks for one shape everywhere.
+// wherever it measured faster, unless the caller asks for one shape everywhere.
 int use_pair(const moe_opts* o, GemmMode m, const moe_dims& d) {
   const int c = (o != nullptr) ? o->cta_pair : 0;
   if (c == 1) return 0;
