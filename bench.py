@@ -439,19 +439,52 @@ def run_ours(args):
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
+    # Timed region: K whole steps, nothing but the layer's own launches in it.  By
+    # default the step's launches (plan, forward, backward: all stream-ordered, no
+    # host synchronisation) are captured once in a CUDA graph and the graph is
+    # replayed K times, which removes the host launch gaps between the kernels.
+    graph = None
+    if not args.no_graph:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        l0 = M.moe_launch_count()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            step()
+        per_step_launches = M.moe_launch_count() - l0
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
     l0 = M.moe_launch_count()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for i in range(args.steps):
-        step(opts_f[i], opts_b[i], evs_p[i], opts_r[i])
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
     t_end.record(stream)
     torch.cuda.synchronize()
-    launches = M.moe_launch_count() - l0
+    launches = M.moe_launch_count() - l0 if graph is None else per_step_launches * args.steps
     barrier(world)
-    clk = clocks.stop()
     ms_local = t_start.elapsed_time(t_end)
     ms_total = max_over_ranks(ms_local, world)
+    # Second timed pass of K steps with a CUDA event pair around every kernel (on the
+    # launching stream) for the per-kernel durations; the events themselves cost a
+    # few percent of a short step, so the headline value comes from the pass above.
+    k_start = torch.cuda.Event(enable_timing=True)
+    k_end = torch.cuda.Event(enable_timing=True)
+    k_start.record(stream)
+    for i in range(args.steps):
+        step(opts_f[i], opts_b[i], evs_p[i], opts_r[i])
+    k_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms_events = k_start.elapsed_time(k_end) / args.steps
     st = layer.status()
     if st[0] != 0:
         raise RuntimeError(f"device status {st}")
@@ -539,20 +572,38 @@ def run_ours(args):
             d_do.copy_(h_do, non_blocking=True)
         ev_in[j].record(cs)
 
-    def e2e_step(i, last):
-        j = i & 1
+    def compute(j):
         d_x, d_lg, d_do = d_in[j]
-        stream.wait_event(ev_in[j])
         if args.router:
             layer.router_forward(d_x, inp["Wr"], opts=base_opts)
         layer.plan(layer.logits if args.router else d_lg)
         layer.forward(d_x, inp["W1"], inp["W3"], inp["W2"], opts=base_opts)
         layer.backward(d_do, inp["W1"], inp["W3"], inp["W2"], opts=base_opts,
                        router=(d_x, inp["Wr"]) if args.router else None)
-        ev_used[j].record(stream)
-        stream.wait_event(ev_out[j])
         d_stage[j][0].copy_(layer.out)
         d_stage[j][1].copy_(layer.dx)
+
+    # One graph per input/staging buffer set, as in the device-timed region.
+    e2e_graphs = [None, None]
+    if graph is not None:
+        side = torch.cuda.Stream(dev)
+        for j in range(2):
+            side.wait_stream(stream)
+            e2e_graphs[j] = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(e2e_graphs[j], stream=side):
+                compute(j)
+            stream.wait_stream(side)
+        torch.cuda.synchronize()
+
+    def e2e_step(i, last):
+        j = i & 1
+        stream.wait_event(ev_in[j])
+        stream.wait_event(ev_out[j])  # staging j downloaded (two steps ago)
+        if e2e_graphs[j] is not None:
+            e2e_graphs[j].replay()
+        else:
+            compute(j)
+        ev_used[j].record(stream)
         ev_staged[j].record(stream)
         if not last:
             upload(j ^ 1)
@@ -613,8 +664,13 @@ def run_ours(args):
         "e2e": {"value": round(world * T * args.steps / (e2e_ms * 1e-3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "copies": "pinned host <-> device on a copy stream, double-buffered: step i+1's upload and "
-                          "step i's download overlap compute"},
+                          "step i's download overlap compute",
+                "launch": "CUDA graph per buffer set" if graph is not None else "eager launches"},
         "gpu_launches": int(launches),
+        "kernel_timing": {"how": "CUDA event pair around each kernel on its launching stream, second timed pass of "
+                                 "the same K steps (eager launches)", "ms_per_step_with_events": round(ms_events, 4)},
+        "launch": ("CUDA graph of one step (plan + forward + backward) replayed K times" if graph is not None
+                   else "eager launches"),
         "clocks": clk,
         "kernels": kern,
         "step_gemm_tflops": round((18 * T * k * H * F + (4 * T * H * E if args.router else 0))
@@ -674,6 +730,8 @@ def main():
                          "multiple of P (static-shape variant)")
     ap.add_argument("--router", action="store_true",
                     help="put the router on the timed path: logits = x Wr on the GPU and its backward")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time the steps as eager launches instead of replaying a CUDA graph of one step")
     ap.add_argument("--profile", action="store_true",
                     help="run the warm-up steps and one more step only (for ncu captures)")
     ap.add_argument("--part", default="step", choices=["step", "plan"],
