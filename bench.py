@@ -553,7 +553,8 @@ def run_ours(args):
     d_in = [(torch.empty_like(inp["x"]), torch.empty_like(inp["logits"]), torch.empty_like(inp["dout"]))
             for _ in range(2)]
     d_stage = [(torch.empty_like(layer.out), torch.empty_like(layer.dx)) for _ in range(2)]
-    cs = torch.cuda.Stream(dev)
+    cs = torch.cuda.Stream(dev)     # uploads
+    cs_d = torch.cuda.Stream(dev)   # downloads (a copy engine of their own)
     ev_in = [torch.cuda.Event() for _ in range(2)]      # inputs j uploaded
     ev_used = [torch.cuda.Event() for _ in range(2)]    # compute done with inputs j
     ev_staged = [torch.cuda.Event() for _ in range(2)]  # results staged in j
@@ -607,11 +608,11 @@ def run_ours(args):
         ev_staged[j].record(stream)
         if not last:
             upload(j ^ 1)
-        cs.wait_event(ev_staged[j])
-        with torch.cuda.stream(cs):
+        cs_d.wait_event(ev_staged[j])
+        with torch.cuda.stream(cs_d):
             h_out.copy_(d_stage[j][0], non_blocking=True)
             h_dx.copy_(d_stage[j][1], non_blocking=True)
-        ev_out[j].record(cs)
+        ev_out[j].record(cs_d)
 
     def e2e_run(n):
         upload(0)
@@ -626,6 +627,7 @@ def run_ours(args):
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     cs.wait_event(e0)
+    cs_d.wait_event(e0)
     e2e_run(args.steps)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -663,8 +665,8 @@ def run_ours(args):
         "roofline": roof,
         "e2e": {"value": round(world * T * args.steps / (e2e_ms * 1e-3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "copies": "pinned host <-> device on a copy stream, double-buffered: step i+1's upload and "
-                          "step i's download overlap compute",
+                "copies": "pinned host <-> device on an upload and a download stream, double-buffered: step "
+                          "i+1's upload and step i's download overlap compute",
                 "launch": "CUDA graph per buffer set" if graph is not None else "eager launches"},
         "gpu_launches": int(launches),
         "kernel_timing": {"how": "CUDA event pair around each kernel on its launching stream, second timed pass of "
