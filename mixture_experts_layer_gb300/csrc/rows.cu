@@ -70,6 +70,16 @@ __device__ __forceinline__ void zero_padding_rows(const int32_t* __restrict__ ro
   }
 }
 
+// The gated combine, with fewer tokens than warps (short batches), gives each
+// token to `parts` warps, each over a contiguous range of the row's 16-byte
+// columns, so that more rows are in flight; every output element is still
+// summed by one lane in slot order, so the bits do not change (fine-grained:
+// 23.9 -> 19.9 us; the dispatch backward measured slower split and stays whole).
+__device__ __forceinline__ int token_parts(int T, int nwarps) {
+  return (T > 0 && nwarps >= 2 * T) ? min(4, nwarps / T) : 1;
+}
+__device__ __forceinline__ int part_span(int hv, int parts) { return ((hv + parts - 1) / parts + 31) / 32 * 32; }
+
 // Dispatch as a gather, one warp per grouped row: Xp[r] = x[row_src[r]], zeros
 // for a padding row.  Used while x fits comfortably in L2 (its re-reads are L2
 // hits), where the R rows give more parallelism than the T tokens.
@@ -194,11 +204,13 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const uint4* __restri
                                                              int T, int k, int R, int hv, WsHeader* ws) {
   const int lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * (kThreads / 32);
-  for (int t = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); t < T; t += nwarps) {
+  const int parts = token_parts(T, nwarps), span = part_span(hv, parts);
+  for (int tw = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); tw < T * parts; tw += nwarps) {
+    const int t = tw / parts, v0 = (tw - t * parts) * span, v1 = min(hv, v0 + span);
     int rows[K];
     float wj[K];
     if (!token_rows<K>(dest, w, t, k, R, lane, rows, wj, ws, 11)) continue;
-    for (int v = lane; v < hv; v += 32) {
+    for (int v = v0 + lane; v < v1; v += 32) {
       uint4 y[K];
 #pragma unroll
       for (int j = 0; j < K; ++j)
