@@ -119,6 +119,9 @@ struct GemmParams {
   // row_src (TMA gather4) and the first N tile of each row block stores them to Xp.
   int gather;
   const int32_t* row_src;
+  // Pair tiles (forward and dgrad modes): an expert's last 256-row block with at
+  // most 128 rows runs as an M = 128 pair tile, 64 rows per CTA.
+  int halfm_ok;
   WsHeader* ws;
 };
 
@@ -144,6 +147,7 @@ struct Tile {
   int nw;     // MMA N of the tile: 256, or 128 for a tail tile
   int kblocks;
   int mt;     // forward/dgrad: index of the 128-row tile in the plan's tile table
+  int halfm = 0;  // pair tiles: 1 when the pair's MMA is M = 128 (this CTA holds 64 rows)
 };
 
 template <int MODE>
@@ -651,8 +655,9 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, const Maps& m, con
     }
     return;
   }
-  // This warp's columns: [c_lo, c_hi) of each output (NC / 2 is a multiple of 32).
-  const int NCall = ModeTraits<MODE>::paired ? 128 : t.nw;
+  // This warp's columns: [c_lo, c_hi) of each output (NC / 2 is a multiple of 16).
+  // An M = 128 pair tile (halfm) holds half of the tile's columns per lane half.
+  const int NCall = ModeTraits<MODE>::paired ? (t.halfm ? 64 : 128) : t.nw;
   const int c_lo = half * (NCall / 2), c_hi = c_lo + NCall / 2;
   if (ModeTraits<MODE>::wgrad) {
     const int y = (MODE == kWgrad13) ? t.e * p.H + t.m0 + q * 32 : t.e * p.F + t.m0 + q * 32;
@@ -702,7 +707,7 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, const Maps& m, con
     if (MODE == kFwd1) {
       uint32_t g[32], u[32];
       tc_ld_32x32b_x32(tacc + c, g);
-      tc_ld_32x32b_x32(tacc + 128 + c, u);
+      tc_ld_32x32b_x32(tacc + (t.halfm ? 64 : 128) + c, u);
       tc_wait_ld();
       if (valid) {
         uint32_t hw[16];
@@ -1067,6 +1072,14 @@ __device__ __forceinline__ Tile pair_decode(const GemmParams& p, const ExpertTab
     t.nrows = max(0, min(kTileRows, n_e - kTileRows * j));
     t.m0 = 0;
     t.mt = x.tstart[e] + j;
+    t.halfm = 0;
+    const int rem = n_e - kTileRows * (j & ~1);  // rows left in this pair's 256-row block
+    if (p.halfm_ok && rem <= kTileRows) {
+      // M = 128 pair tile: CTA r takes rows [64 r, 64 r + 64) of the block.
+      t.halfm = 1;
+      t.row0 = x.offsets[e] + kTileRows * (j & ~1) + 64 * static_cast<int>(rank);
+      t.nrows = max(0, min(64, rem - 64 * static_cast<int>(rank)));
+    }
     const int K = (MODE == kFwd1 || MODE == kDgrad2) ? p.H : (MODE == kFwd2) ? p.F : 2 * p.F;
     t.kblocks = K / BK;
   }
@@ -1091,9 +1104,16 @@ __device__ __forceinline__ void load_kblock_pair(const GemmParams& p, const Maps
   if (MODE == kFwd1) {
     if (sA != nullptr) tma_load_2d(sA, &m.a, bar, k0, t.row0);  // null: A is gathered from x
     const int y = t.e * p.H + k0;
-    const CUtensorMap* w = r ? &m.b1 : &m.b0;  // W1 (G columns) on CTA 0, W3 (U columns) on CTA 1
-    tma_load_2d(sB, w, bar, t.n0, y);
-    tma_load_2d(sB + kPanelBytes, w, bar, t.n0 + 64, y);
+    if (t.halfm) {
+      // M = 128 tiles: CTA r holds W1 and W3 columns [n0 + 64 r, +64), so each lane
+      // half of the accumulator has G and U of the same 64 features.
+      tma_load_2d(sB, &m.b0, bar, t.n0 + 64 * r, y);
+      tma_load_2d(sB + kPanelBytes, &m.b1, bar, t.n0 + 64 * r, y);
+    } else {
+      const CUtensorMap* w = r ? &m.b1 : &m.b0;  // W1 (G columns) on CTA 0, W3 (U columns) on CTA 1
+      tma_load_2d(sB, w, bar, t.n0, y);
+      tma_load_2d(sB + kPanelBytes, w, bar, t.n0 + 64, y);
+    }
   } else if (MODE == kFwd2) {
     if (sA != nullptr) tma_load_2d(sA, &m.a, bar, k0, t.row0);
     const int y = t.e * p.F + k0;
@@ -1172,6 +1192,10 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
   constexpr uint32_t kBStep = TR::b_mn ? 2048u : 32u;
   constexpr uint32_t kIdesc256 = idesc_bf16_f32(256, 256, TR::a_mn, TR::b_mn);
   constexpr uint32_t kIdesc128 = idesc_bf16_f32(256, 128, TR::a_mn, TR::b_mn);
+  // M = 128 pair tiles: 64 rows per CTA; the accumulator's lanes 0-63 hold the
+  // first half of the N columns of those rows, lanes 64-127 the second half.
+  constexpr uint32_t kIdescH256 = idesc_bf16_f32(128, 256, TR::a_mn, TR::b_mn);
+  constexpr uint32_t kIdescH128 = idesc_bf16_f32(128, 128, TR::a_mn, TR::b_mn);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1283,8 +1307,14 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
           // A: the warp's 32 lanes gather the tile's 128 rows of x, 4 rows each.
           tma_gather4(sA + lane * 4 * 128, &maps.gx, &full[s], kb * BK, src[0], src[1], src[2], src[3]);
         } else if (elect_one()) {
-          mbar_arrive_expect_tx(&full[s], kABytes + t.nw * 64);
-          load_kblock_pair<MODE>(p, maps, t, kb, sA, sA + kABytes, &full[s], rank);
+          if (t.halfm) {  // M = 128 pair tile: 64 A rows per CTA
+            mbar_arrive_expect_tx(&full[s], kABytes / 2 + t.nw * 64);
+            tma_load_2d(sA, &maps.a64, &full[s], kb * BK, t.row0);
+            load_kblock_pair<MODE>(p, maps, t, kb, nullptr, sA + kABytes, &full[s], rank);
+          } else {
+            mbar_arrive_expect_tx(&full[s], kABytes + t.nw * 64);
+            load_kblock_pair<MODE>(p, maps, t, kb, sA, sA + kABytes, &full[s], rank);
+          }
         }
         __syncwarp();
         issued |= 1u << s;
@@ -1314,7 +1344,7 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
         tc_fence_after();
       }
       const uint32_t d_tmem = tmem_base + acc * kAccStride;
-      const uint32_t idesc = (t.nw == 256) ? kIdesc256 : kIdesc128;
+      const uint32_t idesc = t.halfm ? ((t.nw == 256) ? kIdescH256 : kIdescH128) : (t.nw == 256) ? kIdesc256 : kIdesc128;
       for (int kb = 0; kb < t.kblocks; ++kb) {
         if (!mbar_wait(&full[s], ph, p.ws, 230 + MODE, abort_flag)) {
           ok = false;
@@ -1413,11 +1443,22 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
         }
         continue;
       }
-      if (MODE == kDgrad2 && mine) dgrad2_prefetch(p, maps, t, q, half, lane, st);  // G/U need no accumulator
+      // M = 128 pair tile: lane quarter q holds rows 32 (q & 1) + lane and the
+      // (q >> 1)-th half of the tile's columns, at accumulator columns [0, N/2).
+      Tile te = t;
+      int qe = q;
+      if (t.halfm) {
+        const int hw = ModeTraits<MODE>::paired ? 64 : t.nw / 2;
+        te.n0 = t.n0 + (q >> 1) * hw;
+        if (!ModeTraits<MODE>::paired) te.nw = hw;
+        qe = q & 1;
+      }
+      const bool mine_e = mine && (!t.halfm || 32 * qe < t.nrows);
+      if (MODE == kDgrad2 && mine_e) dgrad2_prefetch(p, maps, te, qe, half, lane, st);  // G/U need no accumulator
       if (!mbar_wait_cluster(&tfull[acc], acc_ph, p.ws, 250 + MODE, abort_flag)) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccStride;
-      if (mine) epilogue<MODE>(p, maps, t, tacc, q, half, lane, st);
+      if (mine_e) epilogue<MODE>(p, maps, te, tacc, qe, half, lane, st);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -2520,11 +2561,21 @@ cudaError_t launch_gemm_pair(GemmMode mode, const GemmLaunch& L, Maps& m, const 
       default: break;
     }
   }
+  // Expert tails of at most 128 rows as M = 128 pair tiles (not with the
+  // gather-fused A, which loads 128 rows, nor with the combine in GEMM2's
+  // epilogue, which counts column halves of whole rows).
+  GemmParams ph = p;
+  if ((mode == kFwd1 && !L.gather) || (mode == kFwd2 && L.cmb.cnt == nullptr) || mode == kDgrad1 || mode == kDgrad2) {
+    const void* a = mode == kFwd1 ? L.Xp : mode == kFwd2 ? L.h : mode == kDgrad2 ? L.dY : L.dGU;
+    const uint64_t K = mode == kFwd1 || mode == kDgrad2 ? H : mode == kFwd2 ? F : 2 * F;
+    if (!make_map(&m.a64, a, K, static_cast<uint64_t>(L.R), 64, 64)) return cudaErrorInvalidValue;
+    ph.halfm_ok = 1;
+  }
   switch (mode) {
-    case kFwd1: return launch_pair_mode<kFwd1>(L, m, p, s, hook);
-    case kFwd2: return launch_pair_mode<kFwd2>(L, m, p, s, hook);
-    case kDgrad2: return launch_pair_mode<kDgrad2>(L, m, p, s, hook);
-    case kDgrad1: return launch_pair_mode<kDgrad1>(L, m, p, s, hook);
+    case kFwd1: return launch_pair_mode<kFwd1>(L, m, ph, s, hook);
+    case kFwd2: return launch_pair_mode<kFwd2>(L, m, ph, s, hook);
+    case kDgrad2: return launch_pair_mode<kDgrad2>(L, m, ph, s, hook);
+    case kDgrad1: return launch_pair_mode<kDgrad1>(L, m, ph, s, hook);
     case kWgrad13: return launch_pair_mode<kWgrad13>(L, m, p, s, hook);
     case kWgrad2: return launch_pair_mode<kWgrad2>(L, m, p, s, hook);
   }
