@@ -1004,7 +1004,6 @@ constexpr int kPairStageBytes = kABytes + kPairBHalfBytes;
 
 template <int MODE>
 struct PairTraits {
-  static constexpr bool wgrad = ModeTraits<MODE>::wgrad;
   static constexpr int kStages = MODE == kDgrad2 ? 5 : 6;  // dgrad2 gives a stage to its G/U chunk ring
   static constexpr int kStagingBytes = kEpiWarps * epi_stage_bytes<MODE>();
   static constexpr int kSmemBytes = kStages * kPairStageBytes + kStagingBytes + 1024 /*align*/ + 512 /*barriers*/;
