@@ -1,7 +1,9 @@
 // Row-wise, HBM-bound steps of the layer: dispatch (a gather by grouped row,
 // or a scatter of each token's row to its k grouped rows when x is large),
 // gated combine, combine backward, dispatch backward.  One warp per row or
-// token, 16-byte vector loads and stores, grid-stride.
+// token (the combine and the dispatch backward split a token's row over several
+// warps when a batch has fewer tokens than warps), 16-byte vector loads and
+// stores, grid-stride.
 //
 // Sources: "UniEP: Unified Expert-Parallel MoE MegaKernel for LLM Training",
 // section 3.1 (Comm-Worker: one warp per token, 128-bit vector loads) and
@@ -74,7 +76,7 @@ __device__ __forceinline__ void zero_padding_rows(const int32_t* __restrict__ ro
 // token to `parts` warps, each over a contiguous range of the row's 16-byte
 // columns, so that more rows are in flight; every output element is still
 // summed by one lane in slot order, so the bits do not change (fine-grained:
-// 23.9 -> 19.9 us; the dispatch backward measured slower split and stays whole).
+// 23.9 -> 19.9 us).
 __device__ __forceinline__ int token_parts(int T, int nwarps) {
   return (T > 0 && nwarps >= 2 * T) ? min(4, nwarps / T) : 1;
 }
@@ -82,7 +84,8 @@ __device__ __forceinline__ int part_span(int hv, int parts) { return ((hv + part
 
 // The dispatch backward launches one wave of CTAs (below); with fewer tokens
 // than warps it splits each token over enough warps that every warp has rows in
-// flight (fine-grained: 4096 tokens on 4864 warps, two parts per token).
+// flight (fine-grained: 4096 tokens on 4864 warps, two parts per token).  Split
+// on a grid of eight CTAs per SM, at 128 registers, it had measured slower.
 __device__ __forceinline__ int unpermute_parts(int T, int nwarps) {
   return T > 0 ? max(1, min(8, (nwarps + T - 1) / T)) : 1;
 }
