@@ -6,7 +6,7 @@ A step is the whole hot path over one batch of synthetic tokens: routing
 GroupGEMM, gated combine, combine backward, both dgrad GroupGEMMs, the
 weight-gradient Transposed GroupGEMMs and the dispatch backward.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 4] [--impl ours|reference]
 
 Prints one JSON line (rank 0).  `value` is tokens/s over all ranks with the
 inputs resident in HBM; `e2e` is the same metric through the C ABI with the
@@ -244,29 +244,87 @@ def barrier(world: int):
 # ---------------------------------------------------------------------------
 # CPU oracle leg
 # ---------------------------------------------------------------------------
-def oracle_sample_inputs(shape, seed, T_s):
-    """First T_s tokens of the workload (same bits as the GPU's), weights as float64 arrays."""
-    import numpy as np
-    import torch
-
-    import moe_synth as S
-    dev = "cuda" if torch.cuda.is_available() else "cpu"
-    full = S.layer_inputs(shape, seed, device=dev)
-    f64 = lambda t: t.detach().to("cpu", torch.float64).numpy()
-    d = {"x": f64(full["x"][:T_s]), "dout": f64(full["dout"][:T_s]),
-         "logits": full["logits"][:T_s].cpu().numpy(),
-         "W": (f64(full["W1"]), f64(full["W3"]), f64(full["W2"]))}
-    del full
-    if dev == "cuda":
-        torch.cuda.empty_cache()
-    return d
+# Workloads whose float64 weights and weight gradients (6 E H F doubles) fit in
+# this much host memory run the oracle's whole step on a prefix of the tokens;
+# larger ones (large-expert, skewed, long-sequence) run its sampled form.
+ORACLE_FULL_BYTES = 12e9
 
 
-def time_oracle_step(inp, shape):
+class OracleWorkload:
+    """The workload's inputs (generated on the GPU when there is one) and the
+    oracle's routing of all of its tokens.  Inputs reach the oracle as float64
+    arrays through the accessors below, whose conversion time is recorded in
+    `conv_s` so the timed oracle work can leave it out."""
+
+    def __init__(self, shape, seed):
+        import torch
+
+        import moe_synth as S
+        self.shape = shape
+        self.dev = "cuda" if torch.cuda.is_available() else "cpu"
+        self.inp = S.layer_inputs(shape, seed, device=self.dev)
+        self.logits = self.inp["logits"].cpu().numpy()
+        self.conv_s = 0.0
+        self.full = 6.0 * shape.E * shape.H * shape.F * 8 <= ORACLE_FULL_BYTES
+        if self.full:
+            self.W = tuple(self._f64(self.inp[n]) for n in ("W1", "W3", "W2"))
+
+    def _f64(self, t):
+        import torch
+        t0 = time.perf_counter()
+        a = t.detach().to("cpu", torch.float64).numpy()
+        self.conv_s += time.perf_counter() - t0
+        return a
+
+    def weights(self, e):
+        return tuple(self._f64(self.inp[n][e]) for n in ("W1", "W3", "W2"))
+
+    def rows(self, name, toks):
+        import torch
+        return self._f64(self.inp[name][torch.as_tensor(toks, device=self.dev)])
+
+    def close(self):
+        del self.inp
+        import torch
+        if torch.cuda.is_available():
+            torch.cuda.empty_cache()
+
+
+def oracle_prefix_step(ow, T_s):
+    """The oracle's whole step (plan, forward, backward with every weight
+    gradient) on the first T_s tokens; returns the oracle's seconds."""
     import oracle.moe_oracle as O
+    sh = ow.shape
+    x = ow._f64(ow.inp["x"][:T_s])
+    dout = ow._f64(ow.inp["dout"][:T_s])
     t0 = time.perf_counter()
-    O.layer_step(inp["x"], inp["logits"], inp["dout"], inp["W"], shape.k, shape.E, mirror=True)
+    O.layer_step(x, ow.logits[:T_s], dout, ow.W, sh.k, sh.E, mirror=True)
     return time.perf_counter() - t0
+
+
+def oracle_sampled_step(ow, toks, experts):
+    """The oracle's sampled step: routing of all T tokens, out/dx/dgate of the
+    tokens `toks` from their own k rows, and the full weight gradients of the
+    experts `experts` over all of their rows.  Returns (oracle seconds, GEMM
+    FLOPs of the sample); input conversion to float64 is not counted."""
+    import oracle.moe_oracle as O
+    sh = ow.shape
+    c0 = ow.conv_s
+    t0 = time.perf_counter()
+    ids, w = O.route(ow.logits, sh.k)
+    perm = O.permutation(ids, sh.E)
+    xr, dr = ow.rows("x", toks), ow.rows("dout", toks)
+    O.token_rows(toks, xr, dr, ids, w, ow.weights, mirror=True)
+    rows = 0
+    for e in experts:
+        O.expert_grads(e, lambda t: ow.rows("x", t), lambda t: ow.rows("dout", t), ids, w, perm, ow.weights,
+                       mirror=True)
+        rows += int(perm.counts[e])
+    t = time.perf_counter() - t0 - (ow.conv_s - c0)
+    # token_rows: forward and dgrad of the tokens' k rows (12 R H F); expert_grads:
+    # forward, dgrad and weight gradients of each expert's rows (18 n_e H F).
+    flops = 12 * len(toks) * sh.k * sh.H * sh.F + 18 * rows * sh.H * sh.F
+    return t, flops
 
 
 def oracle_threads():
@@ -279,6 +337,57 @@ def oracle_threads():
     return os.cpu_count() or 1
 
 
+def _sample_tokens(shape, n, seed):
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    return sorted(rng.choice(shape.T, size=min(n, shape.T), replace=False).tolist())
+
+
+def oracle_rate(ow, budget_s, steps=1, warm=0):
+    """Times `steps` oracle steps, each a bounded sample of about budget_s seconds.
+
+    Returns (tokens/s, seconds per step, description of the sample).  Small
+    workloads run the whole step on a token prefix (tokens/s = prefix / time);
+    large ones run the sampled step, whose tokens/s is the step's T scaled by
+    the sample's share of the step's GEMM FLOPs (18 T k H F)."""
+    import numpy as np
+    sh = ow.shape
+    if ow.full:
+        # A fixed cost plus a part linear in the tokens, fitted from two probes.
+        t_a = oracle_prefix_step(ow, 16)
+        t_b = oracle_prefix_step(ow, 64)
+        slope = max((t_b - t_a) / 48.0, 1e-9)
+        T_s = int(max(16, min(sh.T, 64 + (budget_s - t_b) / slope)))
+        for _ in range(warm):
+            oracle_prefix_step(ow, T_s)
+        t = sum(oracle_prefix_step(ow, T_s) for _ in range(steps))
+        return (T_s * steps / t, t / steps,
+                f"first {T_s} of {sh.T} tokens per step: plan, forward and backward (every weight gradient over "
+                f"those tokens' rows), numpy float64 oracle")
+    step_flops = 18.0 * sh.T * sh.k * sh.H * sh.F
+    counts = np.bincount(np.asarray(ow.logits.argmax(axis=1)), minlength=sh.E)  # probe only: an expert order
+    order = [int(e) for e in np.argsort(-counts, kind="stable")]
+    # Probe: 32 tokens and one expert, then 96 tokens and the same expert.
+    t_a, f_a = oracle_sampled_step(ow, _sample_tokens(sh, 32, 1), order[:1])
+    t_b, f_b = oracle_sampled_step(ow, _sample_tokens(sh, 96, 2), order[:1])
+    slope = max((t_b - t_a) / 64.0, 1e-9)
+    n_tok = int(max(32, min(sh.T, 96 + (budget_s - t_b) / slope)))
+    for i in range(warm):
+        oracle_sampled_step(ow, _sample_tokens(sh, n_tok, 100 + i), order[i % len(order): i % len(order) + 1])
+    t = fl = 0.0
+    for i in range(steps):
+        dt, df = oracle_sampled_step(ow, _sample_tokens(sh, n_tok, 200 + i),
+                                     order[(i + 1) % len(order): (i + 1) % len(order) + 1])
+        t += dt
+        fl += df
+    value = sh.T * (fl / step_flops) / t
+    return (value, t / steps,
+            f"sampled step: routing of all {sh.T} tokens, out/dx/dgate of {n_tok} seeded tokens from their own "
+            f"{sh.k} rows, and the full weight gradients of one expert per step (forward, dgrad and weight "
+            f"gradients over all its rows); tokens/s = T x (sample GEMM FLOPs / step GEMM FLOPs 18 T k H F) / "
+            f"oracle seconds; numpy float64 oracle, float64 input conversion not timed")
+
+
 def run_reference(args):
     import moe_synth as S
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -286,32 +395,19 @@ def run_reference(args):
     if rank != 0:
         return
     shape = S.CONFIGS[args.config]
-    seed = S.config_seed(args.config)
     steps, warm = args.steps, args.warmup
     # Size the sample so the whole run stays within a few minutes.
     budget = min(8.0, 150.0 / max(1, steps + warm))
-    inp = oracle_sample_inputs(shape, seed, shape.T)
-    sub = lambda n: dict(inp, x=inp["x"][:n], dout=inp["dout"][:n], logits=inp["logits"][:n])
-    # Fixed cost plus a part linear in the tokens, fitted from two probes.
-    t_a = time_oracle_step(sub(16), shape)
-    t_b = time_oracle_step(sub(64), shape)
-    slope = max((t_b - t_a) / 48.0, 1e-9)
-    T_s = int(max(16, min(shape.T, 64 + (budget - t_b) / slope)))
-    sample = sub(T_s)
-    for _ in range(warm):
-        time_oracle_step(sample, shape)
-    t = 0.0
-    for _ in range(steps):
-        t += time_oracle_step(sample, shape)
-    value = T_s * steps / t
+    ow = OracleWorkload(shape, S.config_seed(args.config))
+    value, sec, sample = oracle_rate(ow, budget, steps=steps, warm=warm)
+    ow.close()
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
-        "warmup": warm, "ms_per_step": 1000.0 * t / steps, "higher_is_better": True, "scaling": "weak",
+        "warmup": warm, "ms_per_step": 1000.0 * sec, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(shape, args.config),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
-                         "sample": f"first {T_s} of {shape.T} tokens per step (plan + forward + backward incl. "
-                                   f"weight gradients over those tokens' rows), numpy float64 oracle"},
+                         "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -644,11 +740,10 @@ def run_ours(args):
         "config": dict(workload_config(shape, args.config), parallelism=f"replicas x{world}" if world > 1 else "1 GPU",
                        schedule={0: "one persistent launch per phase", 1: "fused persistent forward, per-GEMM backward",
                                  2: "fused forward, fused backward"}[args.schedule],
-                       gemm_tiles={0: "two-CTA 256x256 pair tiles (cta_group::2) except dgrad2: 128x256 single-CTA",
+                       gemm_tiles={0: "two-CTA 256x256 pair tiles (cta_group::2); dgrad2 on 128x256 single-CTA "
+                                      "tiles unless experts average >= 2048 rows",
                                    1: "single-CTA 128x256 tiles (cta_group::1)",
-                                   2: "two-CTA 256x256 pair tiles (cta_group::2)",
-                                   4: "pair tiles; forward and dgrad GEMM1 in 4-CTA clusters sharing A by TMA "
-                                      "multicast; dgrad2: 128x256 single-CTA"}[args.cta_pair],
+                                   2: "two-CTA 256x256 pair tiles (cta_group::2)"}[args.cta_pair],
                        router="on the path: logits = x Wr on the GPU, gradient through the gating (dlogits, dWr, "
                               "dx share)" if args.router else "off (logits given; the pages time the layer "
                                                                "excluding gating)",
@@ -691,18 +786,11 @@ def run_ours(args):
 def cpu_baseline(shape, idx):
     """The oracle, as it stands, on a bounded sample of the same workload (~10-30 s)."""
     import moe_synth as S
-    inp = oracle_sample_inputs(shape, S.config_seed(idx), shape.T)
-    sub = lambda n: dict(inp, x=inp["x"][:n], dout=inp["dout"][:n], logits=inp["logits"][:n])
-    # The oracle's cost is a fixed part (per-expert weight arrays) plus a part
-    # linear in the tokens: fit both from two probes and size the sample for ~12 s.
-    t_a = time_oracle_step(sub(64), shape)
-    t_b = time_oracle_step(sub(256), shape)
-    slope = max((t_b - t_a) / 192.0, 1e-9)
-    T_s = int(max(256, min(shape.T, 256 + (12.0 - t_b) / slope)))
-    t = time_oracle_step(sub(T_s), shape)
-    return {"value": round(T_s / t, 2), "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
-            "sample": f"first {T_s} of {shape.T} tokens (plan + forward + backward incl. weight gradients over "
-                      f"those tokens' rows), numpy float64 oracle, {t:.1f} s"}
+    ow = OracleWorkload(shape, S.config_seed(idx))
+    value, sec, sample = oracle_rate(ow, 12.0)
+    ow.close()
+    return {"value": round(value, 2), "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
+            "sample": f"{sample}; {sec:.1f} s"}
 
 
 def main():
@@ -710,13 +798,15 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--config", type=int, default=4,
+                    help="workload index: 0 tiny, 1 fine-grained, 2 large-expert, 3 skewed, 4 long-sequence "
+                         "(default: the largest that fits one GPU)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--schedule", type=int, default=0, choices=[0, 1, 2],
                     help="0: one persistent launch per phase; 1: fused persistent forward, one persistent "
                          "kernel per backward GEMM; 2: fused forward and fused backward")
-    ap.add_argument("--cta-pair", type=int, default=0, choices=[0, 1, 2, 4],
+    ap.add_argument("--cta-pair", type=int, default=0, choices=[0, 1, 2],
                     help="grouped GEMMs that run as their own kernels: 0 library default (pair tiles but for "
                          "dgrad2), 1 one CTA per tile, 2 two-CTA pair tiles")
     ap.add_argument("--combine", type=int, default=0, choices=[0, 1],

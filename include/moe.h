@@ -139,10 +139,7 @@ typedef struct {
                        0 (default): 2 for every GEMM but the dgrad GEMM with the SwiGLU backward
                        epilogue, which measured faster with 1 unless the experts average at least
                        2048 rows (T*k >= 2048*E).  Both shapes give the same bits.
-                       4: as 0, and the pair-tile forward GEMMs and dgrad GEMM1 run in clusters
-                       of four CTAs: two pairs on the same 256 rows and neighbouring N tiles,
-                       each CTA loading half of its A rows and multicasting them to its
-                       counterpart in the other pair (a quarter less L2-to-SM traffic).
+                       Other values: MOE_ERR_ARG.
                        The fused forward (schedules 1, 2) takes pair tiles unless cta_pair = 1;
                        the fused backward (schedule 2) always uses single-CTA tiles. */
   int32_t combine;  /* schedule 0 only.  0 (default): a separate gated-combine kernel.
@@ -244,7 +241,9 @@ MOE_API int moe_router_forward(moe_dims d, const void *x, const void *Wr, float 
  * and index reported it (may be NULL).  Returns 0 or MOE_ERR_LAUNCH. */
 MOE_API int moe_get_status(void *ws, void *stream, int32_t *device_status, int32_t *where, int32_t *detail);
 
-/* Clears the status word (asynchronous on stream). */
+/* Clears the status words (status, where, detail: the first 12 bytes of `ws`),
+ * asynchronously on stream.  Safe on a workspace and on moe_plan_noalloc's
+ * 4-int32 status buffer. */
 MOE_API int moe_clear_status(void *ws, void *stream);
 
 /* ---- routing without a workspace ------------------------------------------------ */
@@ -267,12 +266,16 @@ MOE_API int moe_clear_status(void *ws, void *stream);
  *   - Limit: dims whose scratch exceeds the buffer (roughly
  *     ceil(T/256) * E * 40 bytes plus alignment) return MOE_ERR_TOO_LARGE
  *     before anything is launched; e.g. T = 131072 with E = 128 fits.
- *   - status: device pointer to 4 int32 (caller-owned, zero before first use);
- *     the first device-detected error is recorded there as in a workspace and
- *     is read and cleared by moe_get_status(status, ...).
- *   - Set-up: the first call on each device looks up the array's device
- *     address (with that device current) and caches it; make that first call
- *     before any stream capture.
+ *   - status: device pointer to 4 int32 (16 bytes, caller-owned, zero before
+ *     first use); the first device-detected error is recorded in its first
+ *     three words as in a workspace.  moe_get_status(status, ...) reads and
+ *     clears it and moe_clear_status(status, ...) clears it; both touch only
+ *     those three words.
+ *   - Set-up: the first call in each CUDA context (per device, and again after
+ *     cudaDeviceReset or in another context of the same device) looks up the
+ *     array's device address with that context current and caches it, keyed
+ *     on the context's unique id; make that first call before any stream
+ *     capture.
  *   - Every call uses the same array and leaves its contents behind; each
  *     call clears the words that must start at zero (the per-chunk counts)
  *     with an asynchronous memset on `stream` before its kernels run.  Calls

@@ -1142,49 +1142,9 @@ __device__ __forceinline__ void load_kblock_pair(const GemmParams& p, const Maps
   }
 }
 
-// Clusters of four CTAs (CL = 4): two pairs that share the A rows of a
-// super-tile, the same 256 rows of one expert, with pair 0 on N tile 2j and
-// pair 1 on N tile 2j + 1.  Each CTA loads half of its 128 A rows and the TMA
-// multicast delivers them to the CTA with the same rows in the other pair, so
-// the L2 -> SM traffic per MMA drops by a quarter.  With an odd number of N
-// tiles, pair 1 repeats N tile 2j of the last super-tile and stores nothing.
-template <int MODE, int CL>
-__device__ __forceinline__ int cl_n_tiles(const GemmParams& p, const int* pairs) {
-  if (CL == 2) return pair_n_tiles<MODE>(p, pairs);
-  return pairs[p.E] * ((n_ntiles<MODE>(p) + 1) / 2);
-}
-
-template <int MODE, int CL>
-__device__ __forceinline__ Tile cl_decode(const GemmParams& p, const ExpertTables& x, int tile, uint32_t rank,
-                                          bool& dummy) {
-  dummy = false;
-  if (CL == 2) return pair_decode<MODE>(p, x, tile, rank);
-  const int nn = n_ntiles<MODE>(p), nn2 = (nn + 1) / 2;
-  int lo = 0, hi = p.E;  // the last e with pairs[e] * nn2 <= tile (empty experts own no super-tiles)
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (x.pairs[mid] * nn2 <= tile)
-      lo = mid;
-    else
-      hi = mid;
-  }
-  const int first = x.pairs[lo];
-  const int cnt = x.pairs[lo + 1] - first;
-  const int local = tile - nn2 * first;
-  const int j = local / cnt;
-  const int mp = local - j * cnt;  // M pairs fastest, as in the pair order
-  int nt = 2 * j + static_cast<int>(rank >> 1);
-  if (nt >= nn) {
-    nt = 2 * j;
-    dummy = true;
-  }
-  return pair_decode<MODE>(p, x, nn * first + nt * cnt + mp, rank & 1u);
-}
-
-template <int MODE, int CL>
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_constant__ Maps maps,
                                                                 const GemmParams p) {
-  static_assert(CL == 2 || (CL == 4 && !ModeTraits<MODE>::wgrad), "4-CTA clusters: forward and dgrad modes");
   using TR = ModeTraits<MODE>;
   constexpr int S = PairTraits<MODE>::kStages;
   constexpr uint32_t kAStep = TR::a_mn ? 2048u : 32u;
@@ -1222,19 +1182,16 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t crank = cluster_ctarank();  // rank in the cluster
-  const uint32_t rank = crank & 1u;           // rank in the pair
+  const uint32_t rank = cluster_ctarank();  // rank in the pair
   const bool leader = (rank == 0);
-  const uint32_t pair_leader = crank & ~1u;
-  // A stage is free once every pair that reads it has committed: with CL = 4 the
-  // A rows arrive by multicast in both pairs, so both leaders' commits count.
-  constexpr uint16_t kEmptyMask = CL == 4 ? 0xF : 0x3;
-  const uint16_t tfull_mask = static_cast<uint16_t>(0x3u << pair_leader);
+  constexpr uint32_t pair_leader = 0;
+  constexpr uint16_t kEmptyMask = 0x3;  // commits arrive in both CTAs of the pair
+  constexpr uint16_t tfull_mask = 0x3;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], CL / 2);
+      mbar_init(&empty[i], 1);
       mbar_init(&pfull[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -1258,9 +1215,9 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
   cluster_sync();  // both CTAs' barriers exist before any remote arrive
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int ntiles = cl_n_tiles<MODE, CL>(p, xt.pairs);
-  const int npairs = gridDim.x / CL;  // clusters
-  const int pid = blockIdx.x / CL;
+  const int ntiles = pair_n_tiles<MODE>(p, xt.pairs);
+  const int npairs = gridDim.x / 2;  // clusters
+  const int pid = blockIdx.x / 2;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer (every CTA)
@@ -1269,9 +1226,8 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
     uint32_t issued = 0, last_parity = 0;
     bool ok = true;
     for (int tile = pid; tile < ntiles && ok; tile += npairs) {
-      bool dummy;
-      const Tile t = cl_decode<MODE, CL>(p, xt, tile, crank, dummy);
-      const bool gather = (MODE == kFwd1) && CL == 2 && p.gather;
+      const Tile t = pair_decode<MODE>(p, xt, tile, rank);
+      const bool gather = (MODE == kFwd1) && p.gather;
       int src[4] = {0, 0, 0, 0};  // gather: tokens of this lane's 4 rows (rows past R read token 0, never stored)
       if (gather) {
 #pragma unroll
@@ -1287,17 +1243,7 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
           break;
         }
         uint8_t* sA = smem + s * kPairStageBytes;
-        if (CL == 4) {
-          // Half of this CTA's 128 A rows, multicast to the CTA with the same rows in
-          // the other pair; B (this pair's N tile) as usual.
-          if (elect_one()) {
-            mbar_arrive_expect_tx(&full[s], kABytes + t.nw * 64);
-            const int hv = static_cast<int>(crank >> 1);
-            tma_load_2d_mc(sA + hv * (kABytes / 2), &maps.a64, &full[s], kb * BK, t.row0 + 64 * hv,
-                           static_cast<uint16_t>(0x5u << rank));
-            load_kblock_pair<MODE>(p, maps, t, kb, nullptr, sA + kABytes, &full[s], rank);
-          }
-        } else if (gather) {
+        if (gather) {
           if (elect_one()) {
             mbar_arrive_expect_tx(&full[s], kABytes + t.nw * 64);
             load_kblock_pair<MODE>(p, maps, t, kb, nullptr, sA + kABytes, &full[s], rank);  // B only
@@ -1335,8 +1281,7 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
     bool ok = true;
     const uint32_t pfull_leader = mapa_shared(smem_u32(pfull), pair_leader);
     for (int tile = pid; tile < ntiles && ok; tile += npairs) {
-      bool dummy;
-      const Tile t = cl_decode<MODE, CL>(p, xt, tile, crank, dummy);
+      const Tile t = pair_decode<MODE>(p, xt, tile, rank);
       if (t.kblocks == 0) continue;  // empty expert (weight gradients): the epilogue writes zeros
       if (leader) {
         if (!mbar_wait_cluster(&tempty[acc], acc_ph ^ 1u, p.ws, 220 + MODE, abort_flag)) break;
@@ -1358,7 +1303,7 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
         }
         // Gathered A rows of a row block's first N tile go out to Xp (the backward
         // reads them); the store reads the stage before the stage is released.
-        const bool store_xp = (MODE == kFwd1) && CL == 2 && p.gather && t.n0 == 0 && t.nrows > 0;
+        const bool store_xp = (MODE == kFwd1) && p.gather && t.n0 == 0 && t.nrows > 0;
         __syncwarp();
         if (!leader) {
           if (lane == 0) {
@@ -1410,7 +1355,7 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
       acc ^= 1;
       if (acc == 0) acc_ph ^= 1u;
     }
-    if ((MODE == kFwd1) && CL == 2 && p.gather) bulk_wait_all();  // Xp stores complete before exit (any lane)
+    if ((MODE == kFwd1) && p.gather) bulk_wait_all();  // Xp stores complete before exit (any lane)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs, own rows)
@@ -1425,9 +1370,8 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
     int acc = 0;
     uint32_t acc_ph = 0;
     for (int tile = pid; tile < ntiles; tile += npairs) {
-      bool dummy;
-      const Tile t = cl_decode<MODE, CL>(p, xt, tile, crank, dummy);
-      const bool mine = TR::wgrad ? (t.m0 < mext) : (t.nrows > 0 && !dummy);
+      const Tile t = pair_decode<MODE>(p, xt, tile, rank);
+      const bool mine = TR::wgrad ? (t.m0 < mext) : (t.nrows > 0);
       if (t.kblocks == 0) {
         if (TR::wgrad && mine && p.sb != 2) {  // an empty second sub-batch leaves the first one's values
           const int NCall = (MODE == kWgrad13) ? 128 : t.nw;
@@ -2493,17 +2437,17 @@ cudaError_t launch_mode(const GemmLaunch& L, const Maps& maps, const GemmParams&
   return cudaGetLastError();
 }
 
-template <int MODE, int CL = 2>
+template <int MODE>
 cudaError_t launch_pair_mode(const GemmLaunch& L, const Maps& maps, const GemmParams& p, cudaStream_t s,
                              LaunchHook& hook) {
   const int kSmem = PairTraits<MODE>::kSmemBytes + (ModeTraits<MODE>::wgrad ? 0 : static_cast<int>(pair_table_bytes(L.E)));
-  auto kern = pair_gemm_kernel<MODE, CL>;
+  auto kern = pair_gemm_kernel<MODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -2515,7 +2459,7 @@ cudaError_t launch_pair_mode(const GemmLaunch& L, const Maps& maps, const GemmPa
   static int max_pairs = -1, max_pairs_smem = -1;
   if (max_pairs < 0 || max_pairs_smem != kSmem) {
     max_pairs_smem = kSmem;
-    cfg.gridDim = dim3(CL, 1, 1);
+    cfg.gridDim = dim3(2, 1, 1);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
       (void)cudaGetLastError();
@@ -2523,10 +2467,10 @@ cudaError_t launch_pair_mode(const GemmLaunch& L, const Maps& maps, const GemmPa
     }
     max_pairs = n;
   }
-  int pairs = L.grid / CL;
+  int pairs = L.grid / 2;
   if (pairs < 1) pairs = 1;
   if (max_pairs > 0 && pairs > max_pairs) pairs = max_pairs;
-  cfg.gridDim = dim3(CL * pairs, 1, 1);
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
   hook.before(s);
   e = cudaLaunchKernelEx(&cfg, kern, maps, p);
   hook.after(s);
@@ -2546,20 +2490,6 @@ cudaError_t launch_gemm_pair(GemmMode mode, const GemmLaunch& L, Maps& m, const 
     ok = make_map(&m.b0, L.W1, F, E * H, 64, 128) && make_map(&m.b1, L.W3, F, E * H, 64, 128) &&
          make_map(&m.b2, L.W1, F, E * H, 64, 64) && make_map(&m.b3, L.W3, F, E * H, 64, 64);
   if (!ok) return cudaErrorInvalidValue;
-  // Clusters of two pairs sharing A by multicast (not with the gather-fused A).
-  const bool quad = L.quad && !(mode == kFwd1 && L.gather) && mode != kWgrad13 && mode != kWgrad2;
-  if (quad) {
-    const void* a = mode == kFwd1 ? L.Xp : mode == kFwd2 ? L.h : mode == kDgrad2 ? L.dY : L.dGU;
-    const uint64_t K = mode == kFwd1 || mode == kDgrad2 ? H : mode == kFwd2 ? F : 2 * F;
-    if (!make_map(&m.a64, a, K, static_cast<uint64_t>(L.R), 64, 64)) return cudaErrorInvalidValue;
-    switch (mode) {
-      case kFwd1: return launch_pair_mode<kFwd1, 4>(L, m, p, s, hook);
-      case kFwd2: return launch_pair_mode<kFwd2, 4>(L, m, p, s, hook);
-      case kDgrad2: return launch_pair_mode<kDgrad2, 4>(L, m, p, s, hook);
-      case kDgrad1: return launch_pair_mode<kDgrad1, 4>(L, m, p, s, hook);
-      default: break;
-    }
-  }
   // Expert tails of at most 128 rows as M = 128 pair tiles (not with the
   // gather-fused A, which loads 128 rows, nor with the combine in GEMM2's
   // epilogue, which counts column halves of whole rows).

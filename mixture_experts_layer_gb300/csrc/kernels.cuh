@@ -148,7 +148,6 @@ struct GemmLaunch {
   int T, H, F, E, k, R;
   int grid;
   int pair;  // 1: two-SM pair tiles (cta_group::2), 0: one CTA per 128-row tile
-  int quad;  // with pair: clusters of two pairs sharing the A rows by TMA multicast (forward and dgrad modes)
   const int32_t* tiles;
   const int32_t* pairs;  // first 256-row pair of each expert (tiles + tiles_pair_base)
   const int32_t* offsets;

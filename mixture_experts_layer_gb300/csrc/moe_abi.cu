@@ -192,9 +192,6 @@ int use_pair(const moe_opts* o, GemmMode m, const moe_dims& d) {
   return 1;
 }
 
-// cta_pair = 4: the pair-tile forward and dgrad GEMMs run in clusters of two
-// pairs that share their A rows by TMA multicast.
-int use_quad(const moe_opts* o) { return o != nullptr && o->cta_pair == 4; }
 
 const char* const kPlanKernels[] = {"route_topk", "route_scan", "route_rank", nullptr};
 const char* const kFwdKernelsFused[] = {"fused_forward", "combine", nullptr};
@@ -324,7 +321,7 @@ int moe_forward(moe_dims d, const void* x, const void* W1, const void* W3, const
   if (rc) return rc;
   if ((rc = check_ws(d, ws, ws_bytes))) return rc;
   if (opts != nullptr && (opts->schedule < 0 || opts->schedule > 2 || opts->grid < 0 || opts->cta_pair < 0 ||
-                          opts->cta_pair > 4 || opts->cta_pair == 3 || opts->combine < 0 || opts->combine > 1 || opts->debug_drop_task < 0 ||
+                          opts->cta_pair > 2 || opts->combine < 0 || opts->combine > 1 || opts->debug_drop_task < 0 ||
                           opts->dispatch < 0 || opts->dispatch > 2))
     return MOE_ERR_ARG;
   if (d.T == 0) return MOE_OK;
@@ -343,7 +340,6 @@ int moe_forward(moe_dims d, const void* x, const void* W1, const void* W3, const
   r.rows_used = plan->offsets + d.E;
   r.pad = d.pad;
   GemmLaunch g = gemm_common(d, plan, wsh, grid);
-  g.quad = use_quad(opts);
   g.Xp = saved->Xp;
   g.W1 = W1;
   g.W3 = W3;
@@ -398,7 +394,7 @@ int moe_backward(moe_dims d, const void* dout, const void* W1, const void* W3, c
   if (rc) return rc;
   if ((rc = check_ws(d, ws, ws_bytes))) return rc;
   if (opts != nullptr && (opts->schedule < 0 || opts->schedule > 2 || opts->grid < 0 || opts->cta_pair < 0 ||
-                          opts->cta_pair > 4 || opts->cta_pair == 3 || opts->combine < 0 || opts->combine > 1 || opts->debug_drop_task < 0 ||
+                          opts->cta_pair > 2 || opts->combine < 0 || opts->combine > 1 || opts->debug_drop_task < 0 ||
                           opts->wgrad_subbatches < 0 || opts->wgrad_subbatches > 2 ||
                           (opts->wgrad_subbatches == 2 && opts->schedule == 2)))
     return MOE_ERR_ARG;
@@ -452,7 +448,6 @@ int moe_backward(moe_dims d, const void* dout, const void* W1, const void* W3, c
   if (e != cudaSuccess) return MOE_ERR_LAUNCH;
 
   GemmLaunch g = gemm_common(d, plan, wsh, grid);
-  g.quad = use_quad(opts);
   g.W1 = W1;
   g.W3 = W3;
   g.W2 = W2;
@@ -550,7 +545,9 @@ int moe_get_status(void* ws, void* stream, int32_t* device_status, int32_t* wher
 
 int moe_clear_status(void* ws, void* stream) {
   if (ws == nullptr) return MOE_ERR_ARG;
-  return cudaMemsetAsync(ws, 0, sizeof(WsHeader), static_cast<cudaStream_t>(stream)) == cudaSuccess
+  // Only the three status words (status, where, detail): the call is also used
+  // on moe_plan_noalloc's 16-byte status buffer.
+  return cudaMemsetAsync(ws, 0, 3 * sizeof(int32_t), static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? MOE_OK
              : MOE_ERR_LAUNCH;
 }

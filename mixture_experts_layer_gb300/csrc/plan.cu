@@ -738,8 +738,15 @@ cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t s, LaunchHook& hook) {
 // of the three routing kernels (per-chunk counts, bases and bitmaps) lives in
 // the file-scope array below.  Host code must not use the array's name as a
 // device address: it only names a host-side stand-in.  The device address is
-// looked up once per device with cudaGetSymbolAddress (with that device
-// current) and passed to the kernels like any workspace pointer.
+// looked up with cudaGetSymbolAddress (with the device current) and passed to
+// the kernels like any workspace pointer.
+//
+// The address belongs to one CUDA context: another context on the same device
+// (a driver-API context an engine creates, or the primary context recreated
+// after cudaDeviceReset) holds its own copy of the array at another address.
+// The lookup is therefore cached per context, keyed on the context's unique id
+// (cuCtxGetId: ids are never reused within a process, unlike context handles),
+// and redone for every context not seen before.
 // ---------------------------------------------------------------------------
 #include <mutex>
 
@@ -747,31 +754,74 @@ namespace moe {
 namespace {
 
 constexpr size_t kNoAllocBytes = MOE_NOALLOC_SCRATCH_BYTES;
-constexpr int kNoAllocMaxDevices = 64;
+constexpr int kNoAllocCache = 64;
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocBytes];
 
 std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+struct NoAllocEntry {
+  unsigned long long ctx_id;
+  void* ptr;
+};
+NoAllocEntry g_noalloc_cache[kNoAllocCache];
+int g_noalloc_used = 0, g_noalloc_next = 0;
 
 size_t na_align(size_t v) { return (v + 255) & ~size_t(255); }
 
-// Device address of g_noalloc_scratch on the current device (looked up once).
+// Unique id of the calling thread's current context (0 if none or unknown).
+unsigned long long current_ctx_id() {
+  using GetCurrentFn = CUresult (*)(CUcontext*);
+  using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static bool resolved = false;
+  if (!resolved) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(f);
+    resolved = true;
+  }
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of g_noalloc_scratch in the current context (looked up once
+// per context; the lookup itself makes the device's primary context current
+// when the thread has none yet).
 int noalloc_scratch(void** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return MOE_ERR_LAUNCH;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_LAUNCH;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return MOE_ERR_LAUNCH;
+  if (major != 10 || minor != 3) return MOE_ERR_DEVICE;
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (g_noalloc_ptr[dev] == nullptr) {
-    int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-      return MOE_ERR_LAUNCH;
-    if (major != 10 || minor != 3) return MOE_ERR_DEVICE;
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_LAUNCH;
-    g_noalloc_ptr[dev] = p;
+  unsigned long long id = current_ctx_id();
+  if (id != 0)
+    for (int i = 0; i < g_noalloc_used; ++i)
+      if (g_noalloc_cache[i].ctx_id == id) {
+        *out = g_noalloc_cache[i].ptr;
+        return MOE_OK;
+      }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_LAUNCH;
+  if (id == 0) id = current_ctx_id();  // the lookup may have made the primary context current
+  if (id != 0) {
+    const int slot = g_noalloc_used < kNoAllocCache ? g_noalloc_used++ : (g_noalloc_next++ % kNoAllocCache);
+    g_noalloc_cache[slot] = NoAllocEntry{id, p};
   }
-  *out = g_noalloc_ptr[dev];
+  *out = p;
   return MOE_OK;
 }
 

@@ -1,7 +1,8 @@
 """Bitwise reproducibility of the GPU path.
 
 Outputs, weight gradients and tables must be bitwise identical over 10
-repeated runs and across persistent grid sizes (74 CTAs and one per SM):
+repeated runs and across persistent grid sizes (74 and 148 CTAs, one per SM
+of this GPU, and a single CTA):
 every output tile has one owner and a fixed reduction order ("UniEP: Unified
 Expert-Parallel MoE MegaKernel for LLM Training", section 6, Bitwise
 Equivalence Verification: max_diff = 0 and 0% non-bitwise elements).
@@ -10,7 +11,7 @@ import pytest
 import torch
 
 import moe_synth as S
-from helpers import poison, run_gpu, shape_inputs
+from helpers import check_backward, check_forward, check_tables, poison, run_gpu, run_oracle, shape_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -40,7 +41,7 @@ def test_bitwise_over_runs_and_grids(shape, seed):
     run_gpu(layer, inp)
     ref = _snapshot(layer)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    runs = [0] * 9 + [74, sms, 1]
+    runs = [0] * 9 + [74, 148, sms, 1]
     for g in runs:
         opts = layer.opts(grid=g) if g else None
         for n in OUTS:  # poison: a kernel that skipped work cannot pass
@@ -92,3 +93,24 @@ def test_combine_in_gemm2_epilogue_is_bitwise(shape, seed):
         L.out.fill_(float("nan"))
         run_gpu(L, inp, opts=L.opts(grid=g, combine=1))
         assert torch.equal(L.out, ref.out), f"out differs at grid {g}"
+
+
+@pytest.mark.parametrize("shape,seed", [(S.LayerShape(700, 384, 640, 6, 2), 35), (S.LayerShape(300, 256, 128, 4, 4), 36),
+                                        (S.LayerShape(512, 256, 256, 32, 4), 38)])
+def test_combine_in_gemm2_epilogue_matches_oracle(shape, seed):
+    """The gated combine run in GEMM2's epilogue against the oracle's combine
+    (out[t] = sum over the k slots, in slot order, of w[t,j] Y[dest[t,j]];
+    "UniEP", section 3, Top-k accumulation constraint), on its own: tables,
+    the forward's saved tensors and out, and the backward that reads them,
+    from NaN-poisoned buffers, on shapes with ragged and empty experts."""
+    from mixture_experts_layer_gb300.layer import MoELayer
+    inp = shape_inputs(shape, seed)
+    if shape.E == 32:
+        inp["logits"][:, :8] -= 40.0  # eight empty experts
+    L = MoELayer(shape.T, shape.H, shape.F, shape.E, shape.k)
+    poison(L)
+    run_gpu(L, inp, opts=L.opts(combine=1))
+    ref = run_oracle(inp, shape.k, shape.E)
+    check_tables(L, ref)
+    check_forward(L, ref)
+    check_backward(L, ref)

@@ -4,9 +4,10 @@ configuration the benchmark times (one persistent CTA per SM).
 * fine-grained (T=4096, H=2048, F=1408, E=64, k=6): every element of every
   output against the full oracle;
 * large-expert and skewed (T=4096, H=7168, F=2048, E=256, k=8): routing tables
-  bit-exact, a seeded sample of tokens' out/dx/dgate, and the full weight
-  gradients of seeded experts (the hottest one and an empty one on the skewed
-  layer);
+  bit-exact, 512 seeded tokens' out/dx/dgate, and the full weight gradients of
+  at least four experts: the hottest, the coldest non-empty one and two seeded
+  ones (plus, on the skewed layer, two of its empty experts, whose gradients
+  must be exact zeros);
 * long-sequence (T=131072, H=4096, F=1536, E=128, k=8): tables bit-exact, 512
   seeded tokens' out/dx/dgate and the full weight gradients of 4 seeded experts.
 """
@@ -80,17 +81,25 @@ def _sampled(idx, n_tokens, experts_fn):
         assert_close(f"dW2[{e}]", layer.dW2[e], g["dW2"])
 
 
+def _hot_cold_and_seeded(c, rng, n_seeded=2):
+    """The hottest expert, the coldest non-empty one and n_seeded other non-empty ones."""
+    live = np.flatnonzero(c > 0)
+    hot = int(live[np.argmax(c[live])])
+    cold = int(live[np.argmin(c[live])])
+    rest = [int(e) for e in live if e not in (hot, cold)]
+    return [hot, cold] + sorted(rng.choice(rest, n_seeded, replace=False).tolist())
+
+
 def test_large_expert_sampled():
-    _sampled(2, 24, lambda c, rng: sorted(rng.choice(len(c), 3, replace=False).tolist()))
+    _sampled(2, 512, _hot_cold_and_seeded)
 
 
 def test_skewed_sampled():
     def pick(c, rng):
-        hot = int(np.argmax(c))
-        empty = int(np.flatnonzero(c == 0)[0])
         assert (c == 0).sum() >= 16
-        return [hot, empty, int(rng.choice(np.flatnonzero(c > 0)))]
-    _sampled(3, 24, pick)
+        empty = np.flatnonzero(c == 0)
+        return _hot_cold_and_seeded(c, rng) + [int(empty[0]), int(empty[-1])]
+    _sampled(3, 512, pick)
 
 
 def test_long_sequence_sampled():

@@ -107,42 +107,3 @@ def test_fused_forward_pair_tiles_bitwise(shape, seed):
             if n in ("Xp", "GU", "h", "Y"):
                 a, b = a[: L.R], b[: L.R]
             assert torch.equal(a, b), f"{n} differs (grid {g}, cta_pair {pair})"
-
-
-@pytest.mark.parametrize("name", ["tiny", "ragged", "odd_extents", "multi_tile", "one_token", "empty_experts"])
-def test_cluster4_tiles_match_oracle(name):
-    """cta_pair = 4: the pair-tile forward GEMMs and dgrad GEMM1 in clusters of two
-    pairs sharing their A rows by TMA multicast (odd N tile counts leave the second
-    pair a repeated tile that stores nothing)."""
-    from mixture_experts_layer_gb300.layer import MoELayer
-    shape, seed, n_empty = CASES[name]
-    inp = _inputs(shape, seed, n_empty)
-    layer = MoELayer(shape.T, shape.H, shape.F, shape.E, shape.k)
-    poison(layer)
-    run_gpu(layer, inp, opts=layer.opts(schedule=0, cta_pair=4))
-    ref = run_oracle(inp, shape.k, shape.E)
-    check_tables(layer, ref)
-    check_forward(layer, ref)
-    check_backward(layer, ref)
-
-
-@pytest.mark.parametrize("shape,seed", [(S.CONFIGS[1], S.config_seed(1)), (S.LayerShape(700, 384, 640, 6, 2), 46),
-                                        (S.LayerShape(900, 256, 256, 24, 4), 47)])
-def test_cluster4_tiles_give_the_bits_of_pair_tiles(shape, seed):
-    """Same MMA chain per tile: the 4-CTA clusters give the bits of the pair tiles,
-    over grids of 4, 76 and one CTA per SM."""
-    from mixture_experts_layer_gb300.layer import MoELayer
-    inp = shape_inputs(shape, seed)
-    if shape.E == 24:
-        inp["logits"][:, :5] -= 40.0
-    a = MoELayer(shape.T, shape.H, shape.F, shape.E, shape.k)
-    run_gpu(a, inp, opts=a.opts(schedule=0, cta_pair=0))
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    b = MoELayer(shape.T, shape.H, shape.F, shape.E, shape.k)
-    for g in (0, 4, 76, sms):
-        for n in OUTS:
-            getattr(b, n).fill_(float("nan"))
-        run_gpu(b, inp, opts=b.opts(grid=g, schedule=0, cta_pair=4))
-        for n in OUTS:
-            md, frac = _diff(getattr(a, n), getattr(b, n))
-            assert md == 0 and frac == 0, f"{n} differs at grid {g or sms}: max_diff={md} non-bw={frac:.2%}"
