@@ -434,6 +434,11 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     shape = S.CONFIGS[args.config]
+    if args.shape:
+        if not args.profile:
+            raise SystemExit("--shape is for profiler captures (with --profile)")
+        T, H, F, E, k = (int(v) for v in args.shape.split(","))
+        shape = S.LayerShape(T, H, F, E, k, f"shape-T{T}-H{H}-F{F}-E{E}-k{k}")
     T, H, F, E, k = shape.T, shape.H, shape.F, shape.E, shape.k
     seed = S.config_seed(args.config) + 1000 * rank  # each replica its own tokens
     M.lib()
@@ -826,6 +831,9 @@ def main():
                     help="time the steps as eager launches instead of replaying a CUDA graph of one step")
     ap.add_argument("--profile", action="store_true",
                     help="run the warm-up steps and one more step only (for ncu captures)")
+    ap.add_argument("--shape", default="",
+                    help="with --profile: a layer shape T,H,F,E,k of its own instead of a workload (small "
+                         "profiler captures with a workload's expert shapes)")
     ap.add_argument("--part", default="step", choices=["step", "plan"],
                     help="with --profile: the whole step, or the routing kernels alone (plan buffers only)")
     args = ap.parse_args()
