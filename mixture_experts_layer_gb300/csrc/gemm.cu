@@ -1063,8 +1063,14 @@ __device__ __forceinline__ Tile pair_decode(const GemmParams& p, const ExpertTab
     const int first = x.pairs[e];
     const int cnt = x.pairs[e + 1] - first;
     const int local = tile - nn * first;
-    nt = local / cnt;
-    const int j = 2 * (local - nt * cnt) + static_cast<int>(rank);  // this CTA's 128-row tile of the expert
+    // (M pair, N tile) with N fastest: the clusters running side by side share
+    // one expert's weights and a few 256-row blocks of A, so both stay in the L2
+    // (with M fastest, a wave swept every row block of an expert once per N tile
+    // and re-read A from DRAM two to three times).
+    (void)cnt;
+    const int mp = local / nn;
+    nt = local - mp * nn;
+    const int j = 2 * mp + static_cast<int>(rank);  // this CTA's 128-row tile of the expert
     const int n_e = x.counts[e];
     t.e = e;
     t.row0 = x.offsets[e] + kTileRows * j;
