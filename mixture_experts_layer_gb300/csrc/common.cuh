@@ -115,6 +115,19 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
+// TMA tile load of a 3-D view {x, y, z}.  Used with a view whose innermost
+// dimension is 64 columns, y the rows and z the 64-column panels of a row-major
+// matrix, so one instruction brings two neighbouring 64-column panels, each
+// landing as its own swizzled block (panel-major in shared memory).
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int32_t x,
+                                            int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
+      "[%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
 // TMA row gather: rows r0..r3 of a 2D tensor, columns [x, x + box width), into
 // four consecutive box rows at smem_dst (the map's box is one row high).
 __device__ __forceinline__ void tma_gather4(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int32_t x,

@@ -83,8 +83,13 @@ struct Maps {
   CUtensorMap b2;  // B, 128-row box for a 128-wide tail tile (K-major B only)
   CUtensorMap b3;  // W3, 128-row box
   CUtensorMap gx;  // x [T, H], 64 x 1 box: the rows GEMM1 gathers for its A operand
-  CUtensorMap a64; // A operand, 64-row box: each CTA of a 4-CTA cluster loads half of a shared A block
+  CUtensorMap a64; // A operand, 64-row box: the 64 rows of an M = 128 pair tile's CTA
   CUtensorMap gu;  // dgrad2 epilogue: GU [R, 2F], 16-column x 32-row boxes, 32-byte swizzle
+  // Pair tiles, MN-major operands: 3-D views {64 columns, rows, 64-column panels}
+  // whose box holds two neighbouring panels (one TMA instruction instead of two).
+  CUtensorMap a_p2;   // A (weight gradients)
+  CUtensorMap b0_p2;  // B (W1, W2, dGU or dY)
+  CUtensorMap b1_p2;  // second B tensor (W3)
 };
 
 // The gated combine fused into GEMM2's epilogue (null cnt: not fused).
@@ -122,6 +127,9 @@ struct GemmParams {
   // Pair tiles (forward and dgrad modes): an expert's last 256-row block with at
   // most 128 rows runs as an M = 128 pair tile, 64 rows per CTA.
   int halfm_ok;
+  // Pair tiles: the two-panel 3-D maps (a_p2, b0_p2, b1_p2) were encoded, so each
+  // pair of 64-column MN-major panels is one TMA instruction.
+  int panels2;
   WsHeader* ws;
 };
 
@@ -1114,6 +1122,8 @@ __device__ __forceinline__ void load_kblock_pair(const GemmParams& p, const Maps
       // half of the accumulator has G and U of the same 64 features.
       tma_load_2d(sB, &m.b0, bar, t.n0 + 64 * r, y);
       tma_load_2d(sB + kPanelBytes, &m.b1, bar, t.n0 + 64 * r, y);
+    } else if (p.panels2) {
+      tma_load_3d(sB, r ? &m.b1_p2 : &m.b0_p2, bar, 0, y, t.n0 / 64);
     } else {
       const CUtensorMap* w = r ? &m.b1 : &m.b0;  // W1 (G columns) on CTA 0, W3 (U columns) on CTA 1
       tma_load_2d(sB, w, bar, t.n0, y);
@@ -1122,7 +1132,10 @@ __device__ __forceinline__ void load_kblock_pair(const GemmParams& p, const Maps
   } else if (MODE == kFwd2) {
     if (sA != nullptr) tma_load_2d(sA, &m.a, bar, k0, t.row0);
     const int y = t.e * p.F + k0;
-    for (int q = 0; q < hb / 64; ++q) tma_load_2d(sB + q * kPanelBytes, &m.b0, bar, t.n0 + r * hb + 64 * q, y);
+    if (p.panels2 && hb == 128)
+      tma_load_3d(sB, &m.b0_p2, bar, 0, y, (t.n0 + r * hb) / 64);
+    else
+      for (int q = 0; q < hb / 64; ++q) tma_load_2d(sB + q * kPanelBytes, &m.b0, bar, t.n0 + r * hb + 64 * q, y);
   } else if (MODE == kDgrad2) {
     if (sA != nullptr) tma_load_2d(sA, &m.a, bar, k0, t.row0);
     tma_load_2d(sB, hb == 128 ? &m.b0 : &m.b2, bar, k0, t.e * p.F + t.n0 + r * hb);
@@ -1135,16 +1148,28 @@ __device__ __forceinline__ void load_kblock_pair(const GemmParams& p, const Maps
       tma_load_2d(sB, hb == 128 ? &m.b1 : &m.b3, bar, k0 - p.F, yb);
   } else if (MODE == kWgrad13) {
     const int y = t.row0 + k0;
-    tma_load_2d(sA, &m.a, bar, t.m0, y);
-    tma_load_2d(sA + kPanelBytes, &m.a, bar, t.m0 + 64, y);
     const int c = r ? p.F + t.n0 : t.n0;  // dG half on CTA 0, dU half on CTA 1
-    tma_load_2d(sB, &m.b0, bar, c, y);
-    tma_load_2d(sB + kPanelBytes, &m.b0, bar, c + 64, y);
+    if (p.panels2) {
+      tma_load_3d(sA, &m.a_p2, bar, 0, y, t.m0 / 64);
+      tma_load_3d(sB, &m.b0_p2, bar, 0, y, c / 64);
+    } else {
+      tma_load_2d(sA, &m.a, bar, t.m0, y);
+      tma_load_2d(sA + kPanelBytes, &m.a, bar, t.m0 + 64, y);
+      tma_load_2d(sB, &m.b0, bar, c, y);
+      tma_load_2d(sB + kPanelBytes, &m.b0, bar, c + 64, y);
+    }
   } else {  // kWgrad2
     const int y = t.row0 + k0;
-    tma_load_2d(sA, &m.a, bar, t.m0, y);
-    tma_load_2d(sA + kPanelBytes, &m.a, bar, t.m0 + 64, y);
-    for (int q = 0; q < hb / 64; ++q) tma_load_2d(sB + q * kPanelBytes, &m.b0, bar, t.n0 + r * hb + 64 * q, y);
+    if (p.panels2) {
+      tma_load_3d(sA, &m.a_p2, bar, 0, y, t.m0 / 64);
+    } else {
+      tma_load_2d(sA, &m.a, bar, t.m0, y);
+      tma_load_2d(sA + kPanelBytes, &m.a, bar, t.m0 + 64, y);
+    }
+    if (p.panels2 && hb == 128)
+      tma_load_3d(sB, &m.b0_p2, bar, 0, y, (t.n0 + r * hb) / 64);
+    else
+      for (int q = 0; q < hb / 64; ++q) tma_load_2d(sB + q * kPanelBytes, &m.b0, bar, t.n0 + r * hb + 64 * q, y);
   }
 }
 
@@ -2430,6 +2455,22 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D view of a row-major bf16 matrix [outer, inner] as {64 columns, outer rows,
+// inner / 64 panels} (strides: the row pitch, then 128 bytes per panel), box
+// {64, box_rows, 2}: two neighbouring 64-column panels per instruction, each
+// landing as its own 128-byte-swizzled block of box_rows rows.
+bool make_map_panels2(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_rows) {
+  EncodeFn enc = encoder();
+  if (!enc || inner % 64 != 0) return false;
+  const cuuint64_t dims[3] = {64, outer, inner / 64};
+  const cuuint64_t strides[2] = {inner * 2, 128};
+  const cuuint32_t box[3] = {64, box_rows, 2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int MODE>
 cudaError_t launch_mode(const GemmLaunch& L, const Maps& maps, const GemmParams& p, cudaStream_t s,
                         LaunchHook& hook) {
@@ -2506,13 +2547,29 @@ cudaError_t launch_gemm_pair(GemmMode mode, const GemmLaunch& L, Maps& m, const 
     if (!make_map(&m.a64, a, K, static_cast<uint64_t>(L.R), 64, 64)) return cudaErrorInvalidValue;
     ph.halfm_ok = 1;
   }
+  // MN-major operands: two 64-column panels per TMA instruction where the 3-D
+  // views encode (otherwise one instruction per panel, the same bytes).
+  const uint64_t R = static_cast<uint64_t>(L.R);
+  bool p2 = false;
+  switch (mode) {
+    case kFwd1:
+      p2 = make_map_panels2(&m.b0_p2, L.W1, F, E * H, 64) && make_map_panels2(&m.b1_p2, L.W3, F, E * H, 64);
+      break;
+    case kFwd2: p2 = make_map_panels2(&m.b0_p2, L.W2, H, E * F, 64); break;
+    case kWgrad13:
+      p2 = make_map_panels2(&m.a_p2, L.Xp, H, R, 64) && make_map_panels2(&m.b0_p2, L.dGU, 2 * F, R, 64);
+      break;
+    case kWgrad2: p2 = make_map_panels2(&m.a_p2, L.h, F, R, 64) && make_map_panels2(&m.b0_p2, L.dY, H, R, 64); break;
+    default: break;
+  }
+  ph.panels2 = p2 ? 1 : 0;
   switch (mode) {
     case kFwd1: return launch_pair_mode<kFwd1>(L, m, ph, s, hook);
     case kFwd2: return launch_pair_mode<kFwd2>(L, m, ph, s, hook);
     case kDgrad2: return launch_pair_mode<kDgrad2>(L, m, ph, s, hook);
     case kDgrad1: return launch_pair_mode<kDgrad1>(L, m, ph, s, hook);
-    case kWgrad13: return launch_pair_mode<kWgrad13>(L, m, p, s, hook);
-    case kWgrad2: return launch_pair_mode<kWgrad2>(L, m, p, s, hook);
+    case kWgrad13: return launch_pair_mode<kWgrad13>(L, m, ph, s, hook);
+    case kWgrad2: return launch_pair_mode<kWgrad2>(L, m, ph, s, hook);
   }
   return cudaErrorInvalidValue;
 }
