@@ -49,7 +49,7 @@ extern "C" {
 
 /* ---- error codes ---------------------------------------------------------- */
 #define MOE_OK 0
-#define MOE_ERR_ARG (-1)     /* null pointer, non-positive dimension, k > E, k > 32, pad outside [0, 4096], R >= 2^31, T >= 2^30 */
+#define MOE_ERR_ARG (-1)     /* null pointer, non-positive dimension, k > E, k > 32, pad outside [0, 4096], R >= 2^31 */
 #define MOE_ERR_ALIGN (-2)   /* a pointer is not 16-byte aligned */
 #define MOE_ERR_WS (-3)      /* workspace smaller than moe_workspace_bytes() */
 #define MOE_ERR_LAUNCH (-4)  /* a CUDA launch or API call failed */
@@ -259,12 +259,12 @@ MOE_API int moe_clear_status(void *ws, void *stream);
  * or in a process without a device allocator of its own.  There is no
  * counterpart on the pages; it is an interface convenience.
  *
- * Its scratch (look-back words, chunk bases and bitmaps) lives in one file-scope
+ * Its scratch (per-chunk counts, bases and bitmaps) lives in one file-scope
  * device array of MOE_NOALLOC_SCRATCH_BYTES inside the library, which every GPU
  * that loads the library holds until the process exits.  The call allocates
  * and frees nothing.
  *   - Limit: dims whose scratch exceeds the buffer (roughly
- *     ceil(T/256) * E * 52 bytes plus alignment) return MOE_ERR_TOO_LARGE
+ *     ceil(T/256) * E * 40 bytes plus alignment) return MOE_ERR_TOO_LARGE
  *     before anything is launched; e.g. T = 131072 with E = 128 fits.
  *   - status: device pointer to 4 int32 (16 bytes, caller-owned, zero before
  *     first use); the first device-detected error is recorded in its first

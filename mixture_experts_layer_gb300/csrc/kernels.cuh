@@ -7,15 +7,8 @@
 
 namespace moe {
 
-constexpr int kChunk = 256;               // tokens per rank chunk (one CTA of route_rank)
+constexpr int kChunk = 256;               // tokens per routing chunk (one "source" of the mapping)
 constexpr int kChunkWords = kChunk / 32;  // bitmap words per expert and chunk
-constexpr int kBlockTokens = 64;          // tokens per top-k CTA: one "source" of the mapping's prefix
-
-// Words of the routing's look-back area: a 16-word ticket block, then one word
-// per (64-token block, expert).
-__host__ __device__ inline long long plan_lb_words(long long T, int E) {
-  return 16 + (T + kBlockTokens - 1) / kBlockTokens * E;
-}
 constexpr int kTileRows = 128;            // rows of a GEMM tile (the tcgen05 M)
 constexpr int kMaxPad = 4096;             // largest padding granule of an expert's rows
 
@@ -76,9 +69,9 @@ struct PlanLaunch {
   int32_t* ids;
   float* w;
   uint32_t* gbm;
-  int32_t* ticket;  // 16 words (ticket[0]: the top-k blocks' order), then lb; both cleared by launch_plan
-  uint32_t* lb;     // [nblk][E] look-back words of the 64-token blocks = ticket + 16
-  int32_t* cbase;   // [nchunks][E] rows of each expert in the chunks before (exclusive prefix)
+  int32_t* ticket;  // 16 words, then ccount; both cleared by launch_plan
+  int32_t* ccount;  // [E][nchunks] (expert-major) = ticket + 16
+  int32_t* cbase;
   int32_t* counts;
   int32_t* offsets;
   int32_t* tiles;

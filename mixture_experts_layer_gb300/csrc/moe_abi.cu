@@ -52,7 +52,7 @@ int check_dims(const moe_dims& d) {
   if (d.T < 0 || d.H <= 0 || d.F <= 0 || d.E <= 0 || d.k <= 0) return MOE_ERR_ARG;
   if (d.k > d.E || d.k > 32) return MOE_ERR_ARG;
   if (d.pad < 0 || d.pad > kMaxPad) return MOE_ERR_ARG;
-  if (rows_of(d) >= (1ll << 31) || d.T >= (1 << 30)) return MOE_ERR_ARG;
+  if (rows_of(d) >= (1ll << 31)) return MOE_ERR_ARG;
   if (d.H % 128 != 0 || d.F % 128 != 0 || d.E > 1024) return MOE_ERR_SHAPE;
   if (static_cast<long long>(d.E) * d.H >= (1ll << 31) || static_cast<long long>(d.E) * d.F >= (1ll << 31))
     return MOE_ERR_SHAPE;
@@ -86,8 +86,8 @@ WsLayout ws_layout(const moe_dims& d) {
   const size_t nchunks = (static_cast<size_t>(d.T) + kChunk - 1) / kChunk;
   WsLayout L;
   size_t off = align256(sizeof(WsHeader));
-  L.ccount = off;  // 16-word ticket, then the look-back words of the 64-token blocks
-  off = align256(off + static_cast<size_t>(plan_lb_words(d.T, d.E)) * 4);
+  L.ccount = off;  // 16-word ticket, then the per-chunk counts
+  off = align256(off + (16 + nchunks * d.E) * 4);
   L.cbase = off;
   off = align256(off + nchunks * d.E * 4);
   L.gbm = off;
@@ -193,7 +193,7 @@ int use_pair(const moe_opts* o, GemmMode m, const moe_dims& d) {
 }
 
 
-const char* const kPlanKernels[] = {"route_topk", "route_rank", nullptr};
+const char* const kPlanKernels[] = {"route_topk", "route_scan", "route_rank", nullptr};
 const char* const kFwdKernelsFused[] = {"fused_forward", "combine", nullptr};
 const char* const kFwdKernels[] = {"gather_rows", "gemm_fwd1_swiglu", "gemm_fwd2", "combine", nullptr};
 const char* const kFwdKernelsCombineFused[] = {"gather_rows", "gemm_fwd1_swiglu", "gemm_fwd2_combine", nullptr};
@@ -299,7 +299,7 @@ int moe_plan(moe_dims d, const float* logits, const moe_plan_t* plan, void* ws, 
   p.w = plan->topk_w;
   p.gbm = reinterpret_cast<uint32_t*>(w + L.gbm);
   p.ticket = reinterpret_cast<int32_t*>(w + L.ccount);
-  p.lb = reinterpret_cast<uint32_t*>(p.ticket + 16);
+  p.ccount = p.ticket + 16;
   p.cbase = reinterpret_cast<int32_t*>(w + L.cbase);
   p.counts = plan->counts;
   p.offsets = plan->offsets;

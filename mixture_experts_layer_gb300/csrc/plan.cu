@@ -6,22 +6,21 @@
 // source counts its tokens per expert, an exclusive prefix over the sources
 // gives each source its base inside an expert's segment, and a source places
 // its tokens at base + their stable index among its own tokens.  The sources
-// here are 64-token blocks of one GPU instead of ranks, so no atomics decide
+// here are 256-token chunks of one GPU instead of ranks, so no atomics decide
 // any position and the order inside each expert is the original token order.
 //
-//   route_topk  one CTA per 64-token block (blocks taken in ticket order): top-k
-//               per token (four threads per token with a min/max selection
-//               network where E % 4 == 0, E <= 256 and k <= 8; a warp-wide
-//               argmax per pick otherwise), renormalised weights, its part of
-//               the 256-token chunk bitmap bm[e][w] whose bit b says "token
-//               32w+b of the chunk chose expert e", and its counts per expert.
-//               A decoupled look-back over the blocks before it gives each
-//               block its exclusive prefix per expert (Algorithm 1's offsets
-//               over sources); the last block takes the prefix over experts
-//               (counts, offsets, first 128-row GEMM tile of each expert).
-//   route_rank  one CTA per 256-token chunk: stable index = popcount of the
-//               chunk's bitmap below the token; dest, row_src, row_slot; a
-//               share of the GEMM tile entries.
+//   route_topk  one CTA per 64 tokens: top-k per token (four threads per
+//               token with a min/max selection network where E % 4 == 0,
+//               E <= 256 and k <= 8; a warp-wide argmax per pick otherwise),
+//               renormalised weights, and its part of the chunk bitmap bm[e][w]
+//               whose bit b says "token 32w+b of the chunk chose expert e";
+//               per-chunk counts by integer atomics.
+//   route_scan  one warp per expert: exclusive prefix of the counts over
+//               chunks; the last CTA takes the prefix over experts (offsets,
+//               first 128-row GEMM tile of each expert).
+//   route_rank  one CTA per chunk: stable index = popcount of the chunk's
+//               bitmap below the token; dest, row_src, row_slot; a share of
+//               the GEMM tile entries.
 #include <math.h>
 
 #include <type_traits>
@@ -31,159 +30,9 @@
 
 namespace moe {
 
-constexpr int kTopkTokens = kBlockTokens;  // tokens per top-k CTA: two bitmap words per expert
-static_assert(kChunk % kTopkTokens == 0, "a rank chunk is a whole number of top-k blocks");
+constexpr int kTopkTokens = 64;    // tokens per top-k / rank CTA: two bitmap words per expert
 constexpr int kTopkThreads = 256;  // 8 warps x 8 tokens
-
-// What the top-k CTAs produce besides ids and weights: the look-back words,
-// the chunk bases, and (from the last block) the expert-level tables.
-struct ScanArgs {
-  int32_t* ticket;   // [0]: order in which the blocks take their tokens
-  uint32_t* lb;      // [nblk][E] look-back words
-  int32_t* cbase;    // [nchunks][E]
-  int32_t* counts;   // [E]
-  int32_t* offsets;  // [E + 1]
-  int32_t* tiles;    // the plan's tile table ([0], [1 + e])
-  int32_t* pairs;    // first 256-row pair of each expert [E + 1]
-  int32_t* gcounts;  // rows the GEMMs run per expert [E]
-  int32_t* row_src;  // padding rows get -1
-  uint8_t* row_slot; // padding rows get 255
-  int pad, R;
-};
-
-// Look-back words: the value (rows of one expert) in the low 30 bits, the state
-// in the top two: 0 nothing yet, kLbAgg the block's own count, kLbIncl the
-// count of this block and all before it.
-constexpr uint32_t kLbAgg = 1u << 30;
-constexpr uint32_t kLbIncl = 2u << 30;
-constexpr uint32_t kLbVal = (1u << 30) - 1u;
-
-// The exclusive prefix over sources of Algorithm 1 ("UniEP", section 3.1),
-// with 64-token blocks as the sources, computed as a decoupled look-back: a
-// block publishes its count per expert, then walks back over the blocks before
-// it, adding their counts until it meets one that has published its inclusive
-// prefix, and publishes its own.  Blocks take their tokens in ticket order, so
-// every block it reads has already started and never waits on a later one;
-// each wait is bounded.  Integer sums: the result does not depend on timing.
-// On return the first block of each 256-token chunk has stored its base
-// (cbase), and in the last block cnt[e] holds the expert's total.
-__device__ void lookback(int* cnt, int blk, int nblk, int E, const ScanArgs& a, WsHeader* ws) {
-  volatile uint32_t* lb = a.lb;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const uint32_t c = static_cast<uint32_t>(cnt[e]);
-    uint32_t excl = 0;
-    if (blk == 0) {
-      lb[e] = kLbIncl | c;
-    } else {
-      lb[static_cast<size_t>(blk) * E + e] = kLbAgg | c;
-      int q = blk - 1;
-      uint64_t t0 = 0;
-      while (q >= 0) {
-        const uint32_t v = lb[static_cast<size_t>(q) * E + e];
-        const uint32_t f = v & ~kLbVal;
-        if (f == 0) {  // block q has not published yet
-          if (t0 == 0) {
-            t0 = globaltimer();
-          } else if (globaltimer() - t0 > kWaitLimitNs) {
-            report(ws, MOE_ERR_TIMEOUT, 3, blk);
-            break;
-          }
-          continue;
-        }
-        excl += v & kLbVal;
-        if (f == kLbIncl) break;
-        --q;
-      }
-      lb[static_cast<size_t>(blk) * E + e] = kLbIncl | ((excl + c) & kLbVal);
-    }
-    if ((blk % (kChunk / kBlockTokens)) == 0) a.cbase[static_cast<size_t>(blk / (kChunk / kBlockTokens)) * E + e] = excl;
-    if (blk == nblk - 1) cnt[e] = static_cast<int>(excl + c);
-  }
-}
-
-// Last block only (all threads, tot = the experts' totals in shared memory):
-// counts, the exclusive prefix over experts of the rows each expert's GEMMs run
-// (offsets) and of their 128-row tiles and 256-row pairs, the GEMM row counts
-// and, with a padding granule (pad >= 2), the padding rows' markers.
-__device__ void expert_prefix(const int* tot, int E, const ScanArgs& a, WsHeader* ws) {
-  __shared__ int s_wsum_n[32], s_wsum_m[32], s_wsum_p[32];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pad = a.pad;
-  const int per = (E + blockDim.x - 1) / blockDim.x;
-  const int e0 = threadIdx.x * per;
-  auto padded = [pad](int n) { return pad > 1 ? (n + pad - 1) / pad * pad : n; };
-  int my_n = 0, my_m = 0, my_p = 0;
-  for (int i = 0; i < per; ++i) {
-    const int ee = e0 + i;
-    if (ee < E) {
-      const int n = padded(tot[ee]);
-      my_n += n;
-      my_m += (n + kTileRows - 1) / kTileRows;
-      my_p += (n + 2 * kTileRows - 1) / (2 * kTileRows);
-    }
-  }
-  int in_n = my_n, in_m = my_m, in_p = my_p;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int yn = __shfl_up_sync(0xffffffffu, in_n, off);
-    const int ym = __shfl_up_sync(0xffffffffu, in_m, off);
-    const int yp = __shfl_up_sync(0xffffffffu, in_p, off);
-    if (lane >= off) {
-      in_n += yn;
-      in_m += ym;
-      in_p += yp;
-    }
-  }
-  if (lane == 31) {
-    s_wsum_n[warp] = in_n;
-    s_wsum_m[warp] = in_m;
-    s_wsum_p[warp] = in_p;
-  }
-  __syncthreads();
-  int run_n = in_n - my_n, run_m = in_m - my_m, run_p = in_p - my_p;
-  for (int w = 0; w < warp; ++w) {
-    run_n += s_wsum_n[w];
-    run_m += s_wsum_m[w];
-    run_p += s_wsum_p[w];
-  }
-  for (int i = 0; i < per; ++i) {
-    const int ee = e0 + i;
-    if (ee >= E) break;
-    const int real = tot[ee];
-    const int n = padded(real);
-    a.counts[ee] = real;
-    a.gcounts[ee] = n;
-    for (int r = run_n + real; r < run_n + n; ++r) {  // the padding rows of expert ee
-      if (r < 0 || r >= a.R) {
-        report(ws, MOE_ERR_BOUNDS, 1, r);
-        break;
-      }
-      a.row_src[r] = -1;
-      a.row_slot[r] = 255;
-    }
-    a.offsets[ee] = run_n;
-    a.tiles[1 + ee] = run_m;
-    a.pairs[ee] = run_p;
-    run_n += n;
-    run_m += (n + kTileRows - 1) / kTileRows;
-    run_p += (n + 2 * kTileRows - 1) / (2 * kTileRows);
-    if (ee == E - 1) {
-      a.offsets[E] = run_n;
-      a.tiles[1 + E] = run_m;
-      a.tiles[0] = run_m;
-      a.pairs[E] = run_p;
-    }
-  }
-}
-
-// The end of every top-k CTA: its counts (cnt, shared memory, complete) go
-// through the look-back; the last block then writes the expert-level tables.
-__device__ __forceinline__ void finish_block(int* cnt, int blk, int nblk, int E, const ScanArgs& a, WsHeader* ws) {
-  lookback(cnt, blk, nblk, E, a, ws);
-  if (blk != nblk - 1) return;  // uniform over the CTA
-  __syncthreads();
-  expert_prefix(cnt, E, a, ws);
-}
+constexpr int kScanWarps = 8;      // experts per scan CTA
 
 // NV = logits per lane (E <= 32 * NV); TPW = tokens whose logits a warp loads
 // at once, so several rows' loads are in flight before the selection starts.
@@ -194,17 +43,14 @@ template <int NV, int TPW>
 __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float* __restrict__ logits, int T, int E,
                                                                   int k, int32_t* __restrict__ ids,
                                                                   float* __restrict__ wts, uint32_t* __restrict__ gbm,
-                                                                  const ScanArgs a, WsHeader* ws) {
+                                                                  int32_t* __restrict__ ccount, WsHeader* ws) {
   extern __shared__ uint32_t sm[];
-  __shared__ int s_blk;
   uint32_t* bm = sm;            // [E][2] bitmap words of this CTA's 64 tokens
   int* cnt = reinterpret_cast<int*>(sm + 2 * E);  // [E]
   for (int i = threadIdx.x; i < 3 * E; i += blockDim.x) sm[i] = 0;
-  if (threadIdx.x == 0) s_blk = atomicAdd(a.ticket, 1);  // blocks take their tokens in start order
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int blk = s_blk;
-  const int t0 = blk * kTopkTokens;
+  const int t0 = blockIdx.x * kTopkTokens;
   for (int tb = warp * (kTopkTokens / 8); tb < (warp + 1) * (kTopkTokens / 8); tb += TPW) {
     float v[TPW][NV];
 #pragma unroll
@@ -282,7 +128,8 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float* _
   const int w0 = (t0 % kChunk) / 32;
   uint32_t* out = gbm + static_cast<size_t>(chunk) * E * kChunkWords;
   for (int i = threadIdx.x; i < 2 * E; i += blockDim.x) out[(i >> 1) * kChunkWords + w0 + (i & 1)] = bm[i];
-  finish_block(cnt, blk, (T + kTopkTokens - 1) / kTopkTokens, E, a, ws);
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    if (cnt[e] != 0) atomicAdd(&ccount[static_cast<size_t>(e) * ((T + kChunk - 1) / kChunk) + chunk], cnt[e]);
 }
 
 // Fast path of the same selection for E % 4 == 0, E <= 256 and k <= 8: four
@@ -341,21 +188,18 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk4_kernel(const float* 
                                                                    int k, int32_t* __restrict__ ids,
                                                                    float* __restrict__ wts,
                                                                    uint32_t* __restrict__ gbm,
-                                                                   const ScanArgs a, WsHeader* ws) {
+                                                                   int32_t* __restrict__ ccount, WsHeader* ws) {
   constexpr int NV = 4 * NV4;                    // values per thread
   constexpr int NB = (NV + 7) / 8;               // blocks of 8
   extern __shared__ uint32_t sm[];
-  __shared__ int s_blk;
   uint32_t* bm = sm;                             // [E][2]
   int* cnt = reinterpret_cast<int*>(sm + 2 * E); // [E]
   float* cand_x = reinterpret_cast<float*>(cnt + E);  // [64 tokens][8] chosen values (tie path)
   for (int i = threadIdx.x; i < 3 * E; i += blockDim.x) sm[i] = 0;
-  if (threadIdx.x == 0) s_blk = atomicAdd(a.ticket, 1);  // blocks take their tokens in start order
   __syncthreads();
-  const int blk = s_blk;
   const int lane = threadIdx.x & 31;
   const int tl = threadIdx.x >> 2, q = threadIdx.x & 3;
-  const int t = blk * kTopkTokens + tl;
+  const int t = blockIdx.x * kTopkTokens + tl;
   const bool live = t < T;
   const float* row = logits + static_cast<size_t>(live ? t : 0) * E;
 
@@ -540,12 +384,133 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk4_kernel(const float* 
     }
   }
   __syncthreads();
-  const int t0 = blk * kTopkTokens;
+  const int t0 = blockIdx.x * kTopkTokens;
   const int chunk = t0 / kChunk;
   const int w0 = (t0 % kChunk) / 32;
   uint32_t* out = gbm + static_cast<size_t>(chunk) * E * kChunkWords;
   for (int i = threadIdx.x; i < 2 * E; i += blockDim.x) out[(i >> 1) * kChunkWords + w0 + (i & 1)] = bm[i];
-  finish_block(cnt, blk, (T + kTopkTokens - 1) / kTopkTokens, E, a, ws);
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    if (cnt[e] != 0) atomicAdd(&ccount[static_cast<size_t>(e) * ((T + kChunk - 1) / kChunk) + chunk], cnt[e]);
+}
+
+// Per expert (one warp each): exclusive prefix of the chunk counts over the
+// chunks -- the O_all of Algorithm 1 -- and the expert's row count.  The last
+// CTA to finish (ticket) then takes the prefix over experts of the row counts
+// (offsets) and of the 128-row tile counts (first tile of each expert); the
+// tile entries themselves are written by route_rank.  With a padding granule
+// (pad >= 2) each expert's segment is its count rounded up to a multiple of
+// pad: offsets, tiles and pairs count the padded rows, gcounts holds them, and
+// the padding rows get row_src = -1, row_slot = 255.
+__global__ void __launch_bounds__(32 * kScanWarps) route_scan_kernel(const int32_t* __restrict__ ccount,
+                                                                     int nchunks, int E, int32_t* __restrict__ cbase,
+                                                                     int32_t* __restrict__ counts,
+                                                                     int32_t* __restrict__ offsets,
+                                                                     int32_t* __restrict__ tiles,
+                                                                     int32_t* __restrict__ pairs, int32_t* ticket,
+                                                                     int pad, int R, int32_t* __restrict__ gcounts,
+                                                                     int32_t* __restrict__ row_src,
+                                                                     uint8_t* __restrict__ row_slot, WsHeader* ws) {
+  __shared__ int s_last;
+  __shared__ int s_wsum_n[32], s_wsum_m[32], s_wsum_p[32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * kScanWarps + warp;
+  if (e < E) {
+    int run = 0;
+    // 8 x 32 chunks per pass: all of a pass's loads are in flight before its scans.
+    for (int c0 = 0; c0 < nchunks; c0 += 256) {
+      int v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + 32 * u + lane;
+        v[u] = (c < nchunks) ? ccount[static_cast<size_t>(e) * nchunks + c] : 0;  // expert-major: coalesced
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + 32 * u + lane;
+        int incl = v[u];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += y;
+        }
+        if (c < nchunks) cbase[static_cast<size_t>(c) * E + e] = run + incl - v[u];
+        run += __shfl_sync(0xffffffffu, incl, 31);
+      }
+    }
+    if (lane == 0) counts[e] = run;
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = (atomicAdd(ticket, 1) == static_cast<int>(gridDim.x) - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // Last CTA: exclusive prefix over experts of the row counts and of the
+  // 128-row tile counts.  Thread i takes experts [i * per, (i + 1) * per).
+  const int per = (E + blockDim.x - 1) / blockDim.x;
+  const int e0 = threadIdx.x * per;
+  auto padded = [pad](int n) { return pad > 1 ? (n + pad - 1) / pad * pad : n; };
+  int my_n = 0, my_m = 0, my_p = 0;
+  for (int i = 0; i < per; ++i) {
+    const int ee = e0 + i;
+    if (ee < E) {
+      const int n = padded(__ldcg(counts + ee));
+      my_n += n;
+      my_m += (n + kTileRows - 1) / kTileRows;
+      my_p += (n + 2 * kTileRows - 1) / (2 * kTileRows);
+    }
+  }
+  int in_n = my_n, in_m = my_m, in_p = my_p;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int yn = __shfl_up_sync(0xffffffffu, in_n, off);
+    const int ym = __shfl_up_sync(0xffffffffu, in_m, off);
+    const int yp = __shfl_up_sync(0xffffffffu, in_p, off);
+    if (lane >= off) {
+      in_n += yn;
+      in_m += ym;
+      in_p += yp;
+    }
+  }
+  if (lane == 31) {
+    s_wsum_n[warp] = in_n;
+    s_wsum_m[warp] = in_m;
+    s_wsum_p[warp] = in_p;
+  }
+  __syncthreads();
+  int run_n = in_n - my_n, run_m = in_m - my_m, run_p = in_p - my_p;
+  for (int w = 0; w < warp; ++w) {
+    run_n += s_wsum_n[w];
+    run_m += s_wsum_m[w];
+    run_p += s_wsum_p[w];
+  }
+  for (int i = 0; i < per; ++i) {
+    const int ee = e0 + i;
+    if (ee >= E) break;
+    const int real = __ldcg(counts + ee);
+    const int n = padded(real);
+    gcounts[ee] = n;
+    for (int r = run_n + real; r < run_n + n; ++r) {  // the padding rows of expert ee
+      if (r < 0 || r >= R) {
+        report(ws, MOE_ERR_BOUNDS, 1, r);
+        break;
+      }
+      row_src[r] = -1;
+      row_slot[r] = 255;
+    }
+    offsets[ee] = run_n;
+    tiles[1 + ee] = run_m;
+    pairs[ee] = run_p;
+    run_n += n;
+    run_m += (n + kTileRows - 1) / kTileRows;
+    run_p += (n + 2 * kTileRows - 1) / (2 * kTileRows);
+    if (ee == E - 1) {
+      offsets[E] = run_n;
+      tiles[1 + E] = run_m;
+      tiles[0] = run_m;
+      pairs[E] = run_p;
+    }
+  }
 }
 
 // One CTA per 256-token chunk: stable index = popcount of the chunk's bitmap
@@ -696,23 +661,10 @@ cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t s, LaunchHook& hook) {
   const int nchunks = (p.T + kChunk - 1) / kChunk;
   const int nblocks = (p.T + kTopkTokens - 1) / kTopkTokens;
   const int nv = (p.E + 31) / 32;
-  // The ticket and the look-back words start at zero (the bitmap words are all
-  // written by the top-k CTAs).
-  cudaError_t err = cudaMemsetAsync(p.ticket, 0, static_cast<size_t>(plan_lb_words(p.T, p.E)) * 4, s);
+  // The chunk counts and the scan's ticket start at zero (the bitmap words are
+  // all written by the top-k CTAs).
+  cudaError_t err = cudaMemsetAsync(p.ticket, 0, (16 + static_cast<size_t>(nchunks) * p.E) * 4, s);
   if (err != cudaSuccess) return err;
-  ScanArgs a;
-  a.ticket = p.ticket;
-  a.lb = p.lb;
-  a.cbase = p.cbase;
-  a.counts = p.counts;
-  a.offsets = p.offsets;
-  a.tiles = p.tiles;
-  a.pairs = p.pairs;
-  a.gcounts = p.gcounts;
-  a.row_src = p.row_src;
-  a.row_slot = p.row_slot;
-  a.pad = p.pad;
-  a.R = p.R;
   const size_t topk_smem = static_cast<size_t>(p.E) * 3 * 4;
   hook.before(s);
   const int nv4 = (p.E + 15) / 16;
@@ -723,7 +675,7 @@ cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t s, LaunchHook& hook) {
 #define MOE_TOPK4_CASE(NV4, FULL)                                                                              \
   case (FULL ? NV4 : -NV4):                                                                                    \
     route_topk4_kernel<NV4, FULL><<<nblocks, kTopkThreads, smem4, s>>>(p.logits, p.T, p.E, p.k, p.ids, p.w,    \
-                                                                       p.gbm, a, p.ws);                        \
+                                                                       p.gbm, p.ccount, p.ws);                 \
     break;
       MOE_TOPK4_CASE(1, true)
       MOE_TOPK4_CASE(2, true)
@@ -742,7 +694,7 @@ cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t s, LaunchHook& hook) {
 #define MOE_TOPK_CASE(NV, TPW)                                                                                 \
   case NV:                                                                                                     \
     route_topk_kernel<NV, TPW><<<nblocks, kTopkThreads, topk_smem, s>>>(p.logits, p.T, p.E, p.k, p.ids, p.w, \
-                                                                        p.gbm, a, p.ws);                     \
+                                                                        p.gbm, p.ccount, p.ws);              \
     break;
     MOE_TOPK_CASE(1, 8)
     MOE_TOPK_CASE(2, 8)
@@ -753,6 +705,13 @@ cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t s, LaunchHook& hook) {
 #undef MOE_TOPK_CASE
   }
   }
+  hook.after(s);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  hook.before(s);
+  route_scan_kernel<<<(p.E + kScanWarps - 1) / kScanWarps, 32 * kScanWarps, 0, s>>>(
+      p.ccount, nchunks, p.E, p.cbase, p.counts, p.offsets, p.tiles, p.pairs, p.ticket, p.pad, p.R, p.gcounts,
+      p.row_src, p.row_slot, p.ws);
   hook.after(s);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
@@ -875,12 +834,12 @@ extern "C" int moe_plan_noalloc(moe_dims d, const float* logits, const moe_plan_
                                 void* stream) {
   using namespace moe;
   if (d.T < 0 || d.H <= 0 || d.F <= 0 || d.E <= 0 || d.k <= 0 || d.k > d.E || d.k > 32 || d.pad < 0 ||
-      d.pad > kMaxPad || grouped_rows(d.T, d.k, d.E, d.pad) >= (1ll << 31) || d.T >= (1 << 30))
+      d.pad > kMaxPad || grouped_rows(d.T, d.k, d.E, d.pad) >= (1ll << 31))
     return MOE_ERR_ARG;
   if (d.H % 128 != 0 || d.F % 128 != 0 || d.E > 1024) return MOE_ERR_SHAPE;
   const size_t nchunks = (static_cast<size_t>(d.T) + kChunk - 1) / kChunk;
-  const size_t ccount = 0;  // 16-word ticket, then the look-back words of the 64-token blocks
-  const size_t cbase = na_align(ccount + static_cast<size_t>(plan_lb_words(d.T, d.E)) * 4);
+  const size_t ccount = 0;  // 16-word ticket, then the per-chunk counts
+  const size_t cbase = na_align(ccount + (16 + nchunks * d.E) * 4);
   const size_t gbm = na_align(cbase + nchunks * d.E * 4);
   const size_t total = na_align(gbm + nchunks * d.E * kChunkWords * 4);
   if (total > kNoAllocBytes) return MOE_ERR_TOO_LARGE;
@@ -907,7 +866,7 @@ extern "C" int moe_plan_noalloc(moe_dims d, const float* logits, const moe_plan_
   p.ids = plan->topk_ids;
   p.w = plan->topk_w;
   p.ticket = reinterpret_cast<int32_t*>(w + ccount);
-  p.lb = reinterpret_cast<uint32_t*>(p.ticket + 16);
+  p.ccount = p.ticket + 16;
   p.cbase = reinterpret_cast<int32_t*>(w + cbase);
   p.gbm = reinterpret_cast<uint32_t*>(w + gbm);
   p.counts = plan->counts;
