@@ -476,7 +476,7 @@ def run_ours(args):
     nf, nb = len(fwd_names), len(bwd_names)
     router_arg = (inp["x"], inp["Wr"]) if args.router else None
     opt_kw = dict(schedule=args.schedule, cta_pair=args.cta_pair, combine=args.combine,
-                  wgrad_subbatches=args.wgrad_subbatches, dispatch=args.dispatch)
+                  wgrad_subbatches=args.wgrad_subbatches, dispatch=args.dispatch, grid=args.grid)
     base_opts = layer.opts(**opt_kw)
 
     def step(opts_f=None, opts_b=None, ev_plan=None, opts_r=None):
@@ -743,6 +743,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": dict(workload_config(shape, args.config), parallelism=f"replicas x{world}" if world > 1 else "1 GPU",
+                       grid=args.grid if args.grid else "one CTA per SM",
                        schedule={0: "one persistent launch per phase", 1: "fused persistent forward, per-GEMM backward",
                                  2: "fused forward, fused backward"}[args.schedule],
                        gemm_tiles={0: "two-CTA 256x256 pair tiles (cta_group::2); dgrad2 on 128x256 single-CTA "
@@ -814,6 +815,8 @@ def main():
     ap.add_argument("--cta-pair", type=int, default=0, choices=[0, 1, 2],
                     help="grouped GEMMs that run as their own kernels: 0 library default (pair tiles but for "
                          "dgrad2), 1 one CTA per tile, 2 two-CTA pair tiles")
+    ap.add_argument("--grid", type=int, default=0,
+                    help="CTAs of the persistent kernels (0: one per SM); results do not depend on it")
     ap.add_argument("--combine", type=int, default=0, choices=[0, 1],
                     help="schedule 0: 0 a separate gated-combine kernel, 1 the combine in GEMM2's epilogue")
     ap.add_argument("--dispatch", type=int, default=0, choices=[0, 1, 2],

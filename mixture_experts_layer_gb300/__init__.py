@@ -75,17 +75,21 @@ def lib_path() -> str:
     return os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe.so")
 
 
-def lib() -> ctypes.CDLL:
-    """The loaded library; builds it first if it is missing or older than its sources."""
+def lib(path: str | None = None) -> ctypes.CDLL:
+    """The loaded library; builds it first if it is missing or older than its sources.
+
+    path: load this build of the library instead (a diagnosis build such as
+    libmoe_timeline.so); only before the first load in the process."""
     global _LIB
     if _LIB is not None:
         return _LIB
     with _LOCK:
         if _LIB is None:
-            from . import build as _build
-            if not _build.up_to_date():
-                _build.build()
-            L = ctypes.CDLL(lib_path())
+            if path is None:
+                from . import build as _build
+                if not _build.up_to_date():
+                    _build.build()
+            L = ctypes.CDLL(path or lib_path())
             vp = c_void_p
             sig = {
                 "moe_workspace_bytes": (c_size_t, [moe_dims]),

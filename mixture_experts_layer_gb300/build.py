@@ -36,10 +36,10 @@ def _inputs() -> list[str]:
             + [os.path.join(ROOT, "include", "moe.h"), os.path.abspath(__file__)])
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _inputs())
 
 
@@ -50,19 +50,23 @@ def _run(cmd):
     return r.stdout + r.stderr
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compiles libmoe.so if any source is newer than it; returns its path."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, defines=(), out: str = LIB) -> str:
+    """Compiles the library (libmoe.so by default) if any source is newer than it; returns its path.
+
+    defines: extra preprocessor macros, for diagnosis builds written to another
+    file (e.g. MOE_TIMELINE into libmoe_timeline.so); the product build has none."""
+    if not force and up_to_date(out):
+        return out
+    bdir = BUILD if not defines else BUILD + "_" + "_".join(d.lower() for d in defines)
+    os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
     common = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
-                     "-I" + os.path.join(ROOT, "include")]
+                     "-I" + os.path.join(ROOT, "include")] + ["-D" + d for d in defines]
     if ptxas_info:
         common += ["-Xptxas", "-v"]
 
     def compile_one(src):
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(bdir, src.replace(".cu", ".o"))
         out = _run([cc] + common + ["-c", os.path.join(CSRC, src), "-o", obj])
         return obj, out
 
@@ -72,11 +76,11 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         for obj, out in results:
             if out.strip():
                 print(f"== {os.path.basename(obj)}\n{out}")
-    tmp = LIB + ".tmp"
+    tmp = out + ".tmp"
     _run([cc] + ARCH + ["-shared", "-cudart", "static", "-Xlinker", "--exclude-libs,ALL", "-o", tmp]
          + [o for o, _ in results])
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

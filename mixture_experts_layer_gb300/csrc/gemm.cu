@@ -1007,6 +1007,27 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 // read their accumulator.  Tile order and arithmetic are those of the
 // single-CTA kernels, so results do not depend on the grid size either.
 // ---------------------------------------------------------------------------
+// Pipeline timeline of the pair kernels, for diagnosis only: compiled in with
+// -DMOE_TIMELINE (never in a normal build).  With moe_debug_timeline() set,
+// the pair kernel of the selected mode stamps %globaltimer for every k-block
+// n < cap of every CTA into buf[(cta * cap + n) * 5 + event]: 0 the producer
+// found the stage free, 1 the MMA warp saw it land, 2 the leader saw the
+// partner's stage (the relay: the odd CTA's arrive), 3 the MMAs and the commit
+// were issued, 4 (first k-block of a tile) the leader got the accumulator.
+#ifdef MOE_TIMELINE
+__device__ unsigned long long* g_tl_buf = nullptr;
+__device__ int g_tl_cap = 0;
+__device__ int g_tl_mode = -1;
+template <int MODE>
+__device__ __forceinline__ void tl_mark(int n, int ev) {
+  if (g_tl_mode == MODE && g_tl_buf != nullptr && n < g_tl_cap)
+    g_tl_buf[(static_cast<size_t>(blockIdx.x) * g_tl_cap + n) * 5 + ev] = globaltimer();
+}
+#define MOE_TL(n, ev) tl_mark<MODE>((n), (ev))
+#else
+#define MOE_TL(n, ev) ((void)0)
+#endif
+
 constexpr int kPairBHalfBytes = 128 * BK * 2;  // half of a 256-wide B tile
 constexpr int kPairStageBytes = kABytes + kPairBHalfBytes;
 
@@ -1256,6 +1277,8 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
     uint32_t ph = 0;
     uint32_t issued = 0, last_parity = 0;
     bool ok = true;
+    int tl_n = 0;  // k-blocks so far (timeline index)
+    (void)tl_n;
     for (int tile = pid; tile < ntiles && ok; tile += npairs) {
       const Tile t = pair_decode<MODE>(p, xt, tile, rank);
       const bool gather = (MODE == kFwd1) && p.gather;
@@ -1273,6 +1296,8 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
           ok = false;
           break;
         }
+        if (lane == 0) MOE_TL(tl_n, 0);
+        ++tl_n;
         uint8_t* sA = smem + s * kPairStageBytes;
         if (gather) {
           if (elect_one()) {
@@ -1310,6 +1335,8 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
     int acc = 0;
     uint32_t acc_ph = 0;
     bool ok = true;
+    int tl_n = 0;  // k-blocks so far (timeline index)
+    (void)tl_n;
     const uint32_t pfull_leader = mapa_shared(smem_u32(pfull), pair_leader);
     for (int tile = pid; tile < ntiles && ok; tile += npairs) {
       const Tile t = pair_decode<MODE>(p, xt, tile, rank);
@@ -1317,6 +1344,7 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
       if (leader) {
         if (!mbar_wait_cluster(&tempty[acc], acc_ph ^ 1u, p.ws, 220 + MODE, abort_flag)) break;
         tc_fence_after();
+        if (lane == 0) MOE_TL(tl_n, 4);
       }
       const uint32_t d_tmem = tmem_base + acc * kAccStride;
       const uint32_t idesc = t.halfm ? ((t.nw == 256) ? kIdescH256 : kIdescH128) : (t.nw == 256) ? kIdesc256 : kIdesc128;
@@ -1325,6 +1353,7 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
           ok = false;
           break;
         }
+        if (lane == 0) MOE_TL(tl_n, 1);
         uint8_t* sA = smem + s * kPairStageBytes;
         uint8_t* sB = sA + kABytes;
         int nkk = BK / 16;
@@ -1344,6 +1373,7 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
               bulk_wait_read<0>();
             }
             mbar_arrive_cluster(pfull_leader + s * 8);
+            MOE_TL(tl_n, 2);
           }
           __syncwarp();
         } else {
@@ -1351,6 +1381,7 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
             ok = false;
             break;
           }
+          if (lane == 0) MOE_TL(tl_n, 2);
           tc_fence_after();
           // One elected thread issues the Xp store, the MMAs and the commits, so each
           // commit tracks that thread's MMAs and the store's bulk group.
@@ -1370,9 +1401,11 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
             }
             if (store_xp) bulk_wait_read<0>();
             tc_commit_pair(&empty[s], kEmptyMask);
+            MOE_TL(tl_n, 3);
           }
           __syncwarp();
         }
+        ++tl_n;
         if (++s == S) {
           s = 0;
           ph ^= 1u;
@@ -2577,6 +2610,20 @@ cudaError_t launch_gemm_pair(GemmMode mode, const GemmLaunch& L, Maps& m, const 
 }  // namespace
 
 bool tensor_map_encoder_ready() { return encoder() != nullptr; }
+
+#ifdef MOE_TIMELINE
+// Diagnosis builds only (-DMOE_TIMELINE; no declaration in the public header):
+// points the pair kernels' timeline at a device buffer of cap * 5 stamps per
+// CTA, for the GEMM mode `mode` (0 fwd1 ... 5 wgrad2); buf = null switches it off.
+extern "C" MOE_API int moe_debug_timeline(void* buf, int cap, int mode) {
+  unsigned long long* b = static_cast<unsigned long long*>(buf);
+  if (cudaMemcpyToSymbol(g_tl_buf, &b, sizeof(b)) != cudaSuccess ||
+      cudaMemcpyToSymbol(g_tl_cap, &cap, sizeof(cap)) != cudaSuccess ||
+      cudaMemcpyToSymbol(g_tl_mode, &mode, sizeof(mode)) != cudaSuccess)
+    return MOE_ERR_LAUNCH;
+  return MOE_OK;
+}
+#endif
 
 cudaError_t launch_fused_backward(const GemmLaunch& L, int32_t* cursor, int32_t* cnt_d2, int32_t* cnt_e,
                                   cudaStream_t s, LaunchHook& hook) {

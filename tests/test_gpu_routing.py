@@ -1,9 +1,12 @@
 """Routing tables on the GPU vs the CPU oracle, bit-exact, over many (T, E, k).
 
-Covers both top-k kernels (four threads per token where E % 4 == 0, E <= 256
-and k <= 8; one warp per token otherwise), ragged token counts (not multiples
-of the 64-token CTA or the 256-token chunk), and logits with many exact ties:
-values drawn from a few levels, and every logit equal.  Ties must go to the
+Covers the three top-k kernels (one thread per token where E is 32, 64, 128 or
+256 and k <= 8; four threads per token for the other E % 4 == 0, E <= 256,
+k <= 8; one warp per token otherwise), ragged token counts (not multiples of
+the 64-token CTA or the 256-token chunk), logits with many exact ties (values
+drawn from a few levels, and every logit equal) and logits that differ only in
+their last bits (distinct values a few ulps apart, which the one-thread kernel's
+packed keys cannot order and must hand to its exact path).  Ties must go to the
 lower expert id ("UniEP", section 3.1: a deterministic mapping; the gating reading
 of the layer: descending logit, ties to the lower id).
 """
@@ -18,11 +21,11 @@ pytestmark = pytest.mark.gpu
 # (T, E, k): E % 4 == 0 and k <= 8 take the four-threads-per-token kernel.
 SHAPES = [
     (1, 4, 4), (63, 8, 2), (300, 12, 3), (1000, 20, 5), (777, 64, 6), (1500, 100, 8), (2049, 128, 8),
-    (520, 256, 8), (333, 256, 1),
+    (520, 256, 8), (333, 256, 1), (4000, 32, 8), (100, 32, 1), (700, 128, 3), (65, 64, 8),
     # the warp-per-token kernel
     (500, 6, 2), (400, 260, 4), (300, 64, 9), (129, 1, 1),
 ]
-KINDS = ["normal", "levels", "equal"]
+KINDS = ["normal", "levels", "equal", "close"]
 
 
 def _logits(T, E, kind, seed):
@@ -31,6 +34,8 @@ def _logits(T, E, kind, seed):
         return torch.randn(T, E, generator=g)
     if kind == "levels":  # five levels: most rows hold ties at the threshold
         return torch.randint(0, 5, (T, E), generator=g).float() * 0.5 - 1.0
+    if kind == "close":  # 0.5 plus a few multiples of 2^-21: distinct values 8 ulps apart, some exact ties
+        return 0.5 + torch.randint(0, 6, (T, E), generator=g).float() * 2.0 ** -21
     return torch.full((T, E), 0.75)
 
 
