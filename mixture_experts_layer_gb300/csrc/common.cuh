@@ -128,16 +128,6 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
-// Bulk copy of `bytes` contiguous bytes (a multiple of 16; both addresses 16-byte
-// aligned) from global to this CTA's shared memory, completing on an mbarrier.
-__device__ __forceinline__ void bulk_load_1d(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // TMA row gather: rows r0..r3 of a 2D tensor, columns [x, x + box width), into
 // four consecutive box rows at smem_dst (the map's box is one row high).
 __device__ __forceinline__ void tma_gather4(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int32_t x,

@@ -1009,7 +1009,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 // ---------------------------------------------------------------------------
 // Pipeline timeline of the pair kernels, for diagnosis only: compiled in with
 // -DMOE_TIMELINE (never in a normal build).  With moe_debug_timeline() set,
-// the pair kernel of the selected mode stamps %globaltimer for every k-block
+// the pair kernel of the selected mode stamps its SM's cycle counter (clock64,
+// cheap enough not to disturb the pipeline much) for every k-block
 // n < cap of every CTA into buf[(cta * cap + n) * 5 + event]: 0 the producer
 // found the stage free, 1 the MMA warp saw it land, 2 the leader saw the
 // partner's stage (the relay: the odd CTA's arrive), 3 the MMAs and the commit
@@ -1021,7 +1022,7 @@ __device__ int g_tl_mode = -1;
 template <int MODE>
 __device__ __forceinline__ void tl_mark(int n, int ev) {
   if (g_tl_mode == MODE && g_tl_buf != nullptr && n < g_tl_cap)
-    g_tl_buf[(static_cast<size_t>(blockIdx.x) * g_tl_cap + n) * 5 + ev] = globaltimer();
+    g_tl_buf[(static_cast<size_t>(blockIdx.x) * g_tl_cap + n) * 5 + ev] = static_cast<unsigned long long>(clock64());
 }
 #define MOE_TL(n, ev) tl_mark<MODE>((n), (ev))
 #else

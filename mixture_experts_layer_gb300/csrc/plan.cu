@@ -393,258 +393,6 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk4_kernel(const float* 
     if (cnt[e] != 0) atomicAdd(&ccount[static_cast<size_t>(e) * ((T + kChunk - 1) / kChunk) + chunk], cnt[e]);
 }
 
-// ---------------------------------------------------------------------------
-// One thread per token, for E in {32, 64, 128, 256} and k <= 8.
-//
-// The CTA's 64 rows of logits arrive in shared memory by one bulk copy; each
-// thread then selects its token's top k without talking to other threads:
-//   1. the E values form 32 groups of G = E / 32 neighbours; each group's max;
-//   2. the k groups with the largest maxima (a network on 32-bit keys: the
-//      order-preserving image of the max with its low 5 bits replaced by the
-//      group number).  The k-th largest value is at least the k-th largest
-//      group max, so the top k lie in those groups;
-//   3. the top k of those k*G values (the same network on keys carrying the
-//      candidate's index in their low bits), in descending order.
-// Keys drop the low 5 or 6 bits of the value, so two values that agree in the
-// kept bits could be misordered: a token whose chosen keys, or whose boundary
-// at the k-th place (group or value), share the kept bits is instead handled
-// exactly by k scans of its row in the total order (value desc, id asc), as is
-// a token with a non-finite logit (read as -inf, and reported).  Both paths give
-// the same ids and weights as the other top-k kernels.
-// ---------------------------------------------------------------------------
-constexpr int kTopk1Threads = kTopkTokens;  // one thread per token
-
-// Order-preserving map of a float to an unsigned integer (finite values and -inf).
-__device__ __forceinline__ uint32_t ord_key(float f) {
-  const uint32_t u = __float_as_uint(f);
-  return u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
-}
-
-__device__ __forceinline__ void cxu(uint32_t& a, uint32_t& b) {
-  const uint32_t hi = max(a, b), lo = min(a, b);
-  a = hi;
-  b = lo;
-}
-
-// Sorts 8 keys descending (Batcher's odd-even merge sort, 19 comparators).
-__device__ __forceinline__ void sort8u(uint32_t* a) {
-  cxu(a[0], a[1]); cxu(a[2], a[3]); cxu(a[4], a[5]); cxu(a[6], a[7]);
-  cxu(a[0], a[2]); cxu(a[1], a[3]); cxu(a[4], a[6]); cxu(a[5], a[7]);
-  cxu(a[1], a[2]); cxu(a[5], a[6]);
-  cxu(a[0], a[4]); cxu(a[1], a[5]); cxu(a[2], a[6]); cxu(a[3], a[7]);
-  cxu(a[2], a[4]); cxu(a[3], a[5]);
-  cxu(a[1], a[2]); cxu(a[3], a[4]); cxu(a[5], a[6]);
-}
-
-// a := the 8 largest of a and b (both sorted descending), sorted descending.
-__device__ __forceinline__ void merge8u_top(uint32_t* a, const uint32_t* b) {
-#pragma unroll
-  for (int m = 0; m < 8; ++m) a[m] = max(a[m], b[7 - m]);
-#pragma unroll
-  for (int d = 4; d > 0; d >>= 1)
-#pragma unroll
-    for (int m = 0; m < 8; ++m)
-      if ((m & d) == 0) cxu(a[m], a[m + d]);
-}
-
-// s := the 8 largest of the N keys v (N a multiple of 8), sorted descending.
-// v is overwritten.
-template <int N>
-__device__ __forceinline__ void top8u(uint32_t* v, uint32_t* s) {
-#pragma unroll
-  for (int b = 0; b < N / 8; ++b) sort8u(v + 8 * b);
-#pragma unroll
-  for (int m = 0; m < 8; ++m) s[m] = v[m];
-#pragma unroll
-  for (int b = 1; b < N / 8; ++b) merge8u_top(s, v + 8 * b);
-}
-
-// G consecutive floats of shared memory at p (G in {1, 2, 4, 8}; p aligned to 4 G bytes).
-template <int G>
-__device__ __forceinline__ void lds_group(const float* p, float* v) {
-  if (G == 8) {
-    const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-  } else if (G == 4) {
-    const float4 a = *reinterpret_cast<const float4*>(p);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-  } else if (G == 2) {
-    const float2 a = *reinterpret_cast<const float2*>(p);
-    v[0] = a.x; v[1] = a.y;
-  } else {
-    v[0] = p[0];
-  }
-}
-
-template <int E>
-__global__ void __launch_bounds__(kTopk1Threads, 6) route_topk1_kernel(const float* __restrict__ logits, int T, int k,
-                                                                       int32_t* __restrict__ ids,
-                                                                       float* __restrict__ wts,
-                                                                       uint32_t* __restrict__ gbm,
-                                                                       int32_t* __restrict__ ccount, WsHeader* ws) {
-  constexpr int G = E / 32;                                      // values per group
-  constexpr int NC = 8 * G;                                      // candidate values (k <= 8 groups)
-  constexpr int IB = NC <= 8 ? 3 : NC <= 16 ? 4 : NC <= 32 ? 5 : 6;  // index bits of a candidate key
-  constexpr uint32_t IMASK = (1u << IB) - 1u;
-  extern __shared__ __align__(128) uint8_t smraw[];
-  float* rows = reinterpret_cast<float*>(smraw);              // [64][E] this CTA's logits
-  uint32_t* bm = reinterpret_cast<uint32_t*>(rows + kTopkTokens * E);  // [E][2] bitmap words
-  int* cnt = reinterpret_cast<int*>(bm + 2 * E);              // [E]
-  __shared__ __align__(8) uint64_t bar;
-  const int t0 = blockIdx.x * kTopkTokens;
-  const int ntok = min(kTopkTokens, T - t0);
-  for (int i = threadIdx.x; i < 3 * E; i += blockDim.x) bm[i] = 0;  // bm and cnt
-  if (threadIdx.x == 0) {
-    mbar_init(&bar, 1);
-    mbar_fence_init();
-    const uint32_t bytes = static_cast<uint32_t>(ntok) * E * 4;
-    mbar_arrive_expect_tx(&bar, bytes);
-    bulk_load_1d(rows, logits + static_cast<size_t>(t0) * E, bytes, &bar);
-  }
-  __syncthreads();
-  const bool landed = mbar_wait(&bar, 0, ws, 6, nullptr);
-  const int tl = threadIdx.x;
-  const int t = t0 + tl;
-  if (tl < ntok && landed) {
-    const float* row = rows + tl * E;
-    // 1. group maxima (groups visited from a per-thread start: no bank conflicts)
-    float gm[32];
-    float acc = 0.f;  // NaN iff some logit is NaN or infinite
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      float v[G];
-      lds_group<G>(row + ((i + tl) & 31) * G, v);
-      float m = v[0];
-#pragma unroll
-      for (int j = 0; j < G; ++j) {
-        acc = fmaf(v[j], 0.f, acc);
-        if (j > 0) m = fmaxf(m, v[j]);
-      }
-      gm[i] = m;
-    }
-    bool fast = acc == acc;
-    if (!fast) report(ws, MOE_ERR_NONFINITE, 0, t);
-    // 2. the k groups with the largest maxima
-    uint32_t key[NC > 32 ? NC : 32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) key[i] = (ord_key(gm[i]) & ~31u) | (31u - static_cast<uint32_t>((i + tl) & 31));
-    uint32_t gs[8];
-    {
-      uint32_t gk[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) gk[i] = key[i];
-      top8u<32>(gk, gs);
-    }
-    uint32_t gth = gs[0];
-#pragma unroll
-    for (int m = 1; m < 8; ++m)
-      if (m == k - 1) gth = gs[m];
-    int nge = 0;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) nge += (key[i] >> 5) >= (gth >> 5) ? 1 : 0;
-    fast = fast && nge == k;
-    // 3. the top k of the chosen groups' values; gid of chosen group m in bits 5m..5m+4
-    uint64_t gids = 0;
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const uint32_t gid = 31u - (gs[m] & 31u);
-      gids |= static_cast<uint64_t>(gid) << (5 * m);
-      float v[G];
-      lds_group<G>(row + gid * G, v);
-#pragma unroll
-      for (int j = 0; j < G; ++j)
-        key[m * G + j] = (m < k) ? ((ord_key(v[j]) & ~IMASK) | static_cast<uint32_t>(m * G + j)) : 0u;
-    }
-    uint32_t es[8];
-    {
-      uint32_t ck[NC];
-#pragma unroll
-      for (int c = 0; c < NC; ++c) ck[c] = key[c];
-      top8u<NC>(ck, es);
-    }
-    uint32_t eth = es[0];
-#pragma unroll
-    for (int m = 1; m < 8; ++m) {
-      if (m < k) fast = fast && (es[m - 1] >> IB) != (es[m] >> IB);
-      if (m == k - 1) eth = es[m];
-    }
-    int cge = 0;
-#pragma unroll
-    for (int c = 0; c < NC; ++c) cge += (key[c] >> IB) >= (eth >> IB) ? 1 : 0;
-    fast = fast && cge == k;
-
-    int se[8];
-    float sx[8];
-    if (fast) {
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const int idx = static_cast<int>(es[m] & IMASK);
-        const int mg = idx / G, j = idx - mg * G;
-        const int gid = static_cast<int>((gids >> (5 * mg)) & 31u);
-        se[m] = gid * G + j;
-        sx[m] = row[se[m]];
-      }
-    } else {
-      // Exact: the m-th pick is the largest value after the (m-1)-th in the
-      // total order (value desc, id asc); non-finite values count as -inf.
-      float px = INFINITY;
-      int pe = -1;
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        if (m < k) {
-          float bx = -INFINITY;
-          int be = E;
-          for (int e = 0; e < E; ++e) {
-            float x = row[e];
-            if (!isfinite(x)) x = -INFINITY;
-            const bool after = x < px || (x == px && e > pe);
-            if (after && (x > bx || be == E)) {
-              bx = x;
-              be = e;
-            }
-          }
-          se[m] = be;
-          sx[m] = bx;
-          px = bx;
-          pe = be;
-        } else {
-          se[m] = 0;
-          sx[m] = -INFINITY;
-        }
-      }
-    }
-    // Weights: exp(x_m - x_0) / sum over the k in slot order.
-    float ex[8];
-    float sum = 0.f;
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      ex[m] = (m < k) ? expf(sx[m] - sx[0]) : 0.f;
-      if (m < k) sum += ex[m];
-    }
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      if (m < k) {
-        const int e = se[m];
-        if (e < 0 || e >= E) {
-          report(ws, MOE_ERR_BOUNDS, 1, t);
-          continue;
-        }
-        ids[static_cast<size_t>(t) * k + m] = e;
-        wts[static_cast<size_t>(t) * k + m] = ex[m] / sum;
-        atomicOr(&bm[e * 2 + (tl >> 5)], 1u << (tl & 31));
-        atomicAdd(&cnt[e], 1);
-      }
-    }
-  }
-  __syncthreads();
-  const int chunk = t0 / kChunk;
-  const int w0 = (t0 % kChunk) / 32;
-  uint32_t* out = gbm + static_cast<size_t>(chunk) * E * kChunkWords;
-  for (int i = threadIdx.x; i < 2 * E; i += blockDim.x) out[(i >> 1) * kChunkWords + w0 + (i & 1)] = bm[i];
-  for (int e = threadIdx.x; e < E; e += blockDim.x)
-    if (cnt[e] != 0) atomicAdd(&ccount[static_cast<size_t>(e) * ((T + kChunk - 1) / kChunk) + chunk], cnt[e]);
-}
-
 // Per expert (one CTA each): exclusive prefix of the chunk counts over the
 // chunks -- the O_all of Algorithm 1 -- and the expert's row count.  The last
 // CTA to finish (ticket) then takes the prefix over experts of the row counts
@@ -928,26 +676,7 @@ cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t s, LaunchHook& hook) {
   const size_t topk_smem = static_cast<size_t>(p.E) * 3 * 4;
   hook.before(s);
   const int nv4 = (p.E + 15) / 16;
-  if ((p.E == 32 || p.E == 64 || p.E == 128 || p.E == 256) && p.k <= kTopkFastK) {
-    const size_t smem1 = (static_cast<size_t>(kTopkTokens) + 3) * p.E * 4;
-    switch (p.E) {
-#define MOE_TOPK1_CASE(EE)                                                                                      \
-  case EE:                                                                                                      \
-    if (smem1 > 48 * 1024) {                                                                                    \
-      err = cudaFuncSetAttribute(route_topk1_kernel<EE>, cudaFuncAttributeMaxDynamicSharedMemorySize,           \
-                                 static_cast<int>(smem1));                                                      \
-      if (err != cudaSuccess) return err;                                                                       \
-    }                                                                                                           \
-    route_topk1_kernel<EE><<<nblocks, kTopk1Threads, smem1, s>>>(p.logits, p.T, p.k, p.ids, p.w, p.gbm,         \
-                                                                 p.ccount, p.ws);                               \
-    break;
-      MOE_TOPK1_CASE(32)
-      MOE_TOPK1_CASE(64)
-      MOE_TOPK1_CASE(128)
-      MOE_TOPK1_CASE(256)
-#undef MOE_TOPK1_CASE
-    }
-  } else if (p.E % 4 == 0 && p.E <= 256 && p.k <= kTopkFastK) {
+  if (p.E % 4 == 0 && p.E <= 256 && p.k <= kTopkFastK) {
     const size_t smem4 = (static_cast<size_t>(p.E) * 3 + static_cast<size_t>(kTopkTokens) * kTopkFastK) * 4;
     const bool full = (p.E % 16) == 0;
     switch ((nv4 <= 1 ? 1 : nv4 <= 2 ? 2 : nv4 <= 4 ? 4 : nv4 <= 8 ? 8 : 16) * (full ? 1 : -1)) {

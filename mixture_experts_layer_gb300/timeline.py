@@ -5,8 +5,9 @@
 Builds a diagnosis copy of the library with -DMOE_TIMELINE
 (libmoe_timeline.so, never loaded by the product), runs one step of the
 workload, then runs the forward or backward again with the pair kernel of the
-chosen GEMM mode stamping %globaltimer at five points of its pipeline, for
-every k-block of every CTA:
+chosen GEMM mode stamping its SM's cycle counter (clock64) at five points of
+its pipeline, for every k-block of every CTA (the points of one k-block are all
+taken in the same CTA, so they share a clock):
 
     0  the producer warp found the shared-memory stage free (its TMA loads follow)
     1  the MMA warp saw the stage land (both operands of this CTA's half)
@@ -14,9 +15,10 @@ every k-block of every CTA:
     3  the leader issued the k-block's MMAs and their commit
     4  (first k-block of a tile) the leader got a free accumulator
 
-and prints a summary: the k-block cadence of the MMA issue against the time the
-tensor core needs for a k-block at the measured SM clock, the load latency
-(issue to landing), and where the MMA thread waits.  Modes: 0 fwd1, 1 fwd2,
+and prints a summary in SM cycles: the k-block cadence of the MMA issue
+against the cycles the tensor cores need for a pair k-block (256 x 256 x 64 on
+two SMs: 512 cycles), the load latency (issue to landing), and where the MMA
+thread waits.  Modes: 0 fwd1, 1 fwd2,
 2 dgrad2, 3 dgrad1, 4 wgrad13, 5 wgrad2.  Needs a GB300.
 """
 from __future__ import annotations
@@ -41,8 +43,8 @@ def _pct(v, q):
     return v[min(len(v) - 1, int(q * (len(v) - 1)))] if v else float("nan")
 
 
-def summarise(stamps, ncta, cap, sm_mhz, mma_cycles):
-    """stamps: list of ncta*cap*5 integers (ns, 0 = not recorded)."""
+def summarise(stamps, ncta, cap, mma_cycles):
+    """stamps: list of ncta*cap*5 integers (SM cycles, 0 = not recorded)."""
     cad, lat, wait_full, wait_relay, issue_gap = [], [], [], [], []
     kblocks = []
     for c in range(ncta):
@@ -62,15 +64,15 @@ def summarise(stamps, ncta, cap, sm_mhz, mma_cycles):
                     wait_relay.append(max(0, b[2] - b[1]))
                 if b[2]:
                     issue_gap.append(max(0, b[3] - b[2]))
-    mma_ns = mma_cycles / (sm_mhz * 1e-3)
     return {
         "ctas": ncta, "kblocks_recorded_per_cta_median": statistics.median(kblocks) if kblocks else 0,
-        "mma_issue_cadence_ns": {"p10": _pct(cad, 0.1), "median": _pct(cad, 0.5), "p90": _pct(cad, 0.9)},
-        "mma_time_per_kblock_ns_at_clock": round(mma_ns, 1),
-        "load_latency_issue_to_land_ns": {"p10": _pct(lat, 0.1), "median": _pct(lat, 0.5), "p90": _pct(lat, 0.9)},
-        "mma_thread_wait_for_own_stage_ns": {"median": _pct(wait_full, 0.5), "p90": _pct(wait_full, 0.9)},
-        "leader_wait_for_partner_stage_ns": {"median": _pct(wait_relay, 0.5), "p90": _pct(wait_relay, 0.9)},
-        "relay_to_mma_issued_ns": {"median": _pct(issue_gap, 0.5), "p90": _pct(issue_gap, 0.9)},
+        "unit": "SM cycles",
+        "mma_issue_cadence": {"p10": _pct(cad, 0.1), "median": _pct(cad, 0.5), "p90": _pct(cad, 0.9)},
+        "mma_cycles_per_kblock": mma_cycles,
+        "load_latency_issue_to_land": {"p10": _pct(lat, 0.1), "median": _pct(lat, 0.5), "p90": _pct(lat, 0.9)},
+        "mma_thread_wait_for_own_stage": {"median": _pct(wait_full, 0.5), "p90": _pct(wait_full, 0.9)},
+        "leader_wait_for_partner_stage": {"median": _pct(wait_relay, 0.5), "p90": _pct(wait_relay, 0.9)},
+        "relay_to_mma_issued": {"median": _pct(issue_gap, 0.5), "p90": _pct(issue_gap, 0.9)},
     }
 
 
@@ -122,19 +124,10 @@ def main():
     st = layer.status()
     if st[0] != 0:
         raise RuntimeError(f"device status {st}")
-    clk = None
-    try:
-        import subprocess
-        clk = float(subprocess.run(["nvidia-smi", "--query-gpu=clocks.sm", "--format=csv,noheader,nounits", "-i", "0"],
-                                   capture_output=True, text=True).stdout.split()[0])
-    except (OSError, ValueError, IndexError):
-        clk = 2070.0
-    # One pair k-block: 2 * 256 * N * 64 FLOP on two SMs at 8192 dense bf16 FLOP per SM per cycle.
-    n = 256
-    mma_cycles = 2 * 256 * n * 64 / (2 * 8192)
-    out = summarise(buf.cpu().tolist(), ncta, args.cap, clk, mma_cycles)
-    out.update({"workload": shape.name, "mode": MODES[args.mode], "sm_mhz_after": clk,
-                "pass_ms": round(ev[0].elapsed_time(ev[1]), 4)})
+    # One pair k-block: 2 * 256 * 256 * 64 FLOP on two SMs at 8192 dense bf16 FLOP per SM per cycle.
+    mma_cycles = 2 * 256 * 256 * 64 // (2 * 8192)
+    out = summarise(buf.cpu().tolist(), ncta, args.cap, mma_cycles)
+    out.update({"workload": shape.name, "mode": MODES[args.mode], "pass_ms": round(ev[0].elapsed_time(ev[1]), 4)})
     print(json.dumps(out, indent=1))
 
 

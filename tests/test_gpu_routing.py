@@ -1,12 +1,10 @@
 """Routing tables on the GPU vs the CPU oracle, bit-exact, over many (T, E, k).
 
-Covers the three top-k kernels (one thread per token where E is 32, 64, 128 or
-256 and k <= 8; four threads per token for the other E % 4 == 0, E <= 256,
-k <= 8; one warp per token otherwise), ragged token counts (not multiples of
-the 64-token CTA or the 256-token chunk), logits with many exact ties (values
+Covers both top-k kernels (four threads per token where E % 4 == 0, E <= 256
+and k <= 8; one warp per token otherwise), ragged token counts (not multiples
+of the 64-token CTA or the 256-token chunk), logits with many exact ties (values
 drawn from a few levels, and every logit equal) and logits that differ only in
-their last bits (distinct values a few ulps apart, which the one-thread kernel's
-packed keys cannot order and must hand to its exact path).  Ties must go to the
+their last bits (distinct values a few ulps apart).  Ties must go to the
 lower expert id ("UniEP", section 3.1: a deterministic mapping; the gating reading
 of the layer: descending logit, ties to the lower id).
 """
