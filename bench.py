@@ -753,7 +753,7 @@ def run_ours(args):
                        router="on the path: logits = x Wr on the GPU, gradient through the gating (dlogits, dWr, "
                               "dx share)" if args.router else "off (logits given; the pages time the layer "
                                                                "excluding gating)",
-                       dispatch=("inside GEMM1's A-operand load (TMA row gathers, Xp stored from the stages)"
+                       dispatch=("inside GEMM1's A-operand load (cp.async row copies, Xp stored from the stages)"
                                  if gather_fused else "its own kernel" if args.schedule == 0
                                  else "gather tasks of the fused forward"),
                        rows=("padding-free GroupGEMM (R = T*k rows)" if args.pad <= 1 else
@@ -821,7 +821,7 @@ def main():
                     help="schedule 0: 0 a separate gated-combine kernel, 1 the combine in GEMM2's epilogue")
     ap.add_argument("--dispatch", type=int, default=0, choices=[0, 1, 2],
                     help="schedule 0: 0 library default, 1 a dispatch kernel, 2 the dispatch inside GEMM1's "
-                         "A-operand load (TMA row gathers)")
+                         "A-operand load (cp.async row copies)")
     ap.add_argument("--wgrad-subbatches", type=int, default=0, choices=[0, 2],
                     help="0: bitwise-reproducible weight gradients (one reduction chain); 2: the non-bitwise "
                          "variant (two token sub-batches, the second added onto the first)")

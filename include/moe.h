@@ -154,8 +154,8 @@ typedef struct {
                        and returns; the outputs are then undefined.  0 (default): off. */
   int32_t dispatch; /* schedule 0: where the row dispatch Xp = x[row_src] runs.  0 (default) or
                        1: its own kernel (gather by row, or scatter by token when x is large).
-                       2: inside GEMM1's A-operand load: the producer warp gathers the tile's
-                       rows of x with TMA row gathers (four rows per instruction), and the
+                       2: inside GEMM1's A-operand load: the producer warp copies the tile's
+                       rows of x into the swizzled stage with 16-byte cp.async copies, and the
                        first N tile of each row block stores the gathered rows to Xp for the
                        backward ([UniEP] section 3: the dispatch workers write the GEMM's
                        operand rows).  Needs pair tiles for GEMM1 and the padding-free layout;

@@ -128,15 +128,18 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
-// TMA row gather: rows r0..r3 of a 2D tensor, columns [x, x + box width), into
-// four consecutive box rows at smem_dst (the map's box is one row high).
-__device__ __forceinline__ void tma_gather4(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int32_t x,
-                                            int32_t r0, int32_t r1, int32_t r2, int32_t r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], "
-      "[%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
-      : "memory");
+// 16-byte asynchronous copy global -> shared (L2 only), and the arrive on an
+// mbarrier that fires once every cp.async this thread issued before it has
+// landed (.noinc: the barrier's expected arrival count includes it).  The
+// copies are generic-proxy writes: a reader in the async proxy (tcgen05.mma,
+// a TMA store) needs fence.proxy.async.shared::cta after observing the barrier.
+__device__ __forceinline__ void cp_async_16(uint32_t smem_addr, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr), "l"(reinterpret_cast<uint64_t>(gsrc))
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {

@@ -82,7 +82,6 @@ struct Maps {
   CUtensorMap b1;  // second B tensor (W3), full-width box
   CUtensorMap b2;  // B, 128-row box for a 128-wide tail tile (K-major B only)
   CUtensorMap b3;  // W3, 128-row box
-  CUtensorMap gx;  // x [T, H], 64 x 1 box: the rows GEMM1 gathers for its A operand
   CUtensorMap a64; // A operand, 64-row box: the 64 rows of an M = 128 pair tile's CTA
   CUtensorMap gu;  // dgrad2 epilogue: GU [R, 2F], 16-column x 32-row boxes, 32-byte swizzle
   // Pair tiles, MN-major operands: 3-D views {64 columns, rows, 64-column panels}
@@ -121,8 +120,10 @@ struct GemmParams {
   int sb;
   const int32_t* sb_rows;
   // GEMM1 with the dispatch in its A-operand load: A rows are gathered from x by
-  // row_src (TMA gather4) and the first N tile of each row block stores them to Xp.
+  // row_src (16-byte cp.async copies into the swizzled stage) and the first N tile
+  // of each row block stores them to Xp.
   int gather;
+  const __nv_bfloat16* x;  // [T, H] (gather)
   const int32_t* row_src;
   // Pair tiles (forward and dgrad modes): an expert's last 256-row block with at
   // most 128 rows runs as an M = 128 pair tile, 64 rows per CTA.
@@ -1240,10 +1241,13 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
   constexpr uint32_t pair_leader = 0;
   constexpr uint16_t kEmptyMask = 0x3;  // commits arrive in both CTAs of the pair
   constexpr uint16_t tfull_mask = 0x3;
+  // Gathered A (GEMM1 with the dispatch fused): a stage is full after the B
+  // bytes and the 32 producer lanes' cp.async arrivals.
+  const bool gather_a = (MODE == kFwd1) && p.gather;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
-      mbar_init(&full[i], 1);
+      mbar_init(&full[i], gather_a ? 1 + 32 : 1);
       mbar_init(&empty[i], 1);
       mbar_init(&pfull[i], 1);
     }
@@ -1282,14 +1286,16 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
     (void)tl_n;
     for (int tile = pid; tile < ntiles && ok; tile += npairs) {
       const Tile t = pair_decode<MODE>(p, xt, tile, rank);
-      const bool gather = (MODE == kFwd1) && p.gather;
-      int src[4] = {0, 0, 0, 0};  // gather: tokens of this lane's 4 rows (rows past R read token 0, never stored)
+      const bool gather = gather_a;
+      // gather: lane l copies 16-byte chunk (l & 7) of rows 4 i + (l >> 3), i < 32, of the
+      // tile; src[i] is the token of that row (rows past R read token 0 and are never stored).
+      int src[32];
       if (gather) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int r = t.row0 + 4 * lane + j;
+        for (int i = 0; i < 32; ++i) {
+          const int r = t.row0 + 4 * i + (lane >> 3);
           const int tok = r < p.R ? __ldg(p.row_src + r) : 0;
-          src[j] = (tok >= 0 && tok < p.T) ? tok : 0;
+          src[i] = (tok >= 0 && tok < p.T) ? tok : 0;
         }
       }
       for (int kb = 0; kb < t.kblocks; ++kb) {
@@ -1302,12 +1308,21 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
         uint8_t* sA = smem + s * kPairStageBytes;
         if (gather) {
           if (elect_one()) {
-            mbar_arrive_expect_tx(&full[s], kABytes + t.nw * 64);
-            load_kblock_pair<MODE>(p, maps, t, kb, nullptr, sA + kABytes, &full[s], rank);  // B only
+            mbar_arrive_expect_tx(&full[s], t.nw * 64);  // B only: A arrives by cp.async
+            load_kblock_pair<MODE>(p, maps, t, kb, nullptr, sA + kABytes, &full[s], rank);
           }
           __syncwarp();
-          // A: the warp's 32 lanes gather the tile's 128 rows of x, 4 rows each.
-          tma_gather4(sA + lane * 4 * 128, &maps.gx, &full[s], kb * BK, src[0], src[1], src[2], src[3]);
+          // A: 128 rows x 128 bytes of x into the 128-byte-swizzled stage (chunk c of
+          // row r at chunk c ^ (r & 7)); a warp-wide copy covers four whole rows.
+          const int c = lane & 7;
+          const uint32_t a_base = smem_u32(sA);
+          const __nv_bfloat16* xk = p.x + kb * BK + 8 * c;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int r = 4 * i + (lane >> 3);
+            cp_async_16(a_base + r * 128 + ((c ^ (r & 7)) << 4), xk + static_cast<size_t>(src[i]) * p.H);
+          }
+          cp_async_mbar_arrive_noinc(&full[s]);
         } else if (elect_one()) {
           if (t.halfm) {  // M = 128 pair tile: 64 A rows per CTA
             mbar_arrive_expect_tx(&full[s], kABytes / 2 + t.nw * 64);
@@ -1368,6 +1383,7 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
         __syncwarp();
         if (!leader) {
           if (lane == 0) {
+            if (gather_a) fence_proxy_async_smem();  // the cp.async rows, for the MMA and the Xp store
             if (store_xp) {
               tma_store_2d(&maps.a, sA, kb * BK, t.row0);
               bulk_commit();
@@ -1387,6 +1403,7 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
           // One elected thread issues the Xp store, the MMAs and the commits, so each
           // commit tracks that thread's MMAs and the store's bulk group.
           if (elect_one()) {
+            if (gather_a) fence_proxy_async_smem();  // the cp.async rows, for the MMA and the Xp store
             if (store_xp) {
               tma_store_2d(&maps.a, sA, kb * BK, t.row0);
               bulk_commit();
@@ -2805,9 +2822,9 @@ cudaError_t launch_gemm(GemmMode mode, const GemmLaunch& L, cudaStream_t s, Laun
            make_map(&m.b1, L.W3, F, E * H, 64, 64);
       p.out0 = static_cast<__nv_bfloat16*>(L.out_h);
       p.out1 = static_cast<__nv_bfloat16*>(L.out_GU);
-      if (L.gather) {  // pair tiles only: the A rows come from x, one row per box
+      if (L.gather) {  // pair tiles only: the A rows come from x by cp.async
         if (!L.pair) return cudaErrorInvalidValue;
-        ok = ok && make_map(&m.gx, L.x, H, static_cast<uint64_t>(L.T), 64, 1);
+        p.x = static_cast<const __nv_bfloat16*>(L.x);
         p.gather = 1;
         p.row_src = L.row_src;
       }

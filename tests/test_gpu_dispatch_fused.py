@@ -1,6 +1,7 @@
 """The dispatch inside GEMM1's A-operand load (moe_opts.dispatch = 2): the
-producer warp gathers each tile's rows of x with TMA row gathers, and the first
-N tile of each row block stores them to Xp for the backward ("UniEP", section
+producer warp copies each tile's rows of x into the swizzled stage with 16-byte
+cp.async copies, and the first N tile of each row block stores them to Xp for
+the backward ("UniEP", section
 3: the dispatch workers deliver the GEMM's operand rows; "MoonEP": zero-copy
 dispatch into the expert-grouped layout).
 
