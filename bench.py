@@ -644,8 +644,9 @@ def run_ours(args):
     # memory and reads its results (out, dx) back to pinned host memory.  The copies
     # run on a copy stream, double-buffered, the way a training loop overlaps its
     # data movement with compute: step i+1's inputs are uploaded while step i
-    # computes, and step i's results (staged by one device copy) download while
-    # step i+1 computes.  The timed region ends when the last download is done.
+    # computes, and step i's results (written by the layer straight into buffer set
+    # i mod 2: the C ABI takes out and dx per call) download while step i+1 computes.
+    # The timed region ends when the last download is done.
     h_x = inp["x"].cpu().pin_memory()
     h_lg = inp["logits"].cpu().pin_memory()
     h_do = inp["dout"].cpu().pin_memory()
@@ -653,13 +654,13 @@ def run_ours(args):
     h_dx = torch.empty_like(h_x).pin_memory()
     d_in = [(torch.empty_like(inp["x"]), torch.empty_like(inp["logits"]), torch.empty_like(inp["dout"]))
             for _ in range(2)]
-    d_stage = [(torch.empty_like(layer.out), torch.empty_like(layer.dx)) for _ in range(2)]
+    d_res = [(torch.empty_like(layer.out), torch.empty_like(layer.dx)) for _ in range(2)]  # out, dx per buffer set
     cs = torch.cuda.Stream(dev)     # uploads
     cs_d = torch.cuda.Stream(dev)   # downloads (a copy engine of their own)
     ev_in = [torch.cuda.Event() for _ in range(2)]      # inputs j uploaded
     ev_used = [torch.cuda.Event() for _ in range(2)]    # compute done with inputs j
-    ev_staged = [torch.cuda.Event() for _ in range(2)]  # results staged in j
-    ev_out = [torch.cuda.Event() for _ in range(2)]     # staged results j downloaded
+    ev_staged = [torch.cuda.Event() for _ in range(2)]  # results j written
+    ev_out = [torch.cuda.Event() for _ in range(2)]     # results j downloaded
     for j in range(2):
         for ev in (ev_used[j], ev_out[j]):
             ev.record(stream)
@@ -679,11 +680,11 @@ def run_ours(args):
         if args.router:
             layer.router_forward(d_x, inp["Wr"], opts=base_opts)
         layer.plan(layer.logits if args.router else d_lg)
-        layer.forward(d_x, inp["W1"], inp["W3"], inp["W2"], opts=base_opts)
+        # out and dx go straight to buffer set j (the ABI takes them per call), which is
+        # downloaded while the next step computes into set j ^ 1.
+        layer.forward(d_x, inp["W1"], inp["W3"], inp["W2"], opts=base_opts, out=d_res[j][0])
         layer.backward(d_do, inp["W1"], inp["W3"], inp["W2"], opts=base_opts,
-                       router=(d_x, inp["Wr"]) if args.router else None)
-        d_stage[j][0].copy_(layer.out)
-        d_stage[j][1].copy_(layer.dx)
+                       router=(d_x, inp["Wr"]) if args.router else None, dx=d_res[j][1])
 
     # One graph per input/staging buffer set, as in the device-timed region.
     e2e_graphs = [None, None]
@@ -700,7 +701,7 @@ def run_ours(args):
     def e2e_step(i, last):
         j = i & 1
         stream.wait_event(ev_in[j])
-        stream.wait_event(ev_out[j])  # staging j downloaded (two steps ago)
+        stream.wait_event(ev_out[j])  # results j downloaded (two steps ago)
         if e2e_graphs[j] is not None:
             e2e_graphs[j].replay()
         else:
@@ -711,8 +712,8 @@ def run_ours(args):
             upload(j ^ 1)
         cs_d.wait_event(ev_staged[j])
         with torch.cuda.stream(cs_d):
-            h_out.copy_(d_stage[j][0], non_blocking=True)
-            h_dx.copy_(d_stage[j][1], non_blocking=True)
+            h_out.copy_(d_res[j][0], non_blocking=True)
+            h_dx.copy_(d_res[j][1], non_blocking=True)
         ev_out[j].record(cs_d)
 
     def e2e_run(n):

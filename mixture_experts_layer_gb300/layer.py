@@ -103,23 +103,27 @@ class MoELayer:
         check(moe_plan(self.dims, logits.data_ptr(), self.plan_s, self.ws.data_ptr(), self.ws_bytes,
                        self._stream(stream)), "moe_plan")
 
-    def forward(self, x, W1, W3, W2, opts=None, stream=None):
+    def forward(self, x, W1, W3, W2, opts=None, stream=None, out=None):
+        """out: a [T, H] bf16 tensor to write the layer output to (default self.out)."""
+        out = self.out if out is None else out
         check(moe_forward(self.dims, x.data_ptr(), W1.data_ptr(), W3.data_ptr(), W2.data_ptr(), self.plan_s,
-                          self.saved, self.out.data_ptr(), self.ws.data_ptr(), self.ws_bytes, opts,
+                          self.saved, out.data_ptr(), self.ws.data_ptr(), self.ws_bytes, opts,
                           self._stream(stream)), "moe_forward")
-        return self.out
+        return out
 
-    def backward(self, dout, W1, W3, W2, opts=None, stream=None, router=None):
-        """router: (x, Wr) to carry the gradient on through the gating (dlogits, dWr, dx's router share)."""
+    def backward(self, dout, W1, W3, W2, opts=None, stream=None, router=None, dx=None):
+        """router: (x, Wr) to carry the gradient on through the gating (dlogits, dWr, dx's router share).
+        dx: a [T, H] bf16 tensor to write the input gradient to (default self.dx)."""
+        dx = self.dx if dx is None else dx
         r = None
         if router is not None:
             x, Wr = router
             r = moe_router_t(x.data_ptr(), Wr.data_ptr(), self.dlogits.data_ptr(), self.dWr.data_ptr())
         check(moe_backward(self.dims, dout.data_ptr(), W1.data_ptr(), W3.data_ptr(), W2.data_ptr(), self.plan_s,
-                           self.saved, self.grads, self.dx.data_ptr(), self.dW1.data_ptr(), self.dW3.data_ptr(),
+                           self.saved, self.grads, dx.data_ptr(), self.dW1.data_ptr(), self.dW3.data_ptr(),
                            self.dW2.data_ptr(), self.dgate.data_ptr(), self.ws.data_ptr(), self.ws_bytes, opts,
                            self._stream(stream), r), "moe_backward")
-        return self.dx
+        return dx
 
     def router_forward(self, x, Wr, opts=None, stream=None):
         """logits = x Wr (fp32) into self.logits."""
