@@ -655,25 +655,32 @@ def run_ours(args):
     d_in = [(torch.empty_like(inp["x"]), torch.empty_like(inp["logits"]), torch.empty_like(inp["dout"]))
             for _ in range(2)]
     d_res = [(torch.empty_like(layer.out), torch.empty_like(layer.dx)) for _ in range(2)]  # out, dx per buffer set
-    cs = torch.cuda.Stream(dev)     # uploads
-    cs_d = torch.cuda.Stream(dev)   # downloads (a copy engine of their own)
-    ev_in = [torch.cuda.Event() for _ in range(2)]      # inputs j uploaded
+    # Two upload and two download streams, so the two large tensors each way move on
+    # copy engines of their own at the same time.
+    cs, cs2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)       # uploads: x (+ logits), dout
+    cs_d, cs_d2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)   # downloads: out, dx
+    ev_in = [torch.cuda.Event() for _ in range(2)]      # x (and logits) j uploaded
+    ev_in2 = [torch.cuda.Event() for _ in range(2)]     # dout j uploaded
     ev_used = [torch.cuda.Event() for _ in range(2)]    # compute done with inputs j
     ev_staged = [torch.cuda.Event() for _ in range(2)]  # results j written
-    ev_out = [torch.cuda.Event() for _ in range(2)]     # results j downloaded
+    ev_out = [torch.cuda.Event() for _ in range(2)]     # out j downloaded
+    ev_out2 = [torch.cuda.Event() for _ in range(2)]    # dx j downloaded
     for j in range(2):
-        for ev in (ev_used[j], ev_out[j]):
+        for ev in (ev_used[j], ev_out[j], ev_out2[j]):
             ev.record(stream)
 
     def upload(j):
+        d_x, d_lg, d_do = d_in[j]
         cs.wait_event(ev_used[j])
         with torch.cuda.stream(cs):
-            d_x, d_lg, d_do = d_in[j]
             d_x.copy_(h_x, non_blocking=True)
             if not args.router:
                 d_lg.copy_(h_lg, non_blocking=True)
-            d_do.copy_(h_do, non_blocking=True)
         ev_in[j].record(cs)
+        cs2.wait_event(ev_used[j])
+        with torch.cuda.stream(cs2):
+            d_do.copy_(h_do, non_blocking=True)
+        ev_in2[j].record(cs2)
 
     def compute(j):
         d_x, d_lg, d_do = d_in[j]
@@ -701,7 +708,9 @@ def run_ours(args):
     def e2e_step(i, last):
         j = i & 1
         stream.wait_event(ev_in[j])
-        stream.wait_event(ev_out[j])  # results j downloaded (two steps ago)
+        stream.wait_event(ev_in2[j])
+        stream.wait_event(ev_out[j])   # results j downloaded (two steps ago)
+        stream.wait_event(ev_out2[j])
         if e2e_graphs[j] is not None:
             e2e_graphs[j].replay()
         else:
@@ -713,14 +722,18 @@ def run_ours(args):
         cs_d.wait_event(ev_staged[j])
         with torch.cuda.stream(cs_d):
             h_out.copy_(d_res[j][0], non_blocking=True)
-            h_dx.copy_(d_res[j][1], non_blocking=True)
         ev_out[j].record(cs_d)
+        cs_d2.wait_event(ev_staged[j])
+        with torch.cuda.stream(cs_d2):
+            h_dx.copy_(d_res[j][1], non_blocking=True)
+        ev_out2[j].record(cs_d2)
 
     def e2e_run(n):
         upload(0)
         for i in range(n):
             e2e_step(i, i == n - 1)
         stream.wait_event(ev_out[(n - 1) & 1])
+        stream.wait_event(ev_out2[(n - 1) & 1])
 
     e2e_run(max(3, args.warmup))
     torch.cuda.synchronize()
@@ -728,8 +741,8 @@ def run_ours(args):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    cs.wait_event(e0)
-    cs_d.wait_event(e0)
+    for c in (cs, cs2, cs_d, cs_d2):
+        c.wait_event(e0)
     e2e_run(args.steps)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -767,8 +780,8 @@ def run_ours(args):
         "roofline": roof,
         "e2e": {"value": round(world * T * args.steps / (e2e_ms * 1e-3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "copies": "pinned host <-> device on an upload and a download stream, double-buffered: step "
-                          "i+1's upload and step i's download overlap compute",
+                "copies": "pinned host <-> device on two upload and two download streams, double-buffered: "
+                          "step i+1's upload and step i's download overlap compute",
                 "launch": "CUDA graph per buffer set" if graph is not None else "eager launches"},
         "gpu_launches": int(launches),
         "kernel_timing": {"how": "CUDA event pair around each kernel on its launching stream, second timed pass of "
