@@ -30,6 +30,8 @@ CASES = {
     "empty_experts_P128": (S.LayerShape(512, 256, 256, 32, 4), 84, 8, 128),
     "one_token_P128": (S.LayerShape(1, 256, 128, 6, 2), 85, 0, 128),
     "scatter_P128": (S.LayerShape(2100, 8192, 128, 8, 2), 86, 0, 128),
+    # the largest granule the ABI accepts: nearly every grouped row is padding
+    "max_pad_P4096": (S.LayerShape(64, 128, 128, 4, 2), 87, 0, 4096),
 }
 ROWS = ("Xp", "GU", "h", "Y", "dY", "dGU", "dXp")
 TOKEN = ("out", "dx", "dgate", "dW1", "dW3", "dW2")

@@ -1,7 +1,8 @@
 """GPU path vs the CPU oracle, element by element, on small seeded layers.
 
 Sizes span several 128-row tiles, ragged expert tails, empty experts, k = 1,
-E = k, a single token and T = 0, and both N tile widths (128 and 256).
+E = k, a single token and T = 0, both N tile widths (128 and 256), and the
+largest E (1024) and k (32) the ABI accepts.
 """
 import math
 
@@ -24,6 +25,9 @@ CASES = {
     "empty_experts": (S.LayerShape(512, 256, 256, 32, 4), 16, "skew"),
     # x of 34 MB: the dispatch runs as a scatter by token instead of a gather by row
     "scatter_dispatch": (S.LayerShape(2100, 8192, 128, 8, 2), 19, None),
+    # the largest expert count and top-k the ABI accepts (E = 1024, k = 32): the warp-per-token
+    # top-k, ~9 rows per expert, many empty experts and single-row tiles
+    "max_E_k": (S.LayerShape(300, 128, 128, 1024, 32), 21, None),
 }
 
 
