@@ -83,3 +83,19 @@ def test_host_side_rejections():
         o = M.moe_opts()
         o.schedule, o.wgrad_subbatches = sched, sb
         assert M.moe_backward(*args, opts=o) == M.MOE_ERR_ARG, (sched, sb)
+
+
+def test_timeline_diagnosis_build_exports_its_hook():
+    """The pipeline timeline (-DMOE_TIMELINE) builds into a library of its own that exports
+    moe_debug_timeline, and the product library does not export it."""
+    import subprocess
+    import sys
+    from mixture_experts_layer_gb300 import build as B
+    out = os.path.join(os.path.dirname(B.LIB), "libmoe_timeline.so")
+    path = B.build(defines=("MOE_TIMELINE",), out=out)
+    # Load it in a child process: this process keeps the product library.
+    code = ("import ctypes, sys; L = ctypes.CDLL(sys.argv[1]); "
+            "print(hasattr(L, 'moe_debug_timeline'), hasattr(L, 'moe_plan'))")
+    r = subprocess.run([sys.executable, "-c", code, path], capture_output=True, text=True, timeout=120)
+    assert r.stdout.split() == ["True", "True"], r.stdout + r.stderr
+    assert not hasattr(M.lib(), "moe_debug_timeline")
