@@ -183,12 +183,15 @@ __device__ __forceinline__ void merge8_top(float* a, const float* b) {
       if ((m & d) == 0) cx_desc(a[m], a[m + d]);
 }
 
-template <int NV4, bool FULL>
+// KC: k when it is known at compile time (8, the usual value: every `m < k` test
+// of the unrolled 8-slot loops then folds away), 0 for a runtime k.
+template <int NV4, bool FULL, int KC>
 __global__ void __launch_bounds__(kTopkThreads) route_topk4_kernel(const float* __restrict__ logits, int T, int E,
-                                                                   int k, int32_t* __restrict__ ids,
+                                                                   int k_arg, int32_t* __restrict__ ids,
                                                                    float* __restrict__ wts,
                                                                    uint32_t* __restrict__ gbm,
                                                                    int32_t* __restrict__ ccount, WsHeader* ws) {
+  const int k = KC ? KC : k_arg;
   constexpr int NV = 4 * NV4;                    // values per thread
   constexpr int NB = (NV + 7) / 8;               // blocks of 8
   extern __shared__ uint32_t sm[];
@@ -682,8 +685,12 @@ cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t s, LaunchHook& hook) {
     switch ((nv4 <= 1 ? 1 : nv4 <= 2 ? 2 : nv4 <= 4 ? 4 : nv4 <= 8 ? 8 : 16) * (full ? 1 : -1)) {
 #define MOE_TOPK4_CASE(NV4, FULL)                                                                              \
   case (FULL ? NV4 : -NV4):                                                                                    \
-    route_topk4_kernel<NV4, FULL><<<nblocks, kTopkThreads, smem4, s>>>(p.logits, p.T, p.E, p.k, p.ids, p.w,    \
-                                                                       p.gbm, p.ccount, p.ws);                 \
+    if (p.k == 8)                                                                                              \
+      route_topk4_kernel<NV4, FULL, 8><<<nblocks, kTopkThreads, smem4, s>>>(p.logits, p.T, p.E, p.k, p.ids,    \
+                                                                            p.w, p.gbm, p.ccount, p.ws);       \
+    else                                                                                                       \
+      route_topk4_kernel<NV4, FULL, 0><<<nblocks, kTopkThreads, smem4, s>>>(p.logits, p.T, p.E, p.k, p.ids,    \
+                                                                            p.w, p.gbm, p.ccount, p.ws);       \
     break;
       MOE_TOPK4_CASE(1, true)
       MOE_TOPK4_CASE(2, true)
