@@ -50,7 +50,7 @@ BWD_KERNELS_ROUTER = ["router_transpose", "combine_bwd", "gemm_dgrad2_swiglu_bwd
 NB_TAIL = ["subbatch_rows", "gemm_wgrad13_sb0", "gemm_wgrad2_sb0", "gemm_wgrad13_sb1", "gemm_wgrad2_sb1"]
 BWD_KERNELS_NB = BWD_KERNELS[:4] + NB_TAIL
 BWD_KERNELS_ROUTER_NB = BWD_KERNELS_ROUTER[:7] + NB_TAIL
-N_PLAN_KERNELS = 3
+N_PLAN_KERNELS = 2
 
 
 def work_per_kernel(T, H, F, E, k):

@@ -259,12 +259,12 @@ MOE_API int moe_clear_status(void *ws, void *stream);
  * or in a process without a device allocator of its own.  There is no
  * counterpart on the pages; it is an interface convenience.
  *
- * Its scratch (per-chunk counts, bases and bitmaps) lives in one file-scope
+ * Its scratch (per-chunk and per-super-chunk counts and bitmaps) lives in one file-scope
  * device array of MOE_NOALLOC_SCRATCH_BYTES inside the library, which every GPU
  * that loads the library holds until the process exits.  The call allocates
  * and frees nothing.
  *   - Limit: dims whose scratch exceeds the buffer (roughly
- *     ceil(T/256) * E * 40 bytes plus alignment) return MOE_ERR_TOO_LARGE
+ *     ceil(T/256) * E * 37 bytes plus alignment) return MOE_ERR_TOO_LARGE
  *     before anything is launched; e.g. T = 131072 with E = 128 fits.
  *   - status: device pointer to 4 int32 (16 bytes, caller-owned, zero before
  *     first use); the first device-detected error is recorded in its first

@@ -9,6 +9,15 @@ namespace moe {
 
 constexpr int kChunk = 256;               // tokens per routing chunk (one "source" of the mapping)
 constexpr int kChunkWords = kChunk / 32;  // bitmap words per expert and chunk
+constexpr int kSuperChunks = 32;          // chunks per super-chunk (8192 tokens): the coarse level of the chunk prefix
+
+// Words of the routing's count area: a 16-word header, the per-chunk counts
+// [E][nchunks] and the per-super-chunk counts [E][nsuper], both expert-major.
+__host__ __device__ inline long long plan_count_words(long long T, int E) {
+  const long long nchunks = (T + kChunk - 1) / kChunk;
+  const long long nsuper = (nchunks + kSuperChunks - 1) / kSuperChunks;
+  return 16 + (nchunks + nsuper) * E;
+}
 constexpr int kTileRows = 128;            // rows of a GEMM tile (the tcgen05 M)
 constexpr int kMaxPad = 4096;             // largest padding granule of an expert's rows
 
@@ -69,9 +78,8 @@ struct PlanLaunch {
   int32_t* ids;
   float* w;
   uint32_t* gbm;
-  int32_t* ticket;  // 16 words, then ccount; both cleared by launch_plan
-  int32_t* ccount;  // [E][nchunks] (expert-major) = ticket + 16
-  int32_t* cbase;
+  int32_t* ticket;  // 16-word header, then ccount and the super-chunk counts; all cleared by launch_plan
+  int32_t* ccount;  // [E][nchunks] (expert-major) = ticket + 16, then [E][nsuper] super-chunk counts
   int32_t* counts;
   int32_t* offsets;
   int32_t* tiles;

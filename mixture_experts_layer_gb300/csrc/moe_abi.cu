@@ -60,7 +60,7 @@ int check_dims(const moe_dims& d) {
 }
 
 struct WsLayout {
-  size_t ccount, cbase, gbm, sched, sched_bytes, total;
+  size_t ccount, gbm, sched, sched_bytes, total;
   size_t cap;  // capacity of the 128-row tile table
   size_t wrT, dl_slot, dl_bf16, dwr_part;  // router backward
   size_t cmb_cnt, cmb_bytes;               // arrivals of the combine fused into GEMM2
@@ -86,10 +86,8 @@ WsLayout ws_layout(const moe_dims& d) {
   const size_t nchunks = (static_cast<size_t>(d.T) + kChunk - 1) / kChunk;
   WsLayout L;
   size_t off = align256(sizeof(WsHeader));
-  L.ccount = off;  // 16-word ticket, then the per-chunk counts
-  off = align256(off + (16 + nchunks * d.E) * 4);
-  L.cbase = off;
-  off = align256(off + nchunks * d.E * 4);
+  L.ccount = off;  // 16-word header, then the per-chunk and per-super-chunk counts
+  off = align256(off + static_cast<size_t>(plan_count_words(d.T, d.E)) * 4);
   L.gbm = off;
   off = align256(off + nchunks * d.E * kChunkWords * 4);
   // Scheduling words of the persistent kernels: a task cursor (padded to 64 B)
@@ -193,7 +191,7 @@ int use_pair(const moe_opts* o, GemmMode m, const moe_dims& d) {
 }
 
 
-const char* const kPlanKernels[] = {"route_topk", "route_scan", "route_rank", nullptr};
+const char* const kPlanKernels[] = {"route_topk", "route_rank", nullptr};
 const char* const kFwdKernelsFused[] = {"fused_forward", "combine", nullptr};
 const char* const kFwdKernels[] = {"gather_rows", "gemm_fwd1_swiglu", "gemm_fwd2", "combine", nullptr};
 const char* const kFwdKernelsCombineFused[] = {"gather_rows", "gemm_fwd1_swiglu", "gemm_fwd2_combine", nullptr};
@@ -300,7 +298,6 @@ int moe_plan(moe_dims d, const float* logits, const moe_plan_t* plan, void* ws, 
   p.gbm = reinterpret_cast<uint32_t*>(w + L.gbm);
   p.ticket = reinterpret_cast<int32_t*>(w + L.ccount);
   p.ccount = p.ticket + 16;
-  p.cbase = reinterpret_cast<int32_t*>(w + L.cbase);
   p.counts = plan->counts;
   p.offsets = plan->offsets;
   p.tiles = plan->tiles;

@@ -14,13 +14,14 @@
 //               E <= 256 and k <= 8; a warp-wide argmax per pick otherwise),
 //               renormalised weights, and its part of the chunk bitmap bm[e][w]
 //               whose bit b says "token 32w+b of the chunk chose expert e";
-//               per-chunk counts by integer atomics.
-//   route_scan  one CTA per expert: exclusive prefix of the counts over
-//               chunks; the last CTA takes the prefix over experts (offsets,
-//               first 128-row GEMM tile of each expert).
-//   route_rank  one CTA per chunk: stable index = popcount of the chunk's
-//               bitmap below the token; dest, row_src, row_slot; a share of
-//               the GEMM tile entries.
+//               per-chunk and per-super-chunk (32 chunks) counts by integer
+//               atomics.
+//   route_rank  one CTA per chunk: the rows of each expert before the chunk
+//               (super-chunks before it, then chunks before it in its own
+//               super-chunk) and the prefix over experts; stable index =
+//               popcount of the chunk's bitmap below the token; dest, row_src,
+//               row_slot; a share of the GEMM tile entries; CTA 0 writes the
+//               counts, offsets and expert-level tile tables.
 #include <math.h>
 
 #include <type_traits>
@@ -32,7 +33,16 @@ namespace moe {
 
 constexpr int kTopkTokens = 64;    // tokens per top-k / rank CTA: two bitmap words per expert
 constexpr int kTopkThreads = 256;  // 8 warps x 8 tokens
-constexpr int kScanThreads = 256;  // threads of a scan CTA (one CTA per expert)
+
+// A top-k CTA's count of expert e goes to its chunk's count and to its
+// super-chunk's (integer atomics: the sums do not depend on their order).
+// Counts are expert-major: ccount[e][chunk], then sc[e][chunk / kSuperChunks].
+__device__ __forceinline__ void add_counts(int32_t* ccount, int T, int E, int e, int chunk, int c) {
+  const int nchunks = (T + kChunk - 1) / kChunk;
+  const int nsuper = (nchunks + kSuperChunks - 1) / kSuperChunks;
+  atomicAdd(&ccount[static_cast<size_t>(e) * nchunks + chunk], c);
+  atomicAdd(&ccount[static_cast<size_t>(E) * nchunks + static_cast<size_t>(e) * nsuper + chunk / kSuperChunks], c);
+}
 
 // NV = logits per lane (E <= 32 * NV); TPW = tokens whose logits a warp loads
 // at once, so several rows' loads are in flight before the selection starts.
@@ -129,7 +139,7 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float* _
   uint32_t* out = gbm + static_cast<size_t>(chunk) * E * kChunkWords;
   for (int i = threadIdx.x; i < 2 * E; i += blockDim.x) out[(i >> 1) * kChunkWords + w0 + (i & 1)] = bm[i];
   for (int e = threadIdx.x; e < E; e += blockDim.x)
-    if (cnt[e] != 0) atomicAdd(&ccount[static_cast<size_t>(e) * ((T + kChunk - 1) / kChunk) + chunk], cnt[e]);
+    if (cnt[e] != 0) add_counts(ccount, T, E, e, chunk, cnt[e]);
 }
 
 // Fast path of the same selection for E % 4 == 0, E <= 256 and k <= 8: four
@@ -393,135 +403,7 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk4_kernel(const float* 
   uint32_t* out = gbm + static_cast<size_t>(chunk) * E * kChunkWords;
   for (int i = threadIdx.x; i < 2 * E; i += blockDim.x) out[(i >> 1) * kChunkWords + w0 + (i & 1)] = bm[i];
   for (int e = threadIdx.x; e < E; e += blockDim.x)
-    if (cnt[e] != 0) atomicAdd(&ccount[static_cast<size_t>(e) * ((T + kChunk - 1) / kChunk) + chunk], cnt[e]);
-}
-
-// Per expert (one CTA each): exclusive prefix of the chunk counts over the
-// chunks -- the O_all of Algorithm 1 -- and the expert's row count.  The last
-// CTA to finish (ticket) then takes the prefix over experts of the row counts
-// (offsets) and of the 128-row tile counts (first tile of each expert); the
-// tile entries themselves are written by route_rank.  With a padding granule
-// (pad >= 2) each expert's segment is its count rounded up to a multiple of
-// pad: offsets, tiles and pairs count the padded rows, gcounts holds them, and
-// the padding rows get row_src = -1, row_slot = 255.
-__global__ void __launch_bounds__(kScanThreads) route_scan_kernel(const int32_t* __restrict__ ccount,
-                                                                     int nchunks, int E, int32_t* __restrict__ cbase,
-                                                                     int32_t* __restrict__ counts,
-                                                                     int32_t* __restrict__ offsets,
-                                                                     int32_t* __restrict__ tiles,
-                                                                     int32_t* __restrict__ pairs, int32_t* ticket,
-                                                                     int pad, int R, int32_t* __restrict__ gcounts,
-                                                                     int32_t* __restrict__ row_src,
-                                                                     uint8_t* __restrict__ row_slot, WsHeader* ws) {
-  __shared__ int s_last;
-  __shared__ int s_wsum_n[32], s_wsum_m[32], s_wsum_p[32];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // One CTA per expert: thread i takes chunks [c0 + 4i, c0 + 4i + 4) of a pass
-  // of 1024, so a whole pass is one round of loads and one block-wide scan.
-  const int e = blockIdx.x;
-  const int32_t* row = ccount + static_cast<size_t>(e) * nchunks;  // expert-major: coalesced
-  int run = 0;
-  for (int c0 = 0; c0 < nchunks; c0 += 4 * kScanThreads) {
-    int v[4];
-    const int cb = c0 + 4 * static_cast<int>(threadIdx.x);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) v[u] = (cb + u < nchunks) ? __ldg(row + cb + u) : 0;
-    const int mine = v[0] + v[1] + v[2] + v[3];
-    int incl = mine;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += y;
-    }
-    if (lane == 31) s_wsum_n[warp] = incl;
-    __syncthreads();
-    int before = run + incl - mine, pass_total = 0;
-    for (int w = 0; w < kScanThreads / 32; ++w) {
-      const int ws_w = s_wsum_n[w];
-      if (w < warp) before += ws_w;
-      pass_total += ws_w;
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      if (cb + u < nchunks) cbase[static_cast<size_t>(cb + u) * E + e] = before;
-      before += v[u];
-    }
-    run += pass_total;
-    __syncthreads();  // s_wsum_n is reused by the next pass
-  }
-  if (threadIdx.x == 0) counts[e] = run;
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_last = (atomicAdd(ticket, 1) == static_cast<int>(gridDim.x) - 1);
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  // Last CTA: exclusive prefix over experts of the row counts and of the
-  // 128-row tile counts.  Thread i takes experts [i * per, (i + 1) * per).
-  const int per = (E + blockDim.x - 1) / blockDim.x;
-  const int e0 = threadIdx.x * per;
-  auto padded = [pad](int n) { return pad > 1 ? (n + pad - 1) / pad * pad : n; };
-  int my_n = 0, my_m = 0, my_p = 0;
-  for (int i = 0; i < per; ++i) {
-    const int ee = e0 + i;
-    if (ee < E) {
-      const int n = padded(__ldcg(counts + ee));
-      my_n += n;
-      my_m += (n + kTileRows - 1) / kTileRows;
-      my_p += (n + 2 * kTileRows - 1) / (2 * kTileRows);
-    }
-  }
-  int in_n = my_n, in_m = my_m, in_p = my_p;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int yn = __shfl_up_sync(0xffffffffu, in_n, off);
-    const int ym = __shfl_up_sync(0xffffffffu, in_m, off);
-    const int yp = __shfl_up_sync(0xffffffffu, in_p, off);
-    if (lane >= off) {
-      in_n += yn;
-      in_m += ym;
-      in_p += yp;
-    }
-  }
-  if (lane == 31) {
-    s_wsum_n[warp] = in_n;
-    s_wsum_m[warp] = in_m;
-    s_wsum_p[warp] = in_p;
-  }
-  __syncthreads();
-  int run_n = in_n - my_n, run_m = in_m - my_m, run_p = in_p - my_p;
-  for (int w = 0; w < warp; ++w) {
-    run_n += s_wsum_n[w];
-    run_m += s_wsum_m[w];
-    run_p += s_wsum_p[w];
-  }
-  for (int i = 0; i < per; ++i) {
-    const int ee = e0 + i;
-    if (ee >= E) break;
-    const int real = __ldcg(counts + ee);
-    const int n = padded(real);
-    gcounts[ee] = n;
-    for (int r = run_n + real; r < run_n + n; ++r) {  // the padding rows of expert ee
-      if (r < 0 || r >= R) {
-        report(ws, MOE_ERR_BOUNDS, 1, r);
-        break;
-      }
-      row_src[r] = -1;
-      row_slot[r] = 255;
-    }
-    offsets[ee] = run_n;
-    tiles[1 + ee] = run_m;
-    pairs[ee] = run_p;
-    run_n += n;
-    run_m += (n + kTileRows - 1) / kTileRows;
-    run_p += (n + 2 * kTileRows - 1) / (2 * kTileRows);
-    if (ee == E - 1) {
-      offsets[E] = run_n;
-      tiles[1 + E] = run_m;
-      tiles[0] = run_m;
-      pairs[E] = run_p;
-    }
-  }
+    if (cnt[e] != 0) add_counts(ccount, T, E, e, chunk, cnt[e]);
 }
 
 // One CTA per 256-token chunk: stable index = popcount of the chunk's bitmap
@@ -530,24 +412,36 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(const int32_t*
 // first assembled in shared memory in expert order and then written run by
 // run (contiguous stores instead of one scattered store per row).  Each CTA
 // also writes its share of the 128-row tile entries {expert, first row, rows}.
+//
+// The prefix of Algorithm 1 over the sources comes in two levels, with no
+// kernel of its own: the top-k CTAs added every count to its chunk and to its
+// super-chunk (32 chunks), so the rows of expert e in the chunks before this
+// one are the super-chunks before it plus the chunks before it in its own
+// super-chunk (at most 31), and e's total is the sum of its super-chunks.  Every
+// CTA takes the exclusive prefix over experts of the totals itself (offsets,
+// first 128-row tile, first 256-row pair); CTA 0 also writes them, the counts,
+// the GEMM row counts and, with a padding granule, the padding rows' markers.
 constexpr int kRankItems = 8;  // items per thread whose ids are loaded before the prologue
 
 __global__ void __launch_bounds__(256) route_rank_kernel(const int32_t* __restrict__ ids,
                                                          const uint32_t* __restrict__ gbm,
-                                                         const int32_t* __restrict__ cbase,
-                                                         const int32_t* __restrict__ offsets,
-                                                         const int32_t* __restrict__ gcounts,
-                                                         int32_t* __restrict__ tiles, int T, int E, int k, int R,
-                                                         int32_t* __restrict__ dest, int32_t* __restrict__ row_src,
-                                                         uint8_t* __restrict__ row_slot, WsHeader* ws) {
+                                                         const int32_t* __restrict__ ccount, int T, int E, int k,
+                                                         int R, int pad, int32_t* __restrict__ dest,
+                                                         int32_t* __restrict__ row_src,
+                                                         uint8_t* __restrict__ row_slot,
+                                                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                                         int32_t* __restrict__ tiles, int32_t* __restrict__ pairs,
+                                                         int32_t* __restrict__ gcounts, WsHeader* ws) {
   extern __shared__ uint32_t sm[];
-  __shared__ int s_wsum[8];
+  __shared__ int s_wsum[4][8];
   uint32_t* words = sm;                                      // [E][8] the chunk's bitmap words
   uint32_t* lpre = words + kChunkWords * E;                  // [E][8] rank within the chunk of each word's first token
   int* base = reinterpret_cast<int*>(lpre + kChunkWords * E);  // [E] first grouped row of the chunk's run of e
   int* loff = base + E;                                      // [E + 1] start of e's run in the staging arrays
   int* tstart = loff + E + 1;                                // [E + 1] first tile of each expert
-  int* st_src = tstart + E + 1;                              // [256 k] staging: token of each run position
+  int* offs = tstart + E + 1;                                // [E + 1] first grouped row of each expert
+  int* gcnt = offs + E + 1;                                  // [E] rows each expert's GEMMs run (padded)
+  int* st_src = gcnt + E;                                    // [256 k] staging: token of each run position
   uint16_t* st_e = reinterpret_cast<uint16_t*>(st_src + kChunk * k);  // expert of each run position
   uint8_t* st_slot = reinterpret_cast<uint8_t*>(st_e + kChunk * k);   // slot of each run position
   const int chunk = blockIdx.x;
@@ -555,6 +449,7 @@ __global__ void __launch_bounds__(256) route_rank_kernel(const int32_t* __restri
   const int n_items = min(kChunk, T - t0) * k;
   const int32_t* my_ids = ids + static_cast<size_t>(t0) * k;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool writer = blockIdx.x == 0;
   // Item i is slot i % k of token t0 + i / k.  The first kRankItems ids of
   // this thread are loaded before the prologue so their latency overlaps it.
   int ev[kRankItems];
@@ -564,16 +459,62 @@ __global__ void __launch_bounds__(256) route_rank_kernel(const int32_t* __restri
     ev[u] = (i < n_items) ? __ldg(my_ids + i) : 0;
   }
   const uint4* src = reinterpret_cast<const uint4*>(gbm + static_cast<size_t>(chunk) * E * kChunkWords);
+  const int nchunks = static_cast<int>(gridDim.x);
+  const int nsuper = (nchunks + kSuperChunks - 1) / kSuperChunks;
+  const int32_t* sc = ccount + static_cast<size_t>(E) * nchunks;
+  const int s0 = chunk / kSuperChunks;
+  auto padded = [pad](int n) { return pad > 1 ? (n + pad - 1) / pad * pad : n; };
   // Thread tid owns experts [tid * per, tid * per + per): their words, local
-  // prefixes and chunk counts; a block-wide scan of the counts gives loff.
+  // prefixes, chunk counts, rows before this chunk and totals; block-wide scans
+  // give loff (over the chunk's counts) and the expert-level prefixes.
+  // Rows of each expert before this chunk and in all.  Expert e's items are its
+  // super-chunk counts (nsuper) and the counts of the chunks before this one in
+  // its own super-chunk (fewer than 32), both contiguous; a group of tpe
+  // threads (a power of two, 256 / E rounded down, at most 32, at least 1)
+  // shares them and sums them with shuffles.  Every warp runs the same number
+  // of rounds, so the shuffles always have all 32 lanes.
+  {
+    const int c0 = s0 * kSuperChunks;
+    const int n_sup = nsuper, n_items_e = nsuper + (chunk - c0);
+    int tpe = 1;
+    while (tpe < 32 && tpe * 2 * E <= 256) tpe *= 2;
+    const int groups = 256 / tpe, g0 = threadIdx.x / tpe, li = threadIdx.x % tpe;
+    for (int round = 0; round * groups < E; ++round) {
+      const int e = round * groups + g0;
+      int tot = 0, before = 0;
+      if (e < E) {
+        const int32_t* scr = sc + static_cast<size_t>(e) * nsuper;
+        const int32_t* ccr = ccount + static_cast<size_t>(e) * nchunks + c0;
+#pragma unroll 4
+        for (int j = li; j < n_items_e; j += tpe) {
+          if (j < n_sup) {
+            const int v = __ldg(scr + j);
+            tot += v;
+            before += j < s0 ? v : 0;
+          } else {
+            before += __ldg(ccr + (j - n_sup));
+          }
+        }
+      }
+      for (int off = 1; off < tpe; off <<= 1) {
+        tot += __shfl_xor_sync(0xffffffffu, tot, off);
+        before += __shfl_xor_sync(0xffffffffu, before, off);
+      }
+      if (li == 0 && e < E) {
+        base[e] = before;  // the expert's first row is added below
+        gcnt[e] = tot;     // the real total for now; padded below
+      }
+    }
+  }
+  __syncthreads();
   const int per = (E + 255) / 256;
-  int my_cnt = 0;
+  int my_cnt = 0, my_n = 0, my_m = 0, my_p = 0;
   for (int u = 0; u < per; ++u) {
     const int e = threadIdx.x * per + u;
     if (e >= E) break;
     const uint4 a = __ldg(src + 2 * e), b = __ldg(src + 2 * e + 1);
     const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    base[e] = __ldg(offsets + e) + __ldg(cbase + static_cast<size_t>(chunk) * E + e);
+    const int tot = gcnt[e];
     uint32_t run = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -581,26 +522,81 @@ __global__ void __launch_bounds__(256) route_rank_kernel(const int32_t* __restri
       lpre[e * 8 + j] = run;
       run += __popc(w[j]);
     }
-    loff[e] = my_cnt;  // thread-local prefix, completed below
+    loff[e] = my_cnt;  // thread-local prefixes, completed below
     my_cnt += static_cast<int>(run);
+    const int n = padded(tot);
+    my_n += n;
+    my_m += (n + kTileRows - 1) / kTileRows;
+    my_p += (n + 2 * kTileRows - 1) / (2 * kTileRows);
   }
-  int incl = my_cnt;
+  int in_c = my_cnt, in_n = my_n, in_m = my_m, in_p = my_p;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += y;
+    const int yc = __shfl_up_sync(0xffffffffu, in_c, off);
+    const int yn = __shfl_up_sync(0xffffffffu, in_n, off);
+    const int ym = __shfl_up_sync(0xffffffffu, in_m, off);
+    const int yp = __shfl_up_sync(0xffffffffu, in_p, off);
+    if (lane >= off) {
+      in_c += yc;
+      in_n += yn;
+      in_m += ym;
+      in_p += yp;
+    }
   }
-  if (lane == 31) s_wsum[warp] = incl;
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) tstart[e] = __ldg(tiles + 1 + e);
+  if (lane == 31) {
+    s_wsum[0][warp] = in_c;
+    s_wsum[1][warp] = in_n;
+    s_wsum[2][warp] = in_m;
+    s_wsum[3][warp] = in_p;
+  }
   __syncthreads();
-  int excl = incl - my_cnt;
-  for (int w = 0; w < warp; ++w) excl += s_wsum[w];
+  int run_c = in_c - my_cnt, run_n = in_n - my_n, run_m = in_m - my_m, run_p = in_p - my_p;
+  for (int w = 0; w < warp; ++w) {
+    run_c += s_wsum[0][w];
+    run_n += s_wsum[1][w];
+    run_m += s_wsum[2][w];
+    run_p += s_wsum[3][w];
+  }
   for (int u = 0; u < per; ++u) {
     const int e = threadIdx.x * per + u;
     if (e >= E) break;
-    loff[e] += excl;
+    const int real = gcnt[e];
+    const int n = padded(real);
+    loff[e] += run_c;
+    offs[e] = run_n;
+    tstart[e] = run_m;
+    base[e] += run_n;
+    gcnt[e] = n;
+    if (writer) {
+      counts[e] = real;
+      gcounts[e] = n;
+      offsets[e] = run_n;
+      tiles[1 + e] = run_m;
+      pairs[e] = run_p;
+      for (int r = run_n + real; r < run_n + n; ++r) {  // the padding rows of expert e
+        if (r < 0 || r >= R) {
+          report(ws, MOE_ERR_BOUNDS, 1, r);
+          break;
+        }
+        row_src[r] = -1;
+        row_slot[r] = 255;
+      }
+    }
+    run_n += n;
+    run_m += (n + kTileRows - 1) / kTileRows;
+    run_p += (n + 2 * kTileRows - 1) / (2 * kTileRows);
+    if (e == E - 1) {
+      loff[E] = run_c + my_cnt;  // the chunk's items (run_c: this thread's exclusive prefix)
+      offs[E] = run_n;
+      tstart[E] = run_m;
+      if (writer) {
+        offsets[E] = run_n;
+        tiles[1 + E] = run_m;
+        tiles[0] = run_m;
+        pairs[E] = run_p;
+      }
+    }
   }
-  if (threadIdx.x == 255) loff[E] = excl + my_cnt;
   __syncthreads();
 
   auto place = [&](int i, int e) {
@@ -663,8 +659,8 @@ __global__ void __launch_bounds__(256) route_rank_kernel(const int32_t* __restri
         hi = mid;
     }
     const int j = m - tstart[lo];
-    const int n = __ldg(gcounts + lo);  // rows the GEMMs run: n_e, padded
-    ent[m] = make_int4(lo, __ldg(offsets + lo) + kTileRows * j, min(kTileRows, n - kTileRows * j), 0);
+    const int n = gcnt[lo];  // rows the GEMMs run: n_e, padded
+    ent[m] = make_int4(lo, offs[lo] + kTileRows * j, min(kTileRows, n - kTileRows * j), 0);
   }
 }
 
@@ -672,9 +668,9 @@ cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t s, LaunchHook& hook) {
   const int nchunks = (p.T + kChunk - 1) / kChunk;
   const int nblocks = (p.T + kTopkTokens - 1) / kTopkTokens;
   const int nv = (p.E + 31) / 32;
-  // The chunk counts and the scan's ticket start at zero (the bitmap words are
-  // all written by the top-k CTAs).
-  cudaError_t err = cudaMemsetAsync(p.ticket, 0, (16 + static_cast<size_t>(nchunks) * p.E) * 4, s);
+  // The chunk and super-chunk counts start at zero (the bitmap words are all
+  // written by the top-k CTAs).
+  cudaError_t err = cudaMemsetAsync(p.ticket, 0, static_cast<size_t>(plan_count_words(p.T, p.E)) * 4, s);
   if (err != cudaSuccess) return err;
   const size_t topk_smem = static_cast<size_t>(p.E) * 3 * 4;
   hook.before(s);
@@ -724,22 +720,16 @@ cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t s, LaunchHook& hook) {
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   hook.before(s);
-  route_scan_kernel<<<p.E, kScanThreads, 0, s>>>(
-      p.ccount, nchunks, p.E, p.cbase, p.counts, p.offsets, p.tiles, p.pairs, p.ticket, p.pad, p.R, p.gcounts,
-      p.row_src, p.row_slot, p.ws);
-  hook.after(s);
-  err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  hook.before(s);
-  const size_t rank_smem = (static_cast<size_t>(2 * kChunkWords) * p.E + 3 * static_cast<size_t>(p.E) + 2) * 4 +
+  const size_t rank_smem = (static_cast<size_t>(2 * kChunkWords) * p.E + 5 * static_cast<size_t>(p.E) + 3) * 4 +
                            static_cast<size_t>(kChunk) * p.k * 7;
   if (rank_smem > 48 * 1024) {
     err = cudaFuncSetAttribute(route_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(rank_smem));
     if (err != cudaSuccess) return err;
   }
-  route_rank_kernel<<<nchunks, 256, rank_smem, s>>>(p.ids, p.gbm, p.cbase, p.offsets, p.gcounts, p.tiles, p.T,
-                                                    p.E, p.k, p.R, p.dest, p.row_src, p.row_slot, p.ws);
+  route_rank_kernel<<<nchunks, 256, rank_smem, s>>>(p.ids, p.gbm, p.ccount, p.T, p.E, p.k, p.R, p.pad, p.dest,
+                                                    p.row_src, p.row_slot, p.counts, p.offsets, p.tiles, p.pairs,
+                                                    p.gcounts, p.ws);
   hook.after(s);
   return cudaGetLastError();
 }
@@ -853,9 +843,8 @@ extern "C" int moe_plan_noalloc(moe_dims d, const float* logits, const moe_plan_
     return MOE_ERR_ARG;
   if (d.H % 128 != 0 || d.F % 128 != 0 || d.E > 1024) return MOE_ERR_SHAPE;
   const size_t nchunks = (static_cast<size_t>(d.T) + kChunk - 1) / kChunk;
-  const size_t ccount = 0;  // 16-word ticket, then the per-chunk counts
-  const size_t cbase = na_align(ccount + (16 + nchunks * d.E) * 4);
-  const size_t gbm = na_align(cbase + nchunks * d.E * 4);
+  const size_t ccount = 0;  // 16-word header, then the per-chunk and per-super-chunk counts
+  const size_t gbm = na_align(ccount + static_cast<size_t>(plan_count_words(d.T, d.E)) * 4);
   const size_t total = na_align(gbm + nchunks * d.E * kChunkWords * 4);
   if (total > kNoAllocBytes) return MOE_ERR_TOO_LARGE;
   if (d.T == 0) return MOE_OK;
@@ -882,7 +871,6 @@ extern "C" int moe_plan_noalloc(moe_dims d, const float* logits, const moe_plan_
   p.w = plan->topk_w;
   p.ticket = reinterpret_cast<int32_t*>(w + ccount);
   p.ccount = p.ticket + 16;
-  p.cbase = reinterpret_cast<int32_t*>(w + cbase);
   p.gbm = reinterpret_cast<uint32_t*>(w + gbm);
   p.counts = plan->counts;
   p.offsets = plan->offsets;
