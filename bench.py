@@ -796,11 +796,117 @@ def run_ours(args):
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(shape, args.config)
+    extra = [int(c) for c in args.also.split(",") if c.strip()] if args.also else []
+    if world == 1 and extra and not args.router and args.pad <= 1:
+        # Free this workload's buffers, then time the other workloads the same way.
+        del layer, inp, graph, e2e_graphs, d_in, d_res, h_x, h_lg, h_do, h_out, h_dx, opts_f, opts_b, opts_r, keep
+        import gc
+        gc.collect()
+        torch.cuda.empty_cache()
+        line["other_workloads"] = {S.CONFIGS[c].name: time_other_workload(c, args, dev, opt_kw) for c in extra}
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def time_other_workload(idx, args, dev, opt_kw):
+    """ms/step, tokens/s and per-kernel rates of another workload, timed as the headline one
+    (a CUDA graph of one step replayed K times, then a pass with an event pair around every
+    kernel), for the record beside the headline line."""
+    import torch
+
+    import moe_synth as S
+    from mixture_experts_layer_gb300.layer import MoELayer
+    shape = S.CONFIGS[idx]
+    T, H, F, E, k = shape.T, shape.H, shape.F, shape.E, shape.k
+    inp = S.layer_inputs(shape, S.config_seed(idx), device=dev)
+    layer = MoELayer(T, H, F, E, k, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    opts = layer.opts(**opt_kw)
+
+    def step(of=None, ob=None, ep=None):
+        if ep is not None:
+            ep[0].record(stream)
+        layer.plan(inp["logits"])
+        if ep is not None:
+            ep[1].record(stream)
+        layer.forward(inp["x"], inp["W1"], inp["W3"], inp["W2"], opts=of or opts)
+        layer.backward(inp["dout"], inp["W1"], inp["W3"], inp["W2"], opts=ob or opts)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        step()
+    stream.wait_stream(side)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    fwd_names, bwd_names = FWD_KERNELS, BWD_KERNELS
+    evf = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(fwd_names))] for _ in range(args.steps)]
+    evb = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(bwd_names))] for _ in range(args.steps)]
+    evp = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for e in [e for row in evf + evb + evp for e in row]:
+        e.record(stream)
+    torch.cuda.synchronize()
+    keep, of, ob = [], [], []
+    for i in range(args.steps):
+        of.append(layer.opts(events=evf[i], **opt_kw))
+        keep.append(layer._ev_keep)
+        ob.append(layer.opts(events=evb[i], **opt_kw))
+        keep.append(layer._ev_keep)
+    for i in range(args.steps):
+        step(of[i], ob[i], evp[i])
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    st = layer.status()
+    if st[0] != 0:
+        raise RuntimeError(f"device status {st}")
+    per = {"plan": sum(evp[i][0].elapsed_time(evp[i][1]) for i in range(args.steps)) / args.steps}
+    for names, evs in ((fwd_names, evf), (bwd_names, evb)):
+        for j, n in enumerate(names):
+            per[n] = sum(evs[i][2 * j].elapsed_time(evs[i][2 * j + 1]) for i in range(args.steps)) / args.steps
+    flops, bytes_ = work_per_kernel(T, H, F, E, k)
+    peaks = load_peaks()
+    kern = {}
+    for n, t in per.items():
+        ent = {"ms": round(t, 4), "gbs": round(bytes_[n] / (t * 1e-3) / 1e9, 1),
+               "hbm_frac": round(bytes_[n] / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)}
+        if n in flops:
+            tf = flops[n] / (t * 1e-3) / 1e12
+            ent["tflops"] = round(tf, 1)
+            ent["tensor_frac"] = round(tf / peaks["bf16_tflops"], 3)
+        tt = flops.get(n, 0) / (peaks["bf16_tflops"] * 1e12)
+        th = bytes_[n] / (peaks["hbm_gbs"] * 1e9)
+        ent["bound"] = "tensor" if tt >= th else "hbm"
+        ent["roof_frac"] = round(max(tt, th) / (t * 1e-3), 3)
+        kern[n] = ent
+    maxvio = float(layer.counts.max().item()) / (T * k / E) - 1.0
+    out = {"workload": workload_config(shape, idx)["workload"], "ms_per_step": round(ms, 4),
+           "value": round(T / (ms * 1e-3), 1), "unit": UNIT, "steps": args.steps,
+           "timing": "CUDA graph of one step replayed K times; per-kernel times from an event pass",
+           "tensor_peak": "burst bf16 of " + peaks["source"], "maxvio": round(maxvio, 4), "clocks": clk,
+           "kernels": kern}
+    del layer, inp, graph
+    import gc
+    gc.collect()
+    torch.cuda.empty_cache()
+    return out
 
 
 def cpu_baseline(shape, idx):
@@ -822,6 +928,10 @@ def main():
                     help="workload index: 0 tiny, 1 fine-grained, 2 large-expert, 3 skewed, 4 long-sequence "
                          "(default: the largest that fits one GPU)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--also", default=None,
+                    help="comma-separated workload indices timed after the headline one and reported under "
+                         "other_workloads (default with the long-sequence headline: 2,3, the large-expert and "
+                         "skewed workloads; '' for none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--schedule", type=int, default=0, choices=[0, 1, 2],
                     help="0: one persistent launch per phase; 1: fused persistent forward, one persistent "
@@ -856,6 +966,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.also is None:
+        args.also = "2,3" if args.config == 4 and not args.profile else ""
     if args.impl == "reference":
         run_reference(args)
     else:
