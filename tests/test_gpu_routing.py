@@ -20,8 +20,10 @@ pytestmark = pytest.mark.gpu
 SHAPES = [
     (1, 4, 4), (63, 8, 2), (300, 12, 3), (1000, 20, 5), (777, 64, 6), (1500, 100, 8), (2049, 128, 8),
     (520, 256, 8), (333, 256, 1), (4000, 32, 8), (100, 32, 1), (700, 128, 3), (65, 64, 8),
+    # several 8192-token super-chunks (the coarse level of the prefix over chunks), ragged tails
+    (20000, 64, 6), (17000, 128, 8),
     # the warp-per-token kernel
-    (500, 6, 2), (400, 260, 4), (300, 64, 9), (129, 1, 1),
+    (500, 6, 2), (400, 260, 4), (300, 64, 9), (129, 1, 1), (9000, 6, 2),
 ]
 KINDS = ["normal", "levels", "equal", "close"]
 
