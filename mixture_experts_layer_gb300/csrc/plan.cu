@@ -22,17 +22,17 @@
 //               popcount of the chunk's bitmap below the token; dest, row_src,
 //               row_slot; a share of the GEMM tile entries; CTA 0 writes the
 //               counts, offsets and expert-level tile tables.
+#include <limits.h>
 #include <math.h>
-
-#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.cuh"
 
 namespace moe {
 
-constexpr int kTopkTokens = 64;    // tokens per top-k / rank CTA: two bitmap words per expert
+constexpr int kTopkTokens = 64;    // tokens per CTA of the warp-per-token top-k: two bitmap words per expert
 constexpr int kTopkThreads = 256;  // 8 warps x 8 tokens
+constexpr int kTopk4Tokens = 64;   // tokens per CTA of the four-threads-per-token top-k
 
 // A top-k CTA's count of expert e goes to its chunk's count and to its
 // super-chunk's (integer atomics: the sums do not depend on their order).
@@ -145,35 +145,58 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float* _
 // Fast path of the same selection for E % 4 == 0, E <= 256 and k <= 8: four
 // threads per token, each holding a quarter of its logits (16-byte vectors
 // 4i + q of the row, so a warp's loads are whole sectors).
-//   1. Each thread sorts its values in blocks of 8 (Batcher's 19-comparator
-//      network) and merges the blocks keeping the 8 largest (bitonic split +
-//      3-stage sort); two shuffle rounds merge the four threads' lists the same
-//      way.  Only values move, so no id comparisons are needed: the four
-//      threads end with the token's 8 largest values, sorted, s[0] >= ... >= s[7].
-//   2. th = s[k-1]; `need` of the top k equal th.  Each thread lists its values
-//      >= th (with their ids) in shared memory.  When the token has exactly k
-//      such values -- no extra ties at the threshold, the usual case -- all of
-//      them are chosen; otherwise one thread rescans the row in ascending id
-//      order, taking every value > th and the first `need` equal to th.
-//   3. Slot of a chosen (x, e): #{m < k : s[m] > x}, plus, when x occurs more
-//      than once in the top k, the number of chosen equal values with a lower
-//      id -- the total order (value desc, id asc) of the warp-per-token path.
-// Weights: exp(s[m] - s[0]) summed over m < k in slot order, then
-// exp(x - s[0]) / sum: the same arithmetic as the warp-per-token path.
+//
+// Every logit becomes one 32-bit key that carries its expert id:
+//   key = (okey(x) with the low 8 bits cleared) | (255 - e),
+// okey being an integer that orders like the float (-0 and +0 equal).  Keys
+// compare like (x desc, e asc) except between two logits whose okeys agree in
+// their top 24 bits (the key's "prefix"), where only the id decides.
+//   1. Each thread sorts its keys in blocks of 8 (Batcher's 19-comparator
+//      network, one integer min and max per comparator) and merges the blocks
+//      keeping the 8 largest (bitonic split + 3-stage sort); two shuffle rounds
+//      merge the four threads' lists the same way.  The ids ride along in the
+//      keys, so the four threads end with the token's top 8 (value, id) pairs,
+//      in slot order, with no search for the chosen ids.
+//   2. The packed order is the exact order unless a prefix is shared where it
+//      matters: two of the top k with one prefix, or a key outside the top k
+//      with the prefix of the k-th.  The first shows in the sorted list; the
+//      second in how many keys of each thread's own top 8 reach the k-th key's
+//      prefix (a thread whose eight all do may hide more: counted as one more).
+//      Such a token (a shared prefix among ~9 values: rare for real-valued
+//      logits; always for exact ties, which the packed order gets right anyway)
+//      is selected again with 64-bit keys okey << 32 | (255 - e), an exact
+//      total order, through the same networks.
+// Weights: exp(x_m - x_0) summed over m < k in slot order, then
+// exp(x - x_0) / sum, with x_m the chosen logits read back from the row (an L1
+// hit): the same arithmetic as the warp-per-token path.
 // Non-finite logits are detected with one fused multiply-add per value
-// (x * 0 is NaN exactly for NaN and +-inf); a warp that holds one maps them to
-// -inf and reports MOE_ERR_NONFINITE, as the warp-per-token path does.
+// (x * 0 is NaN exactly for NaN and +-inf); they take part as -inf and the
+// warp reports MOE_ERR_NONFINITE, as the warp-per-token path does.
 constexpr int kTopkFastK = 8;
 
+// An integer that orders like the float (NaN excluded); -0 and +0 map to 0.
+__device__ __forceinline__ int32_t okey(float x) {
+  const int32_t i = __float_as_int(x);
+  const int32_t sgn = i >> 31;
+  return ((i & 0x7fffffff) ^ sgn) - sgn;
+}
+
+__device__ __forceinline__ int32_t kmax(int32_t a, int32_t b) { return max(a, b); }
+__device__ __forceinline__ int32_t kmin(int32_t a, int32_t b) { return min(a, b); }
+__device__ __forceinline__ long long kmax(long long a, long long b) { return a > b ? a : b; }
+__device__ __forceinline__ long long kmin(long long a, long long b) { return a > b ? b : a; }
+
 // Compare-exchange, descending.
-__device__ __forceinline__ void cx_desc(float& a, float& b) {
-  const float hi = fmaxf(a, b), lo = fminf(a, b);
+template <class K>
+__device__ __forceinline__ void cx_desc(K& a, K& b) {
+  const K hi = kmax(a, b), lo = kmin(a, b);
   a = hi;
   b = lo;
 }
 
-// Sorts 8 values descending (Batcher's odd-even merge sort, 19 comparators).
-__device__ __forceinline__ void sort8_desc(float* a) {
+// Sorts 8 keys descending (Batcher's odd-even merge sort, 19 comparators).
+template <class K>
+__device__ __forceinline__ void sort8_desc(K* a) {
   cx_desc(a[0], a[1]); cx_desc(a[2], a[3]); cx_desc(a[4], a[5]); cx_desc(a[6], a[7]);
   cx_desc(a[0], a[2]); cx_desc(a[1], a[3]); cx_desc(a[4], a[6]); cx_desc(a[5], a[7]);
   cx_desc(a[1], a[2]); cx_desc(a[5], a[6]);
@@ -183,9 +206,10 @@ __device__ __forceinline__ void sort8_desc(float* a) {
 }
 
 // a := the 8 largest of a and b (both sorted descending), sorted descending.
-__device__ __forceinline__ void merge8_top(float* a, const float* b) {
+template <class K>
+__device__ __forceinline__ void merge8_top(K* a, const K* b) {
 #pragma unroll
-  for (int m = 0; m < 8; ++m) a[m] = fmaxf(a[m], b[7 - m]);
+  for (int m = 0; m < 8; ++m) a[m] = kmax(a[m], b[7 - m]);
 #pragma unroll
   for (int d = 4; d > 0; d >>= 1)
 #pragma unroll
@@ -193,26 +217,70 @@ __device__ __forceinline__ void merge8_top(float* a, const float* b) {
       if ((m & d) == 0) cx_desc(a[m], a[m + d]);
 }
 
+// Value slot j of thread q is expert 16 (j / 4) + 4 q + j % 4.
+__device__ __forceinline__ int topk4_expert(int j, int q) { return 16 * (j >> 2) + 4 * q + (j & 3); }
+
+// Entry m of an 8-list with a runtime m in [0, 8), without local memory.
+template <class K>
+__device__ __forceinline__ K pick8(const K* a, int m) {
+  K r = a[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i)
+    if (m == i) r = a[i];
+  return r;
+}
+
+__device__ __forceinline__ float finite_or_ninf(float x) { return isfinite(x) ? x : -INFINITY; }
+
+// The low byte of value slot j's key before the thread's own id bits are
+// added: 255 - (16 (j / 4) + j % 4), whose bits 2-3 (the thread's 4 q) are set.
+// After the thread's own selection, XOR with 4 q turns it into 255 - e.
+__device__ __forceinline__ int32_t slot_id_bits(int j) { return 0xff - (16 * (j >> 2) + (j & 3)); }
+
+// Unit u's logits held by thread (tl, q): 16-byte vectors 4i + q of the row.
+// Vectors past the row or past the last token are zeros: zeros pass the
+// finiteness test, their keys are replaced, and nothing of a dead token is
+// written.
+template <int NV4, bool FULL, int TOK>
+__device__ __forceinline__ void topk4_load(float4* f, const float* logits, int T, int E, int u, int tl, int q) {
+  const int t = u * TOK + tl;
+  const float* row = logits + static_cast<size_t>(t < T ? t : 0) * E;
+#pragma unroll
+  for (int i = 0; i < NV4; ++i) {
+    const int e0 = 16 * i + 4 * q;
+    f[i] = (t < T && (FULL || e0 < E)) ? __ldg(reinterpret_cast<const float4*>(row + e0))
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// One CTA of 4 TOK threads per TOK-token unit (TOK = 64: a unit owns two
+// bitmap words per expert; 32-token units measured slower).
 // KC: k when it is known at compile time (8, the usual value: every `m < k` test
 // of the unrolled 8-slot loops then folds away), 0 for a runtime k.
-template <int NV4, bool FULL, int KC>
-__global__ void __launch_bounds__(kTopkThreads) route_topk4_kernel(const float* __restrict__ logits, int T, int E,
-                                                                   int k_arg, int32_t* __restrict__ ids,
-                                                                   float* __restrict__ wts,
-                                                                   uint32_t* __restrict__ gbm,
-                                                                   int32_t* __restrict__ ccount, WsHeader* ws) {
+template <int NV4, bool FULL, int KC, int TOK>
+__global__ void __launch_bounds__(4 * TOK) route_topk4_kernel(const float* __restrict__ logits, int T, int E,
+                                                              int k_arg, int32_t* __restrict__ ids,
+                                                              float* __restrict__ wts, uint32_t* __restrict__ gbm,
+                                                              int32_t* __restrict__ ccount, WsHeader* ws) {
   const int k = KC ? KC : k_arg;
   constexpr int NV = 4 * NV4;                    // values per thread
   constexpr int NB = (NV + 7) / 8;               // blocks of 8
+  constexpr int WPU = TOK / 32;                  // bitmap words per expert of the unit
   extern __shared__ uint32_t sm[];
-  uint32_t* bm = sm;                             // [E][2]
-  int* cnt = reinterpret_cast<int*>(sm + 2 * E); // [E]
-  float* cand_x = reinterpret_cast<float*>(cnt + E);  // [64 tokens][8] chosen values (tie path)
-  for (int i = threadIdx.x; i < 3 * E; i += blockDim.x) sm[i] = 0;
-  __syncthreads();
+  uint32_t* bm = sm;                             // [E][WPU]
+  int* cnt = reinterpret_cast<int*>(sm + WPU * E);  // [E]
   const int lane = threadIdx.x & 31;
   const int tl = threadIdx.x >> 2, q = threadIdx.x & 3;
-  const int t = blockIdx.x * kTopkTokens + tl;
+  const int u = blockIdx.x;
+  // Value slot j of this thread holds a logit of the row: its vector j / 4
+  // starts at 16 (j / 4) + 4 q < E (E % 4 == 0), i.e. j / 4 < nh.
+  const int nh = FULL ? NV4 : (E - 4 * q + 15) / 16;
+  auto held = [&](int j) { return j < NV && (FULL || (j >> 2) < nh); };
+  float4 cur[NV4];
+  topk4_load<NV4, FULL, TOK>(cur, logits, T, E, u, tl, q);
+  for (int i = threadIdx.x; i < (WPU + 1) * E; i += blockDim.x) sm[i] = 0;
+  __syncthreads();
+  const int t = u * TOK + tl;
   const bool live = t < T;
   const float* row = logits + static_cast<size_t>(live ? t : 0) * E;
 
@@ -220,110 +288,112 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk4_kernel(const float* 
   float acc = 0.f;
 #pragma unroll
   for (int i = 0; i < NV4; ++i) {
-    const int e0 = 16 * i + 4 * q;
-    float4 f = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-    if (live && (FULL || e0 < E)) {
-      f = __ldg(reinterpret_cast<const float4*>(row + e0));
-      acc = fmaf(f.x, 0.f, acc);
-      acc = fmaf(f.y, 0.f, acc);
-      acc = fmaf(f.z, 0.f, acc);
-      acc = fmaf(f.w, 0.f, acc);
-    }
-    v[4 * i] = f.x;
-    v[4 * i + 1] = f.y;
-    v[4 * i + 2] = f.z;
-    v[4 * i + 3] = f.w;
+    v[4 * i] = cur[i].x;
+    v[4 * i + 1] = cur[i].y;
+    v[4 * i + 2] = cur[i].z;
+    v[4 * i + 3] = cur[i].w;
   }
+#pragma unroll
+  for (int j = 0; j < NV; ++j) acc = fmaf(v[j], 0.f, acc);
 #pragma unroll
   for (int j = NV; j < NB * 8; ++j) v[j] = -INFINITY;
   const bool bad = acc != acc;
   if (__any_sync(0xffffffffu, bad)) {
 #pragma unroll
-    for (int j = 0; j < NV; ++j)
-      if (!isfinite(v[j])) v[j] = -INFINITY;
+    for (int j = 0; j < NV; ++j) v[j] = finite_or_ninf(v[j]);
     if (bad) report(ws, MOE_ERR_NONFINITE, 0, t);
   }
 
-  // 1. the token's 8 largest values, sorted
-  float s[8];
+  // 1. the token's 8 largest keys, sorted; loc = this thread's own 8 largest
+  int32_t loc[8], s[8];
   {
-    float b[NB][8];
+    int32_t b[NB][8];
 #pragma unroll
     for (int blk = 0; blk < NB; ++blk) {
 #pragma unroll
-      for (int m = 0; m < 8; ++m) b[blk][m] = v[8 * blk + m];
+      for (int m = 0; m < 8; ++m) {
+        const int j = 8 * blk + m;
+        b[blk][m] = held(j) ? ((okey(v[j]) & ~0xff) | slot_id_bits(j)) : INT_MIN;
+      }
       sort8_desc(b[blk]);
     }
 #pragma unroll
-    for (int m = 0; m < 8; ++m) s[m] = b[0][m];
+    for (int m = 0; m < 8; ++m) loc[m] = b[0][m];
 #pragma unroll
-    for (int blk = 1; blk < NB; ++blk) merge8_top(s, b[blk]);
+    for (int blk = 1; blk < NB; ++blk) merge8_top(loc, b[blk]);
+  }
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    loc[m] ^= 4 * q;  // low byte: 255 - e (a padding key stays below every logit's key)
+    s[m] = loc[m];
   }
 #pragma unroll
   for (int mask = 1; mask <= 2; mask <<= 1) {
-    float o[8];
+    int32_t o[8];
 #pragma unroll
     for (int m = 0; m < 8; ++m) o[m] = __shfl_xor_sync(0xffffffffu, s[m], mask);
     merge8_top(s, o);
   }
-  float th = s[0];
+
+  // 2. exact unless a prefix is shared within the top k or across its edge
+  int32_t sk = s[0];
 #pragma unroll
   for (int m = 1; m < 8; ++m)
-    if (m < k) th = s[m];
-  int need = 0;
+    if (m < k) sk = s[m];
+  const int32_t edge = sk & ~0xff;  // the smallest key with the k-th key's prefix
+  int c = 0;
 #pragma unroll
-  for (int m = 0; m < 8; ++m) need += (m < k && s[m] == th) ? 1 : 0;
-
-  // 2. this thread's values >= th, as a bit mask over its value index j
-  //    (value j of thread q is expert 16 (j / 4) + 4 q + j % 4)
-  using Mask = typename std::conditional<(NV > 32), unsigned long long, uint32_t>::type;
-  Mask msk = 0;
+  for (int m = 0; m < 8; ++m) c += loc[m] >= edge ? 1 : 0;
+  c += c == 8 ? 1 : 0;
+  c += __shfl_xor_sync(0xffffffffu, c, 1);
+  c += __shfl_xor_sync(0xffffffffu, c, 2);
+  bool amb = c > k;
 #pragma unroll
-  for (int j = 0; j < NV; ++j) {
-    const int e = 16 * (j >> 2) + 4 * q + (j & 3);
-    if ((FULL || e < E) && v[j] >= th) msk |= Mask(1) << j;
-  }
-  const int n = (NV > 32) ? __popcll(static_cast<unsigned long long>(msk)) : __popc(static_cast<uint32_t>(msk));
-  int ntot = n;
-  ntot += __shfl_xor_sync(0xffffffffu, ntot, 1);
-  ntot += __shfl_xor_sync(0xffffffffu, ntot, 2);
-  int nq[4];
-  Mask mq[4];
+  for (int m = 0; m + 1 < 8; ++m)
+    if (m + 1 < k) amb = amb || (static_cast<uint32_t>(s[m] ^ s[m + 1]) >> 8) == 0;
+  if (live && amb) {
+    // The four threads of the token agree on amb: they alone take this branch.
+    const unsigned grp = 0xfu << (lane & ~3);
+    long long x8[8];
 #pragma unroll
-  for (int qq = 0; qq < 4; ++qq) {
-    nq[qq] = __shfl_sync(0xffffffffu, n, (lane & ~3) + qq);
-    if (NV > 32) {
-      const uint32_t lo = __shfl_sync(0xffffffffu, static_cast<uint32_t>(msk), (lane & ~3) + qq);
-      const uint32_t hi = __shfl_sync(0xffffffffu, static_cast<uint32_t>(static_cast<unsigned long long>(msk) >> 32),
-                                      (lane & ~3) + qq);
-      mq[qq] = static_cast<Mask>((static_cast<unsigned long long>(hi) << 32) | lo);
-    } else {
-      mq[qq] = static_cast<Mask>(__shfl_sync(0xffffffffu, static_cast<uint32_t>(msk), (lane & ~3) + qq));
+    for (int m = 0; m < 8; ++m) x8[m] = LLONG_MIN;
+#pragma unroll
+    for (int blk = 0; blk < NB; ++blk) {
+      long long b[8];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int j = 8 * blk + m;
+        const int e = topk4_expert(j, q);
+        b[m] = held(j) ? static_cast<long long>(
+                             (static_cast<unsigned long long>(static_cast<uint32_t>(okey(finite_or_ninf(row[e]))))
+                              << 32) |
+                             static_cast<unsigned long long>(0xff - e))
+                       : LLONG_MIN;
+      }
+      sort8_desc(b);
+      merge8_top(x8, b);
     }
-  }
-  // Expert of the li-th set bit of thread qq's mask.
-  auto expert_of = [&](int qq, int li) {
-    const Mask m = qq == 0 ? mq[0] : qq == 1 ? mq[1] : qq == 2 ? mq[2] : mq[3];
-    int j;
-    if (NV > 32) {
-      const uint32_t lo = static_cast<uint32_t>(static_cast<unsigned long long>(m));
-      const int nlo = __popc(lo);
-      j = li < nlo ? static_cast<int>(__fns(lo, 0, li + 1))
-                   : 32 + static_cast<int>(__fns(static_cast<uint32_t>(static_cast<unsigned long long>(m) >> 32),
-                                                 0, li - nlo + 1));
-    } else {
-      j = static_cast<int>(__fns(static_cast<uint32_t>(m), 0, li + 1));
+#pragma unroll
+    for (int mask = 1; mask <= 2; mask <<= 1) {
+      long long o[8];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) o[m] = __shfl_xor_sync(grp, x8[m], mask);
+      merge8_top(x8, o);
     }
-    return 16 * (j >> 2) + 4 * qq + (j & 3);
-  };
+#pragma unroll
+    for (int m = 0; m < 8; ++m) s[m] = static_cast<int32_t>(x8[m]);  // the low word: 255 - e
+  }
 
-  // Weights: exp(s[m] - s[0]) for m = q and q + 4 here, gathered over the
-  // token's four threads and summed in slot order.
-  const float m0 = s[0];
-  const float sq = q == 0 ? s[0] : q == 1 ? s[1] : q == 2 ? s[2] : s[3];
-  const float sq4 = q == 0 ? s[4] : q == 1 ? s[5] : q == 2 ? s[6] : s[7];
-  const float exa = (live && q < k) ? expf(sq - m0) : 0.f;
-  const float exb = (live && q + 4 < k) ? expf(sq4 - m0) : 0.f;
+  // 3. slots q and q + 4 of this token; weights in slot order
+  const int ea = 0xff - (pick8(s, q) & 0xff);
+  const int eb = 0xff - (pick8(s, q + 4) & 0xff);
+  const bool has_a = live && q < k, has_b = live && q + 4 < k;
+  const bool ok_a = has_a && ea < E, ok_b = has_b && eb < E;
+  const float xa = ok_a ? finite_or_ninf(__ldg(row + ea)) : 0.f;
+  const float xb = ok_b ? finite_or_ninf(__ldg(row + eb)) : 0.f;
+  const float x0 = __shfl_sync(0xffffffffu, xa, lane & ~3);
+  const float exa = has_a ? expf(xa - x0) : 0.f;
+  const float exb = has_b ? expf(xb - x0) : 0.f;
   float ex[8];
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
@@ -334,74 +404,21 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk4_kernel(const float* 
 #pragma unroll
   for (int m = 0; m < 8; ++m)
     if (m < k) sum += ex[m];
-  if (live) {
-    // 3. slots of the chosen values; writes
-    auto emit = [&](float x, int e, int ties_below) {
-      int slot = ties_below;
-#pragma unroll
-      for (int m = 0; m < 8; ++m) slot += (m < k && s[m] > x) ? 1 : 0;
-      if (e < 0 || e >= E || slot >= k) {
-        report(ws, MOE_ERR_BOUNDS, 1, t);
-        return;
-      }
-      float exs = ex[0];
-#pragma unroll
-      for (int m = 1; m < 8; ++m)
-        if (slot == m) exs = ex[m];
-      ids[static_cast<size_t>(t) * k + slot] = e;
-      wts[static_cast<size_t>(t) * k + slot] = exs / sum;
-      atomicOr(&bm[e * 2 + (tl >> 5)], 1u << (tl & 31));
-      atomicAdd(&cnt[e], 1);
-    };
-    if (ntot == k) {
-      // The token's k chosen values, spread evenly: this thread takes entries
-      // q and q + 4 of the concatenation of the four threads' lists; the
-      // values are read back from the row (an L1 hit).
-      for (int c = q; c < k; c += 4) {
-        const int qq = c < nq[0] ? 0 : c < nq[0] + nq[1] ? 1 : c < nq[0] + nq[1] + nq[2] ? 2 : 3;
-        const int li = c - (qq > 0 ? nq[0] : 0) - (qq > 1 ? nq[1] : 0) - (qq > 2 ? nq[2] : 0);
-        const int e = expert_of(qq, li);
-        float x = __ldg(row + e);
-        if (!isfinite(x)) x = -INFINITY;
-        int dup = 0;
-#pragma unroll
-        for (int m = 0; m < 8; ++m) dup += (m < k && s[m] == x) ? 1 : 0;
-        int ties_below = 0;
-        if (dup > 1) {  // equal chosen values: the lower ids take the earlier slots
-          for (int q2 = 0; q2 < 4; ++q2)
-            for (int l2 = 0; l2 < nq[q2]; ++l2) {
-              const int e2 = expert_of(q2, l2);
-              float x2 = __ldg(row + e2);
-              if (!isfinite(x2)) x2 = -INFINITY;
-              ties_below += (x2 == x && e2 < e) ? 1 : 0;
-            }
-        }
-        emit(x, e, ties_below);
-      }
-    } else if (q == 0) {
-      // More values equal th than slots left: ascending id order, every value
-      // > th and the first `need` equal to th; equal chosen values take slots
-      // in id order.
-      float* chosen = cand_x + tl * kTopkFastK;
-      int left = need, nch = 0;
-      for (int e = 0; e < E && nch < k; ++e) {
-        float x = row[e];
-        if (!isfinite(x)) x = -INFINITY;
-        if (!(x > th || (x == th && left > 0))) continue;
-        if (!(x > th)) --left;
-        int below = 0;
-        for (int c = 0; c < nch; ++c) below += (chosen[c] == x) ? 1 : 0;
-        chosen[nch++] = x;
-        emit(x, e, below);
-      }
-    }
-  }
+  auto emit = [&](int e, int slot, float exs) {
+    ids[static_cast<size_t>(t) * k + slot] = e;
+    wts[static_cast<size_t>(t) * k + slot] = exs / sum;
+    atomicOr(&bm[e * WPU + (tl >> 5)], 1u << (tl & 31));
+    atomicAdd(&cnt[e], 1);
+  };
+  if ((has_a && !ok_a) || (has_b && !ok_b)) report(ws, MOE_ERR_BOUNDS, 1, t);
+  if (ok_a) emit(ea, q, exa);
+  if (ok_b) emit(eb, q + 4, exb);
   __syncthreads();
-  const int t0 = blockIdx.x * kTopkTokens;
+  const int t0 = u * TOK;
   const int chunk = t0 / kChunk;
   const int w0 = (t0 % kChunk) / 32;
   uint32_t* out = gbm + static_cast<size_t>(chunk) * E * kChunkWords;
-  for (int i = threadIdx.x; i < 2 * E; i += blockDim.x) out[(i >> 1) * kChunkWords + w0 + (i & 1)] = bm[i];
+  for (int i = threadIdx.x; i < WPU * E; i += blockDim.x) out[(i / WPU) * kChunkWords + w0 + (i % WPU)] = bm[i];
   for (int e = threadIdx.x; e < E; e += blockDim.x)
     if (cnt[e] != 0) add_counts(ccount, T, E, e, chunk, cnt[e]);
 }
@@ -423,22 +440,29 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk4_kernel(const float* 
 // the GEMM row counts and, with a padding granule, the padding rows' markers.
 constexpr int kRankItems = 8;  // items per thread whose ids are loaded before the prologue
 
+// Shared memory is laid out for the random expert of each item: a warp's 32
+// items share their bitmap word w but not their expert, so the word table is
+// [w][E] (consecutive experts in consecutive banks) and each lookup is one
+// 8-byte load of {word, rank of the word's first token}; likewise one 8-byte
+// load gives an expert's {first grouped row of the chunk's run, start of its
+// run in the staging arrays}.
+// KC: k when it is known at compile time (8), 0 for a runtime k.
+template <int KC>
 __global__ void __launch_bounds__(256) route_rank_kernel(const int32_t* __restrict__ ids,
                                                          const uint32_t* __restrict__ gbm,
-                                                         const int32_t* __restrict__ ccount, int T, int E, int k,
+                                                         const int32_t* __restrict__ ccount, int T, int E, int k_arg,
                                                          int R, int pad, int32_t* __restrict__ dest,
                                                          int32_t* __restrict__ row_src,
                                                          uint8_t* __restrict__ row_slot,
                                                          int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                                          int32_t* __restrict__ tiles, int32_t* __restrict__ pairs,
                                                          int32_t* __restrict__ gcounts, WsHeader* ws) {
+  const int k = KC ? KC : k_arg;
   extern __shared__ uint32_t sm[];
   __shared__ int s_wsum[4][8];
-  uint32_t* words = sm;                                      // [E][8] the chunk's bitmap words
-  uint32_t* lpre = words + kChunkWords * E;                  // [E][8] rank within the chunk of each word's first token
-  int* base = reinterpret_cast<int*>(lpre + kChunkWords * E);  // [E] first grouped row of the chunk's run of e
-  int* loff = base + E;                                      // [E + 1] start of e's run in the staging arrays
-  int* tstart = loff + E + 1;                                // [E + 1] first tile of each expert
+  uint2* wl = reinterpret_cast<uint2*>(sm);                  // [8][E] {bitmap word, rank of its first token}
+  int2* bl = reinterpret_cast<int2*>(wl + kChunkWords * E);  // [E + 1] {first row of e's run, start of its staging run}
+  int* tstart = reinterpret_cast<int*>(bl + E + 1);          // [E + 1] first tile of each expert
   int* offs = tstart + E + 1;                                // [E + 1] first grouped row of each expert
   int* gcnt = offs + E + 1;                                  // [E] rows each expert's GEMMs run (padded)
   int* st_src = gcnt + E;                                    // [256 k] staging: token of each run position
@@ -459,6 +483,13 @@ __global__ void __launch_bounds__(256) route_rank_kernel(const int32_t* __restri
     ev[u] = (i < n_items) ? __ldg(my_ids + i) : 0;
   }
   const uint4* src = reinterpret_cast<const uint4*>(gbm + static_cast<size_t>(chunk) * E * kChunkWords);
+  // The bitmap words of this thread's first expert, also before the prologue.
+  const int per = (E + 255) / 256;
+  uint4 wa0 = make_uint4(0, 0, 0, 0), wb0 = make_uint4(0, 0, 0, 0);
+  if (threadIdx.x * per < E) {
+    wa0 = __ldg(src + 2 * threadIdx.x * per);
+    wb0 = __ldg(src + 2 * threadIdx.x * per + 1);
+  }
   const int nchunks = static_cast<int>(gridDim.x);
   const int nsuper = (nchunks + kSuperChunks - 1) / kSuperChunks;
   const int32_t* sc = ccount + static_cast<size_t>(E) * nchunks;
@@ -466,7 +497,7 @@ __global__ void __launch_bounds__(256) route_rank_kernel(const int32_t* __restri
   auto padded = [pad](int n) { return pad > 1 ? (n + pad - 1) / pad * pad : n; };
   // Thread tid owns experts [tid * per, tid * per + per): their words, local
   // prefixes, chunk counts, rows before this chunk and totals; block-wide scans
-  // give loff (over the chunk's counts) and the expert-level prefixes.
+  // give the staging run starts (over the chunk's counts) and the expert-level prefixes.
   // Rows of each expert before this chunk and in all.  Expert e's items are its
   // super-chunk counts (nsuper) and the counts of the chunks before this one in
   // its own super-chunk (fewer than 32), both contiguous; a group of tpe
@@ -476,6 +507,9 @@ __global__ void __launch_bounds__(256) route_rank_kernel(const int32_t* __restri
   {
     const int c0 = s0 * kSuperChunks;
     const int n_sup = nsuper, n_items_e = nsuper + (chunk - c0);
+    // Both count rows 16-byte aligned (ccount itself is: 16 words past a
+    // 16-byte aligned place in the workspace).
+    const bool vec = (nchunks & 3) == 0 && (nsuper & 3) == 0;
     int tpe = 1;
     while (tpe < 32 && tpe * 2 * E <= 256) tpe *= 2;
     const int groups = 256 / tpe, g0 = threadIdx.x / tpe, li = threadIdx.x % tpe;
@@ -485,14 +519,34 @@ __global__ void __launch_bounds__(256) route_rank_kernel(const int32_t* __restri
       if (e < E) {
         const int32_t* scr = sc + static_cast<size_t>(e) * nsuper;
         const int32_t* ccr = ccount + static_cast<size_t>(e) * nchunks + c0;
+        if (vec) {
+          // 16-byte vectors, all in flight at once: nsuper / 4 of super-chunk
+          // counts, then the chunk counts from c0 (a multiple of 32) up to this
+          // chunk, the last vector masked (it ends inside the row: nchunks % 4 == 0).
+          const int nvs = nsuper >> 2, lim = chunk - c0, nvc = (lim + 3) >> 2;
+#pragma unroll 8
+          for (int j = li; j < nvs + nvc; j += tpe) {
+            if (j < nvs) {
+              const int4 v = __ldg(reinterpret_cast<const int4*>(scr) + j);
+              const int b = 4 * j;
+              tot += v.x + v.y + v.z + v.w;
+              before += (b < s0 ? v.x : 0) + (b + 1 < s0 ? v.y : 0) + (b + 2 < s0 ? v.z : 0) + (b + 3 < s0 ? v.w : 0);
+            } else {
+              const int4 v = __ldg(reinterpret_cast<const int4*>(ccr) + (j - nvs));
+              const int b = 4 * (j - nvs);
+              before += (b < lim ? v.x : 0) + (b + 1 < lim ? v.y : 0) + (b + 2 < lim ? v.z : 0) + (b + 3 < lim ? v.w : 0);
+            }
+          }
+        } else {
 #pragma unroll 4
-        for (int j = li; j < n_items_e; j += tpe) {
-          if (j < n_sup) {
-            const int v = __ldg(scr + j);
-            tot += v;
-            before += j < s0 ? v : 0;
-          } else {
-            before += __ldg(ccr + (j - n_sup));
+          for (int j = li; j < n_items_e; j += tpe) {
+            if (j < n_sup) {
+              const int v = __ldg(scr + j);
+              tot += v;
+              before += j < s0 ? v : 0;
+            } else {
+              before += __ldg(ccr + (j - n_sup));
+            }
           }
         }
       }
@@ -501,28 +555,26 @@ __global__ void __launch_bounds__(256) route_rank_kernel(const int32_t* __restri
         before += __shfl_xor_sync(0xffffffffu, before, off);
       }
       if (li == 0 && e < E) {
-        base[e] = before;  // the expert's first row is added below
+        bl[e].x = before;  // the expert's first row is added below
         gcnt[e] = tot;     // the real total for now; padded below
       }
     }
   }
   __syncthreads();
-  const int per = (E + 255) / 256;
   int my_cnt = 0, my_n = 0, my_m = 0, my_p = 0;
   for (int u = 0; u < per; ++u) {
     const int e = threadIdx.x * per + u;
     if (e >= E) break;
-    const uint4 a = __ldg(src + 2 * e), b = __ldg(src + 2 * e + 1);
+    const uint4 a = u == 0 ? wa0 : __ldg(src + 2 * e), b = u == 0 ? wb0 : __ldg(src + 2 * e + 1);
     const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     const int tot = gcnt[e];
     uint32_t run = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      words[e * 8 + j] = w[j];
-      lpre[e * 8 + j] = run;
+      wl[j * E + e] = make_uint2(w[j], run);
       run += __popc(w[j]);
     }
-    loff[e] = my_cnt;  // thread-local prefixes, completed below
+    bl[e].y = my_cnt;  // thread-local prefixes, completed below
     my_cnt += static_cast<int>(run);
     const int n = padded(tot);
     my_n += n;
@@ -562,10 +614,10 @@ __global__ void __launch_bounds__(256) route_rank_kernel(const int32_t* __restri
     if (e >= E) break;
     const int real = gcnt[e];
     const int n = padded(real);
-    loff[e] += run_c;
+    bl[e].y += run_c;
     offs[e] = run_n;
     tstart[e] = run_m;
-    base[e] += run_n;
+    bl[e].x += run_n;
     gcnt[e] = n;
     if (writer) {
       counts[e] = real;
@@ -586,7 +638,7 @@ __global__ void __launch_bounds__(256) route_rank_kernel(const int32_t* __restri
     run_m += (n + kTileRows - 1) / kTileRows;
     run_p += (n + 2 * kTileRows - 1) / (2 * kTileRows);
     if (e == E - 1) {
-      loff[E] = run_c + my_cnt;  // the chunk's items (run_c: this thread's exclusive prefix)
+      bl[E].y = run_c + my_cnt;  // the chunk's items (run_c: this thread's exclusive prefix)
       offs[E] = run_n;
       tstart[E] = run_m;
       if (writer) {
@@ -607,14 +659,16 @@ __global__ void __launch_bounds__(256) route_rank_kernel(const int32_t* __restri
       return;
     }
     const int w = tl >> 5, b = tl & 31;
-    const int rho = static_cast<int>(lpre[e * 8 + w] + __popc(words[e * 8 + w] & ((1u << b) - 1u)));
-    const int r = base[e] + rho;
+    const uint2 wr = wl[w * E + e];
+    const int rho = static_cast<int>(wr.y + __popc(wr.x & ((1u << b) - 1u)));
+    const int2 be = bl[e];
+    const int r = be.x + rho;
     if (r < 0 || r >= R) {
       report(ws, MOE_ERR_BOUNDS, 2, t);
       return;
     }
     dest[static_cast<size_t>(t0) * k + i] = r;
-    const int pos = loff[e] + rho;
+    const int pos = be.y + rho;
     if (pos < 0 || pos >= kChunk * k) {
       report(ws, MOE_ERR_BOUNDS, 2, t);
       return;
@@ -631,10 +685,11 @@ __global__ void __launch_bounds__(256) route_rank_kernel(const int32_t* __restri
   for (int i = threadIdx.x + 256 * kRankItems; i < n_items; i += 256) place(i, __ldg(my_ids + i));
   __syncthreads();
   // Run positions in expert order -> consecutive grouped rows.
-  const int n_pos = min(loff[E], kChunk * k);
+  const int n_pos = min(bl[E].y, kChunk * k);
   for (int pos = threadIdx.x; pos < n_pos; pos += 256) {
     const int e = st_e[pos];
-    const int r = e < E ? base[e] + (pos - loff[e]) : -1;
+    const int2 be = e < E ? bl[e] : make_int2(-1, 0);
+    const int r = e < E ? be.x + (pos - be.y) : -1;
     if (r < 0 || r >= R) {
       report(ws, MOE_ERR_BOUNDS, 2, t0);
       continue;
@@ -676,17 +731,20 @@ cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t s, LaunchHook& hook) {
   hook.before(s);
   const int nv4 = (p.E + 15) / 16;
   if (p.E % 4 == 0 && p.E <= 256 && p.k <= kTopkFastK) {
-    const size_t smem4 = (static_cast<size_t>(p.E) * 3 + static_cast<size_t>(kTopkTokens) * kTopkFastK) * 4;
-    const bool full = (p.E % 16) == 0;
-    switch ((nv4 <= 1 ? 1 : nv4 <= 2 ? 2 : nv4 <= 4 ? 4 : nv4 <= 8 ? 8 : 16) * (full ? 1 : -1)) {
-#define MOE_TOPK4_CASE(NV4, FULL)                                                                              \
-  case (FULL ? NV4 : -NV4):                                                                                    \
-    if (p.k == 8)                                                                                              \
-      route_topk4_kernel<NV4, FULL, 8><<<nblocks, kTopkThreads, smem4, s>>>(p.logits, p.T, p.E, p.k, p.ids,    \
-                                                                            p.w, p.gbm, p.ccount, p.ws);       \
-    else                                                                                                       \
-      route_topk4_kernel<NV4, FULL, 0><<<nblocks, kTopkThreads, smem4, s>>>(p.logits, p.T, p.E, p.k, p.ids,    \
-                                                                            p.w, p.gbm, p.ccount, p.ws);       \
+    const int nv4p = nv4 <= 1 ? 1 : nv4 <= 2 ? 2 : nv4 <= 4 ? 4 : nv4 <= 8 ? 8 : 16;
+    const bool full = p.E == 16 * nv4p;  // every one of the 16 * NV4 value slots is a logit of the row
+    constexpr int tok = kTopk4Tokens;
+    const size_t smem4 = static_cast<size_t>(p.E) * (tok / 32 + 1) * 4;
+    const int nunits = (p.T + tok - 1) / tok;
+    switch (nv4p * (full ? 1 : -1)) {
+#define MOE_TOPK4_CASE(NV4, FULL)                                                                  \
+  case (FULL ? NV4 : -NV4):                                                                        \
+    if (p.k == 8)                                                                                  \
+      route_topk4_kernel<NV4, FULL, 8, tok><<<nunits, 4 * tok, smem4, s>>>(                        \
+          p.logits, p.T, p.E, p.k, p.ids, p.w, p.gbm, p.ccount, p.ws);                             \
+    else                                                                                           \
+      route_topk4_kernel<NV4, FULL, 0, tok><<<nunits, 4 * tok, smem4, s>>>(                        \
+          p.logits, p.T, p.E, p.k, p.ids, p.w, p.gbm, p.ccount, p.ws);                             \
     break;
       MOE_TOPK4_CASE(1, true)
       MOE_TOPK4_CASE(2, true)
@@ -720,16 +778,15 @@ cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t s, LaunchHook& hook) {
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   hook.before(s);
-  const size_t rank_smem = (static_cast<size_t>(2 * kChunkWords) * p.E + 5 * static_cast<size_t>(p.E) + 3) * 4 +
+  const size_t rank_smem = (static_cast<size_t>(2 * kChunkWords) * p.E + 5 * static_cast<size_t>(p.E) + 4) * 4 +
                            static_cast<size_t>(kChunk) * p.k * 7;
+  auto rank = p.k == 8 ? route_rank_kernel<8> : route_rank_kernel<0>;
   if (rank_smem > 48 * 1024) {
-    err = cudaFuncSetAttribute(route_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(rank_smem));
+    err = cudaFuncSetAttribute(rank, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(rank_smem));
     if (err != cudaSuccess) return err;
   }
-  route_rank_kernel<<<nchunks, 256, rank_smem, s>>>(p.ids, p.gbm, p.ccount, p.T, p.E, p.k, p.R, p.pad, p.dest,
-                                                    p.row_src, p.row_slot, p.counts, p.offsets, p.tiles, p.pairs,
-                                                    p.gcounts, p.ws);
+  rank<<<nchunks, 256, rank_smem, s>>>(p.ids, p.gbm, p.ccount, p.T, p.E, p.k, p.R, p.pad, p.dest, p.row_src,
+                                       p.row_slot, p.counts, p.offsets, p.tiles, p.pairs, p.gcounts, p.ws);
   hook.after(s);
   return cudaGetLastError();
 }

@@ -3,8 +3,10 @@
 Covers both top-k kernels (four threads per token where E % 4 == 0, E <= 256
 and k <= 8; one warp per token otherwise), ragged token counts (not multiples
 of the 64-token CTA or the 256-token chunk), logits with many exact ties (values
-drawn from a few levels, and every logit equal) and logits that differ only in
-their last bits (distinct values a few ulps apart).  Ties must go to the
+drawn from a few levels, every logit equal, and -0 next to +0) and logits that
+differ only in their last bits (distinct values a few ulps apart).  Row widths
+E that are multiples of 16 without being 16 times a power of two leave value
+slots of the four-thread kernel past the row's end.  Ties must go to the
 lower expert id ("UniEP", section 3.1: a deterministic mapping; the gating reading
 of the layer: descending logit, ties to the lower id).
 """
@@ -22,10 +24,12 @@ SHAPES = [
     (520, 256, 8), (333, 256, 1), (4000, 32, 8), (100, 32, 1), (700, 128, 3), (65, 64, 8),
     # several 8192-token super-chunks (the coarse level of the prefix over chunks), ragged tails
     (20000, 64, 6), (17000, 128, 8),
+    # E a multiple of 16 but not 16 times a power of two: the row is narrower than the value slots
+    (700, 48, 8), (1000, 80, 4), (900, 96, 6), (5000, 112, 8), (300, 192, 8), (257, 240, 5),
     # the warp-per-token kernel
     (500, 6, 2), (400, 260, 4), (300, 64, 9), (129, 1, 1), (9000, 6, 2),
 ]
-KINDS = ["normal", "levels", "equal", "close"]
+KINDS = ["normal", "levels", "equal", "close", "zeros"]
 
 
 def _logits(T, E, kind, seed):
@@ -36,6 +40,9 @@ def _logits(T, E, kind, seed):
         return torch.randint(0, 5, (T, E), generator=g).float() * 0.5 - 1.0
     if kind == "close":  # 0.5 plus a few multiples of 2^-21: distinct values 8 ulps apart, some exact ties
         return 0.5 + torch.randint(0, 6, (T, E), generator=g).float() * 2.0 ** -21
+    if kind == "zeros":  # -0 and +0 (equal values: ids decide), the smallest subnormals of both signs, one level
+        levels = torch.tensor([-0.0, 0.0, -1e-45, 1e-45, 0.25])
+        return levels[torch.randint(0, 5, (T, E), generator=g)]
     return torch.full((T, E), 0.75)
 
 
