@@ -194,7 +194,7 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, mx, reasons = [], 0.0, set()
+        sm, mx, reasons, pw = [], 0.0, set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
@@ -205,12 +205,19 @@ class ClockSampler:
                 mx = max(mx, float(parts[1]))
             except ValueError:
                 continue
+            try:
+                pw.append(float(parts[2]))
+            except ValueError:
+                pass
             for n, v in zip(names, parts[4:8]):
                 if v.lower() == "active":
                     reasons.add(n)
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        if pw:
+            out["power_w"] = statistics.median(pw)
+        return out
 
 
 def dist_setup():
@@ -740,12 +747,16 @@ def run_ours(args):
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    e2e_clocks = ClockSampler(local)
+    e2e_clocks.start()
+    time.sleep(0.3)
     e0.record(stream)
     for c in (cs, cs2, cs_d, cs_d2):
         c.wait_event(e0)
     e2e_run(args.steps)
     e1.record(stream)
     torch.cuda.synchronize()
+    e2e_clk = e2e_clocks.stop()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
     h2d = h_x.numel() * 2 + (0 if args.router else h_lg.numel() * 4) + h_do.numel() * 2
     d2h = h_out.numel() * 2 + h_dx.numel() * 2
@@ -782,7 +793,8 @@ def run_ours(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "copies": "pinned host <-> device on two upload and two download streams, double-buffered: "
                           "step i+1's upload and step i's download overlap compute",
-                "launch": "CUDA graph per buffer set" if graph is not None else "eager launches"},
+                "launch": "CUDA graph per buffer set" if graph is not None else "eager launches",
+                "clocks": e2e_clk},
         "gpu_launches": int(launches),
         "kernel_timing": {"how": "CUDA event pair around each kernel on its launching stream, second timed pass of "
                                  "the same K steps (eager launches)", "ms_per_step_with_events": round(ms_events, 4)},
