@@ -744,6 +744,18 @@ def run_ours(args):
 
     e2e_run(max(3, args.warmup))
     torch.cuda.synchronize()
+    # This machine's host copy rates (one 1 GB-class copy each way on one stream), a
+    # reference for the end-to-end number: its copies must hide behind the step.
+    probe = {}
+    for name, dst, src in (("h2d", d_in[0][0], h_x), ("d2h", h_out, d_res[0][0])):
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(cs)
+        with torch.cuda.stream(cs):
+            dst.copy_(src, non_blocking=True)
+        c1.record(cs)
+        c1.synchronize()
+        probe[name] = round(src.numel() * src.element_size() / (c0.elapsed_time(c1) * 1e-3) / 1e9, 1)
+    torch.cuda.synchronize()
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -794,7 +806,7 @@ def run_ours(args):
                 "copies": "pinned host <-> device on two upload and two download streams, double-buffered: "
                           "step i+1's upload and step i's download overlap compute",
                 "launch": "CUDA graph per buffer set" if graph is not None else "eager launches",
-                "clocks": e2e_clk},
+                "host_copy_gbs": probe, "clocks": e2e_clk},
         "gpu_launches": int(launches),
         "kernel_timing": {"how": "CUDA event pair around each kernel on its launching stream, second timed pass of "
                                  "the same K steps (eager launches)", "ms_per_step_with_events": round(ms_events, 4)},
