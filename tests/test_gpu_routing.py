@@ -22,8 +22,9 @@ pytestmark = pytest.mark.gpu
 SHAPES = [
     (1, 4, 4), (63, 8, 2), (300, 12, 3), (1000, 20, 5), (777, 64, 6), (1500, 100, 8), (2049, 128, 8),
     (520, 256, 8), (333, 256, 1), (4000, 32, 8), (100, 32, 1), (700, 128, 3), (65, 64, 8),
-    # several 8192-token super-chunks (the coarse level of the prefix over chunks), ragged tails
-    (20000, 64, 6), (17000, 128, 8),
+    # several 8192-token super-chunks (the coarse level of the prefix over chunks), ragged tails;
+    # 32768 tokens: chunk and super-chunk counts both a multiple of 4 (the rank kernel's 16-byte loads)
+    (20000, 64, 6), (17000, 128, 8), (32768, 64, 8), (32768, 128, 3),
     # E a multiple of 16 but not 16 times a power of two: the row is narrower than the value slots
     (700, 48, 8), (1000, 80, 4), (900, 96, 6), (5000, 112, 8), (300, 192, 8), (257, 240, 5),
     # the warp-per-token kernel
