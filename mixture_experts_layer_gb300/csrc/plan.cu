@@ -797,7 +797,7 @@ cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t s, LaunchHook& hook) {
 // Routing without a caller-provided workspace (moe_plan_noalloc).
 //
 // For callers that may not allocate device memory while they run, the scratch
-// of the three routing kernels (per-chunk counts, bases and bitmaps) lives in
+// of the routing kernels (per-chunk and per-super-chunk counts, bitmaps) lives in
 // the file-scope array below.  Host code must not use the array's name as a
 // device address: it only names a host-side stand-in.  The device address is
 // looked up with cudaGetSymbolAddress (with the device current) and passed to
