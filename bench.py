@@ -706,7 +706,7 @@ def run_ours(args):
 
     # End-to-end through the C ABI: every step copies its inputs from pinned host
     # memory and reads its results (out, dx) back to pinned host memory.  The copies
-    # run on a copy stream, double-buffered, the way a training loop overlaps its
+    # run on copy streams, double-buffered, the way a training loop overlaps its
     # data movement with compute: step i+1's inputs are uploaded while step i
     # computes, and step i's results (written by the layer straight into buffer set
     # i mod 2: the C ABI takes out and dx per call) download while step i+1 computes.
@@ -720,32 +720,42 @@ def run_ours(args):
     d_in = [(torch.empty_like(inp["x"]), torch.empty_like(inp["logits"]), torch.empty_like(inp["dout"]))
             for _ in range(2)]
     d_res = [(torch.empty_like(layer.out), torch.empty_like(layer.dx)) for _ in range(2)]  # out, dx per buffer set
-    # Two upload and two download streams, so the two large tensors each way move on
-    # copy engines of their own at the same time.
-    cs, cs2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)       # uploads: x (+ logits), dout
-    cs_d, cs_d2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)   # downloads: out, dx
-    ev_in = [torch.cuda.Event() for _ in range(2)]      # x (and logits) j uploaded
-    ev_in2 = [torch.cuda.Event() for _ in range(2)]     # dout j uploaded
-    ev_used = [torch.cuda.Event() for _ in range(2)]    # compute done with inputs j
-    ev_staged = [torch.cuda.Event() for _ in range(2)]  # results j written
-    ev_out = [torch.cuda.Event() for _ in range(2)]     # out j downloaded
-    ev_out2 = [torch.cuda.Event() for _ in range(2)]    # dx j downloaded
+    # NS upload and NS download streams: every tensor moves as NS row slices, one per
+    # stream, so the copies spread over several copy engines each way.
+    NS = 4
+    ups = [torch.cuda.Stream(dev) for _ in range(NS)]
+    downs = [torch.cuda.Stream(dev) for _ in range(NS)]
+    bounds = [T * q // NS for q in range(NS + 1)]
+    rows = [(bounds[q], bounds[q + 1]) for q in range(NS)]  # token rows of slice q
+    ev_in = [[torch.cuda.Event() for _ in range(NS)] for _ in range(2)]   # slice q of inputs j uploaded
+    ev_used = [torch.cuda.Event() for _ in range(2)]                       # compute done with inputs j
+    ev_staged = [torch.cuda.Event() for _ in range(2)]                     # results j written
+    ev_out = [[torch.cuda.Event() for _ in range(NS)] for _ in range(2)]  # slice q of results j downloaded
     for j in range(2):
-        for ev in (ev_used[j], ev_out[j], ev_out2[j]):
-            ev.record(stream)
+        ev_used[j].record(stream)
+        for q in range(NS):
+            ev_out[j][q].record(stream)
 
     def upload(j):
         d_x, d_lg, d_do = d_in[j]
-        cs.wait_event(ev_used[j])
-        with torch.cuda.stream(cs):
-            d_x.copy_(h_x, non_blocking=True)
-            if not args.router:
-                d_lg.copy_(h_lg, non_blocking=True)
-        ev_in[j].record(cs)
-        cs2.wait_event(ev_used[j])
-        with torch.cuda.stream(cs2):
-            d_do.copy_(h_do, non_blocking=True)
-        ev_in2[j].record(cs2)
+        for q, st in enumerate(ups):
+            a_, b_ = rows[q]
+            st.wait_event(ev_used[j])
+            with torch.cuda.stream(st):
+                d_x[a_:b_].copy_(h_x[a_:b_], non_blocking=True)
+                d_do[a_:b_].copy_(h_do[a_:b_], non_blocking=True)
+                if not args.router:
+                    d_lg[a_:b_].copy_(h_lg[a_:b_], non_blocking=True)
+            ev_in[j][q].record(st)
+
+    def download(j):
+        for q, st in enumerate(downs):
+            a_, b_ = rows[q]
+            st.wait_event(ev_staged[j])
+            with torch.cuda.stream(st):
+                h_out[a_:b_].copy_(d_res[j][0][a_:b_], non_blocking=True)
+                h_dx[a_:b_].copy_(d_res[j][1][a_:b_], non_blocking=True)
+            ev_out[j][q].record(st)
 
     def compute(j):
         d_x, d_lg, d_do = d_in[j]
@@ -772,10 +782,9 @@ def run_ours(args):
 
     def e2e_step(i, last):
         j = i & 1
-        stream.wait_event(ev_in[j])
-        stream.wait_event(ev_in2[j])
-        stream.wait_event(ev_out[j])   # results j downloaded (two steps ago)
-        stream.wait_event(ev_out2[j])
+        for q in range(NS):
+            stream.wait_event(ev_in[j][q])
+            stream.wait_event(ev_out[j][q])  # results j downloaded (two steps ago)
         if e2e_graphs[j] is not None:
             e2e_graphs[j].replay()
         else:
@@ -784,35 +793,36 @@ def run_ours(args):
         ev_staged[j].record(stream)
         if not last:
             upload(j ^ 1)
-        cs_d.wait_event(ev_staged[j])
-        with torch.cuda.stream(cs_d):
-            h_out.copy_(d_res[j][0], non_blocking=True)
-        ev_out[j].record(cs_d)
-        cs_d2.wait_event(ev_staged[j])
-        with torch.cuda.stream(cs_d2):
-            h_dx.copy_(d_res[j][1], non_blocking=True)
-        ev_out2[j].record(cs_d2)
+        download(j)
 
     def e2e_run(n):
         upload(0)
         for i in range(n):
             e2e_step(i, i == n - 1)
-        stream.wait_event(ev_out[(n - 1) & 1])
-        stream.wait_event(ev_out2[(n - 1) & 1])
+        for q in range(NS):
+            stream.wait_event(ev_out[(n - 1) & 1][q])
 
     e2e_run(max(3, args.warmup))
     torch.cuda.synchronize()
-    # This machine's host copy rates (one 1 GB-class copy each way on one stream), a
-    # reference for the end-to-end number: its copies must hide behind the step.
+    # This machine's host copy rates for one x-sized tensor each way, on one stream
+    # and as NS row slices on NS streams: a reference for the end-to-end number,
+    # whose copies must hide behind the step.
     probe = {}
     for name, dst, src in (("h2d", d_in[0][0], h_x), ("d2h", h_out, d_res[0][0])):
-        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        c0.record(cs)
-        with torch.cuda.stream(cs):
-            dst.copy_(src, non_blocking=True)
-        c1.record(cs)
-        c1.synchronize()
-        probe[name] = round(src.numel() * src.element_size() / (c0.elapsed_time(c1) * 1e-3) / 1e9, 1)
+        for nst in (1, NS):
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            c0.record(stream)
+            for q in range(nst):
+                st = (ups if name == "h2d" else downs)[q]
+                st.wait_event(c0)
+                a_, b_ = (T * q // nst, T * (q + 1) // nst)
+                with torch.cuda.stream(st):
+                    dst[a_:b_].copy_(src[a_:b_], non_blocking=True)
+                stream.wait_stream(st)
+            c1.record(stream)
+            c1.synchronize()
+            key = name if nst == 1 else f"{name}_{nst}_streams"
+            probe[key] = round(src.numel() * src.element_size() / (c0.elapsed_time(c1) * 1e-3) / 1e9, 1)
     torch.cuda.synchronize()
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
@@ -821,7 +831,7 @@ def run_ours(args):
     e2e_clocks.start()
     time.sleep(0.3)
     e0.record(stream)
-    for c in (cs, cs2, cs_d, cs_d2):
+    for c in ups + downs:
         c.wait_event(e0)
     e2e_run(args.steps)
     e1.record(stream)
@@ -861,8 +871,8 @@ def run_ours(args):
         "roofline": roof,
         "e2e": {"value": round(world * T * args.steps / (e2e_ms * 1e-3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "copies": "pinned host <-> device on two upload and two download streams, double-buffered: "
-                          "step i+1's upload and step i's download overlap compute",
+                "copies": f"pinned host <-> device as {NS} row slices on {NS} upload and {NS} download streams, "
+                          "double-buffered: step i+1's upload and step i's download overlap compute",
                 "launch": "CUDA graph per buffer set" if graph is not None else "eager launches",
                 "host_buffers": ("anonymous mappings advised for transparent huge pages, page-locked with "
                                  "cudaHostRegister") if hb.fallbacks == 0 else "torch pin_memory (in part)",
