@@ -465,9 +465,9 @@ __global__ void __launch_bounds__(256) route_rank_kernel(const int32_t* __restri
   int* tstart = reinterpret_cast<int*>(bl + E + 1);          // [E + 1] first tile of each expert
   int* offs = tstart + E + 1;                                // [E + 1] first grouped row of each expert
   int* gcnt = offs + E + 1;                                  // [E] rows each expert's GEMMs run (padded)
-  int* st_src = gcnt + E;                                    // [256 k] staging: token of each run position
-  uint16_t* st_e = reinterpret_cast<uint16_t*>(st_src + kChunk * k);  // expert of each run position
-  uint8_t* st_slot = reinterpret_cast<uint8_t*>(st_e + kChunk * k);   // slot of each run position
+  // [256 k] staging, one word per run position: token in the chunk (bits 0-7),
+  // slot (bits 8-12, k <= 32), expert (bits 13-22, E <= 1024).
+  uint32_t* st = reinterpret_cast<uint32_t*>(gcnt + E);
   const int chunk = blockIdx.x;
   const int t0 = chunk * kChunk;
   const int n_items = min(kChunk, T - t0) * k;
@@ -673,9 +673,7 @@ __global__ void __launch_bounds__(256) route_rank_kernel(const int32_t* __restri
       report(ws, MOE_ERR_BOUNDS, 2, t);
       return;
     }
-    st_src[pos] = t;
-    st_e[pos] = static_cast<uint16_t>(e);
-    st_slot[pos] = static_cast<uint8_t>(j);
+    st[pos] = static_cast<uint32_t>(tl) | (static_cast<uint32_t>(j) << 8) | (static_cast<uint32_t>(e) << 13);
   };
 #pragma unroll
   for (int u = 0; u < kRankItems; ++u) {
@@ -687,15 +685,16 @@ __global__ void __launch_bounds__(256) route_rank_kernel(const int32_t* __restri
   // Run positions in expert order -> consecutive grouped rows.
   const int n_pos = min(bl[E].y, kChunk * k);
   for (int pos = threadIdx.x; pos < n_pos; pos += 256) {
-    const int e = st_e[pos];
+    const uint32_t word = st[pos];
+    const int e = static_cast<int>(word >> 13);
     const int2 be = e < E ? bl[e] : make_int2(-1, 0);
     const int r = e < E ? be.x + (pos - be.y) : -1;
     if (r < 0 || r >= R) {
       report(ws, MOE_ERR_BOUNDS, 2, t0);
       continue;
     }
-    row_src[r] = st_src[pos];
-    row_slot[r] = st_slot[pos];
+    row_src[r] = t0 + static_cast<int>(word & 0xffu);
+    row_slot[r] = static_cast<uint8_t>((word >> 8) & 0x1fu);
   }
 
   // Tile entries [m0, m1) of this CTA: the expert of tile m is the last e
@@ -779,7 +778,7 @@ cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t s, LaunchHook& hook) {
   if (err != cudaSuccess) return err;
   hook.before(s);
   const size_t rank_smem = (static_cast<size_t>(2 * kChunkWords) * p.E + 5 * static_cast<size_t>(p.E) + 4) * 4 +
-                           static_cast<size_t>(kChunk) * p.k * 7;
+                           static_cast<size_t>(kChunk) * p.k * 4;
   auto rank = p.k == 8 ? route_rank_kernel<8> : route_rank_kernel<0>;
   if (rank_smem > 48 * 1024) {
     err = cudaFuncSetAttribute(rank, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(rank_smem));
