@@ -736,26 +736,52 @@ def run_ours(args):
         for q in range(NS):
             ev_out[j][q].record(stream)
 
+    # With `windows` set, every copy slice is bracketed by timing events, so the timed
+    # region also reports the copy rates it got (other work on the machine can slow
+    # host memory down while the region runs).
+    windows = None
+
+    def bracket(st):
+        if windows is None:
+            return None
+        a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_ev.record(st)
+        return a_ev, b_ev
+
     def upload(j):
         d_x, d_lg, d_do = d_in[j]
+        evs = []
         for q, st in enumerate(ups):
             a_, b_ = rows[q]
             st.wait_event(ev_used[j])
+            br = bracket(st)
             with torch.cuda.stream(st):
                 d_x[a_:b_].copy_(h_x[a_:b_], non_blocking=True)
                 d_do[a_:b_].copy_(h_do[a_:b_], non_blocking=True)
                 if not args.router:
                     d_lg[a_:b_].copy_(h_lg[a_:b_], non_blocking=True)
+            if br is not None:
+                br[1].record(st)
+                evs.append(br)
             ev_in[j][q].record(st)
+        if windows is not None:
+            windows["h2d"].append(evs)
 
     def download(j):
+        evs = []
         for q, st in enumerate(downs):
             a_, b_ = rows[q]
             st.wait_event(ev_staged[j])
+            br = bracket(st)
             with torch.cuda.stream(st):
                 h_out[a_:b_].copy_(d_res[j][0][a_:b_], non_blocking=True)
                 h_dx[a_:b_].copy_(d_res[j][1][a_:b_], non_blocking=True)
+            if br is not None:
+                br[1].record(st)
+                evs.append(br)
             ev_out[j][q].record(st)
+        if windows is not None:
+            windows["d2h"].append(evs)
 
     def compute(j):
         d_x, d_lg, d_do = d_in[j]
@@ -833,10 +859,25 @@ def run_ours(args):
     e0.record(stream)
     for c in ups + downs:
         c.wait_event(e0)
+    windows = {"h2d": [], "d2h": []}
     e2e_run(args.steps)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_clk = e2e_clocks.stop()
+    # Each step's upload (download) window: first slice start to last slice end.
+    in_region = {}
+    for name, nbytes in (("h2d", (h_x.numel() + h_do.numel()) * 2 + (0 if args.router else h_lg.numel() * 4)),
+                         ("d2h", (h_out.numel() + h_dx.numel()) * 2)):
+        spans = []
+        for evs in windows[name]:
+            t0_ = min(range(len(evs)), key=lambda q: e0.elapsed_time(evs[q][0]))
+            start = e0.elapsed_time(evs[t0_][0])
+            end = max(e0.elapsed_time(b_) for _, b_ in evs)
+            spans.append(end - start)
+        if spans:
+            in_region[name] = round(nbytes / (statistics.median(spans) * 1e-3) / 1e9, 1)
+            in_region[name + "_ms_median"] = round(statistics.median(spans), 3)
+    windows = None
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
     h2d = h_x.numel() * 2 + (0 if args.router else h_lg.numel() * 4) + h_do.numel() * 2
     d2h = h_out.numel() * 2 + h_dx.numel() * 2
@@ -876,7 +917,7 @@ def run_ours(args):
                 "launch": "CUDA graph per buffer set" if graph is not None else "eager launches",
                 "host_buffers": ("anonymous mappings advised for transparent huge pages, page-locked with "
                                  "cudaHostRegister") if hb.fallbacks == 0 else "torch pin_memory (in part)",
-                "host_copy_gbs": probe, "clocks": e2e_clk},
+                "host_copy_gbs": probe, "copy_gbs_in_region": in_region, "clocks": e2e_clk},
         "gpu_launches": int(launches),
         "kernel_timing": {"how": "CUDA event pair around each kernel on its launching stream, second timed pass of "
                                  "the same K steps (eager launches)", "ms_per_step_with_events": round(ms_events, 4)},
